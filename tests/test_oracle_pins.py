@@ -1,0 +1,454 @@
+"""Pins for the oracle: what the pages and the mathematics fix, independent of
+the oracle's own code.
+
+Each ``check_*`` helper takes the implementation under test as arguments so
+that ``test_pins_catch_planted_mistakes`` can run the same checks against
+deliberately broken copies of the oracle (on the CPU) and show that each
+plausible mistake fails at least one pin.
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(path):
+    out = []
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                out.append(line.split())
+    return out
+
+
+def _tagged_pool(N, L, bs, H, D, dtype=np.float32):
+    """Pool whose every element encodes (block, layer, row, head, d), so a
+    gathered row tells where it came from."""
+    idx = np.arange(N * L * bs * H * D, dtype=np.int64).reshape(N, L, bs, H, D)
+    if dtype == np.uint16:
+        return (idx % 65521).astype(np.uint16)
+    return idx.astype(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# reusable checks
+# ---------------------------------------------------------------------------
+
+def check_block_table_example(slot_of, build_slot_mapping, gather_loop):
+    rows = _rows(os.path.join(GOLDEN, "block_table_7_3_12.txt"))
+    table = [7, 3, 12]
+    for tok, blk, row, slot in ((int(a), int(b), int(c), int(d)) for a, b, c, d in rows):
+        assert slot_of(table, 0, tok, 16) == slot
+        assert slot // 16 == blk and slot % 16 == row
+    sm = build_slot_mapping(np.array([table], np.int32), np.array([0], np.int32),
+                            np.zeros(48, np.int32), np.arange(48, dtype=np.int32), 16)
+    assert sm.tolist() == [int(r[3]) for r in rows]
+    pool = _tagged_pool(16, 1, 16, 1, 1)
+    got = gather_loop(pool, 0, table, 48, 0)[:, 0, 0]
+    want = np.array([pool[int(r[1]), 0, int(r[2]), 0, 0] for r in rows])
+    assert np.array_equal(got, want)
+
+
+def check_slot_walk(slot_of):
+    """Brute force: enumerate a table's rows in storage order (first block
+    from the offset, later blocks from row 0) and number the tokens; every
+    token's slot must match."""
+    rng = np.random.default_rng(5)
+    for bs in (1, 2, 4, 16):
+        for _ in range(20):
+            N = 40
+            nblk = int(rng.integers(1, 6))
+            table = rng.permutation(N)[:nblk]
+            off = int(rng.integers(0, bs))
+            tok = 0
+            for k, blk in enumerate(table):
+                for r in range(off if k == 0 else 0, bs):
+                    assert slot_of(table, off, tok, bs) == int(blk) * bs + r
+                    tok += 1
+
+
+def check_gather_forms(gather_loop, gather_indexed):
+    rng = np.random.default_rng(6)
+    for bs in (1, 4, 16):
+        pool = _tagged_pool(32, 3, bs, 2, 4)
+        for _ in range(15):
+            nblk = int(rng.integers(1, 6))
+            table = rng.permutation(32)[:nblk]
+            off = int(rng.integers(0, bs))
+            n = int(rng.integers(0, nblk * bs - off + 1))
+            layer = int(rng.integers(0, 3))
+            a = gather_loop(pool, layer, table, n, off)
+            b = gather_indexed(pool, layer, table, n, off)
+            assert a.shape == (n, 2, 4)
+            assert np.array_equal(a, b)
+
+
+def check_identity_table(gather_loop):
+    """Table 0,1,2,... : the sequence is a contiguous run of the layer."""
+    N, L, bs = 12, 2, 4
+    pool = _tagged_pool(N, L, bs, 3, 2)
+    for layer in range(L):
+        flat = pool[:, layer].reshape(N * bs, 3, 2)
+        for off in range(bs):
+            for n in (0, 1, 5, N * bs - off):
+                got = gather_loop(pool, layer, list(range(N)), n, off)
+                assert np.array_equal(got, flat[off:off + n])
+
+
+def check_scatter_round_trip(build_slot_mapping, write_slots, gather_loop):
+    rng = np.random.default_rng(7)
+    N, L, bs, H, D = 24, 2, 4, 2, 3
+    for _ in range(10):
+        k = rng.standard_normal((N, L, bs, H, D)).astype(np.float32)
+        v = rng.standard_normal((N, L, bs, H, D)).astype(np.float32)
+        k0, v0 = k.copy(), v.copy()
+        nblk = int(rng.integers(1, 6))
+        table = rng.permutation(N)[:nblk]
+        off = int(rng.integers(0, bs))
+        n = int(rng.integers(1, nblk * bs - off + 1))
+        layer = int(rng.integers(0, L))
+        seq = np.zeros(n, np.int32)
+        pad = rng.random(n) < 0.3
+        seq[pad] = -1
+        pos = np.arange(n, dtype=np.int32)
+        sm = build_slot_mapping(np.array([table], np.int32), np.array([off], np.int32),
+                                seq, pos, bs)
+        assert np.all(sm[pad] == -1) and np.all(sm[~pad] >= 0)
+        kn = rng.standard_normal((n, H, D)).astype(np.float32)
+        vn = rng.standard_normal((n, H, D)).astype(np.float32)
+        write_slots(k, v, layer, kn, vn, sm)
+        gk = gather_loop(k, layer, table, n, off)
+        gv = gather_loop(v, layer, table, n, off)
+        # written rows come back; padded rows keep the old contents
+        assert np.array_equal(gk[~pad], kn[~pad])
+        assert np.array_equal(gv[~pad], vn[~pad])
+        assert np.array_equal(gk[pad], gather_loop(k0, layer, table, n, off)[pad])
+        # nothing outside the written rows changed
+        touched = np.zeros((N, L, bs), bool)
+        for s in sm[sm >= 0]:
+            touched[s // bs, layer, s % bs] = True
+        assert np.array_equal(k[~touched], k0[~touched])
+        assert np.array_equal(v[~touched], v0[~touched])
+
+
+def check_identity_scatter(build_slot_mapping, write_slots):
+    """With the identity table, a scatter lays tokens out in pool order."""
+    N, L, bs, H, D = 6, 1, 4, 1, 2
+    k = np.zeros((N, L, bs, H, D), np.float32)
+    v = np.zeros((N, L, bs, H, D), np.float32)
+    n = N * bs - 1
+    kn = np.arange(n * H * D, dtype=np.float32).reshape(n, H, D) + 1
+    sm = build_slot_mapping(np.array([list(range(N))], np.int32), np.array([1], np.int32),
+                            np.zeros(n, np.int32), np.arange(n, dtype=np.int32), bs)
+    write_slots(k, v, 0, kn, -kn, sm)
+    flat = k[:, 0].reshape(N * bs, H, D)
+    assert np.array_equal(flat[1:], kn) and np.all(flat[0] == 0)
+
+
+def _rand_case(rng, N=20, L=2, bs=4, Hkv=2, group=2, D=8, B=3, maxlen=30):
+    k = rng.standard_normal((N, L, bs, Hkv, D)).astype(np.float32)
+    v = rng.standard_normal((N, L, bs, Hkv, D)).astype(np.float32)
+    q = rng.standard_normal((B, Hkv * group, D)).astype(np.float32)
+    lens = rng.integers(0, maxlen + 1, size=B).astype(np.int32)
+    offs = rng.integers(0, bs, size=B).astype(np.int32)
+    mb = max(1, max(O.blocks_needed(int(n), bs, int(o)) for n, o in zip(lens, offs)))
+    bt = np.full((B, mb), -1, np.int32)
+    for b in range(B):
+        nb = O.blocks_needed(int(lens[b]), bs, int(offs[b]))
+        bt[b, :nb] = rng.choice(N, size=nb, replace=False)
+    return k, v, q, bt, lens, offs
+
+
+def check_attention_vs_sdpa(decode_attention):
+    """Library cross-check: torch's scaled_dot_product_attention in fp64 on
+    the gathered K/V, with kv heads repeated for grouped queries."""
+    rng = np.random.default_rng(8)
+    for group in (1, 2, 4):
+        k, v, q, bt, lens, offs = _rand_case(rng, group=group)
+        scale = 0.37
+        got = decode_attention(k, v, 1, q, bt, lens, offs, scale)
+        for b in range(len(lens)):
+            kb = O.gather_indexed(k, 1, bt[b], int(lens[b]), int(offs[b])).astype(np.float64)
+            vb = O.gather_indexed(v, 1, bt[b], int(lens[b]), int(offs[b])).astype(np.float64)
+            if lens[b] == 0:
+                assert np.all(got[b] == 0)
+                continue
+            qt = torch.from_numpy(q[b].astype(np.float64))[:, None, :]          # [Hq,1,D]
+            kt = torch.from_numpy(kb).permute(1, 0, 2).repeat_interleave(group, 0)
+            vt = torch.from_numpy(vb).permute(1, 0, 2).repeat_interleave(group, 0)
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qt, kt, vt, scale=scale)[:, 0, :].numpy()
+            np.testing.assert_allclose(got[b], ref, rtol=0, atol=1e-12)
+
+
+def check_attention_closed_forms(attention_fp64):
+    rng = np.random.default_rng(9)
+    D = 6
+    q = rng.standard_normal(D)
+    v = rng.standard_normal((5, D))
+    # one token: softmax of a single logit is 1
+    assert np.array_equal(attention_fp64(q, rng.standard_normal((1, D)), v[:1], 0.5), v[0])
+    # equal keys: uniform weights, the output is the mean of V
+    k_eq = np.tile(rng.standard_normal(D), (5, 1))
+    np.testing.assert_allclose(attention_fp64(q, k_eq, v, 0.5), v.mean(0), atol=1e-14)
+    # one key aligned with q far above the rest: the output is that V row
+    k = rng.standard_normal((5, D)) * 0.01
+    k[3] = q * 1e3
+    np.testing.assert_allclose(attention_fp64(q, k, v, 1.0), v[3], atol=1e-12)
+    # two tokens: logistic weights in closed form
+    k2 = rng.standard_normal((2, D))
+    s = 0.7 * (k2 @ q)
+    w1 = 1.0 / (1.0 + math.exp(s[0] - s[1]))
+    np.testing.assert_allclose(attention_fp64(q, k2, v[:2], 0.7),
+                               (1 - w1) * v[0] + w1 * v[1], atol=1e-14)
+    # no tokens: zeros
+    assert np.array_equal(attention_fp64(q, np.zeros((0, D)), np.zeros((0, D)), 1.0),
+                          np.zeros(D))
+
+
+def check_block_permutation_invariance(decode_attention):
+    """Moving blocks to other physical ids and relabelling the tables to
+    match must not change the result (logical order is all that counts)."""
+    rng = np.random.default_rng(10)
+    k, v, q, bt, lens, offs = _rand_case(rng)
+    a = decode_attention(k, v, 0, q, bt, lens, offs, 0.3)
+    perm = rng.permutation(k.shape[0])          # new id of old block i
+    k2 = np.empty_like(k); v2 = np.empty_like(v)
+    k2[perm] = k; v2[perm] = v
+    bt2 = np.where(bt >= 0, perm[np.maximum(bt, 0)], -1).astype(np.int32)
+    b = decode_attention(k2, v2, 0, q, bt2, lens, offs, 0.3)
+    np.testing.assert_allclose(a, b, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# the pins, against the real oracle
+# ---------------------------------------------------------------------------
+
+def test_block_table_example():
+    check_block_table_example(O.slot_of, O.build_slot_mapping, O.gather_loop)
+
+
+def test_exercise_30_tokens():
+    for n, bs, blocks, slots, last, util, frag in _rows(
+            os.path.join(GOLDEN, "exercise_30_tokens.txt")):
+        n, bs, blocks, slots, last = int(n), int(bs), int(blocks), int(slots), int(last)
+        assert oracle.blocks_needed(n, bs) == blocks
+        assert oracle.capacity(blocks, bs, 0) == slots
+        assert oracle.last_block_fill(n, bs) == last
+        assert oracle.last_block_fill(n, bs) / bs == float(util)
+        assert oracle.fragmentation_ratio(blocks, bs, n) == float(frag)
+
+
+def test_waste_example():
+    (req, bs, per_req, kb, wasted, wasted_kb), = _rows(os.path.join(GOLDEN, "waste_example.txt"))
+    req, bs, per_req = int(req), int(bs), int(per_req)
+    # each request uses one block, half filled: allocated slots minus used tokens
+    frag = oracle.fragmentation_ratio(req, bs, req * (bs - per_req))
+    assert frag * req * bs == int(wasted)
+    assert int(wasted) * int(kb) == int(wasted_kb)
+    assert abs(int(wasted_kb) * 1024 / 1e6 - 74) < 2      # the page's "about 74 MB"
+
+
+def test_capacity_and_offsets():
+    assert oracle.capacity(3, 16, 5) == 43
+    assert oracle.blocks_needed(43, 16, 5) == 3
+    assert oracle.blocks_needed(44, 16, 5) == 4
+    assert oracle.blocks_needed(0, 16, 5) == 0
+    assert oracle.last_block_fill(43, 16, 5) == 16
+    pool = _tagged_pool(8, 1, 16, 1, 1)
+    assert oracle.gather_loop(pool, 0, [1, 2, 3], 43, 5).shape[0] == 43
+    with pytest.raises(IndexError):
+        oracle.gather_loop(pool, 0, [1, 2, 3], 44, 5)
+
+
+def test_slot_walk():
+    check_slot_walk(O.slot_of)
+
+
+def test_gather_forms_agree():
+    check_gather_forms(O.gather_loop, O.gather_indexed)
+
+
+def test_identity_table_is_contiguous():
+    check_identity_table(O.gather_loop)
+
+
+def test_scatter_round_trip_and_canaries():
+    check_scatter_round_trip(O.build_slot_mapping, O.write_slots, O.gather_loop)
+
+
+def test_identity_scatter():
+    check_identity_scatter(O.build_slot_mapping, O.write_slots)
+
+
+def test_scatter_rejects_bad_slots():
+    k = np.zeros((4, 1, 4, 1, 1), np.float32)
+    v = k.copy()
+    row = np.ones((1, 1, 1), np.float32)
+    with pytest.raises(IndexError):
+        oracle.write_slots(k, v, 0, row, row, np.array([-2]))
+    with pytest.raises(IndexError):
+        oracle.write_slots(k, v, 0, row, row, np.array([16]))
+    with pytest.raises(ValueError):
+        oracle.write_slots(k, v, 0, np.ones((2, 1, 1), np.float32),
+                           np.ones((2, 1, 1), np.float32), np.array([3, 3]))
+    k[:] = 0
+    v[:] = 0
+    oracle.write_slots(k, v, 0, row, row, np.array([-1]))
+    assert not k.any() and not v.any()
+
+
+def test_attention_vs_sdpa():
+    check_attention_vs_sdpa(O.decode_attention)
+
+
+def test_attention_closed_forms():
+    check_attention_closed_forms(O.attention_fp64)
+
+
+def test_block_permutation_invariance():
+    check_block_permutation_invariance(O.decode_attention)
+
+
+def test_decode_pairs_match_full():
+    rng = np.random.default_rng(11)
+    k, v, q, bt, lens, offs = _rand_case(rng, group=4)
+    full = O.decode_attention(k, v, 1, q, bt, lens, offs, 0.25)
+    pairs = [(b, h) for b in range(len(lens)) for h in range(q.shape[1])]
+    sel = O.decode_attention_pairs(k, v, 1, q, bt, lens, offs, 0.25, pairs)
+    for (b, h), x in sel.items():
+        np.testing.assert_allclose(x, full[b, h], atol=1e-13)
+
+
+def test_split_combine_equals_direct():
+    rng = np.random.default_rng(12)
+    D = 16
+    for n in (1, 2, 17, 100):
+        q = rng.standard_normal(D)
+        k = rng.standard_normal((n, D)) * 2
+        v = rng.standard_normal((n, D))
+        direct = O.attention_fp64(q, k, v, 0.9)
+        for nsplit in (1, 2, 3, 7, n):
+            cuts = sorted(set([0, n] + list(rng.integers(0, n + 1, size=nsplit - 1))))
+            got = O.combine_partials(O.split_partials(q, k, v, 0.9, cuts), D)
+            np.testing.assert_allclose(got, direct, atol=1e-13)
+    assert np.array_equal(O.combine_partials([], 4), np.zeros(4))
+
+
+def test_widen_bf16_bits():
+    bits = np.array([0x3F80, 0xC000, 0x3E20, 0x0000, 0x8000, 0x7F7F], np.uint16)
+    want = np.array([1.0, -2.0, 0.15625, 0.0, -0.0, 3.3895313892515355e38])
+    got = O.widen(bits)
+    assert np.array_equal(got, want)
+    assert np.signbit(got[4])
+    # torch agrees on the bit meaning of bf16
+    t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.array_equal(t, want)
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: each broken copy of the oracle must fail some pin
+# ---------------------------------------------------------------------------
+
+def _slot_no_offset(table, offset, i, bs):
+    return int(table[i // bs]) * bs + i % bs
+
+
+def _slot_swapped(table, offset, i, bs):
+    p = offset + i
+    return int(table[p % bs if p % bs < len(table) else 0]) * bs + p // bs
+
+
+def _gather_loop_ignores_offset(pool, layer, table, n, offset=0):
+    return O.gather_loop(pool, layer, table, n, 0)
+
+
+def _gather_loop_one_short(pool, layer, table, n, offset=0):
+    out = O.gather_loop(pool, layer, table, n, offset)
+    if n > 1:
+        out = out.copy()
+        out[-1] = out[-2]
+    return out
+
+
+def _build_sm_with(slot_fn):
+    def f(bt, offs, seq, pos, bs):
+        return np.array([-1 if s < 0 else slot_fn(bt[s], int(offs[s]), int(p), bs)
+                         for s, p in zip(seq, pos)], dtype=np.int64)
+    return f
+
+
+def _write_writes_padding(k, v, layer, kn, vn, sm):
+    bs = k.shape[2]
+    for t, s in enumerate(sm):
+        s = int(s) if s >= 0 else 0
+        k[s // bs, layer, s % bs] = kn[t]
+        v[s // bs, layer, s % bs] = vn[t]
+
+
+def _attn_no_scale(q, k, v, scale):
+    return O.attention_fp64(q, k, v, 1.0)
+
+
+def _attn_wrong_sign(q, k, v, scale):
+    return O.attention_fp64(q, k, v, -scale)
+
+
+def _attn_unnormalised(q, k, v, scale):
+    if k.shape[0] == 0:
+        return np.zeros(v.shape[1])
+    s = scale * (k @ q)
+    return np.exp(s - s.max()) @ v
+
+
+def _attn_keys_for_values(q, k, v, scale):
+    return O.attention_fp64(q, k, k, scale)
+
+
+def _decode_with(attn=None, gqa_mod=False):
+    def f(k_cache, v_cache, layer, q, bt, lens, offs, scale):
+        B, Hq, D = q.shape
+        Hkv = k_cache.shape[3]
+        out = np.zeros((B, Hq, D))
+        for b in range(B):
+            kb = O.widen(O.gather_loop(k_cache, layer, bt[b], int(lens[b]), int(offs[b])))
+            vb = O.widen(O.gather_loop(v_cache, layer, bt[b], int(lens[b]), int(offs[b])))
+            for h in range(Hq):
+                g = h % Hkv if gqa_mod else h // (Hq // Hkv)
+                out[b, h] = (attn or O.attention_fp64)(O.widen(q[b, h]), kb[:, g], vb[:, g], scale)
+        return out
+    return f
+
+
+PLANTED = [
+    ("slot ignores offset", lambda: check_slot_walk(_slot_no_offset)),
+    ("slot quotient/remainder swapped", lambda: check_slot_walk(_slot_swapped)),
+    ("example with swapped slot", lambda: check_block_table_example(
+        _slot_swapped, _build_sm_with(_slot_swapped), O.gather_loop)),
+    ("gather ignores offset", lambda: check_identity_table(_gather_loop_ignores_offset)),
+    ("gather drops last row", lambda: check_gather_forms(_gather_loop_one_short, O.gather_indexed)),
+    ("scatter writes padding", lambda: check_scatter_round_trip(
+        O.build_slot_mapping, _write_writes_padding, O.gather_loop)),
+    ("scatter slots ignore offset", lambda: check_identity_scatter(
+        _build_sm_with(_slot_no_offset), O.write_slots)),
+    ("attention without scale", lambda: check_attention_vs_sdpa(_decode_with(_attn_no_scale))),
+    ("attention with sign flipped", lambda: check_attention_vs_sdpa(_decode_with(_attn_wrong_sign))),
+    ("attention unnormalised", lambda: check_attention_closed_forms(_attn_unnormalised)),
+    ("attention reads K for V", lambda: check_attention_closed_forms(_attn_keys_for_values)),
+    ("GQA head map h % Hkv", lambda: check_attention_vs_sdpa(_decode_with(gqa_mod=True))),
+]
+
+
+@pytest.mark.parametrize("name,run", PLANTED, ids=[p[0] for p in PLANTED])
+def test_pins_catch_planted_mistakes(name, run):
+    with pytest.raises((AssertionError, IndexError)):
+        run()
