@@ -1,0 +1,548 @@
+"""Benchmark of the paged KV cache hot path on GB300.
+
+A step is one decode iteration of the decode-GQA workload (pool
+16384x32x16x8x128 bf16, layer 7, 32 query heads, batch 64, seq_len
+U[1024, 8192]): build the slots of the 64 new tokens, scatter their K/V rows
+into the pool, then run fused paged decode attention (partial pass + combine)
+over every sequence.  `value` is the KV bytes the attention reads per step
+(sum of seq_len x 2 x row bytes) divided by the step time, in GB/s.  The
+gather and scatter bandwidths are measured on the gather/scatter workload
+(pool 16384x32x16x8x128 bf16, 32 sequences, seq_len U[512, 4096]) and
+reported under "legs".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (no
+collective on the data path); rank 0 prints one JSON line.  `--impl
+reference` times the CPU oracle on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import os
+
+# The oracle baseline runs single-threaded; set before numpy is imported.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import make_workload, fill_pool, new_pool, rand_rows, to_numpy_bits  # noqa: E402
+
+METRIC = "paged decode-attn KV-read GB/s & % of HBM peak; gather/scatter GB/s"
+WORKLOAD = "decode_gqa"
+LEG_WORKLOAD = "gather_scatter"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------------------
+# small helpers (also exercised by the CPU tests)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def reduce_max(x: float) -> float:
+    """Max over ranks (identity without torch.distributed)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def aggregate(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time (units per second)."""
+    return units_per_rank * world / (ms_max / 1e3)
+
+
+def decode_bytes(batch, row_bytes: int, hq: int, head_dim: int, elem: int, bs: int) -> dict:
+    """Algorithmic bytes of one decode call: K and V rows read once per token,
+    the query and output rows, and the block-table entries and per-sequence
+    scalars read."""
+    lens = batch.seq_lens.astype(np.int64)
+    offs = batch.offsets.astype(np.int64)
+    nblk = np.where(lens > 0, -(-(offs + lens) // bs), 0)
+    kv = int(lens.sum()) * 2 * row_bytes
+    qo = 2 * batch.batch * hq * head_dim * elem
+    tables = int(nblk.sum()) * 4 + batch.batch * 8
+    return {"kv": kv, "total": kv + qo + tables}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    src = os.path.join(ROOT, "paged_kv_cache_blk_gb300", "csrc", "decode.cu")
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the decode partial kernel from the committed
+    ncu summary, only if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "decode_partial_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("decode_cu_sha256_16") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------
+
+class DecodeStep:
+    """Device state of one decode-GQA replica and its step."""
+
+    def __init__(self, dev, seed_shift: int):
+        import paged_kv_cache_blk_gb300 as pkv
+        self.pkv = pkv
+        w = make_workload(WORKLOAD)
+        self.w = w
+        self.dev = dev
+        k, v = new_pool(w.pool, dev)
+        fill_pool(k, v, w.pool, w.layer, w.seed + seed_shift)
+        self.pool = pkv.Pool(k, v)
+        t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+        b = w.batch
+        self.host = {
+            "bt": torch.from_numpy(b.block_tables).pin_memory(),
+            "lens": torch.from_numpy(b.seq_lens).pin_memory(),
+            "offs": torch.from_numpy(b.offsets).pin_memory(),
+            "seq": torch.from_numpy(w.tokens.token_seq).pin_memory(),
+            "pos": torch.from_numpy(w.tokens.token_pos).pin_memory(),
+        }
+        self.bt, self.lens, self.offs = (t(b.block_tables, torch.int32),
+                                         t(b.seq_lens, torch.int32), t(b.offsets, torch.int32))
+        self.seq = t(w.tokens.token_seq, torch.int32)
+        self.pos = t(w.tokens.token_pos, torch.int32)
+        B, hq, D = b.batch, w.num_q_heads, w.pool.head_dim
+        T = w.tokens.num_tokens
+        row = (w.pool.num_kv_heads, D)
+        self.q = rand_rows((B, hq, D), "bf16", 1000 + seed_shift, dev)
+        self.k_new = rand_rows((T,) + row, "bf16", 1001 + seed_shift, dev)
+        self.v_new = rand_rows((T,) + row, "bf16", 1002 + seed_shift, dev)
+        self.out = torch.empty_like(self.q)
+        self.slots = torch.empty(T, dtype=torch.int64, device=dev)
+        self.ws = torch.empty(pkv.decode_workspace_size(B, hq, D, dev), dtype=torch.uint8,
+                              device=dev)
+        for name in ("q", "k_new", "v_new"):
+            self.host[name] = getattr(self, name).cpu().pin_memory()
+        self.host_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.bytes = decode_bytes(b, w.pool.row_bytes, hq, D, w.pool.elem_size,
+                                  w.pool.block_size)
+        self.launches_per_step = 4  # slot mapping, scatter, decode partial, combine
+
+    def step(self):
+        pkv = self.pkv
+        pkv.build_slot_mapping(self.pool, self.bt, self.offs, self.seq, self.pos, self.slots)
+        pkv.write_slots(self.pool, self.w.layer, self.k_new, self.v_new, self.slots)
+        pkv.decode_attention(self.pool, self.w.layer, self.q, self.w.scale, self.bt, self.lens,
+                             self.offs, self.out, self.ws)
+
+    def step_e2e(self):
+        """The same step from pinned host buffers: every input of the step is
+        copied host->device and the attention output device->host."""
+        h = self.host
+        for name in ("bt", "lens", "offs", "seq", "pos"):
+            getattr(self, name).copy_(h[name], non_blocking=True)
+        self.q.copy_(h["q"], non_blocking=True)
+        self.k_new.copy_(h["k_new"], non_blocking=True)
+        self.v_new.copy_(h["v_new"], non_blocking=True)
+        self.step()
+        self.host_out.copy_(self.out, non_blocking=True)
+
+    def e2e_bytes(self):
+        h = self.host
+        hin = sum(h[n].numel() * h[n].element_size()
+                  for n in ("bt", "lens", "offs", "seq", "pos", "q", "k_new", "v_new"))
+        return hin, self.host_out.numel() * self.host_out.element_size()
+
+
+def timed(fn, steps: int, flush: torch.Tensor, events_hook=None):
+    """Per-step device times (ms) with CUDA events on the current stream and
+    an L2 flush between steps outside the events."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    inner = []
+    for i in range(steps):
+        flush.zero_()
+        if events_hook is not None:
+            inner.append(events_hook())
+        starts[i].record()
+        fn()
+        ends[i].record()
+    torch.cuda.synchronize()
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return times, inner
+
+
+def run_ours(args, rank, local_rank, world):
+    import paged_kv_cache_blk_gb300 as pkv
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pkv.build()
+    pkv.load()
+    pkv.set_validate(False)
+    pkv.set_decode_ctas(0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    st = DecodeStep(dev, seed_shift=rank)
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+
+    # decode partial-kernel events, recorded by the library on its stream
+    def hook():
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(); e1.record()
+        pkv.set_decode_events(e0, e1)
+        return e0, e1
+
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        times, kev = timed(st.step, args.steps, flush, hook)
+    pkv.set_decode_events(None, None)
+    torch.cuda.synchronize()
+    barrier()
+    ms = statistics.mean(times)
+    ms_max = reduce_max(ms)
+    kv = st.bytes["kv"]
+    value_gbs = aggregate(kv, world, ms_max) / 1e9
+    tokens_s = aggregate(st.w.batch.batch, world, ms_max)
+    part_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+
+    # end to end from pinned host buffers
+    for _ in range(max(1, args.warmup // 2)):
+        st.step_e2e()
+    torch.cuda.synchronize()
+    barrier()
+    e2e_times, _ = timed(st.step_e2e, args.steps, flush)
+    barrier()
+    e2e_ms = reduce_max(statistics.mean(e2e_times))
+    h2d, d2h = st.e2e_bytes()
+
+    launches = st.launches_per_step * args.steps
+
+    # gather / scatter legs on their own workload
+    legs = run_legs(args, dev, rank, flush, pkv)
+    del st
+    torch.cuda.empty_cache()
+
+    peak, peak_kind = load_peaks()
+    w = make_workload(WORKLOAD)
+    db = decode_bytes(w.batch, w.pool.row_bytes, w.num_q_heads, w.pool.head_dim,
+                      w.pool.elem_size, w.pool.block_size)
+    achieved = db["total"] / (part_ms / 1e3) / 1e9
+    traffic = recorded_traffic()
+    result = {
+        "metric": METRIC,
+        "value": round(value_gbs, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "decode_gqa: pool 16384x32x16x8x128 bf16 (layer 7), Hq 32 (GQA 4), "
+                        "batch 64, seq_len U[1024,8192], random non-contiguous tables; step = "
+                        "slot mapping + scatter of 64 new tokens + paged decode attention",
+            "batch": int(w.batch.batch),
+            "kv_read_bytes_per_step": kv,
+            "l2": "flushed between steps (512 MiB write); inputs (1.2 GB/step) exceed L2",
+            "parallelism": f"replicas x{world}",
+        },
+        "hbm_pct_of_peak": {"measured": round(100 * value_gbs / world / peak, 1),
+                            "nominal_8000": round(100 * value_gbs / world / NOMINAL_HBM_GBS, 1),
+                            "peak_kind": peak_kind},
+        "tokens_per_s": round(tokens_s, 1),
+        "roofline": {
+            "kernel": "decode_partial_kernel<bf16,128,4>",
+            "bound": "hbm",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": db["total"],
+            "avg_launch_ms": round(part_ms, 4),
+            "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
+        },
+        "legs": legs,
+        "e2e": {"value": round(aggregate(kv, world, e2e_ms) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds, seed_shift=0, dev=dev)
+    return result
+
+
+def run_legs(args, dev, rank, flush, pkv):
+    w = make_workload(LEG_WORKLOAD)
+    k, v = new_pool(w.pool, dev)
+    fill_pool(k, v, w.pool, w.layer, w.seed + rank)
+    pool = pkv.Pool(k, v)
+    b = w.batch
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+    bt, lens, offs, cu = (t(b.block_tables, torch.int32), t(b.seq_lens, torch.int32),
+                          t(b.offsets, torch.int32), t(b.cu_seqlens, torch.int64))
+    seq, pos = t(w.tokens.token_seq, torch.int32), t(w.tokens.token_pos, torch.int32)
+    T = w.tokens.num_tokens
+    row = (w.pool.num_kv_heads, w.pool.head_dim)
+    k_new = rand_rows((T,) + row, "bf16", 2000 + rank, dev)
+    v_new = rand_rows((T,) + row, "bf16", 2001 + rank, dev)
+    slots = torch.empty(T, dtype=torch.int64, device=dev)
+    pkv.build_slot_mapping(pool, bt, offs, seq, pos, slots)
+    ko = torch.empty((b.total_tokens,) + row, dtype=torch.bfloat16, device=dev)
+    vo = torch.empty_like(ko)
+    scatter = lambda: pkv.write_slots(pool, w.layer, k_new, v_new, slots)
+    gather = lambda: pkv.gather(pool, w.layer, bt, lens, offs, cu, ko, vo)
+    for _ in range(args.warmup):
+        scatter(); gather()
+    torch.cuda.synchronize()
+    rb = w.pool.row_bytes
+    s_bytes = T * 4 * rb + T * 8
+    nblk = int((b.block_tables >= 0).sum())
+    g_bytes = b.total_tokens * 4 * rb + nblk * 4 + b.batch * 12
+    out = {}
+    for name, fn, nbytes in (("scatter", scatter, s_bytes), ("gather", gather, g_bytes)):
+        times, _ = timed(fn, args.steps, flush)
+        ms = reduce_max(statistics.mean(times))
+        out[name] = {"GB/s": round(nbytes / (ms / 1e3) / 1e9, 1), "ms": round(ms, 4),
+                     "algorithmic_bytes": nbytes, "tokens": T if name == "scatter" else
+                     b.total_tokens,
+                     "workload": "gather_scatter: pool 16384x32x16x8x128 bf16 layer 0, 32 "
+                                 "seqs U[512,4096]"}
+    del pool, k, v, ko, vo
+    torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_inputs(dev=None, seed_shift=0):
+    """Layer 7 of the decode-GQA pool and the queries, as oracle arrays."""
+    w = make_workload(WORKLOAD)
+    spec = w.pool
+    d = dev if dev is not None else torch.device("cpu")
+    from workloads.gen import PoolSpec
+    one = PoolSpec(spec.num_blocks, 1, spec.block_size, spec.num_kv_heads, spec.head_dim,
+                   spec.dtype)
+    k, v = new_pool(one, d)
+    fill_pool(k, v, one, 0, w.seed + seed_shift)
+    q = rand_rows((w.batch.batch, w.num_q_heads, spec.head_dim), "bf16", 1000 + seed_shift, d)
+    return w, to_numpy_bits(k), to_numpy_bits(v), to_numpy_bits(q)
+
+
+def _oracle_sample(w, kh, vh, qh, seqs):
+    import oracle
+    b = w.batch
+    t0 = time.perf_counter()
+    oracle.decode_attention(kh, vh, 0, qh[seqs], b.block_tables[seqs], b.seq_lens[seqs],
+                            b.offsets[seqs], w.scale)
+    dt = time.perf_counter() - t0
+    kv = int(b.seq_lens[seqs].astype(np.int64).sum()) * 2 * w.pool.row_bytes
+    return kv, dt
+
+
+def cpu_baseline(seconds: float, seed_shift=0, dev=None):
+    w, kh, vh, qh = _oracle_inputs(dev, seed_shift)
+    kv_total, t_total, n = 0, 0.0, 0
+    order = list(range(w.batch.batch))
+    while t_total < seconds and n < len(order):
+        kv, dt = _oracle_sample(w, kh, vh, qh, [order[n]])
+        kv_total += kv
+        t_total += dt
+        n += 1
+    return {"value": round(kv_total / t_total / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"oracle.decode_attention (numpy, fp64, per-block gather) on the first {n} "
+                      f"of 64 decode_gqa sequences ({kv_total / 1e6:.0f} MB of K/V), "
+                      f"{t_total:.1f} s, single thread"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w, kh, vh, qh = _oracle_inputs(None, 0)
+    per_step = 2  # sequences per step: a bounded sample (a few seconds of CPU work)
+    for i in range(args.warmup):
+        _oracle_sample(w, kh, vh, qh, [i % 64])
+    kv_total, t_total = 0, 0.0
+    times = []
+    for i in range(args.steps):
+        seqs = [(i * per_step + j) % 64 for j in range(per_step)]
+        kv, dt = _oracle_sample(w, kh, vh, qh, seqs)
+        kv_total += kv
+        t_total += dt
+        times.append(dt * 1e3)
+    value = kv_total / t_total / 1e9
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(statistics.mean(times), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "decode_gqa: pool 16384x32x16x8x128 bf16 (layer 7), Hq 32, "
+                               "batch 64, seq_len U[1024,8192]; oracle on 2 sequences per step",
+                   "parallelism": "single host thread"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} decode_gqa sequences per step, "
+                                   f"{args.steps} steps"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, local_rank, world = dist_env()
+    if world != args.gpus and world > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE {world}")
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "reference" and rank != 0:
+            return 0
+        if args.impl == "ours":
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(local_rank)
+            dist.init_process_group(backend)
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, local_rank, world)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,213 @@
+/*
+ * pkv.h - C ABI of the GB300 paged KV cache library (libpkv.so).
+ *
+ * The library implements the data-parallel hot path of a paged KV cache:
+ *   - the logical -> physical index step that turns (sequence, position)
+ *     pairs into slot numbers      (pkv_build_slot_mapping),
+ *   - the slot_mapping scatter     (pkv_write_slots),
+ *   - the block_table gather       (pkv_gather),
+ *   - fused paged decode attention that reads K/V through the block table
+ *     with a split-K partial pass and a combine pass (pkv_decode_attention).
+ *
+ * Sources restated (cited by page title and section):
+ *   [step14_2]  mini-vLLM tutorial "step14_2 - index_select gather"
+ *   [vllm-notes] "vLLM PagedAttention source notes"
+ *   [ch12]      mini-runtime "ch.12 Paged KV Cache"
+ *
+ * Conventions shared by every call
+ *   Pool layout.  A pool descriptor names two caller-owned device tensors,
+ *     k_cache and v_cache, each row-major [num_blocks, num_layers, block_size,
+ *     num_kv_heads, head_dim] ([vllm-notes] §2.2, PagedKVCache paragraph: K
+ *     and V held separately).  A token row (all kv heads of one token) of
+ *     block b, layer l, row j starts at element ((b*L + l)*bs + j)*Hkv*D.
+ *   Slots.  slot = block * block_size + row ([vllm-notes] §2.2); a slot
+ *     addresses a row within one layer, the layer is a separate argument.
+ *   Block tables.  int32 [batch, max_blocks_per_seq], row-major; entry k of
+ *     row b is the physical block of logical block k of sequence b ([ch12]
+ *     §2.2 BlockTable._block_ids).  offsets[b] (0 <= offsets[b] < block_size,
+ *     NULL means all zero) is the first-block offset ([ch12] §2.2): logical
+ *     token i of sequence b sits at table position p = offsets[b] + i, in
+ *     block table[b][p / bs], row p % bs.  Capacity of a row of the table is
+ *     max_blocks_per_seq * block_size - offsets[b] ([ch12] §2.2); entries past
+ *     the blocks a sequence spans are never read.
+ *   Memory.  Every pointer argument except `pool` itself is a DEVICE pointer
+ *     owned by the caller; the descriptor struct is read on the host during
+ *     the call only.  The library never allocates, frees or keeps device
+ *     memory; scratch for the decode pass is the caller's workspace.
+ *     k_cache, v_cache, k_new, v_new, k_out, v_out, q, out and workspace
+ *     must be 16-byte aligned; index arrays must be naturally aligned.
+ *   Streams.  Work is enqueued on `stream` (0 = the legacy default stream)
+ *     and is asynchronous; nothing synchronises unless validate mode is on.
+ *     The current CUDA device must be the device that owns the pointers.
+ *   Errors.  Argument checks on host-visible values run before anything is
+ *     enqueued and return a status without side effects.  Values that live
+ *     in device memory (slots, block ids, offsets, lengths) are checked by
+ *     the kernels themselves: an out-of-range index is never dereferenced;
+ *     the access is skipped and a sticky device error word is set.  With
+ *     validate mode on (pkv_set_validate), each call also runs a validation
+ *     pass over its index inputs before the main kernel, synchronises the
+ *     stream and returns PKV_ERR_INDEX / PKV_ERR_CAPACITY instead of running
+ *     the main kernel; without it, pkv_device_error() reports the word.
+ *     A failed CUDA launch returns PKV_ERR_CUDA.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad layer, misaligned pointer */
+  PKV_ERR_CAPACITY = 2,     /* a sequence does not fit its table row, or bad offset */
+  PKV_ERR_UNSUPPORTED = 3,  /* shape or dtype outside the compiled kernels */
+  PKV_ERR_WORKSPACE = 4,    /* workspace null or smaller than pkv_decode_workspace_size */
+  PKV_ERR_INDEX = 5,        /* slot or block id outside the pool, bad packed layout */
+  PKV_ERR_CUDA = 6,         /* a CUDA runtime call failed */
+  PKV_ERR_TIMEOUT = 7       /* a bounded device-side wait gave up */
+} pkv_status;
+
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Pool descriptor: two device tensors [num_blocks, num_layers, block_size,
+ * num_kv_heads, head_dim] of `dtype`.  block_size must be a power of two in
+ * [1, 1024]; num_kv_heads * head_dim * element size must be a multiple of 16
+ * bytes.  ([vllm-notes] §2.2 layout; [ch12] §4.2 uses block_size 16.) */
+typedef struct {
+  void* k_cache;
+  void* v_cache;
+  int64_t num_blocks;
+  int32_t num_layers;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t dtype; /* pkv_dtype */
+} pkv_pool;
+
+/* Logical -> physical index ([vllm-notes] §2.2 slot_mapping definition;
+ * [step14_2] "Solution": position // block_size and position % block_size;
+ * [ch12] §2.2 first-block offset).
+ *
+ * For t < num_tokens: if token_seq[t] < 0 the entry is padding and
+ * slot_mapping[t] = -1; otherwise with b = token_seq[t] and
+ * p = offsets[b] + token_pos[t]:
+ *     slot_mapping[t] = block_tables[b][p / bs] * bs + p % bs.
+ * token_seq, token_pos: int32 [num_tokens]; slot_mapping: int64 [num_tokens]
+ * (written).  offsets may be NULL.  A token whose position lies outside its
+ * table row (p >= max_blocks_per_seq * bs, b >= batch, negative position) or
+ * whose block id is outside [0, num_blocks) gets slot -1 and sets the device
+ * error word (PKV_ERR_INDEX in validate mode). */
+PKV_API pkv_status pkv_build_slot_mapping(const pkv_pool* pool, const int32_t* block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t* offsets,
+                                  int32_t batch, const int32_t* token_seq,
+                                  const int32_t* token_pos, int64_t num_tokens,
+                                  int64_t* slot_mapping, cudaStream_t stream);
+
+/* Scatter ([step14_2] "Relation to step14_1": kv_pool[blocks, rows] = K;
+ * [vllm-notes] §2.2: rows addressed as [block_id, layer, offset], -1 = padding).
+ *
+ * For t < num_tokens with s = slot_mapping[t] >= 0:
+ *     k_cache[s / bs][layer][s % bs] = k_new[t],  v_cache[...] = v_new[t].
+ * k_new, v_new: [num_tokens, Hkv, D] in the pool dtype, contiguous.  Entries
+ * equal to -1 are skipped and their rows untouched.  Other negative entries
+ * and entries >= num_blocks * bs are skipped and set the device error word
+ * (PKV_ERR_INDEX in validate mode).  Non-negative slots must be distinct; a
+ * repeated slot leaves that row holding one of the written rows. */
+PKV_API pkv_status pkv_write_slots(const pkv_pool* pool, int32_t layer, const void* k_new,
+                           const void* v_new, const int64_t* slot_mapping,
+                           int64_t num_tokens, cudaStream_t stream);
+
+/* Gather ([step14_2] "Problem" and "Solution"; [vllm-notes] §2.3
+ * gather_kv_for_attention; [ch12] §2.2 offset, §2.5 read_layer).
+ *
+ * For every sequence b and i < seq_lens[b], with p = offsets[b] + i:
+ *     k_out[cu_seqlens[b] + i] = k_cache[block_tables[b][p / bs]][layer][p % bs]
+ * and the same for V.  k_out, v_out: [total_tokens, Hkv, D] contiguous, pool
+ * dtype.  cu_seqlens: int64 [batch + 1], the packed output layout, with
+ * cu_seqlens[0] = 0, cu_seqlens[b+1] - cu_seqlens[b] = seq_lens[b] and
+ * cu_seqlens[batch] = total_tokens (validate mode checks all three).
+ * total_tokens is the number of output rows the caller allocated.  A row
+ * whose block id is outside the pool, or which lies past its table row's
+ * capacity, is left unwritten and sets the device error word. */
+PKV_API pkv_status pkv_gather(const pkv_pool* pool, int32_t layer, const int32_t* block_tables,
+                      int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                      const int32_t* offsets, int32_t batch, const int64_t* cu_seqlens,
+                      int64_t total_tokens, void* k_out, void* v_out, cudaStream_t stream);
+
+/* Bytes of workspace pkv_decode_attention needs for this shape on the
+ * current device (it depends on the device's SM count).  0 on a bad shape. */
+PKV_API size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t head_dim);
+
+/* Paged decode attention, one query token per sequence ([step14_2] comparison
+ * with vLLM: attention reads the pool through the block table and K/V are
+ * never copied to contiguous memory; [vllm-notes] §2.3 the same result as
+ * gather + standard attention; [ch12] §3.1 PagedAttention).
+ *
+ * For each sequence b and query head h, with kv head g = h / (Hq / Hkv):
+ *     s_i  = scale * dot(q[b][h], K_i[g])  over the seq_lens[b] tokens read
+ *            through the table as in pkv_gather,
+ *     out[b][h] = sum_i softmax(s)_i * V_i[g].
+ * q, out: [batch, num_q_heads, head_dim] contiguous in the pool dtype.
+ * seq_lens[b] == 0 gives an all-zero row.  Accumulation is fp32.
+ * The work is split along the sequence across the GPU; partial softmax
+ * states go to `workspace` (>= pkv_decode_workspace_size bytes, contents
+ * need no initialisation and are overwritten) and a second kernel combines
+ * them.  Supported: head_dim 64 or 128; num_kv_heads 1, 2, 4 or 8;
+ * num_q_heads / num_kv_heads 1, 2, 4 or 8; either dtype; any block_size the
+ * pool allows.  Others return PKV_ERR_UNSUPPORTED.  A sequence whose offset
+ * is out of range or whose length exceeds its table row's capacity is
+ * treated as empty and sets the device error word (PKV_ERR_CAPACITY in
+ * validate mode); a block id outside the pool is skipped (PKV_ERR_INDEX). */
+PKV_API pkv_status pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void* q,
+                                int32_t num_q_heads, float scale,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* seq_lens, const int32_t* offsets,
+                                int32_t batch, void* out, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
+/* Number of CTAs the decode partial pass uses on the current device; 0 (the
+ * default) means one per SM.  A positive value forces that grid size, which
+ * changes how sequences are split (1 = no split).  Process-wide. */
+PKV_API pkv_status pkv_set_decode_ctas(int32_t num_ctas);
+
+/* Profiling hook for the decode partial pass.  When both events are
+ * non-null, each later pkv_decode_attention call records `start` on its
+ * stream right before its first partial-pass kernel and `stop` right after
+ * its last one (before the combine kernel), so the caller can time that
+ * kernel alone with cudaEventElapsedTime.  Events are the caller's (created
+ * with timing enabled); pass NULLs to stop recording.  Process-wide. */
+PKV_API pkv_status pkv_set_decode_events(cudaEvent_t start, cudaEvent_t stop);
+
+/* Validate mode (process-wide, default off): see "Errors" above. */
+PKV_API pkv_status pkv_set_validate(int32_t on);
+PKV_API int32_t pkv_get_validate(void);
+
+/* Synchronises the current device, stores the sticky device error word's
+ * status (PKV_OK, PKV_ERR_INDEX, PKV_ERR_CAPACITY or PKV_ERR_TIMEOUT) in
+ * *status and, if clear != 0, resets it.  Returns PKV_ERR_CUDA if the
+ * device cannot be read. */
+PKV_API pkv_status pkv_device_error(pkv_status* status, int32_t clear);
+
+/* Static description of a status code. */
+PKV_API const char* pkv_status_string(pkv_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+PKV_API int32_t pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,24 @@
+"""GB300 paged KV cache hot path: slot mapping, scatter, gather and fused
+paged decode attention, as hand-written CUDA kernels behind the C ABI in
+``include/pkv.h`` (``libpkv.so``), with this thin ctypes binding."""
+
+from ._binding import (  # noqa: F401
+    Pool,
+    PkvError,
+    STATUS_CODES,
+    build_slot_mapping,
+    decode_attention,
+    decode_workspace_size,
+    device_error,
+    gather,
+    get_validate,
+    library_path,
+    load,
+    set_decode_ctas,
+    set_decode_events,
+    set_validate,
+    status_string,
+    version,
+    write_slots,
+)
+from .build import build  # noqa: F401

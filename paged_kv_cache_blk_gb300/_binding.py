@@ -1,0 +1,229 @@
+"""ctypes binding of libpkv: argument marshalling only.
+
+Each function has the name of the C call without the ``pkv_`` prefix, takes
+torch tensors, passes their device pointers and the current torch stream to
+the library, and raises :class:`PkvError` on any status other than
+``PKV_OK``.  Every step of the path runs in the library's CUDA kernels; there
+is no Python or CPU fallback, and a missing library is an error.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+_STATUS = {
+    0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_CAPACITY", 3: "PKV_ERR_UNSUPPORTED",
+    4: "PKV_ERR_WORKSPACE", 5: "PKV_ERR_INDEX", 6: "PKV_ERR_CUDA", 7: "PKV_ERR_TIMEOUT",
+}
+STATUS_CODES = {v: k for k, v in _STATUS.items()}
+_DTYPE = {torch.float32: 0, torch.bfloat16: 1}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, where: str, message: str):
+        self.status = status
+        self.name = _STATUS.get(status, str(status))
+        super().__init__(f"{where}: {self.name} ({message})")
+
+
+class _PoolStruct(ctypes.Structure):
+    _fields_ = [
+        ("k_cache", ctypes.c_void_p),
+        ("v_cache", ctypes.c_void_p),
+        ("num_blocks", ctypes.c_int64),
+        ("num_layers", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+    ]
+
+
+_lib = None
+_P, _I32, _I64, _F32, _SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                             ctypes.c_size_t)
+_SIGS = {
+    "pkv_build_slot_mapping": (_I32, [_P, _P, _I32, _P, _I32, _P, _P, _I64, _P, _P]),
+    "pkv_write_slots": (_I32, [_P, _I32, _P, _P, _P, _I64, _P]),
+    "pkv_gather": (_I32, [_P, _I32, _P, _I32, _P, _P, _I32, _P, _I64, _P, _P, _P]),
+    "pkv_decode_workspace_size": (_SZ, [_I32, _I32, _I32]),
+    "pkv_decode_attention": (_I32, [_P, _I32, _P, _I32, _F32, _P, _I32, _P, _P, _I32, _P, _P,
+                                    _SZ, _P]),
+    "pkv_set_decode_ctas": (_I32, [_I32]),
+    "pkv_set_decode_events": (_I32, [_P, _P]),
+    "pkv_set_validate": (_I32, [_I32]),
+    "pkv_get_validate": (_I32, []),
+    "pkv_device_error": (_I32, [ctypes.POINTER(ctypes.c_int32), _I32]),
+    "pkv_status_string": (ctypes.c_char_p, [_I32]),
+    "pkv_version": (_I32, []),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libpkv.so (built by ``build()``); raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB
+    if not os.path.exists(p):
+        raise RuntimeError(f"libpkv is not built ({p} missing): run __graft_entry__.build() "
+                           "or python -m paged_kv_cache_blk_gb300.build")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        msg = load().pkv_status_string(status).decode()
+        raise PkvError(status, where, msg)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(dev: torch.device) -> int:
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+class Pool:
+    """K and V block pools ``[num_blocks, num_layers, block_size, num_kv_heads,
+    head_dim]`` on one CUDA device, as the library's pool descriptor."""
+
+    def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor):
+        if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+            raise ValueError("k_cache and v_cache must have the same shape and dtype")
+        if k_cache.dim() != 5 or not k_cache.is_contiguous() or not v_cache.is_contiguous():
+            raise ValueError("pools must be contiguous [N, L, bs, Hkv, D] tensors")
+        if k_cache.dtype not in _DTYPE:
+            raise ValueError(f"unsupported pool dtype {k_cache.dtype}")
+        self.k_cache, self.v_cache = k_cache, v_cache
+        N, L, bs, H, D = k_cache.shape
+        self.struct = _PoolStruct(k_cache.data_ptr(), v_cache.data_ptr(), N, L, bs, H, D,
+                                  _DTYPE[k_cache.dtype])
+        self.device = k_cache.device
+        self.num_blocks, self.num_layers, self.block_size = N, L, bs
+        self.num_kv_heads, self.head_dim = H, D
+        self.dtype = k_cache.dtype
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.struct)
+
+
+def _dev(pool: Pool):
+    return torch.cuda.device(pool.device)
+
+
+def build_slot_mapping(pool: Pool, block_tables: torch.Tensor, offsets: Optional[torch.Tensor],
+                       token_seq: torch.Tensor, token_pos: torch.Tensor,
+                       slot_mapping: torch.Tensor) -> torch.Tensor:
+    """Fill ``slot_mapping`` (int64 [T]) from (sequence, position) pairs."""
+    lib = load()
+    B = block_tables.shape[0]
+    with _dev(pool):
+        st = lib.pkv_build_slot_mapping(pool.ref, _ptr(block_tables), block_tables.shape[1],
+                                        _ptr(offsets), B, _ptr(token_seq), _ptr(token_pos),
+                                        token_seq.numel(), _ptr(slot_mapping),
+                                        _stream(pool.device))
+    _check(st, "pkv_build_slot_mapping")
+    return slot_mapping
+
+
+def write_slots(pool: Pool, layer: int, k_new: torch.Tensor, v_new: torch.Tensor,
+                slot_mapping: torch.Tensor) -> None:
+    """Scatter ``k_new``/``v_new`` ([T, Hkv, D]) into the pools at the slots."""
+    lib = load()
+    with _dev(pool):
+        st = lib.pkv_write_slots(pool.ref, layer, _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                                 slot_mapping.numel(), _stream(pool.device))
+    _check(st, "pkv_write_slots")
+
+
+def gather(pool: Pool, layer: int, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+           offsets: Optional[torch.Tensor], cu_seqlens: torch.Tensor, k_out: torch.Tensor,
+           v_out: torch.Tensor) -> None:
+    """Gather every sequence to packed contiguous ``k_out``/``v_out``."""
+    lib = load()
+    with _dev(pool):
+        st = lib.pkv_gather(pool.ref, layer, _ptr(block_tables), block_tables.shape[1],
+                            _ptr(seq_lens), _ptr(offsets), seq_lens.numel(), _ptr(cu_seqlens),
+                            k_out.shape[0], _ptr(k_out), _ptr(v_out), _stream(pool.device))
+    _check(st, "pkv_gather")
+
+
+def decode_workspace_size(batch: int, num_q_heads: int, head_dim: int,
+                          device: Optional[torch.device] = None) -> int:
+    lib = load()
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        n = lib.pkv_decode_workspace_size(batch, num_q_heads, head_dim)
+    if n == 0:
+        raise PkvError(1, "pkv_decode_workspace_size", "bad shape or no CUDA device")
+    return n
+
+
+def decode_attention(pool: Pool, layer: int, q: torch.Tensor, scale: float,
+                     block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                     offsets: Optional[torch.Tensor], out: torch.Tensor,
+                     workspace: torch.Tensor) -> None:
+    """Paged decode attention of ``q`` [B, Hq, D] into ``out`` [B, Hq, D]."""
+    lib = load()
+    with _dev(pool):
+        st = lib.pkv_decode_attention(pool.ref, layer, _ptr(q), q.shape[1], float(scale),
+                                      _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+                                      _ptr(offsets), seq_lens.numel(), _ptr(out),
+                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream(pool.device))
+    _check(st, "pkv_decode_attention")
+
+
+def set_decode_ctas(n: int) -> None:
+    _check(load().pkv_set_decode_ctas(n), "pkv_set_decode_ctas")
+
+
+def set_decode_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cuda.Event]) -> None:
+    """Have later decode calls record ``start``/``stop`` around the partial
+    pass kernel (``None`` stops it).  The events must have been recorded once
+    so that torch has created them."""
+    a = start.cuda_event if start is not None else None
+    b = stop.cuda_event if stop is not None else None
+    _check(load().pkv_set_decode_events(a, b), "pkv_set_decode_events")
+
+
+def set_validate(on: bool) -> None:
+    _check(load().pkv_set_validate(1 if on else 0), "pkv_set_validate")
+
+
+def get_validate() -> bool:
+    return bool(load().pkv_get_validate())
+
+
+def device_error(clear: bool = True) -> str:
+    """Status name of the sticky device error word (synchronises the device)."""
+    s = ctypes.c_int32(0)
+    _check(load().pkv_device_error(ctypes.byref(s), 1 if clear else 0), "pkv_device_error")
+    return _STATUS[s.value]
+
+
+def status_string(status: int) -> str:
+    return load().pkv_status_string(status).decode()
+
+
+def version() -> int:
+    return load().pkv_version()

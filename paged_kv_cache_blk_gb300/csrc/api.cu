@@ -1,0 +1,364 @@
+// C ABI of libpkv: argument checks, device bookkeeping, validate mode and
+// dispatch to the kernels.  See include/pkv.h for the contract of each call.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "common.cuh"
+#include "pkv.h"
+
+namespace {
+
+// Sticky device error word (one per device context); kernels OR pkv::kErr*
+// bits into it through the pointer obtained for the current device.
+__device__ int g_pkv_error_word;
+
+std::atomic<int> g_validate{0};
+std::atomic<int> g_decode_ctas{0};
+std::atomic<cudaEvent_t> g_ev_start{nullptr};
+std::atomic<cudaEvent_t> g_ev_stop{nullptr};
+
+constexpr int kMaxDevices = 64;
+
+struct DevInfo {
+  std::atomic<bool> ready{false};
+  int sm_count = 0;
+  int smem_optin = 0;
+  int* err = nullptr;
+};
+
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+pkv_status current_device(DevInfo** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_UNSUPPORTED;
+  DevInfo& d = g_dev[dev];
+  if (!d.ready.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (!d.ready.load(std::memory_order_relaxed)) {
+      int sms = 0, optin = 0;
+      void* err = nullptr;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+              cudaSuccess ||
+          cudaGetSymbolAddress(&err, g_pkv_error_word) != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+      }
+      d.sm_count = sms;
+      d.smem_optin = optin;
+      d.err = static_cast<int*>(err);
+      d.ready.store(true, std::memory_order_release);
+    }
+  }
+  *out = &d;
+  return PKV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int elem_size(int32_t dtype) { return dtype == PKV_F32 ? 4 : dtype == PKV_BF16 ? 2 : 0; }
+
+// Geometry checks shared by every call; `need_ptrs` also checks the tensors.
+pkv_status check_pool(const pkv_pool* p, bool need_ptrs, pkv::PoolView* v) {
+  if (!p) return PKV_ERR_INVALID_ARG;
+  const int es = elem_size(p->dtype);
+  if (es == 0) return PKV_ERR_UNSUPPORTED;
+  if (p->num_blocks <= 0 || p->num_layers <= 0 || p->num_kv_heads <= 0 || p->head_dim <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!pow2(p->block_size) || p->block_size > 1024) return PKV_ERR_INVALID_ARG;
+  const long long row = (long long)p->num_kv_heads * p->head_dim * es;
+  if (row % 16 != 0 || row > (1ll << 30)) return PKV_ERR_UNSUPPORTED;
+  if (need_ptrs) {
+    if (!p->k_cache || !p->v_cache) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(p->k_cache) || !aligned16(p->v_cache)) return PKV_ERR_INVALID_ARG;
+  }
+  v->k = static_cast<const char*>(p->k_cache);
+  v->v = static_cast<const char*>(p->v_cache);
+  v->k_mut = static_cast<char*>(p->k_cache);
+  v->v_mut = static_cast<char*>(p->v_cache);
+  v->num_blocks = p->num_blocks;
+  v->num_layers = p->num_layers;
+  v->block_size = p->block_size;
+  v->num_kv_heads = p->num_kv_heads;
+  v->head_dim = p->head_dim;
+  v->elem_size = es;
+  v->row_bytes = (int)row;
+  return PKV_OK;
+}
+
+pkv_status map_bits(int bits) {
+  if (bits & pkv::kErrTimeout) return PKV_ERR_TIMEOUT;
+  if (bits & pkv::kErrIndex) return PKV_ERR_INDEX;
+  if (bits & pkv::kErrCapacity) return PKV_ERR_CAPACITY;
+  return PKV_OK;
+}
+
+// Wait for `s`, read the error word and reset it.
+pkv_status read_and_clear(int* err, cudaStream_t s) {
+  int h = 0;
+  if (cudaMemcpyAsync(&h, err, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  if (h != 0) {
+    if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+      cudaGetLastError();
+      return PKV_ERR_CUDA;
+    }
+  }
+  return map_bits(h);
+}
+
+pkv_status clear_word(int* err, cudaStream_t s) {
+  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+pkv_status launched(cudaError_t e) {
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+int decode_grid(const DevInfo& d) {
+  const int forced = g_decode_ctas.load();
+  return forced > 0 ? forced : d.sm_count;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_build_slot_mapping(const pkv_pool* pool, const int32_t* block_tables,
+                                  int32_t max_blocks_per_seq, const int32_t* offsets,
+                                  int32_t batch, const int32_t* token_seq,
+                                  const int32_t* token_pos, int64_t num_tokens,
+                                  int64_t* slot_mapping, cudaStream_t stream) {
+  pkv::PoolView v;
+  pkv_status st = check_pool(pool, false, &v);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0 || batch < 0) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!token_seq || !token_pos || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  if (!aligned(slot_mapping, 8) || !aligned(token_seq, 4) || !aligned(token_pos, 4))
+    return PKV_ERR_INVALID_ARG;
+  if (batch > 0 && (!block_tables || max_blocks_per_seq <= 0)) return PKV_ERR_INVALID_ARG;
+  DevInfo* d;
+  if ((st = current_device(&d)) != PKV_OK) return st;
+  const bool validate = g_validate.load() != 0;
+  if (validate) {
+    if ((st = clear_word(d->err, stream)) != PKV_OK) return st;
+    if ((st = launched(pkv::launch_validate_tokens(v, block_tables, max_blocks_per_seq, offsets,
+                                                   batch, token_seq, token_pos, num_tokens,
+                                                   d->err, stream))) != PKV_OK)
+      return st;
+    if ((st = read_and_clear(d->err, stream)) != PKV_OK) return st;
+  }
+  if ((st = launched(pkv::launch_slot_mapping(v, block_tables, max_blocks_per_seq, offsets, batch,
+                                              token_seq, token_pos, num_tokens, slot_mapping,
+                                              d->err, stream))) != PKV_OK)
+    return st;
+  return validate ? read_and_clear(d->err, stream) : PKV_OK;
+}
+
+pkv_status pkv_write_slots(const pkv_pool* pool, int32_t layer, const void* k_new,
+                           const void* v_new, const int64_t* slot_mapping, int64_t num_tokens,
+                           cudaStream_t stream) {
+  pkv::PoolView v;
+  pkv_status st = check_pool(pool, true, &v);
+  if (st != PKV_OK) return st;
+  if (layer < 0 || layer >= pool->num_layers || num_tokens < 0) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_new || !v_new || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned(slot_mapping, 8))
+    return PKV_ERR_INVALID_ARG;
+  DevInfo* d;
+  if ((st = current_device(&d)) != PKV_OK) return st;
+  const bool validate = g_validate.load() != 0;
+  if (validate) {
+    if ((st = clear_word(d->err, stream)) != PKV_OK) return st;
+    if ((st = launched(pkv::launch_validate_slots(v, slot_mapping, num_tokens, d->err, stream))) !=
+        PKV_OK)
+      return st;
+    if ((st = read_and_clear(d->err, stream)) != PKV_OK) return st;
+  }
+  if ((st = launched(pkv::launch_write_slots(v, layer, k_new, v_new, slot_mapping, num_tokens,
+                                             d->err, d->sm_count, stream))) != PKV_OK)
+    return st;
+  return validate ? read_and_clear(d->err, stream) : PKV_OK;
+}
+
+pkv_status pkv_gather(const pkv_pool* pool, int32_t layer, const int32_t* block_tables,
+                      int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                      const int32_t* offsets, int32_t batch, const int64_t* cu_seqlens,
+                      int64_t total_tokens, void* k_out, void* v_out, cudaStream_t stream) {
+  pkv::PoolView v;
+  pkv_status st = check_pool(pool, true, &v);
+  if (st != PKV_OK) return st;
+  if (layer < 0 || layer >= pool->num_layers || batch < 0 || total_tokens < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (batch == 0) return total_tokens == 0 ? PKV_OK : PKV_ERR_INVALID_ARG;
+  if (!block_tables || max_blocks_per_seq <= 0 || !seq_lens || !cu_seqlens)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(cu_seqlens, 8)) return PKV_ERR_INVALID_ARG;
+  if (total_tokens > 0) {
+    if (!k_out || !v_out || !aligned16(k_out) || !aligned16(v_out)) return PKV_ERR_INVALID_ARG;
+  }
+  DevInfo* d;
+  if ((st = current_device(&d)) != PKV_OK) return st;
+  const bool validate = g_validate.load() != 0;
+  if (validate) {
+    if ((st = clear_word(d->err, stream)) != PKV_OK) return st;
+    if ((st = launched(pkv::launch_validate_tables(v, block_tables, max_blocks_per_seq, seq_lens,
+                                                   offsets, batch, cu_seqlens, total_tokens,
+                                                   d->err, stream))) != PKV_OK)
+      return st;
+    if ((st = read_and_clear(d->err, stream)) != PKV_OK) return st;
+  }
+  if ((st = launched(pkv::launch_gather(v, layer, block_tables, max_blocks_per_seq, offsets, batch,
+                                        cu_seqlens, total_tokens, k_out, v_out, d->err,
+                                        stream))) != PKV_OK)
+    return st;
+  return validate ? read_and_clear(d->err, stream) : PKV_OK;
+}
+
+size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t head_dim) {
+  if (batch < 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+  DevInfo* d;
+  if (current_device(&d) != PKV_OK) return 0;
+  return pkv::decode_workspace_bytes(batch, num_q_heads, head_dim, decode_grid(*d));
+}
+
+pkv_status pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void* q,
+                                int32_t num_q_heads, float scale, const int32_t* block_tables,
+                                int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                const int32_t* offsets, int32_t batch, void* out, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+  pkv::PoolView v;
+  pkv_status st = check_pool(pool, true, &v);
+  if (st != PKV_OK) return st;
+  if (layer < 0 || layer >= pool->num_layers || batch < 0 || num_q_heads <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (pkv::decode_supported(v, num_q_heads) != 0) return PKV_ERR_UNSUPPORTED;
+  if (batch == 0) return PKV_OK;
+  if (!q || !out || !block_tables || !seq_lens || max_blocks_per_seq <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
+  DevInfo* d;
+  if ((st = current_device(&d)) != PKV_OK) return st;
+  const int grid = decode_grid(*d);
+  if (workspace_bytes < pkv::decode_workspace_bytes(batch, num_q_heads, v.head_dim, grid))
+    return PKV_ERR_WORKSPACE;
+  const bool validate = g_validate.load() != 0;
+  if (validate) {
+    if ((st = clear_word(d->err, stream)) != PKV_OK) return st;
+    if ((st = launched(pkv::launch_validate_tables(v, block_tables, max_blocks_per_seq, seq_lens,
+                                                   offsets, batch, nullptr, 0, d->err,
+                                                   stream))) != PKV_OK)
+      return st;
+    if ((st = read_and_clear(d->err, stream)) != PKV_OK) return st;
+  }
+  const size_t row_elems = (size_t)num_q_heads * v.head_dim;
+  cudaEvent_t ev_start = g_ev_start.load(), ev_stop = g_ev_stop.load();
+  if (!ev_start || !ev_stop) ev_start = ev_stop = nullptr;
+  for (int b0 = 0; b0 < batch; b0 += pkv::kDecodeMaxBatch) {
+    const int nb = batch - b0 < pkv::kDecodeMaxBatch ? batch - b0 : pkv::kDecodeMaxBatch;
+    pkv::DecodeLaunch a;
+    a.pool = v;
+    a.layer = layer;
+    a.q = static_cast<const char*>(q) + b0 * row_elems * v.elem_size;
+    a.out = static_cast<char*>(out) + b0 * row_elems * v.elem_size;
+    a.num_q_heads = num_q_heads;
+    a.scale = scale;
+    a.bt = block_tables + (size_t)b0 * max_blocks_per_seq;
+    a.mb = max_blocks_per_seq;
+    a.lens = seq_lens + b0;
+    a.offs = offsets ? offsets + b0 : nullptr;
+    a.batch = nb;
+    a.workspace = workspace;
+    a.grid = grid;
+    a.err = d->err;
+    a.smem_optin = d->smem_optin;
+    a.ev_start = b0 == 0 ? ev_start : nullptr;
+    a.ev_stop = b0 + nb >= batch ? ev_stop : nullptr;
+    const cudaError_t e = pkv::launch_decode(a, stream);
+    if (e == cudaErrorInvalidConfiguration) return PKV_ERR_UNSUPPORTED;
+    if ((st = launched(e)) != PKV_OK) return st;
+  }
+  return validate ? read_and_clear(d->err, stream) : PKV_OK;
+}
+
+pkv_status pkv_set_decode_ctas(int32_t num_ctas) {
+  if (num_ctas < 0) return PKV_ERR_INVALID_ARG;
+  g_decode_ctas.store(num_ctas);
+  return PKV_OK;
+}
+
+pkv_status pkv_set_decode_events(cudaEvent_t start, cudaEvent_t stop) {
+  g_ev_start.store(start);
+  g_ev_stop.store(stop);
+  return PKV_OK;
+}
+
+pkv_status pkv_set_validate(int32_t on) {
+  g_validate.store(on ? 1 : 0);
+  return PKV_OK;
+}
+
+int32_t pkv_get_validate(void) { return g_validate.load(); }
+
+pkv_status pkv_device_error(pkv_status* status, int32_t clear) {
+  if (!status) return PKV_ERR_INVALID_ARG;
+  DevInfo* d;
+  pkv_status st = current_device(&d);
+  if (st != PKV_OK) return st;
+  int h = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(&h, d->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  if (clear && h != 0 && cudaMemset(d->err, 0, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return PKV_ERR_CUDA;
+  }
+  *status = map_bits(h);
+  return PKV_OK;
+}
+
+const char* pkv_status_string(pkv_status status) {
+  switch (status) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_CAPACITY: return "sequence exceeds its block table capacity or bad offset";
+    case PKV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_INDEX: return "slot or block id out of range";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+int32_t pkv_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,188 @@
+// Device helpers and internal launch interface shared by the libpkv sources.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace pkv {
+
+// Bits of the sticky device error word.
+enum : int {
+  kErrIndex = 1,     // slot / block id / packed row outside its range
+  kErrCapacity = 2,  // sequence longer than its table row, or bad offset / length
+  kErrTimeout = 4,   // a bounded mbarrier wait gave up
+};
+
+// Upper bound on a bounded wait, in nanoseconds of %globaltimer.  A healthy
+// wait in these kernels lasts microseconds; this only ends a wait that can
+// never complete.
+constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;
+
+__device__ __forceinline__ void set_error(int* err, int bits) {
+  if (err) atomicOr(err, bits);
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---- mbarrier (shared::cta) -------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of parity `parity` to complete, giving up after
+// kWaitTimeoutNs (or 2^30 polls): on giving up, set kErrTimeout and return
+// false so the caller can leave cleanly.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) break;
+  }
+  set_error(err, kErrTimeout);
+  return false;
+}
+
+// ---- bulk (TMA, non-tensor) copy global -> shared ---------------------------
+// dst and src 16-byte aligned, bytes a multiple of 16; completion is counted
+// on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// ---- element conversion ------------------------------------------------------
+// bf16 is the upper half of an IEEE fp32 word, so widening is a shift.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return a | (b << 16);
+}
+
+// ---- 16-byte global accesses ------------------------------------------------
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void st_global(void* p, const uint4& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+}  // namespace pkv
+
+// ---- internal launch interface (host side, C++ linkage) ---------------------
+namespace pkv {
+
+struct PoolView {
+  const char* k;  // k_cache bytes
+  const char* v;
+  char* k_mut;
+  char* v_mut;
+  long long num_blocks;
+  int num_layers;
+  int block_size;
+  int num_kv_heads;
+  int head_dim;
+  int elem_size;
+  int row_bytes;  // num_kv_heads * head_dim * elem_size
+};
+
+cudaError_t launch_slot_mapping(const PoolView& p, const int32_t* bt, int mb, const int32_t* offs,
+                                int batch, const int32_t* tok_seq, const int32_t* tok_pos,
+                                long long n, int64_t* slots, int* err, cudaStream_t s);
+
+cudaError_t launch_write_slots(const PoolView& p, int layer, const void* k_new, const void* v_new,
+                               const int64_t* slots, long long n, int* err, int sm_count,
+                               cudaStream_t s);
+
+cudaError_t launch_gather(const PoolView& p, int layer, const int32_t* bt, int mb,
+                          const int32_t* offs, int batch, const int64_t* cu, long long total,
+                          void* k_out, void* v_out, int* err, cudaStream_t s);
+
+cudaError_t launch_validate_tables(const PoolView& p, const int32_t* bt, int mb,
+                                   const int32_t* lens, const int32_t* offs, int batch,
+                                   const int64_t* cu, long long total, int* err, cudaStream_t s);
+
+cudaError_t launch_validate_slots(const PoolView& p, const int64_t* slots, long long n, int* err,
+                                  cudaStream_t s);
+
+cudaError_t launch_validate_tokens(const PoolView& p, const int32_t* bt, int mb,
+                                   const int32_t* offs, int batch, const int32_t* tok_seq,
+                                   const int32_t* tok_pos, long long n, int* err, cudaStream_t s);
+
+struct DecodeLaunch {
+  PoolView pool;
+  int layer;
+  const void* q;
+  void* out;
+  int num_q_heads;
+  float scale;
+  const int32_t* bt;
+  int mb;
+  const int32_t* lens;
+  const int32_t* offs;
+  int batch;  // <= kDecodeMaxBatch
+  void* workspace;
+  int grid;  // CTAs of the partial pass
+  int* err;
+  int smem_optin;  // max dynamic shared memory per block on this device
+  cudaEvent_t ev_start = nullptr;  // recorded right before the partial kernel
+  cudaEvent_t ev_stop = nullptr;   // recorded right after it
+};
+
+constexpr int kDecodeMaxBatch = 2048;
+
+size_t decode_workspace_bytes(int batch, int num_q_heads, int head_dim, int grid);
+// 0 = ok; 1 = unsupported shape
+int decode_supported(const PoolView& p, int num_q_heads);
+cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s);
+
+}  // namespace pkv

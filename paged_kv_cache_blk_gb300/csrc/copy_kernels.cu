@@ -1,0 +1,285 @@
+// Index and copy kernels of the paged KV cache:
+//   slot mapping  - logical (sequence, position) -> physical slot
+//                   ("vLLM PagedAttention source notes" §2.2 slot_mapping;
+//                    mini-runtime ch.12 §2.2 first-block offset)
+//   scatter       - slot_mapping write of new K/V rows
+//                   ("step14_2 - index_select gather", Relation to step14_1)
+//   gather        - block_table read to contiguous [seq_len, Hkv, D]
+//                   ("step14_2 - index_select gather", Problem / Solution)
+//   validation    - index checks run before the main kernels in validate mode
+//
+// Scatter and gather are pure copies of whole token rows (Hkv * D elements,
+// 16-byte multiple).  One warp moves one token's K row and V row with 16-byte
+// vector accesses: 32 lanes cover 512 contiguous bytes per instruction, so
+// every access is fully coalesced, and each lane keeps all its loads in
+// flight before storing.  Rows are independent, so the grid simply has one
+// warp per row; the HBM system sees (rows x 4 x row_bytes) of traffic and no
+// re-reads.
+#include "common.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kCopyWarps = 8;              // warps per CTA
+constexpr int kCopyThreads = kCopyWarps * 32;
+constexpr int kMaxVecPerLane = 4;          // vectors per lane kept in flight per tensor
+
+// Copy one K row and one V row (row_vecs 16-byte vectors each) with the
+// whole warp: all loads of a chunk are issued before any store.
+__device__ __forceinline__ void copy_row_pair(char* dk, const char* sk, char* dv, const char* sv,
+                                              int row_vecs, int lane) {
+  for (int base = 0; base < row_vecs; base += 32 * kMaxVecPerLane) {
+    uint4 a[kMaxVecPerLane], b[kMaxVecPerLane];
+#pragma unroll
+    for (int u = 0; u < kMaxVecPerLane; ++u) {
+      const int v = base + u * 32 + lane;
+      if (v < row_vecs) {
+        a[u] = ld_stream(sk + 16 * (size_t)v);
+        b[u] = ld_stream(sv + 16 * (size_t)v);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kMaxVecPerLane; ++u) {
+      const int v = base + u * 32 + lane;
+      if (v < row_vecs) {
+        st_global(dk + 16 * (size_t)v, a[u]);
+        st_global(dv + 16 * (size_t)v, b[u]);
+      }
+    }
+  }
+}
+
+// Byte offset of row j of block `blk` in layer `layer`.
+__device__ __forceinline__ long long row_offset(long long blk, int layer, int j, int L, int bs,
+                                                int row_bytes) {
+  return ((blk * L + layer) * (long long)bs + j) * (long long)row_bytes;
+}
+
+// ---------------------------------------------------------------------------
+// slot mapping: one thread per token
+// ---------------------------------------------------------------------------
+__global__ void slot_mapping_kernel(const int32_t* __restrict__ bt, int mb,
+                                    const int32_t* __restrict__ offs, int batch,
+                                    const int32_t* __restrict__ tok_seq,
+                                    const int32_t* __restrict__ tok_pos, long long n,
+                                    long long num_blocks, int bs, int64_t* __restrict__ slots,
+                                    int* err) {
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n;
+       t += (long long)gridDim.x * blockDim.x) {
+    const int b = tok_seq[t];
+    int64_t slot = -1;
+    if (b >= batch) {
+      set_error(err, kErrIndex);
+    } else if (b >= 0) {
+      const int off = offs ? offs[b] : 0;
+      const long long p = (long long)off + tok_pos[t];
+      if (off < 0 || off >= bs || tok_pos[t] < 0 || p >= (long long)mb * bs) {
+        set_error(err, kErrCapacity);
+      } else {
+        const int blk = bt[(long long)b * mb + p / bs];
+        if (blk < 0 || blk >= num_blocks) {
+          set_error(err, kErrIndex);
+        } else {
+          slot = (int64_t)blk * bs + p % bs;
+        }
+      }
+    }
+    slots[t] = slot;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// scatter: one warp per token (K row + V row)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kCopyThreads) write_slots_kernel(
+    char* __restrict__ kc, char* __restrict__ vc, const char* __restrict__ k_new,
+    const char* __restrict__ v_new, const int64_t* __restrict__ slots, long long n,
+    long long num_blocks, int L, int layer, int bs, int row_bytes, int* err) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * kCopyWarps;
+  const int row_vecs = row_bytes >> 4;
+  for (long long t = blockIdx.x * (long long)kCopyWarps + (threadIdx.x >> 5); t < n; t += warps) {
+    const int64_t s = slots[t];
+    if (s < 0) {
+      if (s != -1 && lane == 0) set_error(err, kErrIndex);
+      continue;  // -1 is padding: that row is not written
+    }
+    if (s >= num_blocks * bs) {
+      if (lane == 0) set_error(err, kErrIndex);
+      continue;
+    }
+    const long long dst = row_offset(s / bs, layer, (int)(s % bs), L, bs, row_bytes);
+    const long long src = t * (long long)row_bytes;
+    copy_row_pair(kc + dst, k_new + src, vc + dst, v_new + src, row_vecs, lane);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// gather: one warp per output row; the owning sequence is found by binary
+// search in the packed layout cu_seqlens (small and cache-resident)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kCopyThreads) gather_kernel(
+    const char* __restrict__ kc, const char* __restrict__ vc, const int32_t* __restrict__ bt,
+    int mb, const int32_t* __restrict__ offs, int batch, const int64_t* __restrict__ cu,
+    long long total, char* __restrict__ k_out, char* __restrict__ v_out, long long num_blocks,
+    int L, int layer, int bs, int row_bytes, int* err) {
+  const int lane = threadIdx.x & 31;
+  const int row_vecs = row_bytes >> 4;
+  const long long warps = (long long)gridDim.x * kCopyWarps;
+  for (long long r = blockIdx.x * (long long)kCopyWarps + (threadIdx.x >> 5); r < total;
+       r += warps) {
+    // largest b with cu[b] <= r
+    int lo = 0, hi = batch;  // answer in [0, batch)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (cu[mid] <= r) lo = mid; else hi = mid;
+    }
+    const int b = lo;
+    const long long i = r - cu[b];
+    if (i < 0 || r >= cu[b + 1]) {  // row not covered by the packed layout
+      if (lane == 0) set_error(err, kErrIndex);
+      continue;
+    }
+    const int off = offs ? offs[b] : 0;
+    const long long p = (long long)off + i;
+    if (off < 0 || off >= bs || p >= (long long)mb * bs) {
+      if (lane == 0) set_error(err, kErrCapacity);
+      continue;
+    }
+    const int blk = bt[(long long)b * mb + p / bs];
+    if (blk < 0 || blk >= num_blocks) {
+      if (lane == 0) set_error(err, kErrIndex);
+      continue;
+    }
+    const long long src = row_offset(blk, layer, (int)(p % bs), L, bs, row_bytes);
+    const long long dst = r * (long long)row_bytes;
+    copy_row_pair(k_out + dst, kc + src, v_out + dst, vc + src, row_vecs, lane);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// validation (validate mode only): index inputs, never the pools
+// ---------------------------------------------------------------------------
+__global__ void validate_tables_kernel(const int32_t* __restrict__ bt, int mb,
+                                       const int32_t* __restrict__ lens,
+                                       const int32_t* __restrict__ offs, int batch,
+                                       const int64_t* __restrict__ cu, long long total,
+                                       long long num_blocks, int bs, int* err) {
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < batch; b += gridDim.x * blockDim.x) {
+    const int off = offs ? offs[b] : 0;
+    const int len = lens ? lens[b] : 0;
+    if (off < 0 || off >= bs || len < 0 || (long long)off + len > (long long)mb * bs) {
+      set_error(err, kErrCapacity);
+      continue;
+    }
+    const long long nblk = len > 0 ? ((long long)off + len + bs - 1) / bs : 0;
+    for (long long k = 0; k < nblk; ++k) {
+      const int blk = bt[(long long)b * mb + k];
+      if (blk < 0 || blk >= num_blocks) {
+        set_error(err, kErrIndex);
+        break;
+      }
+    }
+    if (cu) {
+      if (cu[b + 1] - cu[b] != len) set_error(err, kErrIndex);
+      if (b == 0 && cu[0] != 0) set_error(err, kErrIndex);
+      if (b == batch - 1 && cu[batch] != total) set_error(err, kErrIndex);
+    }
+  }
+}
+
+__global__ void validate_slots_kernel(const int64_t* __restrict__ slots, long long n,
+                                      long long limit, int* err) {
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n;
+       t += (long long)gridDim.x * blockDim.x) {
+    const int64_t s = slots[t];
+    if (s < -1 || s >= limit) set_error(err, kErrIndex);
+  }
+}
+
+__global__ void validate_tokens_kernel(const int32_t* __restrict__ bt, int mb,
+                                       const int32_t* __restrict__ offs, int batch,
+                                       const int32_t* __restrict__ tok_seq,
+                                       const int32_t* __restrict__ tok_pos, long long n,
+                                       long long num_blocks, int bs, int* err) {
+  for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n;
+       t += (long long)gridDim.x * blockDim.x) {
+    const int b = tok_seq[t];
+    if (b < 0) continue;
+    if (b >= batch) { set_error(err, kErrIndex); continue; }
+    const int off = offs ? offs[b] : 0;
+    if (off < 0 || off >= bs) { set_error(err, kErrCapacity); continue; }
+    const long long p = (long long)off + tok_pos[t];
+    if (tok_pos[t] < 0 || p >= (long long)mb * bs) { set_error(err, kErrCapacity); continue; }
+    const int blk = bt[(long long)b * mb + p / bs];
+    if (blk < 0 || blk >= num_blocks) set_error(err, kErrIndex);
+  }
+}
+
+int grid_for(long long items, int per_block, int cap) {
+  long long g = (items + per_block - 1) / per_block;
+  if (g < 1) g = 1;
+  if (g > cap) g = cap;
+  return (int)g;
+}
+
+}  // namespace
+
+cudaError_t launch_slot_mapping(const PoolView& p, const int32_t* bt, int mb, const int32_t* offs,
+                                int batch, const int32_t* tok_seq, const int32_t* tok_pos,
+                                long long n, int64_t* slots, int* err, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  slot_mapping_kernel<<<grid_for(n, 256, 1 << 20), 256, 0, s>>>(
+      bt, mb, offs, batch, tok_seq, tok_pos, n, p.num_blocks, p.block_size, slots, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_write_slots(const PoolView& p, int layer, const void* k_new, const void* v_new,
+                               const int64_t* slots, long long n, int* err, int sm_count,
+                               cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  (void)sm_count;
+  write_slots_kernel<<<grid_for(n, kCopyWarps, 1 << 24), kCopyThreads, 0, s>>>(
+      p.k_mut, p.v_mut, static_cast<const char*>(k_new), static_cast<const char*>(v_new), slots, n,
+      p.num_blocks, p.num_layers, layer, p.block_size, p.row_bytes, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const PoolView& p, int layer, const int32_t* bt, int mb,
+                          const int32_t* offs, int batch, const int64_t* cu, long long total,
+                          void* k_out, void* v_out, int* err, cudaStream_t s) {
+  if (total == 0 || batch == 0) return cudaSuccess;
+  gather_kernel<<<grid_for(total, kCopyWarps, 1 << 24), kCopyThreads, 0, s>>>(
+      p.k, p.v, bt, mb, offs, batch, cu, total, static_cast<char*>(k_out),
+      static_cast<char*>(v_out), p.num_blocks, p.num_layers, layer, p.block_size, p.row_bytes,
+      err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_validate_tables(const PoolView& p, const int32_t* bt, int mb,
+                                   const int32_t* lens, const int32_t* offs, int batch,
+                                   const int64_t* cu, long long total, int* err, cudaStream_t s) {
+  if (batch == 0) return cudaSuccess;
+  validate_tables_kernel<<<grid_for(batch, 128, 4096), 128, 0, s>>>(
+      bt, mb, lens, offs, batch, cu, total, p.num_blocks, p.block_size, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_validate_slots(const PoolView& p, const int64_t* slots, long long n, int* err,
+                                  cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  validate_slots_kernel<<<grid_for(n, 256, 1 << 20), 256, 0, s>>>(
+      slots, n, p.num_blocks * p.block_size, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_validate_tokens(const PoolView& p, const int32_t* bt, int mb,
+                                   const int32_t* offs, int batch, const int32_t* tok_seq,
+                                   const int32_t* tok_pos, long long n, int* err, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  validate_tokens_kernel<<<grid_for(n, 256, 1 << 20), 256, 0, s>>>(
+      bt, mb, offs, batch, tok_seq, tok_pos, n, p.num_blocks, p.block_size, err);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

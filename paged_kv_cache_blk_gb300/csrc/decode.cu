@@ -1,0 +1,754 @@
+// Paged decode attention: split-K partial pass + combine pass.
+//
+// What is computed ("step14_2 - index_select gather", comparison with vLLM;
+// "vLLM PagedAttention source notes" §2.3; mini-runtime ch.12 §3.1): for each
+// sequence b and query head h (kv head g = h / (Hq/Hkv)), attention of the one
+// query over the seq_len[b] K/V rows that the block table names, read in place
+// from the pool; no contiguous copy of K/V is ever made.
+//
+// Design (GB300, one GPU):
+//  * Work is the flat list of (sequence, logical block) pairs of the batch in
+//    order.  A persistent grid of `grid` CTAs (one per SM by default) splits
+//    that list into equal contiguous ranges, so every CTA streams the same
+//    number of blocks whatever the length mix.  A CTA range cuts sequences
+//    into segments; the segment of sequence b inside CTA c has index c + b
+//    (unique because both the ranges and the sequences are in order).
+//  * Inside a CTA, one producer warp streams the K and V rows of each block
+//    into a ring of shared-memory stages with 1-D bulk copies
+//    (cp.async.bulk, completion counted on an mbarrier).  For the layout
+//    [N, L, bs, Hkv, D] the rows [r0, r1) of one (block, layer) are ONE
+//    contiguous run covering all kv heads (32 KB for bs 16, Hkv 8, D 128
+//    bf16), so a block costs two copy instructions and every byte fetched is
+//    used.  Only the rows the sequence covers are fetched (first-block offset
+//    and the partly filled last block are trimmed).
+//  * Eight consumer warps compute.  Warp w serves kv head w % Hkv (and, when
+//    Hkv < 8, a share of the tokens) for all G = Hq/Hkv query heads of that
+//    group, so each K/V byte is read from shared memory by one warp and used
+//    for all G heads (GQA grouping).
+//      QK: 8 lanes per token, 4 tokens per pass; each lane holds D/8 query
+//          elements per head (pre-scaled by scale*log2(e)) and does
+//          G*D/8 FMAs, then a butterfly over the 8 lanes both sums and
+//          spreads the G head scores.
+//      softmax: running max / sum per head in the log2 domain (exp2f).
+//      PV: each lane owns D/32 output elements for all G heads.
+//    fp32 accumulation throughout; fp32 pools use the same path.
+//  * At a segment end the warp either writes the normalised output (sequence
+//    entirely inside this CTA) or the partial state (m, l, acc) to the
+//    workspace; the combine kernel merges partial states with the log-sum-exp
+//    rule  out = sum_c 2^(m_c-M) acc_c / sum_c 2^(m_c-M) l_c.
+//  * Every mbarrier wait is bounded (mbar_wait); a wait that gives up sets the
+//    error word and the warp leaves after the producer has drained its copies.
+#include <cfloat>
+#include <cmath>
+
+#include "common.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kNW = 8;                    // consumer warps
+constexpr int kThreads = (kNW + 1) * 32;  // + one producer warp
+constexpr int kMaxStageTokens = 16;
+constexpr int kMaxPW = kMaxStageTokens / 4;  // passes of 4 tokens per warp per stage
+constexpr int kMaxStages = 8;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned kFull = 0xffffffffu;
+
+enum : int { kStart = 1, kEnd = 2, kLast = 4, kSingle = 8 };
+
+struct Params {
+  const char* k_base;  // block 0, this layer, row 0
+  const char* v_base;
+  long long block_stride;  // bytes from one block to the next (L * bs * row_bytes)
+  long long num_blocks;
+  const void* q;
+  void* out;
+  const int32_t* bt;
+  const int32_t* lens;
+  const int32_t* offs;
+  float* ws_acc;
+  float* ws_ml;
+  long long* ws_cu;
+  long long* ws_meta;
+  int* err;
+  int mb, batch, hq, hkv, bs, row_bytes, st, stages;
+  float qscale;
+  // shared-memory carve (bytes from the start of dynamic smem)
+  int off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf;
+};
+
+template <typename T, int D, int G>
+struct Cfg {
+  static constexpr int E = sizeof(T);
+  static constexpr int VEC = 16 / E;    // elements per 16-byte vector
+  static constexpr int EPL = D / 8;     // QK elements per lane
+  static constexpr int NV = EPL / VEC;  // 16-byte vectors per lane per row
+  static constexpr int PVE = D / 32;    // PV output elements per lane
+  static constexpr int LOG2G = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+  static constexpr int HSHIFT = 3 - LOG2G;  // after the butterfly lane i holds head i >> HSHIFT
+  static_assert(NV >= 1 && PVE >= 2, "unsupported head_dim");
+};
+
+template <typename T>
+__device__ __forceinline__ void widen16(const uint4& r, float* f) {
+  if constexpr (sizeof(T) == 2) {
+    f[0] = bf16_lo(r.x); f[1] = bf16_hi(r.x); f[2] = bf16_lo(r.y); f[3] = bf16_hi(r.y);
+    f[4] = bf16_lo(r.z); f[5] = bf16_hi(r.z); f[6] = bf16_lo(r.w); f[7] = bf16_hi(r.w);
+  } else {
+    f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+    f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+  }
+}
+
+template <typename T, int PVE>
+__device__ __forceinline__ void load_pv(const char* p, float (&f)[PVE]) {
+  if constexpr (sizeof(T) == 2) {
+    if constexpr (PVE == 4) {
+      const uint2 r = *reinterpret_cast<const uint2*>(p);
+      f[0] = bf16_lo(r.x); f[1] = bf16_hi(r.x); f[2] = bf16_lo(r.y); f[3] = bf16_hi(r.y);
+    } else {
+      const uint32_t r = *reinterpret_cast<const uint32_t*>(p);
+      f[0] = bf16_lo(r); f[1] = bf16_hi(r);
+    }
+  } else {
+    if constexpr (PVE == 4) {
+      const float4 r = *reinterpret_cast<const float4*>(p);
+      f[0] = r.x; f[1] = r.y; f[2] = r.z; f[3] = r.w;
+    } else {
+      const float2 r = *reinterpret_cast<const float2*>(p);
+      f[0] = r.x; f[1] = r.y;
+    }
+  }
+}
+
+template <typename T, int PVE>
+__device__ __forceinline__ void store_out(void* p, const float (&f)[PVE]) {
+  if constexpr (sizeof(T) == 2) {
+    if constexpr (PVE == 4) {
+      *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+    } else {
+      *reinterpret_cast<uint32_t*>(p) = pack_bf16x2(f[0], f[1]);
+    }
+  } else {
+    if constexpr (PVE == 4) {
+      *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+    } else {
+      *reinterpret_cast<float2*>(p) = make_float2(f[0], f[1]);
+    }
+  }
+}
+
+template <int PVE>
+__device__ __forceinline__ void store_f32(float* p, const float (&f)[PVE]) {
+  if constexpr (PVE == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+  } else {
+    *reinterpret_cast<float2*>(p) = make_float2(f[0], f[1]);
+  }
+}
+
+// Sum partial dot products over the 8 lanes of a token group while spreading
+// the G heads over them: each step either halves the heads a lane holds
+// (keeping one half, sending the other) or, once a lane holds one head, adds
+// its partner's copy.  At the end lane i (within the group) holds the full
+// score of head i >> HSHIFT.
+template <int G>
+__device__ __forceinline__ float butterfly(float (&v)[G], int lane) {
+#pragma unroll
+  for (int step = 0; step < 3; ++step) {
+    const int m = 4 >> step;
+    const int nh = (G >> step) > 1 ? (G >> step) : 1;  // heads held before this step
+    if (nh > 1) {
+      const int half = nh / 2;
+      const bool upper = (lane & m) != 0;
+#pragma unroll
+      for (int x = 0; x < half; ++x) {
+        const float send = upper ? v[x] : v[x + half];
+        const float keep = upper ? v[x + half] : v[x];
+        v[x] = keep + __shfl_xor_sync(kFull, send, m);
+      }
+    } else {
+      v[0] += __shfl_xor_sync(kFull, v[0], m);
+    }
+  }
+  return v[0];
+}
+
+// Blocks spanned by sequence b; 0 for an empty or invalid sequence (reported
+// by CTA 0 only, so the error word is touched once per launch).
+__device__ __forceinline__ long long seq_blocks(const Params& p, int b, bool report) {
+  const int len = p.lens[b];
+  const int off = p.offs ? p.offs[b] : 0;
+  if (len < 0 || off < 0 || off >= p.bs || (long long)off + len > (long long)p.mb * p.bs) {
+    if (report) set_error(p.err, kErrCapacity);
+    return 0;
+  }
+  if (len == 0) return 0;
+  return ((long long)off + len + p.bs - 1) / p.bs;
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Params p) {
+  using C = Cfg<T, D, G>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  long long* s_cu = reinterpret_cast<long long*>(smem + p.off_cu);
+  long long* s_scan = reinterpret_cast<long long*>(smem + p.off_scan);
+  int4* s_desc = reinterpret_cast<int4*>(smem + p.off_desc);
+  const uint32_t bar0 = smem_addr(smem + p.off_bar);
+  // full[s] at bar0 + 8s, empty[s] at bar0 + 8(stages+s), group barrier after
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (p.stages + s); };
+  const uint32_t group_bar = bar0 + 8u * (2 * p.stages);
+
+  // ---- 1. block counts and their exclusive scan (every CTA, same result) ----
+  const int B = p.batch;
+  const int per = (B + kThreads - 1) / kThreads;
+  const int beg = min(B, tid * per), end = min(B, beg + per);
+  const bool report = blockIdx.x == 0;
+  long long local = 0;
+  for (int b = beg; b < end; ++b) local += seq_blocks(p, b, report);
+  long long x = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_scan[warp] = x;
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), kNW);
+    }
+    mbar_init(group_bar, kNW);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  long long run = x - local;
+  for (int w = 0; w < warp; ++w) run += s_scan[w];
+  for (int b = beg; b < end; ++b) {
+    s_cu[b] = run;
+    run += seq_blocks(p, b, false);
+  }
+  long long total = 0;
+  for (int w = 0; w < kThreads / 32; ++w) total += s_scan[w];
+  if (tid == 0) s_cu[B] = total;
+  __syncthreads();
+
+  const long long W = (total + gridDim.x - 1) / gridDim.x;
+  const long long x0 = min(total, (long long)blockIdx.x * W);
+  const long long x1 = min(total, x0 + W);
+  if (blockIdx.x == 0) {
+    for (int b = tid; b <= B; b += kThreads) p.ws_cu[b] = s_cu[b];
+    if (tid == 0) { p.ws_meta[0] = W; p.ws_meta[1] = total; }
+  }
+  if (x0 >= x1) return;
+
+  const int S = p.stages;
+  const int ST = p.st;
+  const int stage_bytes = 2 * ST * p.row_bytes;
+
+  if (warp == kNW) {
+    // ======================= producer warp =======================
+    int lo = 0, hi = B;  // sequence holding block x0: largest b with s_cu[b] <= x0
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_cu[mid] <= x0) lo = mid; else hi = mid;
+    }
+    int bseq = lo;
+    while (s_cu[bseq + 1] <= x0) ++bseq;  // skip empty sequences
+    int s = 0;
+    uint32_t ph = 1;  // producer waits on "empty" starting from the completed phase
+    uint32_t filled = 0, fill_par = 0;
+    bool ok = true;
+    for (long long base = x0; base < x1 && ok; base += 32) {
+      const long long xl = base + lane;
+      const bool valid = xl < x1;
+      int bl = bseq;
+      if (valid) while (s_cu[bl + 1] <= xl) ++bl;
+      const long long j = valid ? xl - s_cu[bl] : 0;
+      const long long nb = s_cu[bl + 1] - s_cu[bl];
+      int blk = 0, r0 = 0, r1 = p.bs;
+      if (valid) {
+        blk = p.bt[(long long)bl * p.mb + j];
+        const int off = p.offs ? p.offs[bl] : 0;
+        if (j == 0) r0 = off;
+        if (j == nb - 1) r1 = (int)(((long long)off + p.lens[bl] - 1) % p.bs) + 1;
+      }
+      const int cnt = (int)min((long long)32, x1 - base);
+      for (int k = 0; k < cnt && ok; ++k) {
+        const int kb = __shfl_sync(kFull, bl, k);
+        const int kblk = __shfl_sync(kFull, blk, k);
+        const int kr0 = __shfl_sync(kFull, r0, k);
+        const int kr1 = __shfl_sync(kFull, r1, k);
+        const long long kj = __shfl_sync(kFull, j, k);
+        const long long knb = __shfl_sync(kFull, nb, k);
+        const long long kx = base + k;
+        const bool blk_ok = kblk >= 0 && (long long)kblk < p.num_blocks;
+        if (!blk_ok && lane == 0) set_error(p.err, kErrIndex);
+        const bool seg_start = (kj == 0) || (kx == x0);
+        const bool seg_end = (kj == knb - 1) || (kx == x1 - 1);
+        const bool single = s_cu[kb] >= x0 && s_cu[kb + 1] <= x1;
+        for (int rs = kr0; rs < kr1;) {
+          const int re = min(kr1, (rs / ST + 1) * ST);
+          const int n = re - rs;
+          int flags = 0;
+          if (seg_start && rs == kr0) flags |= kStart;
+          if (seg_end && re == kr1) flags |= kEnd;
+          if (kx == x1 - 1 && re == kr1) flags |= kLast;
+          if (single) flags |= kSingle;
+          if (!mbar_wait(empty_bar(s), ph, p.err)) { ok = false; break; }
+          if (lane == 0) {
+            s_desc[s] = make_int4(kb, blk_ok ? n : 0, flags, (int)blockIdx.x + kb);
+            if (blk_ok) {
+              const uint32_t bytes = (uint32_t)n * (uint32_t)p.row_bytes;
+              const long long src = (long long)kblk * p.block_stride + (long long)rs * p.row_bytes;
+              const uint32_t dk = smem_addr(smem + (size_t)s * stage_bytes);
+              mbar_arrive_expect_tx(full_bar(s), 2 * bytes);
+              bulk_g2s(dk, p.k_base + src, bytes, full_bar(s));
+              bulk_g2s(dk + ST * p.row_bytes, p.v_base + src, bytes, full_bar(s));
+            } else {
+              mbar_arrive(full_bar(s));
+            }
+          }
+          __syncwarp();
+          filled |= 1u << s;
+          fill_par = (fill_par & ~(1u << s)) | (((ph ^ 1u) & 1u) << s);
+          if (++s == S) { s = 0; ph ^= 1; }
+          rs = re;
+        }
+      }
+      bseq = __shfl_sync(kFull, bl, cnt - 1);
+    }
+    if (!ok) {
+      // a consumer stopped answering: let the copies already issued land
+      // before the CTA (and its shared memory) goes away
+      for (int t = 0; t < S; ++t)
+        if (filled & (1u << t)) mbar_wait(full_bar(t), (fill_par >> t) & 1u, p.err);
+    }
+    return;
+  }
+
+  // ======================= consumer warps =======================
+  const int hkv = p.hkv;
+  const int g = warp % hkv;
+  const int wsub = warp / hkv;
+  const int wph = kNW / hkv;
+  const int jg = lane >> 3;  // token slot within a pass
+  const int il = lane & 7;   // lane within the token group
+  const int hs = il >> C::HSHIFT;
+  const bool writer = (il & ((1 << C::HSHIFT) - 1)) == 0;
+  const int head_off = g * D * C::E;
+  const int rb = p.row_bytes;
+  float* pbuf = reinterpret_cast<float*>(smem + p.off_pbuf) + warp * ST * G;
+  float* mbuf = reinterpret_cast<float*>(smem + p.off_mbuf);
+
+  float qr[G][C::EPL];
+  float acc[G][C::PVE];
+  float m_run = -FLT_MAX, l_run = 0.f;
+  bool m_valid = false;
+
+  int s = 0;
+  uint32_t ph = 0, gph = 0;
+  while (true) {
+    if (!mbar_wait(full_bar(s), ph, p.err)) return;
+    const int4 d = s_desc[s];
+    const int b = d.x, n = d.y, flags = d.z, seg = d.w;
+    const char* sK = reinterpret_cast<const char*>(smem) + (size_t)s * stage_bytes;
+    const char* sV = sK + ST * rb;
+
+    if (flags & kStart) {
+      m_run = -FLT_MAX;
+      m_valid = false;
+      l_run = 0.f;
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+        for (int e = 0; e < C::PVE; ++e) acc[hh][e] = 0.f;
+      const char* qb = static_cast<const char*>(p.q) +
+                       ((long long)b * p.hq + (long long)g * G) * D * C::E;
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+        for (int k = 0; k < C::NV; ++k) {
+          const uint4 r = ld_stream(qb + ((long long)hh * D + (il + 8 * k) * C::VEC) * C::E);
+          float f[C::VEC];
+          widen16<T>(r, f);
+#pragma unroll
+          for (int v = 0; v < C::VEC; ++v) qr[hh][k * C::VEC + v] = f[v] * p.qscale;
+        }
+    }
+
+    if (n > 0) {
+      // ---- QK^T: scores of this warp's tokens, one head per lane ----
+      float sc[kMaxPW];
+#pragma unroll
+      for (int pi = 0; pi < kMaxPW; ++pi) {
+        const int pass = wsub + pi * wph;
+        float sval = -FLT_MAX;
+        bool have = false;
+        if (pass * 4 < n) {
+          const int t = pass * 4 + jg;
+          float part[G];
+#pragma unroll
+          for (int hh = 0; hh < G; ++hh) part[hh] = 0.f;
+          if (t < n) {
+            const char* kr = sK + t * rb + head_off;
+#pragma unroll
+            for (int k = 0; k < C::NV; ++k) {
+              const uint4 r = *reinterpret_cast<const uint4*>(kr + (il + 8 * k) * 16);
+              float e[C::VEC];
+              widen16<T>(r, e);
+#pragma unroll
+              for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+                for (int v = 0; v < C::VEC; ++v)
+                  part[hh] = fmaf(qr[hh][k * C::VEC + v], e[v], part[hh]);
+            }
+          }
+          const float tot = butterfly<G>(part, lane);
+          if (t < n) { sval = tot; have = true; }
+        }
+        sc[pi] = have ? sval : -INFINITY;
+      }
+      // ---- online softmax (log2 domain) ----
+      float mx = -INFINITY;
+#pragma unroll
+      for (int pi = 0; pi < kMaxPW; ++pi) mx = fmaxf(mx, sc[pi]);
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+      float alpha = 1.f, psum = 0.f;
+      if (mx != -INFINITY) {
+        const float m_new = m_valid ? fmaxf(m_run, mx) : mx;
+        alpha = m_valid ? exp2f(m_run - m_new) : 0.f;
+#pragma unroll
+        for (int pi = 0; pi < kMaxPW; ++pi) {
+          const float pv = sc[pi] == -INFINITY ? 0.f : exp2f(sc[pi] - m_new);
+          sc[pi] = pv;
+          psum += pv;
+        }
+        m_run = m_new;
+        m_valid = true;
+      } else {
+#pragma unroll
+        for (int pi = 0; pi < kMaxPW; ++pi) sc[pi] = 0.f;
+      }
+      psum += __shfl_xor_sync(kFull, psum, 8);
+      psum += __shfl_xor_sync(kFull, psum, 16);
+      l_run = l_run * alpha + psum;
+      if (writer) {
+#pragma unroll
+        for (int pi = 0; pi < kMaxPW; ++pi) {
+          const int t = (wsub + pi * wph) * 4 + jg;
+          if (t < n) pbuf[t * G + hs] = sc[pi];
+        }
+      }
+      float ah[G];
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) ah[hh] = __shfl_sync(kFull, alpha, hh << C::HSHIFT);
+      __syncwarp();
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+        for (int e = 0; e < C::PVE; ++e) acc[hh][e] *= ah[hh];
+      // ---- PV ----
+      const char* vbase = sV + head_off + lane * C::PVE * C::E;
+#pragma unroll
+      for (int pi = 0; pi < kMaxPW; ++pi) {
+        const int pass = wsub + pi * wph;
+        if (pass * 4 < n) {
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int t = pass * 4 + jj;
+            if (t < n) {
+              float vv[C::PVE];
+              load_pv<T, C::PVE>(vbase + t * rb, vv);
+              float pr[G];
+#pragma unroll
+              for (int hh = 0; hh < G; ++hh) pr[hh] = pbuf[t * G + hh];
+#pragma unroll
+              for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+                for (int e = 0; e < C::PVE; ++e) acc[hh][e] = fmaf(pr[hh], vv[e], acc[hh][e]);
+            }
+          }
+        }
+      }
+    }
+
+    if (flags & kEnd) {
+      float lh[G], mh[G];
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        lh[hh] = __shfl_sync(kFull, l_run, hh << C::HSHIFT);
+        mh[hh] = __shfl_sync(kFull, m_valid ? m_run : -INFINITY, hh << C::HSHIFT);
+      }
+      bool alive = true;
+      if (wph > 1) {
+        // merge the token shares of the warps serving the same kv head
+        float* mw = mbuf + warp * G * (D + 2);
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+#pragma unroll
+          for (int e = 0; e < C::PVE; ++e) mw[hh * (D + 2) + lane * C::PVE + e] = acc[hh][e];
+          if (lane == 0) { mw[hh * (D + 2) + D] = mh[hh]; mw[hh * (D + 2) + D + 1] = lh[hh]; }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(group_bar);
+        alive = mbar_wait(group_bar, gph, p.err);
+        gph ^= 1;
+        if (!alive) return;
+        if (wsub == 0) {
+#pragma unroll
+          for (int hh = 0; hh < G; ++hh) {
+            float M = -INFINITY;
+            for (int w2 = g; w2 < kNW; w2 += hkv) M = fmaxf(M, mbuf[(w2 * G + hh) * (D + 2) + D]);
+            float l = 0.f, a[C::PVE];
+#pragma unroll
+            for (int e = 0; e < C::PVE; ++e) a[e] = 0.f;
+            if (M != -INFINITY) {
+              for (int w2 = g; w2 < kNW; w2 += hkv) {
+                const float* src = mbuf + (w2 * G + hh) * (D + 2);
+                const float mm = src[D];
+                if (mm == -INFINITY) continue;
+                const float wgt = exp2f(mm - M);
+                l += wgt * src[D + 1];
+#pragma unroll
+                for (int e = 0; e < C::PVE; ++e) a[e] += wgt * src[lane * C::PVE + e];
+              }
+            }
+            lh[hh] = l;
+            mh[hh] = M;
+#pragma unroll
+            for (int e = 0; e < C::PVE; ++e) acc[hh][e] = a[e];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(group_bar);
+        alive = mbar_wait(group_bar, gph, p.err);
+        gph ^= 1;
+        if (!alive) return;
+      }
+      if (wsub == 0) {
+        if (flags & kSingle) {
+#pragma unroll
+          for (int hh = 0; hh < G; ++hh) {
+            const float inv = lh[hh] > 0.f ? 1.f / lh[hh] : 0.f;
+            float o[C::PVE];
+#pragma unroll
+            for (int e = 0; e < C::PVE; ++e) o[e] = acc[hh][e] * inv;
+            const long long idx = ((long long)b * p.hq + g * G + hh) * D + lane * C::PVE;
+            store_out<T, C::PVE>(static_cast<char*>(p.out) + idx * C::E, o);
+          }
+        } else {
+#pragma unroll
+          for (int hh = 0; hh < G; ++hh) {
+            const long long row = (long long)seg * p.hq + g * G + hh;
+            store_f32<C::PVE>(p.ws_acc + row * D + lane * C::PVE, acc[hh]);
+            if (lane == 0) {
+              p.ws_ml[row * 2] = mh[hh];
+              p.ws_ml[row * 2 + 1] = lh[hh];
+            }
+          }
+        }
+      }
+    }
+
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar(s));
+    if (++s == S) { s = 0; ph ^= 1; }
+    if (flags & kLast) break;
+  }
+}
+
+// One CTA per sequence: merge the partial states of every segment of that
+// sequence (sequences handled by a single CTA were written already).
+template <typename T>
+__global__ void decode_combine_kernel(const float* __restrict__ ws_acc,
+                                      const float* __restrict__ ws_ml,
+                                      const long long* __restrict__ ws_cu,
+                                      const long long* __restrict__ ws_meta, int hq, int D,
+                                      T* __restrict__ out) {
+  const int b = blockIdx.x;
+  const long long c0 = ws_cu[b], c1 = ws_cu[b + 1];
+  T* o = out + (long long)b * hq * D;
+  if (c1 <= c0) {  // no tokens (or an invalid sequence): zeros
+    for (int i = threadIdx.x; i < hq * D; i += blockDim.x) o[i] = T(0.f);
+    return;
+  }
+  const long long W = ws_meta[0];
+  const long long cf = c0 / W, cl = (c1 - 1) / W;
+  if (cf == cl) return;
+  for (int i = threadIdx.x; i < hq * D; i += blockDim.x) {
+    const int h = i / D, d = i - h * D;
+    float M = -INFINITY;
+    for (long long c = cf; c <= cl; ++c) M = fmaxf(M, ws_ml[((c + b) * hq + h) * 2]);
+    float num = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+      for (long long c = cf; c <= cl; ++c) {
+        const long long row = (c + b) * hq + h;
+        const float m = ws_ml[row * 2];
+        if (m == -INFINITY) continue;
+        const float w = exp2f(m - M);
+        num += w * ws_acc[row * D + d];
+        den += w * ws_ml[row * 2 + 1];
+      }
+    }
+    o[i] = T(den > 0.f ? num / den : 0.f);
+  }
+}
+
+int stage_tokens(int bs, int row_bytes) {
+  int st = 1;
+  while (st * 2 <= kMaxStageTokens && st * 2 <= bs && st * 2 * row_bytes <= 32768) st *= 2;
+  return st;
+}
+
+struct Layout {
+  int st, stages, smem, off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf;
+};
+
+int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int smem_optin) {
+  Layout L{};
+  L.st = stage_tokens(bs, row_bytes);
+  const int stage_bytes = 2 * L.st * row_bytes;
+  int fixed = 0;
+  fixed += 8 * (2 * kMaxStages + 1);            // barriers
+  fixed = align_up(fixed, 16) + 16 * kMaxStages;  // descriptors
+  fixed = align_up(fixed, 16) + 8 * (batch + 1);  // cu
+  fixed = align_up(fixed, 16) + 8 * 16;           // scan scratch
+  fixed = align_up(fixed, 16) + 4 * kNW * L.st * G;
+  if (hkv < kNW) fixed = align_up(fixed, 16) + 4 * kNW * G * (D + 2);
+  fixed = align_up(fixed, 128);
+  int stages = (smem_optin - fixed) / stage_bytes;
+  if (stages > kMaxStages) stages = kMaxStages;
+  L.stages = stages;
+  int off = align_up(stages * stage_bytes, 128);
+  L.off_bar = off;   off += 8 * (2 * stages + 1);
+  off = align_up(off, 16); L.off_desc = off; off += 16 * stages;
+  off = align_up(off, 16); L.off_cu = off;   off += 8 * (batch + 1);
+  off = align_up(off, 16); L.off_scan = off; off += 8 * 16;
+  off = align_up(off, 16); L.off_pbuf = off; off += 4 * kNW * L.st * G;
+  off = align_up(off, 16); L.off_mbuf = off;
+  if (hkv < kNW) off += 4 * kNW * G * (D + 2);
+  L.smem = align_up(off, 16);
+  return L;
+}
+
+// Workspace carve (bytes): meta [W, total] | cu[batch+1] (int64) |
+// (m, l) per (segment, q head) | acc per (segment, q head, d); segments are
+// indexed c + b, so grid + batch of them suffice.
+struct WsLayout {
+  size_t meta, cu, ml, acc, total;
+};
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+WsLayout ws_layout(int batch, int hq, int D, int grid) {
+  WsLayout w{};
+  const size_t parts = (size_t)grid + (size_t)batch;
+  w.meta = 0;
+  w.cu = 256;
+  w.ml = w.cu + round256(8 * ((size_t)batch + 1));
+  w.acc = w.ml + round256(parts * hq * 2 * 4);
+  w.total = w.acc + round256(parts * hq * D * 4);
+  return w;
+}
+
+template <typename T, int D, int G>
+cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
+  const PoolView& pv = a.pool;
+  Params p{};
+  const long long layer_off = (long long)a.layer * pv.block_size * pv.row_bytes;
+  p.k_base = pv.k + layer_off;
+  p.v_base = pv.v + layer_off;
+  p.block_stride = (long long)pv.num_layers * pv.block_size * pv.row_bytes;
+  p.num_blocks = pv.num_blocks;
+  p.q = a.q;
+  p.out = a.out;
+  p.bt = a.bt;
+  p.lens = a.lens;
+  p.offs = a.offs;
+  const int grid = a.grid;
+  const WsLayout W = ws_layout(a.batch, a.num_q_heads, pv.head_dim, grid);
+  char* ws = static_cast<char*>(a.workspace);
+  p.ws_meta = reinterpret_cast<long long*>(ws + W.meta);
+  p.ws_cu = reinterpret_cast<long long*>(ws + W.cu);
+  p.ws_ml = reinterpret_cast<float*>(ws + W.ml);
+  p.ws_acc = reinterpret_cast<float*>(ws + W.acc);
+  p.err = a.err;
+  p.mb = a.mb;
+  p.batch = a.batch;
+  p.hq = a.num_q_heads;
+  p.hkv = pv.num_kv_heads;
+  p.bs = pv.block_size;
+  p.row_bytes = pv.row_bytes;
+  p.st = L.st;
+  p.stages = L.stages;
+  p.qscale = a.scale * kLog2e;
+  p.off_bar = L.off_bar;
+  p.off_desc = L.off_desc;
+  p.off_cu = L.off_cu;
+  p.off_scan = L.off_scan;
+  p.off_pbuf = L.off_pbuf;
+  p.off_mbuf = L.off_mbuf;
+
+  auto kern = decode_partial_kernel<T, D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
+  if (e != cudaSuccess) return e;
+  if (a.ev_start && (e = cudaEventRecord(a.ev_start, s)) != cudaSuccess) return e;
+  kern<<<grid, kThreads, L.smem, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (a.ev_stop && (e = cudaEventRecord(a.ev_stop, s)) != cudaSuccess) return e;
+  decode_combine_kernel<T><<<a.batch, 128, 0, s>>>(p.ws_acc, p.ws_ml, p.ws_cu, p.ws_meta, p.hq, D,
+                                                   static_cast<T*>(a.out));
+  return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t run_g(const DecodeLaunch& a, const Layout& L, int G, cudaStream_t s) {
+  switch (G) {
+    case 1: return run<T, D, 1>(a, L, s);
+    case 2: return run<T, D, 2>(a, L, s);
+    case 4: return run<T, D, 4>(a, L, s);
+    case 8: return run<T, D, 8>(a, L, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+size_t decode_workspace_bytes(int batch, int num_q_heads, int head_dim, int grid) {
+  const int bmax = batch < kDecodeMaxBatch ? batch : kDecodeMaxBatch;
+  return ws_layout(bmax > 0 ? bmax : 0, num_q_heads, head_dim, grid).total;
+}
+
+int decode_supported(const PoolView& p, int num_q_heads) {
+  if (p.head_dim != 64 && p.head_dim != 128) return 1;
+  const int hkv = p.num_kv_heads;
+  if (hkv != 1 && hkv != 2 && hkv != 4 && hkv != 8) return 1;
+  if (num_q_heads % hkv) return 1;
+  const int G = num_q_heads / hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return 1;
+  return 0;
+}
+
+cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s) {
+  const PoolView& pv = a.pool;
+  const int G = a.num_q_heads / pv.num_kv_heads;
+  const Layout L = make_layout(pv.block_size, pv.row_bytes, pv.num_kv_heads, G, pv.head_dim,
+                               a.batch, a.smem_optin);
+  if (L.stages < 2) return cudaErrorInvalidConfiguration;
+  if (pv.elem_size == 2) {
+    return pv.head_dim == 128 ? run_g<__nv_bfloat16, 128>(a, L, G, s)
+                              : run_g<__nv_bfloat16, 64>(a, L, G, s);
+  }
+  return pv.head_dim == 128 ? run_g<float, 128>(a, L, G, s) : run_g<float, 64>(a, L, G, s);
+}
+
+}  // namespace pkv
