@@ -126,7 +126,9 @@ def recorded_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    """nvidia-smi sampled every 200 ms around the timed region.  Samples are
+    time-stamped so the summary keeps only those taken while the GPU was
+    loaded (from the pre-load steps before the region to its end)."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -135,12 +137,13 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (time, line)
+        self.window = None
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
@@ -151,9 +154,9 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
-    def __exit__(self, *exc):
+    def stop(self):
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -165,7 +168,9 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for ts, line in self.lines:
+            if self.window and not (self.window[0] <= ts <= self.window[1]):
+                continue
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -181,6 +186,19 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def preload(fn, clocks: "ClockSampler", min_s: float = 0.6, max_s: float = 5.0):
+    """Untimed steps until the clock sampler has samples under load."""
+    t0 = time.time()
+    n0 = len(clocks.lines)
+    while time.time() - t0 < max_s:
+        for _ in range(20):
+            fn()
+        torch.cuda.synchronize()
+        if time.time() - t0 >= min_s and (clocks.proc is None or len(clocks.lines) >= n0 + 2):
+            break
+    return t0
 
 
 # ---------------------------------------------------------------------------
@@ -295,12 +313,17 @@ def run_ours(args, rank, local_rank, world):
         pkv.set_decode_events(e0, e1)
         return e0, e1
 
+    clocks = ClockSampler(dev.index).start()
+    t_load = preload(st.step, clocks)
     barrier()
     torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clocks:
-        times, kev = timed(st.step, args.steps, flush, hook)
+    times, kev = timed(st.step, args.steps, flush, hook)
     pkv.set_decode_events(None, None)
     torch.cuda.synchronize()
+    t_end = time.time()
+    time.sleep(0.25)
+    clocks.stop()
+    clocks.window = (t_load, t_end + 0.25)
     barrier()
     ms = statistics.mean(times)
     ms_max = reduce_max(ms)
@@ -455,17 +478,17 @@ def _oracle_sample(w, kh, vh, qh, seqs):
 def cpu_baseline(seconds: float, seed_shift=0, dev=None):
     w, kh, vh, qh = _oracle_inputs(dev, seed_shift)
     kv_total, t_total, n = 0, 0.0, 0
-    order = list(range(w.batch.batch))
-    while t_total < seconds and n < len(order):
-        kv, dt = _oracle_sample(w, kh, vh, qh, [order[n]])
+    B = w.batch.batch
+    while t_total < seconds and n < 16 * B:
+        kv, dt = _oracle_sample(w, kh, vh, qh, [n % B])
         kv_total += kv
         t_total += dt
         n += 1
     return {"value": round(kv_total / t_total / 1e9, 4), "unit": "GB/s", "cores": 1,
             "kind": "oracle",
-            "sample": f"oracle.decode_attention (numpy, fp64, per-block gather) on the first {n} "
-                      f"of 64 decode_gqa sequences ({kv_total / 1e6:.0f} MB of K/V), "
-                      f"{t_total:.1f} s, single thread"}
+            "sample": f"oracle.decode_attention (numpy, fp64, per-block gather) over {n} "
+                      f"decode_gqa sequences taken in order, cycling over the 64 "
+                      f"({kv_total / 1e6:.0f} MB of K/V), {t_total:.1f} s, single thread"}
 
 
 def run_reference(args, rank, world):
@@ -509,15 +532,67 @@ def run_reference(args, rank, world):
     }
 
 
+def ncu_case(kind: str, launches: int = 4) -> int:
+    """A small-footprint run of one kernel for ncu: the decode-GQA batch
+    (1.27 GB of K/V per launch, larger than L2) over a 1-layer copy of its
+    pool (1 GB), or the gather/scatter legs over a 1-layer pool."""
+    import paged_kv_cache_blk_gb300 as pkv
+    from workloads.gen import PoolSpec
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pkv.build()
+    pkv.load()
+    name = WORKLOAD if kind == "decode" else LEG_WORKLOAD
+    w = make_workload(name)
+    sp = w.pool
+    one = PoolSpec(sp.num_blocks, 1, sp.block_size, sp.num_kv_heads, sp.head_dim, sp.dtype)
+    k, v = new_pool(one, dev)
+    fill_pool(k, v, one, 0, w.seed)
+    pool = pkv.Pool(k, v)
+    b = w.batch
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+    bt, lens, offs, cu = (t(b.block_tables, torch.int32), t(b.seq_lens, torch.int32),
+                          t(b.offsets, torch.int32), t(b.cu_seqlens, torch.int64))
+    row = (sp.num_kv_heads, sp.head_dim)
+    if kind == "decode":
+        q = rand_rows((b.batch, w.num_q_heads, sp.head_dim), "bf16", 1, dev)
+        out = torch.empty_like(q)
+        ws = torch.empty(pkv.decode_workspace_size(b.batch, w.num_q_heads, sp.head_dim, dev),
+                         dtype=torch.uint8, device=dev)
+        fn = lambda: pkv.decode_attention(pool, 0, q, w.scale, bt, lens, offs, out, ws)
+    else:
+        T = w.tokens.num_tokens
+        slots = torch.empty(T, dtype=torch.int64, device=dev)
+        pkv.build_slot_mapping(pool, bt, offs, t(w.tokens.token_seq, torch.int32),
+                               t(w.tokens.token_pos, torch.int32), slots)
+        kn = rand_rows((T,) + row, "bf16", 2, dev)
+        vn = rand_rows((T,) + row, "bf16", 3, dev)
+        ko = torch.empty((b.total_tokens,) + row, dtype=torch.bfloat16, device=dev)
+        vo = torch.empty_like(ko)
+        if kind == "scatter":
+            fn = lambda: pkv.write_slots(pool, 0, kn, vn, slots)
+        else:
+            fn = lambda: pkv.gather(pool, 0, bt, lens, offs, cu, ko, vo)
+    for _ in range(launches):
+        fn()
+    torch.cuda.synchronize()
+    print(f"ncu case {kind}: {launches} launches done")
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ncu-case", choices=["decode", "gather", "scatter"],
+                    help="run a small-footprint case of one kernel (for ncu) and exit")
     args = ap.parse_args(argv)
+    if args.ncu_case:
+        return ncu_case(args.ncu_case)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, local_rank, world = dist_env()
