@@ -127,7 +127,22 @@ class Pool:
         return ctypes.byref(self.struct)
 
 
+class _NoSwitch:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
+_NO_SWITCH = _NoSwitch()
+
+
 def _dev(pool: Pool):
+    """Make the pool's device current for the call (no-op when it already is)."""
+    idx = pool.device.index
+    if idx is None or idx == torch.cuda.current_device():
+        return _NO_SWITCH
     return torch.cuda.device(pool.device)
 
 

@@ -13,25 +13,27 @@
 //    number of blocks whatever the length mix.  A CTA range cuts sequences
 //    into segments; the segment of sequence b inside CTA c has index c + b
 //    (unique because both the ranges and the sequences are in order).
-//  * Inside a CTA, one producer warp streams the K and V rows of each block
-//    into a ring of shared-memory stages with 1-D bulk copies
-//    (cp.async.bulk, completion counted on an mbarrier).  For the layout
-//    [N, L, bs, Hkv, D] the rows [r0, r1) of one (block, layer) are ONE
-//    contiguous run covering all kv heads (32 KB for bs 16, Hkv 8, D 128
-//    bf16), so a block costs two copy instructions and every byte fetched is
-//    used.  Only the rows the sequence covers are fetched (first-block offset
-//    and the partly filled last block are trimmed).
-//  * Eight consumer warps compute.  Warp w serves kv head w % Hkv (and, when
-//    Hkv < 8, a share of the tokens) for all G = Hq/Hkv query heads of that
-//    group, so each K/V byte is read from shared memory by one warp and used
-//    for all G heads (GQA grouping).
-//      QK: 8 lanes per token, 4 tokens per pass; each lane holds D/8 query
-//          elements per head (pre-scaled by scale*log2(e)) and does
-//          G*D/8 FMAs, then a butterfly over the 8 lanes both sums and
-//          spreads the G head scores.
-//      softmax: running max / sum per head in the log2 domain (exp2f).
-//      PV: each lane owns D/32 output elements for all G heads.
-//    fp32 accumulation throughout; fp32 pools use the same path.
+//  * Inside a CTA one producer warp streams the K and V rows of each block
+//    into a ring of shared-memory stages with bulk copies (cp.async.bulk,
+//    completion counted on an mbarrier).  The 32 lanes issue the 2 x 16 row
+//    copies of a block at once; each token row (all kv heads, 2 KB for Hkv 8,
+//    D 128, bf16) lands in a shared-memory row padded by 16 bytes, so the 8
+//    rows an ldmatrix reads fall in 8 different bank groups.  Only the rows a
+//    sequence covers are fetched (first-block offset and partly filled last
+//    block are trimmed): every byte read from HBM is used once.
+//  * Eight consumer warps compute; warp w serves kv head w % Hkv for all
+//    G = Hq/Hkv query heads of that group, so each K/V byte is read from HBM
+//    once and used by all G heads (GQA grouping).
+//      bf16 pools: tensor cores (mma.sync m16n8k16, fp32 accumulate).
+//        S^T[t][h] = K[t][:] . Q[h][:] with the 16 tokens of a stage as M and
+//        the G heads as N (8 columns); online softmax in registers (exp2 of
+//        pre-scaled scores); P^T goes to shared memory as bf16 and
+//        O^T[d][h] += V^T[d][t] P^T[t][h] with d as M.  About 110
+//        instructions per (stage, head) keep the SM far below its issue rate,
+//        so the bulk-copy pipeline alone sets the speed.
+//      fp32 pools: CUDA-core FMAs in fp32 (8 lanes per token for Q.K with a
+//        butterfly that sums and spreads the G scores; each lane owns D/32
+//        output elements for PV).
 //  * At a segment end the warp either writes the normalised output (sequence
 //    entirely inside this CTA) or the partial state (m, l, acc) to the
 //    workspace; the combine kernel merges partial states with the log-sum-exp
@@ -48,9 +50,10 @@ namespace {
 
 constexpr int kNW = 8;                    // consumer warps
 constexpr int kThreads = (kNW + 1) * 32;  // + one producer warp
-constexpr int kMaxStageTokens = 16;
-constexpr int kMaxPW = kMaxStageTokens / 4;  // passes of 4 tokens per warp per stage
+constexpr int kMaxStageTokens = 16;       // rows per stage (one mma M tile)
+constexpr int kMaxPW = kMaxStageTokens / 4;
 constexpr int kMaxStages = 8;
+constexpr int kRowPad = 16;               // bytes of padding after each staged row
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -71,23 +74,13 @@ struct Params {
   long long* ws_cu;
   long long* ws_meta;
   int* err;
-  int mb, batch, hq, hkv, bs, row_bytes, st, stages;
+  int mb, batch, hq, hkv, bs, row_bytes, rs, st, stages;
   float qscale;
   // shared-memory carve (bytes from the start of dynamic smem)
   int off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf;
 };
 
-template <typename T, int D, int G>
-struct Cfg {
-  static constexpr int E = sizeof(T);
-  static constexpr int VEC = 16 / E;    // elements per 16-byte vector
-  static constexpr int EPL = D / 8;     // QK elements per lane
-  static constexpr int NV = EPL / VEC;  // 16-byte vectors per lane per row
-  static constexpr int PVE = D / 32;    // PV output elements per lane
-  static constexpr int LOG2G = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
-  static constexpr int HSHIFT = 3 - LOG2G;  // after the butterfly lane i holds head i >> HSHIFT
-  static_assert(NV >= 1 && PVE >= 2, "unsupported head_dim");
-};
+// ---- small helpers ----------------------------------------------------------
 
 template <typename T>
 __device__ __forceinline__ void widen16(const uint4& r, float* f) {
@@ -121,37 +114,51 @@ __device__ __forceinline__ void load_pv(const char* p, float (&f)[PVE]) {
   }
 }
 
-template <typename T, int PVE>
-__device__ __forceinline__ void store_out(void* p, const float (&f)[PVE]) {
+template <typename T>
+__device__ __forceinline__ void store_elem(void* base, long long idx, float x) {
   if constexpr (sizeof(T) == 2) {
-    if constexpr (PVE == 4) {
-      *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
-    } else {
-      *reinterpret_cast<uint32_t*>(p) = pack_bf16x2(f[0], f[1]);
-    }
+    static_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(x);
   } else {
-    if constexpr (PVE == 4) {
-      *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
-    } else {
-      *reinterpret_cast<float2*>(p) = make_float2(f[0], f[1]);
-    }
+    static_cast<float*>(base)[idx] = x;
   }
 }
 
-template <int PVE>
-__device__ __forceinline__ void store_f32(float* p, const float (&f)[PVE]) {
-  if constexpr (PVE == 4) {
-    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
-  } else {
-    *reinterpret_cast<float2*>(p) = make_float2(f[0], f[1]);
-  }
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x2_t(uint32_t (&r)[2], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(addr)
+               : "memory");
+}
+
+// D[16x8] += A[16x16] * B[16x8], bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // Sum partial dot products over the 8 lanes of a token group while spreading
 // the G heads over them: each step either halves the heads a lane holds
 // (keeping one half, sending the other) or, once a lane holds one head, adds
 // its partner's copy.  At the end lane i (within the group) holds the full
-// score of head i >> HSHIFT.
+// score of head i >> (3 - log2 G).
 template <int G>
 __device__ __forceinline__ float butterfly(float (&v)[G], int lane) {
 #pragma unroll
@@ -187,151 +194,335 @@ __device__ __forceinline__ long long seq_blocks(const Params& p, int b, bool rep
   return ((long long)off + len + p.bs - 1) / p.bs;
 }
 
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Params p) {
-  using C = Cfg<T, D, G>;
-  extern __shared__ __align__(128) unsigned char smem[];
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
+// Shared-memory pipeline handles.
+struct Pipe {
+  unsigned char* smem;
+  int4* desc;
+  uint32_t bar0;
+  int stages;
+  int stage_bytes;
+  __device__ uint32_t full(int s) const { return bar0 + 8u * s; }
+  __device__ uint32_t empty(int s) const { return bar0 + 8u * (stages + s); }
+  __device__ uint32_t group() const { return bar0 + 8u * (2 * stages); }
+};
 
-  long long* s_cu = reinterpret_cast<long long*>(smem + p.off_cu);
-  long long* s_scan = reinterpret_cast<long long*>(smem + p.off_scan);
-  int4* s_desc = reinterpret_cast<int4*>(smem + p.off_desc);
-  const uint32_t bar0 = smem_addr(smem + p.off_bar);
-  // full[s] at bar0 + 8s, empty[s] at bar0 + 8(stages+s), group barrier after
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (p.stages + s); };
-  const uint32_t group_bar = bar0 + 8u * (2 * p.stages);
+// Reusable barrier over the consumer warps (mbarrier with kNW arrivals),
+// bounded like every other wait.
+__device__ __forceinline__ bool group_sync(const Pipe& pp, uint32_t& gph, int lane, int* err) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(pp.group());
+  const bool ok = mbar_wait(pp.group(), gph, err);
+  gph ^= 1;
+  return ok;
+}
 
-  // ---- 1. block counts and their exclusive scan (every CTA, same result) ----
+// ---- producer warp -----------------------------------------------------------
+
+__device__ void run_producer(const Params& p, const Pipe& pp, const long long* s_cu, int lane,
+                             long long x0, long long x1) {
   const int B = p.batch;
-  const int per = (B + kThreads - 1) / kThreads;
-  const int beg = min(B, tid * per), end = min(B, beg + per);
-  const bool report = blockIdx.x == 0;
-  long long local = 0;
-  for (int b = beg; b < end; ++b) local += seq_blocks(p, b, report);
-  long long x = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const long long y = __shfl_up_sync(kFull, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) s_scan[warp] = x;
-  if (tid == 0) {
-    for (int s = 0; s < p.stages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), kNW);
-    }
-    mbar_init(group_bar, kNW);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  long long run = x - local;
-  for (int w = 0; w < warp; ++w) run += s_scan[w];
-  for (int b = beg; b < end; ++b) {
-    s_cu[b] = run;
-    run += seq_blocks(p, b, false);
-  }
-  long long total = 0;
-  for (int w = 0; w < kThreads / 32; ++w) total += s_scan[w];
-  if (tid == 0) s_cu[B] = total;
-  __syncthreads();
-
-  const long long W = (total + gridDim.x - 1) / gridDim.x;
-  const long long x0 = min(total, (long long)blockIdx.x * W);
-  const long long x1 = min(total, x0 + W);
-  if (blockIdx.x == 0) {
-    for (int b = tid; b <= B; b += kThreads) p.ws_cu[b] = s_cu[b];
-    if (tid == 0) { p.ws_meta[0] = W; p.ws_meta[1] = total; }
-  }
-  if (x0 >= x1) return;
-
-  const int S = p.stages;
   const int ST = p.st;
-  const int stage_bytes = 2 * ST * p.row_bytes;
-
-  if (warp == kNW) {
-    // ======================= producer warp =======================
-    int lo = 0, hi = B;  // sequence holding block x0: largest b with s_cu[b] <= x0
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_cu[mid] <= x0) lo = mid; else hi = mid;
+  int lo = 0, hi = B;  // sequence holding block x0: largest b with s_cu[b] <= x0
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_cu[mid] <= x0) lo = mid; else hi = mid;
+  }
+  int bseq = lo;
+  while (s_cu[bseq + 1] <= x0) ++bseq;  // skip empty sequences
+  int s = 0;
+  uint32_t ph = 1;  // "empty" waits start on the already completed phase
+  uint32_t filled = 0, fill_par = 0;
+  bool ok = true;
+  const int r_lane = lane & 15;
+  const bool v_lane = lane >= 16;
+  for (long long base = x0; base < x1 && ok; base += 32) {
+    // lane-parallel lookup of 32 consecutive blocks: sequence, table entry, rows
+    const long long xl = base + lane;
+    const bool valid = xl < x1;
+    int bl = bseq;
+    if (valid) while (s_cu[bl + 1] <= xl) ++bl;
+    const long long j = valid ? xl - s_cu[bl] : 0;
+    const long long nb = s_cu[bl + 1] - s_cu[bl];
+    int blk = 0, r0 = 0, r1 = p.bs;
+    if (valid) {
+      blk = p.bt[(long long)bl * p.mb + j];
+      const int off = p.offs ? p.offs[bl] : 0;
+      if (j == 0) r0 = off;
+      if (j == nb - 1) r1 = (int)(((long long)off + p.lens[bl] - 1) % p.bs) + 1;
     }
-    int bseq = lo;
-    while (s_cu[bseq + 1] <= x0) ++bseq;  // skip empty sequences
-    int s = 0;
-    uint32_t ph = 1;  // producer waits on "empty" starting from the completed phase
-    uint32_t filled = 0, fill_par = 0;
-    bool ok = true;
-    for (long long base = x0; base < x1 && ok; base += 32) {
-      const long long xl = base + lane;
-      const bool valid = xl < x1;
-      int bl = bseq;
-      if (valid) while (s_cu[bl + 1] <= xl) ++bl;
-      const long long j = valid ? xl - s_cu[bl] : 0;
-      const long long nb = s_cu[bl + 1] - s_cu[bl];
-      int blk = 0, r0 = 0, r1 = p.bs;
-      if (valid) {
-        blk = p.bt[(long long)bl * p.mb + j];
-        const int off = p.offs ? p.offs[bl] : 0;
-        if (j == 0) r0 = off;
-        if (j == nb - 1) r1 = (int)(((long long)off + p.lens[bl] - 1) % p.bs) + 1;
+    const int cnt = (int)min((long long)32, x1 - base);
+    for (int k = 0; k < cnt && ok; ++k) {
+      const int kb = __shfl_sync(kFull, bl, k);
+      const int kblk = __shfl_sync(kFull, blk, k);
+      const int kr0 = __shfl_sync(kFull, r0, k);
+      const int kr1 = __shfl_sync(kFull, r1, k);
+      const long long kj = __shfl_sync(kFull, j, k);
+      const long long knb = __shfl_sync(kFull, nb, k);
+      const long long kx = base + k;
+      const bool blk_ok = kblk >= 0 && (long long)kblk < p.num_blocks;
+      if (!blk_ok && lane == 0) set_error(p.err, kErrIndex);
+      const bool seg_start = (kj == 0) || (kx == x0);
+      const bool seg_end = (kj == knb - 1) || (kx == x1 - 1);
+      const bool single = s_cu[kb] >= x0 && s_cu[kb + 1] <= x1;
+      const long long blk_src = (long long)kblk * p.block_stride;
+      for (int rs0 = kr0; rs0 < kr1;) {
+        const int re = min(kr1, (rs0 / ST + 1) * ST);
+        const int n = re - rs0;
+        int flags = 0;
+        if (seg_start && rs0 == kr0) flags |= kStart;
+        if (seg_end && re == kr1) flags |= kEnd;
+        if (kx == x1 - 1 && re == kr1) flags |= kLast;
+        if (single) flags |= kSingle;
+        if (!mbar_wait(pp.empty(s), ph, p.err)) { ok = false; break; }
+        if (lane == 0) {
+          pp.desc[s] = make_int4(kb, blk_ok ? n : 0, flags, (int)blockIdx.x + kb);
+          if (blk_ok) mbar_arrive_expect_tx(pp.full(s), 2u * n * p.row_bytes);
+          else mbar_arrive(pp.full(s));
+        }
+        __syncwarp();
+        if (blk_ok && r_lane < n) {
+          const long long src = blk_src + (long long)(rs0 + r_lane) * p.row_bytes;
+          const uint32_t dst = smem_addr(pp.smem + (size_t)s * pp.stage_bytes +
+                                         (v_lane ? ST * p.rs : 0) + r_lane * p.rs);
+          bulk_g2s(dst, (v_lane ? p.v_base : p.k_base) + src, p.row_bytes, pp.full(s));
+        }
+        __syncwarp();
+        filled |= 1u << s;
+        fill_par = (fill_par & ~(1u << s)) | (((ph ^ 1u) & 1u) << s);
+        if (++s == pp.stages) { s = 0; ph ^= 1; }
+        rs0 = re;
       }
-      const int cnt = (int)min((long long)32, x1 - base);
-      for (int k = 0; k < cnt && ok; ++k) {
-        const int kb = __shfl_sync(kFull, bl, k);
-        const int kblk = __shfl_sync(kFull, blk, k);
-        const int kr0 = __shfl_sync(kFull, r0, k);
-        const int kr1 = __shfl_sync(kFull, r1, k);
-        const long long kj = __shfl_sync(kFull, j, k);
-        const long long knb = __shfl_sync(kFull, nb, k);
-        const long long kx = base + k;
-        const bool blk_ok = kblk >= 0 && (long long)kblk < p.num_blocks;
-        if (!blk_ok && lane == 0) set_error(p.err, kErrIndex);
-        const bool seg_start = (kj == 0) || (kx == x0);
-        const bool seg_end = (kj == knb - 1) || (kx == x1 - 1);
-        const bool single = s_cu[kb] >= x0 && s_cu[kb + 1] <= x1;
-        for (int rs = kr0; rs < kr1;) {
-          const int re = min(kr1, (rs / ST + 1) * ST);
-          const int n = re - rs;
-          int flags = 0;
-          if (seg_start && rs == kr0) flags |= kStart;
-          if (seg_end && re == kr1) flags |= kEnd;
-          if (kx == x1 - 1 && re == kr1) flags |= kLast;
-          if (single) flags |= kSingle;
-          if (!mbar_wait(empty_bar(s), ph, p.err)) { ok = false; break; }
-          if (lane == 0) {
-            s_desc[s] = make_int4(kb, blk_ok ? n : 0, flags, (int)blockIdx.x + kb);
-            if (blk_ok) {
-              const uint32_t bytes = (uint32_t)n * (uint32_t)p.row_bytes;
-              const long long src = (long long)kblk * p.block_stride + (long long)rs * p.row_bytes;
-              const uint32_t dk = smem_addr(smem + (size_t)s * stage_bytes);
-              mbar_arrive_expect_tx(full_bar(s), 2 * bytes);
-              bulk_g2s(dk, p.k_base + src, bytes, full_bar(s));
-              bulk_g2s(dk + ST * p.row_bytes, p.v_base + src, bytes, full_bar(s));
-            } else {
-              mbar_arrive(full_bar(s));
+    }
+    bseq = __shfl_sync(kFull, bl, cnt - 1);
+  }
+  if (!ok) {
+    // a consumer stopped answering: let the copies already issued land before
+    // the CTA (and its shared memory) goes away
+    for (int t = 0; t < pp.stages; ++t)
+      if (filled & (1u << t)) mbar_wait(pp.full(t), (fill_par >> t) & 1u, p.err);
+  }
+}
+
+// ---- bf16 consumer: tensor cores ---------------------------------------------
+
+template <int D, int G>
+__device__ void run_consumer_mma(const Params& p, const Pipe& pp, int warp, int lane) {
+  constexpr int KS = D / 16;  // k-steps of Q.K = m-tiles of P.V
+  const int hkv = p.hkv;
+  const int g = warp % hkv;
+  const int wsub = warp / hkv;
+  const int wph = kNW / hkv;
+  const int gl = lane >> 2;  // mma group row
+  const int qi = lane & 3;   // mma thread in group
+  const int rs = p.rs;
+  const int ST = p.st;
+  const uint32_t head_off = g * D * 2;
+  const int ld_t = (lane & 7) + ((lane >> 3) & 1) * 8;  // K rows (A of Q.K, non-trans)
+  const int ld_c = lane >> 4;
+  const int pv_t = (lane & 7) + (lane >> 4) * 8;        // V rows (A of P.V, trans)
+  const int pv_c = (lane >> 3) & 1;
+  unsigned char* ptile = pp.smem + p.off_pbuf + warp * 256;  // P^T [16 t][8 h] bf16
+  const uint32_t pt_addr = smem_addr(ptile);
+  float* mbuf = reinterpret_cast<float*>(pp.smem + p.off_mbuf);
+  const float qs = p.qscale;
+
+  uint32_t qb[KS][2];
+  float o[KS][4];
+  float m0 = 0.f, m1 = 0.f, l0 = 0.f, l1 = 0.f;
+  bool mv = false;
+
+  int s = 0;
+  uint32_t ph = 0, gph = 0;
+  while (true) {
+    if (!mbar_wait(pp.full(s), ph, p.err)) return;
+    const int4 dsc = pp.desc[s];
+    const int b = dsc.x, n = dsc.y, flags = dsc.z, seg = dsc.w;
+    const uint32_t sK = smem_addr(pp.smem + (size_t)s * pp.stage_bytes) + head_off;
+    const uint32_t sV = sK + ST * rs;
+
+    if (flags & kStart) {
+      mv = false;
+      m0 = m1 = l0 = l1 = 0.f;
+#pragma unroll
+      for (int kt = 0; kt < KS; ++kt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[kt][c] = 0.f;
+      // B fragments of Q^T: column gl is query head g*G + gl
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+          static_cast<const char*>(p.q) + (((long long)b * p.hq + g * G + gl) * D + 2 * qi) * 2);
+#pragma unroll
+      for (int j = 0; j < KS; ++j) {
+        qb[j][0] = gl < G ? __ldg(qrow + 8 * j) : 0u;
+        qb[j][1] = gl < G ? __ldg(qrow + 8 * j + 4) : 0u;
+      }
+    }
+
+    for (int mt = wsub; mt * 16 < n; mt += wph) {
+      const int t_lo = mt * 16;
+      // rows past n hold stale data: read a valid row instead (it is masked)
+      const int rk = min(t_lo + ld_t, n - 1);
+      const int rv = min(t_lo + pv_t, n - 1);
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < KS; ++j) {
+        uint32_t a[4];
+        ldsm_x4(a, sK + rk * rs + (2 * j + ld_c) * 16);
+        mma_bf16(sc, a, qb[j][0], qb[j][1]);
+      }
+      const int t0 = t_lo + gl, t1 = t0 + 8;
+      sc[0] = t0 < n ? sc[0] * qs : -INFINITY;
+      sc[1] = t0 < n ? sc[1] * qs : -INFINITY;
+      sc[2] = t1 < n ? sc[2] * qs : -INFINITY;
+      sc[3] = t1 < n ? sc[3] * qs : -INFINITY;
+      float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o2));
+      }
+      const float n0 = mv ? fmaxf(m0, mx0) : mx0;
+      const float n1 = mv ? fmaxf(m1, mx1) : mx1;
+      const float a0 = mv ? exp2f(m0 - n0) : 0.f;
+      const float a1 = mv ? exp2f(m1 - n1) : 0.f;
+      const float p0 = exp2f(sc[0] - n0), p1 = exp2f(sc[1] - n1);
+      const float p2 = exp2f(sc[2] - n0), p3 = exp2f(sc[3] - n1);
+      l0 = l0 * a0 + p0 + p2;  // this thread's share; summed over rows at the end
+      l1 = l1 * a1 + p1 + p3;
+      m0 = n0;
+      m1 = n1;
+      mv = true;
+#pragma unroll
+      for (int kt = 0; kt < KS; ++kt) {
+        o[kt][0] *= a0; o[kt][1] *= a1; o[kt][2] *= a0; o[kt][3] *= a1;
+      }
+      *reinterpret_cast<uint32_t*>(ptile + gl * 16 + qi * 4) = pack_bf16x2(p0, p1);
+      *reinterpret_cast<uint32_t*>(ptile + (gl + 8) * 16 + qi * 4) = pack_bf16x2(p2, p3);
+      __syncwarp();
+      uint32_t pb[2];
+      ldsm_x2_t(pb, pt_addr + (lane & 15) * 16);
+#pragma unroll
+      for (int kt = 0; kt < KS; ++kt) {
+        uint32_t a[4];
+        ldsm_x4_t(a, sV + rv * rs + (2 * kt + pv_c) * 16);
+        mma_bf16(o[kt], a, pb[0], pb[1]);
+      }
+      __syncwarp();
+    }
+
+    if (flags & kEnd) {
+      // row sums: each thread held the share of its token rows
+      float L0 = l0, L1 = l1;
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) {
+        L0 += __shfl_xor_sync(kFull, L0, o2);
+        L1 += __shfl_xor_sync(kFull, L1, o2);
+      }
+      float M0 = mv ? m0 : -INFINITY, M1 = mv ? m1 : -INFINITY;
+      const int h0 = 2 * qi, h1 = h0 + 1;
+      if (wph > 1) {
+        // merge the token shares of the warps serving the same kv head
+        float* mw = mbuf + warp * G * (D + 2);
+#pragma unroll
+        for (int kt = 0; kt < KS; ++kt) {
+          const int d0 = kt * 16 + gl, d1 = d0 + 8;
+          if (h0 < G) { mw[h0 * (D + 2) + d0] = o[kt][0]; mw[h0 * (D + 2) + d1] = o[kt][2]; }
+          if (h1 < G) { mw[h1 * (D + 2) + d0] = o[kt][1]; mw[h1 * (D + 2) + d1] = o[kt][3]; }
+        }
+        if (gl == 0) {
+          if (h0 < G) { mw[h0 * (D + 2) + D] = M0; mw[h0 * (D + 2) + D + 1] = L0; }
+          if (h1 < G) { mw[h1 * (D + 2) + D] = M1; mw[h1 * (D + 2) + D + 1] = L1; }
+        }
+        if (!group_sync(pp, gph, lane, p.err)) return;
+        if (wsub == 0) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int h = h0 + hh;
+            if (h >= G) continue;
+            float Mx = -INFINITY;
+            for (int w2 = g; w2 < kNW; w2 += hkv) Mx = fmaxf(Mx, mbuf[(w2 * G + h) * (D + 2) + D]);
+            float Ls = 0.f;
+            float acc[KS][2];
+#pragma unroll
+            for (int kt = 0; kt < KS; ++kt) acc[kt][0] = acc[kt][1] = 0.f;
+            if (Mx != -INFINITY) {
+              for (int w2 = g; w2 < kNW; w2 += hkv) {
+                const float* src = mbuf + (w2 * G + h) * (D + 2);
+                if (src[D] == -INFINITY) continue;
+                const float wgt = exp2f(src[D] - Mx);
+                Ls += wgt * src[D + 1];
+#pragma unroll
+                for (int kt = 0; kt < KS; ++kt) {
+                  acc[kt][0] += wgt * src[kt * 16 + gl];
+                  acc[kt][1] += wgt * src[kt * 16 + gl + 8];
+                }
+              }
+            }
+#pragma unroll
+            for (int kt = 0; kt < KS; ++kt) {
+              o[kt][hh] = acc[kt][0];
+              o[kt][2 + hh] = acc[kt][1];
+            }
+            if (hh == 0) { M0 = Mx; L0 = Ls; } else { M1 = Mx; L1 = Ls; }
+          }
+        }
+        if (!group_sync(pp, gph, lane, p.err)) return;
+      }
+      if (wsub == 0) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int h = h0 + hh;
+          if (h >= G) continue;
+          const float Lh = hh == 0 ? L0 : L1;
+          const float Mh = hh == 0 ? M0 : M1;
+          const long long row_out = (long long)b * p.hq + g * G + h;
+          const long long row_ws = (long long)seg * p.hq + g * G + h;
+          if (flags & kSingle) {
+            const float inv = Lh > 0.f ? 1.f / Lh : 0.f;
+#pragma unroll
+            for (int kt = 0; kt < KS; ++kt) {
+              store_elem<__nv_bfloat16>(p.out, row_out * D + kt * 16 + gl, o[kt][hh] * inv);
+              store_elem<__nv_bfloat16>(p.out, row_out * D + kt * 16 + gl + 8,
+                                        o[kt][2 + hh] * inv);
+            }
+          } else {
+#pragma unroll
+            for (int kt = 0; kt < KS; ++kt) {
+              p.ws_acc[row_ws * D + kt * 16 + gl] = o[kt][hh];
+              p.ws_acc[row_ws * D + kt * 16 + gl + 8] = o[kt][2 + hh];
+            }
+            if (gl == 0) {
+              p.ws_ml[row_ws * 2] = Mh;
+              p.ws_ml[row_ws * 2 + 1] = Lh;
             }
           }
-          __syncwarp();
-          filled |= 1u << s;
-          fill_par = (fill_par & ~(1u << s)) | (((ph ^ 1u) & 1u) << s);
-          if (++s == S) { s = 0; ph ^= 1; }
-          rs = re;
         }
       }
-      bseq = __shfl_sync(kFull, bl, cnt - 1);
     }
-    if (!ok) {
-      // a consumer stopped answering: let the copies already issued land
-      // before the CTA (and its shared memory) goes away
-      for (int t = 0; t < S; ++t)
-        if (filled & (1u << t)) mbar_wait(full_bar(t), (fill_par >> t) & 1u, p.err);
-    }
-    return;
-  }
 
-  // ======================= consumer warps =======================
+    __syncwarp();
+    if (lane == 0) mbar_arrive(pp.empty(s));
+    if (++s == pp.stages) { s = 0; ph ^= 1; }
+    if (flags & kLast) break;
+  }
+}
+
+// ---- fp32 consumer: CUDA-core FMAs -------------------------------------------
+
+template <typename T, int D, int G>
+struct FmaCfg {
+  static constexpr int E = sizeof(T);
+  static constexpr int VEC = 16 / E;    // elements per 16-byte vector
+  static constexpr int EPL = D / 8;     // QK elements per lane
+  static constexpr int NV = EPL / VEC;  // 16-byte vectors per lane per row
+  static constexpr int PVE = D / 32;    // PV output elements per lane
+  static constexpr int LOG2G = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+  static constexpr int HSHIFT = 3 - LOG2G;  // after the butterfly lane i holds head i >> HSHIFT
+  static_assert(NV >= 1 && PVE >= 2, "unsupported head_dim");
+};
+
+template <typename T, int D, int G>
+__device__ void run_consumer_fma(const Params& p, const Pipe& pp, int warp, int lane) {
+  using C = FmaCfg<T, D, G>;
   const int hkv = p.hkv;
   const int g = warp % hkv;
   const int wsub = warp / hkv;
@@ -341,9 +532,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
   const int hs = il >> C::HSHIFT;
   const bool writer = (il & ((1 << C::HSHIFT) - 1)) == 0;
   const int head_off = g * D * C::E;
-  const int rb = p.row_bytes;
-  float* pbuf = reinterpret_cast<float*>(smem + p.off_pbuf) + warp * ST * G;
-  float* mbuf = reinterpret_cast<float*>(smem + p.off_mbuf);
+  const int rs = p.rs;
+  const int ST = p.st;
+  float* pbuf = reinterpret_cast<float*>(pp.smem + p.off_pbuf) + warp * ST * G;
+  float* mbuf = reinterpret_cast<float*>(pp.smem + p.off_mbuf);
 
   float qr[G][C::EPL];
   float acc[G][C::PVE];
@@ -353,11 +545,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
   int s = 0;
   uint32_t ph = 0, gph = 0;
   while (true) {
-    if (!mbar_wait(full_bar(s), ph, p.err)) return;
-    const int4 d = s_desc[s];
+    if (!mbar_wait(pp.full(s), ph, p.err)) return;
+    const int4 d = pp.desc[s];
     const int b = d.x, n = d.y, flags = d.z, seg = d.w;
-    const char* sK = reinterpret_cast<const char*>(smem) + (size_t)s * stage_bytes;
-    const char* sV = sK + ST * rb;
+    const char* sK = reinterpret_cast<const char*>(pp.smem) + (size_t)s * pp.stage_bytes;
+    const char* sV = sK + ST * rs;
 
     if (flags & kStart) {
       m_run = -FLT_MAX;
@@ -382,7 +574,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
     }
 
     if (n > 0) {
-      // ---- QK^T: scores of this warp's tokens, one head per lane ----
       float sc[kMaxPW];
 #pragma unroll
       for (int pi = 0; pi < kMaxPW; ++pi) {
@@ -395,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
 #pragma unroll
           for (int hh = 0; hh < G; ++hh) part[hh] = 0.f;
           if (t < n) {
-            const char* kr = sK + t * rb + head_off;
+            const char* kr = sK + t * rs + head_off;
 #pragma unroll
             for (int k = 0; k < C::NV; ++k) {
               const uint4 r = *reinterpret_cast<const uint4*>(kr + (il + 8 * k) * 16);
@@ -413,7 +604,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
         }
         sc[pi] = have ? sval : -INFINITY;
       }
-      // ---- online softmax (log2 domain) ----
       float mx = -INFINITY;
 #pragma unroll
       for (int pi = 0; pi < kMaxPW; ++pi) mx = fmaxf(mx, sc[pi]);
@@ -453,7 +643,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
       for (int hh = 0; hh < G; ++hh)
 #pragma unroll
         for (int e = 0; e < C::PVE; ++e) acc[hh][e] *= ah[hh];
-      // ---- PV ----
       const char* vbase = sV + head_off + lane * C::PVE * C::E;
 #pragma unroll
       for (int pi = 0; pi < kMaxPW; ++pi) {
@@ -464,7 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
             const int t = pass * 4 + jj;
             if (t < n) {
               float vv[C::PVE];
-              load_pv<T, C::PVE>(vbase + t * rb, vv);
+              load_pv<T, C::PVE>(vbase + t * rs, vv);
               float pr[G];
 #pragma unroll
               for (int hh = 0; hh < G; ++hh) pr[hh] = pbuf[t * G + hh];
@@ -485,9 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
         lh[hh] = __shfl_sync(kFull, l_run, hh << C::HSHIFT);
         mh[hh] = __shfl_sync(kFull, m_valid ? m_run : -INFINITY, hh << C::HSHIFT);
       }
-      bool alive = true;
       if (wph > 1) {
-        // merge the token shares of the warps serving the same kv head
         float* mw = mbuf + warp * G * (D + 2);
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
@@ -495,11 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
           for (int e = 0; e < C::PVE; ++e) mw[hh * (D + 2) + lane * C::PVE + e] = acc[hh][e];
           if (lane == 0) { mw[hh * (D + 2) + D] = mh[hh]; mw[hh * (D + 2) + D + 1] = lh[hh]; }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(group_bar);
-        alive = mbar_wait(group_bar, gph, p.err);
-        gph ^= 1;
-        if (!alive) return;
+        if (!group_sync(pp, gph, lane, p.err)) return;
         if (wsub == 0) {
 #pragma unroll
           for (int hh = 0; hh < G; ++hh) {
@@ -525,31 +708,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
             for (int e = 0; e < C::PVE; ++e) acc[hh][e] = a[e];
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(group_bar);
-        alive = mbar_wait(group_bar, gph, p.err);
-        gph ^= 1;
-        if (!alive) return;
+        if (!group_sync(pp, gph, lane, p.err)) return;
       }
       if (wsub == 0) {
-        if (flags & kSingle) {
 #pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
+        for (int hh = 0; hh < G; ++hh) {
+          const long long row_out = (long long)b * p.hq + g * G + hh;
+          const long long row_ws = (long long)seg * p.hq + g * G + hh;
+          if (flags & kSingle) {
             const float inv = lh[hh] > 0.f ? 1.f / lh[hh] : 0.f;
-            float o[C::PVE];
 #pragma unroll
-            for (int e = 0; e < C::PVE; ++e) o[e] = acc[hh][e] * inv;
-            const long long idx = ((long long)b * p.hq + g * G + hh) * D + lane * C::PVE;
-            store_out<T, C::PVE>(static_cast<char*>(p.out) + idx * C::E, o);
-          }
-        } else {
+            for (int e = 0; e < C::PVE; ++e)
+              store_elem<T>(p.out, row_out * D + lane * C::PVE + e, acc[hh][e] * inv);
+          } else {
 #pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            const long long row = (long long)seg * p.hq + g * G + hh;
-            store_f32<C::PVE>(p.ws_acc + row * D + lane * C::PVE, acc[hh]);
+            for (int e = 0; e < C::PVE; ++e) p.ws_acc[row_ws * D + lane * C::PVE + e] = acc[hh][e];
             if (lane == 0) {
-              p.ws_ml[row * 2] = mh[hh];
-              p.ws_ml[row * 2 + 1] = lh[hh];
+              p.ws_ml[row_ws * 2] = mh[hh];
+              p.ws_ml[row_ws * 2 + 1] = lh[hh];
             }
           }
         }
@@ -557,9 +733,78 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
     }
 
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty_bar(s));
-    if (++s == S) { s = 0; ph ^= 1; }
+    if (lane == 0) mbar_arrive(pp.empty(s));
+    if (++s == pp.stages) { s = 0; ph ^= 1; }
     if (flags & kLast) break;
+  }
+}
+
+// ---- the partial-pass kernel -------------------------------------------------
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Params p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  long long* s_cu = reinterpret_cast<long long*>(smem + p.off_cu);
+  long long* s_scan = reinterpret_cast<long long*>(smem + p.off_scan);
+  Pipe pp;
+  pp.smem = smem;
+  pp.desc = reinterpret_cast<int4*>(smem + p.off_desc);
+  pp.bar0 = smem_addr(smem + p.off_bar);
+  pp.stages = p.stages;
+  pp.stage_bytes = 2 * p.st * p.rs;
+
+  // ---- block counts and their exclusive scan (every CTA, same result) ----
+  const int B = p.batch;
+  const int per = (B + kThreads - 1) / kThreads;
+  const int beg = min(B, tid * per), end = min(B, beg + per);
+  const bool report = blockIdx.x == 0;
+  long long local = 0;
+  for (int b = beg; b < end; ++b) local += seq_blocks(p, b, report);
+  long long x = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_scan[warp] = x;
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(pp.full(s), 1);
+      mbar_init(pp.empty(s), kNW);
+    }
+    mbar_init(pp.group(), kNW);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  long long run = x - local;
+  for (int w = 0; w < warp; ++w) run += s_scan[w];
+  for (int b = beg; b < end; ++b) {
+    s_cu[b] = run;
+    run += seq_blocks(p, b, false);
+  }
+  long long total = 0;
+  for (int w = 0; w < kThreads / 32; ++w) total += s_scan[w];
+  if (tid == 0) s_cu[B] = total;
+  __syncthreads();
+
+  const long long W = (total + gridDim.x - 1) / gridDim.x;
+  const long long x0 = min(total, (long long)blockIdx.x * W);
+  const long long x1 = min(total, x0 + W);
+  if (blockIdx.x == 0) {
+    for (int b = tid; b <= B; b += kThreads) p.ws_cu[b] = s_cu[b];
+    if (tid == 0) { p.ws_meta[0] = W; p.ws_meta[1] = total; }
+  }
+  if (x0 >= x1) return;
+
+  if (warp == kNW) {
+    run_producer(p, pp, s_cu, lane, x0, x1);
+  } else if constexpr (sizeof(T) == 2) {
+    run_consumer_mma<D, G>(p, pp, warp, lane);
+  } else {
+    run_consumer_fma<T, D, G>(p, pp, warp, lane);
   }
 }
 
@@ -600,6 +845,8 @@ __global__ void decode_combine_kernel(const float* __restrict__ ws_acc,
   }
 }
 
+// ---- host side -----------------------------------------------------------------
+
 int stage_tokens(int bs, int row_bytes) {
   int st = 1;
   while (st * 2 <= kMaxStageTokens && st * 2 <= bs && st * 2 * row_bytes <= 32768) st *= 2;
@@ -607,7 +854,7 @@ int stage_tokens(int bs, int row_bytes) {
 }
 
 struct Layout {
-  int st, stages, smem, off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf;
+  int st, rs, stages, smem, off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf;
 };
 
 int align_up(int x, int a) { return (x + a - 1) / a * a; }
@@ -615,13 +862,15 @@ int align_up(int x, int a) { return (x + a - 1) / a * a; }
 Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int smem_optin) {
   Layout L{};
   L.st = stage_tokens(bs, row_bytes);
-  const int stage_bytes = 2 * L.st * row_bytes;
+  L.rs = row_bytes + kRowPad;
+  const int stage_bytes = 2 * L.st * L.rs;
+  const int pbuf = kNW * (L.st * G * 4 > 256 ? L.st * G * 4 : 256);
   int fixed = 0;
-  fixed += 8 * (2 * kMaxStages + 1);            // barriers
+  fixed += 8 * (2 * kMaxStages + 1);              // barriers
   fixed = align_up(fixed, 16) + 16 * kMaxStages;  // descriptors
   fixed = align_up(fixed, 16) + 8 * (batch + 1);  // cu
   fixed = align_up(fixed, 16) + 8 * 16;           // scan scratch
-  fixed = align_up(fixed, 16) + 4 * kNW * L.st * G;
+  fixed = align_up(fixed, 16) + pbuf;
   if (hkv < kNW) fixed = align_up(fixed, 16) + 4 * kNW * G * (D + 2);
   fixed = align_up(fixed, 128);
   int stages = (smem_optin - fixed) / stage_bytes;
@@ -632,7 +881,7 @@ Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int 
   off = align_up(off, 16); L.off_desc = off; off += 16 * stages;
   off = align_up(off, 16); L.off_cu = off;   off += 8 * (batch + 1);
   off = align_up(off, 16); L.off_scan = off; off += 8 * 16;
-  off = align_up(off, 16); L.off_pbuf = off; off += 4 * kNW * L.st * G;
+  off = align_up(off, 16); L.off_pbuf = off; off += pbuf;
   off = align_up(off, 16); L.off_mbuf = off;
   if (hkv < kNW) off += 4 * kNW * G * (D + 2);
   L.smem = align_up(off, 16);
@@ -657,6 +906,19 @@ WsLayout ws_layout(int batch, int hq, int D, int grid) {
   w.acc = w.ml + round256(parts * hq * 2 * 4);
   w.total = w.acc + round256(parts * hq * D * 4);
   return w;
+}
+
+// Dynamic shared memory, configured once per kernel instance and device
+// (`configured` is the caller's per-instance cache).
+template <typename K>
+cudaError_t ensure_smem(K kern, int smem, int (&configured)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && configured[dev] >= smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) configured[dev] = smem;
+  return e;
 }
 
 template <typename T, int D, int G>
@@ -687,6 +949,7 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   p.hkv = pv.num_kv_heads;
   p.bs = pv.block_size;
   p.row_bytes = pv.row_bytes;
+  p.rs = L.rs;
   p.st = L.st;
   p.stages = L.stages;
   p.qscale = a.scale * kLog2e;
@@ -698,7 +961,8 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   p.off_mbuf = L.off_mbuf;
 
   auto kern = decode_partial_kernel<T, D, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem);
+  static int configured[64] = {0};
+  cudaError_t e = ensure_smem(kern, L.smem, configured);
   if (e != cudaSuccess) return e;
   if (a.ev_start && (e = cudaEventRecord(a.ev_start, s)) != cudaSuccess) return e;
   kern<<<grid, kThreads, L.smem, s>>>(p);
