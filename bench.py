@@ -291,6 +291,28 @@ def timed(fn, steps: int, flush: torch.Tensor, events_hook=None):
     return times, inner
 
 
+def step_breakdown(st: "DecodeStep", flush: torch.Tensor, steps: int) -> dict:
+    """Eager per-call device times of the step (events between the calls)."""
+    pkv = st.pkv
+    names = ("slot_mapping", "scatter", "decode_attention")
+    acc = {n: 0.0 for n in names}
+    for _ in range(steps):
+        flush.zero_()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev[0].record()
+        pkv.build_slot_mapping(st.pool, st.bt, st.offs, st.seq, st.pos, st.slots)
+        ev[1].record()
+        pkv.write_slots(st.pool, st.w.layer, st.k_new, st.v_new, st.slots)
+        ev[2].record()
+        pkv.decode_attention(st.pool, st.w.layer, st.q, st.w.scale, st.bt, st.lens, st.offs,
+                             st.out, st.ws)
+        ev[3].record()
+        torch.cuda.synchronize()
+        for i, n in enumerate(names):
+            acc[n] += ev[i].elapsed_time(ev[i + 1])
+    return {n: round(v / steps, 4) for n, v in acc.items()}
+
+
 def run_ours(args, rank, local_rank, world):
     import paged_kv_cache_blk_gb300 as pkv
     dev = torch.device("cuda", local_rank)
@@ -364,6 +386,7 @@ def run_ours(args, rank, local_rank, world):
     h2d, d2h = st.e2e_bytes()
 
     launches = st.launches_per_step * args.steps
+    breakdown = step_breakdown(st, flush, max(10, args.steps // 4))
 
     # gather / scatter legs on their own workload
     legs = run_legs(args, dev, rank, flush, pkv)
@@ -416,6 +439,7 @@ def run_ours(args, rank, local_rank, world):
             "avg_launch_ms": round(part_ms, 4),
             "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
         },
+        "step_breakdown_ms": breakdown,
         "legs": legs,
         "e2e": {"value": round(aggregate(kv, world, e2e_ms) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,

@@ -808,41 +808,42 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
   }
 }
 
-// One CTA per sequence: merge the partial states of every segment of that
-// sequence (sequences handled by a single CTA were written already).
+// Merge the partial states of every segment of a sequence, one thread per
+// output element (sequence, q head, d); sequences handled by a single CTA were
+// written by the partial pass already.  Grid: (ceil(hq*D / 256), batch).
 template <typename T>
-__global__ void decode_combine_kernel(const float* __restrict__ ws_acc,
-                                      const float* __restrict__ ws_ml,
-                                      const long long* __restrict__ ws_cu,
-                                      const long long* __restrict__ ws_meta, int hq, int D,
-                                      T* __restrict__ out) {
-  const int b = blockIdx.x;
+__global__ void __launch_bounds__(256) decode_combine_kernel(const float* __restrict__ ws_acc,
+                                                             const float* __restrict__ ws_ml,
+                                                             const long long* __restrict__ ws_cu,
+                                                             const long long* __restrict__ ws_meta,
+                                                             int hq, int D, T* __restrict__ out) {
+  const int b = blockIdx.y;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= hq * D) return;
   const long long c0 = ws_cu[b], c1 = ws_cu[b + 1];
   T* o = out + (long long)b * hq * D;
   if (c1 <= c0) {  // no tokens (or an invalid sequence): zeros
-    for (int i = threadIdx.x; i < hq * D; i += blockDim.x) o[i] = T(0.f);
+    o[i] = T(0.f);
     return;
   }
   const long long W = ws_meta[0];
   const long long cf = c0 / W, cl = (c1 - 1) / W;
   if (cf == cl) return;
-  for (int i = threadIdx.x; i < hq * D; i += blockDim.x) {
-    const int h = i / D, d = i - h * D;
-    float M = -INFINITY;
-    for (long long c = cf; c <= cl; ++c) M = fmaxf(M, ws_ml[((c + b) * hq + h) * 2]);
-    float num = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-      for (long long c = cf; c <= cl; ++c) {
-        const long long row = (c + b) * hq + h;
-        const float m = ws_ml[row * 2];
-        if (m == -INFINITY) continue;
-        const float w = exp2f(m - M);
-        num += w * ws_acc[row * D + d];
-        den += w * ws_ml[row * 2 + 1];
-      }
+  const int h = i / D, d = i - h * D;
+  float M = -INFINITY;
+  for (long long c = cf; c <= cl; ++c) M = fmaxf(M, ws_ml[((c + b) * hq + h) * 2]);
+  float num = 0.f, den = 0.f;
+  if (M != -INFINITY) {
+    for (long long c = cf; c <= cl; ++c) {
+      const long long row = (c + b) * hq + h;
+      const float m = ws_ml[row * 2];
+      if (m == -INFINITY) continue;
+      const float w = exp2f(m - M);
+      num += w * ws_acc[row * D + d];
+      den += w * ws_ml[row * 2 + 1];
     }
-    o[i] = T(den > 0.f ? num / den : 0.f);
   }
+  o[i] = T(den > 0.f ? num / den : 0.f);
 }
 
 // ---- host side -----------------------------------------------------------------
@@ -969,8 +970,9 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (a.ev_stop && (e = cudaEventRecord(a.ev_stop, s)) != cudaSuccess) return e;
-  decode_combine_kernel<T><<<a.batch, 128, 0, s>>>(p.ws_acc, p.ws_ml, p.ws_cu, p.ws_meta, p.hq, D,
-                                                   static_cast<T*>(a.out));
+  const dim3 cgrid((p.hq * D + 255) / 256, a.batch);
+  decode_combine_kernel<T><<<cgrid, 256, 0, s>>>(p.ws_acc, p.ws_ml, p.ws_cu, p.ws_meta, p.hq, D,
+                                                 static_cast<T*>(a.out));
   return cudaGetLastError();
 }
 
