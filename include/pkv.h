@@ -177,6 +177,40 @@ PKV_API pkv_status pkv_decode_attention(const pkv_pool* pool, int32_t layer, con
                                 int32_t batch, void* out, void* workspace,
                                 size_t workspace_bytes, cudaStream_t stream);
 
+/* Allocation-free paged decode attention.  The paper has no counterpart:
+ * this is a library convenience.  Same computation, arguments, results and
+ * error behaviour as pkv_decode_attention, except that the caller passes no
+ * workspace: the split-K scratch lives in a fixed device array defined inside
+ * libpkv (PKV_DECODE_STATIC_SCRATCH_BYTES per GPU, held by every GPU that
+ * loads the library until the process exits).
+ *
+ * It is meant for callers that cannot allocate device memory where they run
+ * decode attention: code that runs while a stream is being captured in
+ * global capture mode (cudaMalloc is refused there), serving hosts and
+ * plugin runtimes that own all device memory and forbid allocation on the
+ * hot path, and plain C programs that link only this library and have no
+ * device allocator for scratch.  The call itself allocates nothing.
+ *
+ * Limits and rules:
+ *   - A shape whose scratch (pkv_decode_workspace_size for the same batch,
+ *     num_q_heads and head_dim) exceeds PKV_DECODE_STATIC_SCRATCH_BYTES is
+ *     refused with PKV_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on a device looks up the array's device address for that
+ *     device; make that first call before any stream capture starts.
+ *   - All calls on a device share the one array: calls whose kernels overlap
+ *     on the GPU (different streams, or concurrent host threads) race and
+ *     give wrong results.  Calls on one stream are ordered and safe.  The
+ *     array keeps the previous call's contents; nothing in it needs to start
+ *     at zero (every scratch word is written before it is read). */
+#define PKV_DECODE_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+PKV_API pkv_status pkv_decode_attention_static(const pkv_pool* pool, int32_t layer,
+                                               const void* q, int32_t num_q_heads, float scale,
+                                               const int32_t* block_tables,
+                                               int32_t max_blocks_per_seq,
+                                               const int32_t* seq_lens, const int32_t* offsets,
+                                               int32_t batch, void* out, cudaStream_t stream);
+
 /* Number of CTAs the decode partial pass uses on the current device; 0 (the
  * default) means one per SM.  A positive value forces that grid size, which
  * changes how sequences are split (1 = no split).  Process-wide. */

@@ -8,6 +8,7 @@ from ._binding import (  # noqa: F401
     STATUS_CODES,
     build_slot_mapping,
     decode_attention,
+    decode_attention_static,
     decode_workspace_size,
     device_error,
     gather,

@@ -55,6 +55,8 @@ _SIGS = {
     "pkv_decode_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "pkv_decode_attention": (_I32, [_P, _I32, _P, _I32, _F32, _P, _I32, _P, _P, _I32, _P, _P,
                                     _SZ, _P]),
+    "pkv_decode_attention_static": (_I32, [_P, _I32, _P, _I32, _F32, _P, _I32, _P, _P, _I32,
+                                           _P, _P]),
     "pkv_set_decode_ctas": (_I32, [_I32]),
     "pkv_set_decode_events": (_I32, [_P, _P]),
     "pkv_set_validate": (_I32, [_I32]),
@@ -206,6 +208,22 @@ def decode_attention(pool: Pool, layer: int, q: torch.Tensor, scale: float,
                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _stream(pool.device))
     _check(st, "pkv_decode_attention")
+
+
+def decode_attention_static(pool: Pool, layer: int, q: torch.Tensor, scale: float,
+                            block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                            offsets: Optional[torch.Tensor], out: torch.Tensor) -> None:
+    """Paged decode attention without a workspace argument: the library keeps
+    the scratch in its own fixed device array (for callers that cannot
+    allocate device memory where they run; shapes beyond the array's size
+    raise PKV_ERR_WORKSPACE, and calls that overlap on the GPU race)."""
+    lib = load()
+    with _dev(pool):
+        st = lib.pkv_decode_attention_static(pool.ref, layer, _ptr(q), q.shape[1], float(scale),
+                                             _ptr(block_tables), block_tables.shape[1],
+                                             _ptr(seq_lens), _ptr(offsets), seq_lens.numel(),
+                                             _ptr(out), _stream(pool.device))
+    _check(st, "pkv_decode_attention_static")
 
 
 def set_decode_ctas(n: int) -> None:

@@ -143,6 +143,25 @@ int decode_grid(const DevInfo& d) {
 
 }  // namespace
 
+namespace pkv {
+
+int device_facts(int* smem_optin, int** err_word, int* grid, int* validate) {
+  DevInfo* d;
+  const pkv_status st = current_device(&d);
+  if (st != PKV_OK) return st;
+  *smem_optin = d->smem_optin;
+  *err_word = d->err;
+  *grid = decode_grid(*d);
+  *validate = g_validate.load();
+  return PKV_OK;
+}
+
+int clear_error_word(int* err, cudaStream_t s) { return clear_word(err, s); }
+
+int read_and_clear_error_word(int* err, cudaStream_t s) { return read_and_clear(err, s); }
+
+}  // namespace pkv
+
 extern "C" {
 
 pkv_status pkv_build_slot_mapping(const pkv_pool* pool, const int32_t* block_tables,

@@ -185,4 +185,12 @@ size_t decode_workspace_bytes(int batch, int num_q_heads, int head_dim, int grid
 int decode_supported(const PoolView& p, int num_q_heads);
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s);
 
+// Current-device facts for entry points defined outside api.cu: dynamic
+// shared memory limit, the sticky error word, the decode grid size and the
+// validate flag.  Returns a pkv_status value.
+int device_facts(int* smem_optin, int** err_word, int* decode_grid, int* validate);
+// Validate-mode helpers of api.cu (pkv_status values).
+int clear_error_word(int* err, cudaStream_t s);
+int read_and_clear_error_word(int* err, cudaStream_t s);
+
 }  // namespace pkv
