@@ -327,7 +327,7 @@ pkv_status pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void*
 }
 
 pkv_status pkv_set_decode_ctas(int32_t num_ctas) {
-  if (num_ctas < 0) return PKV_ERR_INVALID_ARG;
+  if (num_ctas < 0 || num_ctas > 65536) return PKV_ERR_INVALID_ARG;
   g_decode_ctas.store(num_ctas);
   return PKV_OK;
 }
