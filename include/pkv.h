@@ -161,10 +161,12 @@ PKV_API size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int
  *     out[b][h] = sum_i softmax(s)_i * V_i[g].
  * q, out: [batch, num_q_heads, head_dim] contiguous in the pool dtype.
  * seq_lens[b] == 0 gives an all-zero row.  Accumulation is fp32.
- * The work is split along the sequence across the GPU in one kernel launch;
- * partial softmax states go to `workspace` (>= pkv_decode_workspace_size
- * bytes; its contents need no initialisation and are overwritten) and the
- * CTA that finishes a sequence's last segment merges them (split-K combine).  Supported: head_dim 64 or 128; num_kv_heads 1, 2, 4 or 8;
+ * The work is split along the sequence across the GPU; partial softmax
+ * states go to `workspace` (>= pkv_decode_workspace_size bytes, contents
+ * need no initialisation and are overwritten) and a second kernel combines
+ * them.  Both kernels are launched as programmatic dependents of the work
+ * before them on the stream and wait for it before reading any input, so the
+ * call may be captured in a CUDA graph and replayed.  Supported: head_dim 64 or 128; num_kv_heads 1, 2, 4 or 8;
  * num_q_heads / num_kv_heads 1, 2, 4 or 8; either dtype; any block_size the
  * pool allows.  Others return PKV_ERR_UNSUPPORTED.  A sequence whose offset
  * is out of range or whose length exceeds its table row's capacity is

@@ -90,6 +90,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// ---- programmatic dependent launch -------------------------------------------
+// Every kernel of the library starts with griddep_wait(): when it was launched
+// as a programmatic dependent, this waits until the grids before it on the
+// stream have completed and their memory is visible (a no-op otherwise).  It
+// then lets its own dependents launch early; they wait the same way.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- element conversion ------------------------------------------------------
 // bf16 is the upper half of an IEEE fp32 word, so widening is a shift.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -120,6 +132,24 @@ __device__ __forceinline__ void st_global(void* p, const uint4& v) {
 
 // ---- internal launch interface (host side, C++ linkage) ---------------------
 namespace pkv {
+
+// Launch `kern` on `s`; with `pdl` as a programmatic dependent of the work
+// before it (the kernel must call griddep_wait() before reading inputs).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
 struct PoolView {
   const char* k;  // k_cache bytes

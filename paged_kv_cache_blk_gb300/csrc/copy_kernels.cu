@@ -64,6 +64,8 @@ __global__ void slot_mapping_kernel(const int32_t* __restrict__ bt, int mb,
                                     const int32_t* __restrict__ tok_pos, long long n,
                                     long long num_blocks, int bs, int64_t* __restrict__ slots,
                                     int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n;
        t += (long long)gridDim.x * blockDim.x) {
     const int b = tok_seq[t];
@@ -95,6 +97,8 @@ __global__ void __launch_bounds__(kCopyThreads) write_slots_kernel(
     char* __restrict__ kc, char* __restrict__ vc, const char* __restrict__ k_new,
     const char* __restrict__ v_new, const int64_t* __restrict__ slots, long long n,
     long long num_blocks, int L, int layer, int bs, int row_bytes, int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long warps = (long long)gridDim.x * kCopyWarps;
   const int row_vecs = row_bytes >> 4;
@@ -123,6 +127,8 @@ __global__ void __launch_bounds__(kCopyThreads) gather_kernel(
     int mb, const int32_t* __restrict__ offs, int batch, const int64_t* __restrict__ cu,
     long long total, char* __restrict__ k_out, char* __restrict__ v_out, long long num_blocks,
     int L, int layer, int bs, int row_bytes, int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int row_vecs = row_bytes >> 4;
   const long long warps = (long long)gridDim.x * kCopyWarps;
@@ -165,6 +171,8 @@ __global__ void validate_tables_kernel(const int32_t* __restrict__ bt, int mb,
                                        const int32_t* __restrict__ offs, int batch,
                                        const int64_t* __restrict__ cu, long long total,
                                        long long num_blocks, int bs, int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
   for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < batch; b += gridDim.x * blockDim.x) {
     const int off = offs ? offs[b] : 0;
     const int len = lens ? lens[b] : 0;
@@ -190,6 +198,8 @@ __global__ void validate_tables_kernel(const int32_t* __restrict__ bt, int mb,
 
 __global__ void validate_slots_kernel(const int64_t* __restrict__ slots, long long n,
                                       long long limit, int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n;
        t += (long long)gridDim.x * blockDim.x) {
     const int64_t s = slots[t];
@@ -202,6 +212,8 @@ __global__ void validate_tokens_kernel(const int32_t* __restrict__ bt, int mb,
                                        const int32_t* __restrict__ tok_seq,
                                        const int32_t* __restrict__ tok_pos, long long n,
                                        long long num_blocks, int bs, int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n;
        t += (long long)gridDim.x * blockDim.x) {
     const int b = tok_seq[t];
@@ -229,9 +241,9 @@ cudaError_t launch_slot_mapping(const PoolView& p, const int32_t* bt, int mb, co
                                 int batch, const int32_t* tok_seq, const int32_t* tok_pos,
                                 long long n, int64_t* slots, int* err, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  slot_mapping_kernel<<<grid_for(n, 256, 1 << 20), 256, 0, s>>>(
-      bt, mb, offs, batch, tok_seq, tok_pos, n, p.num_blocks, p.block_size, slots, err);
-  return cudaGetLastError();
+  return launch_kernel(slot_mapping_kernel, dim3(grid_for(n, 256, 1 << 20)), dim3(256), 0, s, true,
+                       bt, mb, offs, batch, tok_seq, tok_pos, n, p.num_blocks, p.block_size, slots,
+                       err);
 }
 
 cudaError_t launch_write_slots(const PoolView& p, int layer, const void* k_new, const void* v_new,
@@ -239,21 +251,20 @@ cudaError_t launch_write_slots(const PoolView& p, int layer, const void* k_new, 
                                cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   (void)sm_count;
-  write_slots_kernel<<<grid_for(n, kCopyWarps, 1 << 24), kCopyThreads, 0, s>>>(
-      p.k_mut, p.v_mut, static_cast<const char*>(k_new), static_cast<const char*>(v_new), slots, n,
-      p.num_blocks, p.num_layers, layer, p.block_size, p.row_bytes, err);
-  return cudaGetLastError();
+  return launch_kernel(write_slots_kernel, dim3(grid_for(n, kCopyWarps, 1 << 24)),
+                       dim3(kCopyThreads), 0, s, true, p.k_mut, p.v_mut,
+                       static_cast<const char*>(k_new), static_cast<const char*>(v_new), slots, n,
+                       p.num_blocks, p.num_layers, layer, p.block_size, p.row_bytes, err);
 }
 
 cudaError_t launch_gather(const PoolView& p, int layer, const int32_t* bt, int mb,
                           const int32_t* offs, int batch, const int64_t* cu, long long total,
                           void* k_out, void* v_out, int* err, cudaStream_t s) {
   if (total == 0 || batch == 0) return cudaSuccess;
-  gather_kernel<<<grid_for(total, kCopyWarps, 1 << 24), kCopyThreads, 0, s>>>(
-      p.k, p.v, bt, mb, offs, batch, cu, total, static_cast<char*>(k_out),
-      static_cast<char*>(v_out), p.num_blocks, p.num_layers, layer, p.block_size, p.row_bytes,
-      err);
-  return cudaGetLastError();
+  return launch_kernel(gather_kernel, dim3(grid_for(total, kCopyWarps, 1 << 24)),
+                       dim3(kCopyThreads), 0, s, true, p.k, p.v, bt, mb, offs, batch, cu, total,
+                       static_cast<char*>(k_out), static_cast<char*>(v_out), p.num_blocks,
+                       p.num_layers, layer, p.block_size, p.row_bytes, err);
 }
 
 cudaError_t launch_validate_tables(const PoolView& p, const int32_t* bt, int mb,

@@ -36,18 +36,11 @@
 //        output elements for PV).
 //  * At a segment end the warp either writes the normalised output (sequence
 //    entirely inside this CTA) or the partial state (m, l, acc) to the
-//    workspace.  Split-K combine in the same launch: each CTA counts its
-//    arrival on the sequence's arrival word (tagged with the launch's epoch,
-//    so the workspace needs no clearing), and the CTA that completes the
-//    count merges every segment with the log-sum-exp rule
-//    out = sum_c 2^(m_c-M) acc_c / sum_c 2^(m_c-M) l_c.  A segment's
-//    sequence ends the CTA's range exactly when the CTA is not its last
-//    owner, so merges happen at the ends of the ranges.
+//    workspace; the combine kernel merges partial states with the log-sum-exp
+//    rule  out = sum_c 2^(m_c-M) acc_c / sum_c 2^(m_c-M) l_c.
 //  * Every mbarrier wait is bounded (mbar_wait); a wait that gives up sets the
 //    error word and the warp leaves after the producer has drained its copies.
-#include <atomic>
 #include <cfloat>
-#include <chrono>
 #include <cmath>
 
 #include "common.cuh"
@@ -78,13 +71,13 @@ struct Params {
   const int32_t* offs;
   float* ws_acc;
   float* ws_ml;
-  unsigned long long* ws_ctr;  // per-sequence arrival words (epoch << 24 | count)
-  unsigned long long epoch;    // this launch's tag, 40 bits, never 0
+  long long* ws_cu;
+  long long* ws_meta;
   int* err;
   int mb, batch, hq, hkv, bs, row_bytes, rs, st, stages;
   float qscale;
   // shared-memory carve (bytes from the start of dynamic smem)
-  int off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf, off_merge;
+  int off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf;
 };
 
 // ---- small helpers ----------------------------------------------------------
@@ -208,11 +201,6 @@ struct Pipe {
   uint32_t bar0;
   int stages;
   int stage_bytes;
-  const long long* cu;  // block-count prefix sums (shared memory)
-  long long W;          // blocks per CTA range
-  volatile int* flag;   // "this CTA merges the sequence" (shared memory)
-  float* sM;            // per-head max and 1/sum for a merge (shared memory)
-  float* sInv;
   __device__ uint32_t full(int s) const { return bar0 + 8u * s; }
   __device__ uint32_t empty(int s) const { return bar0 + 8u * (stages + s); }
   __device__ uint32_t group() const { return bar0 + 8u * (2 * stages); }
@@ -226,77 +214,6 @@ __device__ __forceinline__ bool group_sync(const Pipe& pp, uint32_t& gph, int la
   const bool ok = mbar_wait(pp.group(), gph, err);
   gph ^= 1;
   return ok;
-}
-
-// Count this CTA's arrival at sequence b's arrival word for launch `epoch`
-// and return the number of arrivals so far.  A word left by another launch
-// carries another epoch and restarts at 1, so the workspace needs no
-// clearing.  The compare-and-swap retries only under contention from the
-// other CTAs of the same sequence; the bound only guards against a broken
-// invariant.
-__device__ __forceinline__ unsigned arrive_count(unsigned long long* ctr, unsigned long long epoch,
-                                                 int* err) {
-  unsigned long long old = atomicAdd(ctr, 0ull);
-  for (int it = 0; it < (1 << 20); ++it) {
-    const unsigned long long want = ((old >> 24) == epoch) ? old + 1 : ((epoch << 24) | 1ull);
-    const unsigned long long prev = atomicCAS(ctr, old, want);
-    if (prev == old) return (unsigned)(want & 0xFFFFFFull);
-    old = prev;
-  }
-  set_error(err, kErrTimeout);
-  return 0;
-}
-
-// Split-K combine, fused into the partial pass.  Called by all consumer warps
-// after a segment end whose sequence b spans several CTAs (its partial state
-// is already in the workspace).  The CTA whose arrival completes b merges
-// every segment of b with the log-sum-exp rule:
-//   out = sum_c 2^(m_c - M) acc_c / sum_c 2^(m_c - M) l_c,  M = max_c m_c.
-template <typename T, int D>
-__device__ bool segment_done(const Params& p, const Pipe& pp, int b, int warp, int lane,
-                             uint32_t& gph) {
-  if (!group_sync(pp, gph, lane, p.err)) return false;  // all heads' partials written
-  const long long cf = pp.cu[b] / pp.W, cl = (pp.cu[b + 1] - 1) / pp.W;
-  if (warp == 0 && lane == 0) {
-    __threadfence();
-    const unsigned n = arrive_count(p.ws_ctr + b, p.epoch, p.err);
-    *pp.flag = (n == (unsigned)(cl - cf + 1)) ? 1 : 0;
-    __threadfence();
-  }
-  if (!group_sync(pp, gph, lane, p.err)) return false;
-  if (*pp.flag == 0) return true;
-  const int t = warp * 32 + lane;
-  const int nthr = kNW * 32;
-  const int hq = p.hq;
-  for (int h = t; h < hq; h += nthr) {
-    float M = -INFINITY;
-    for (long long c = cf; c <= cl; ++c) M = fmaxf(M, __ldcg(p.ws_ml + ((c + b) * hq + h) * 2));
-    float L = 0.f;
-    if (M != -INFINITY) {
-      for (long long c = cf; c <= cl; ++c) {
-        const long long row = (c + b) * hq + h;
-        const float m = __ldcg(p.ws_ml + row * 2);
-        if (m != -INFINITY) L += exp2f(m - M) * __ldcg(p.ws_ml + row * 2 + 1);
-      }
-    }
-    pp.sM[h] = M;
-    pp.sInv[h] = L > 0.f ? 1.f / L : 0.f;
-  }
-  if (!group_sync(pp, gph, lane, p.err)) return false;
-  for (int i = t; i < hq * D; i += nthr) {
-    const int h = i / D, d = i - h * D;
-    const float M = pp.sM[h];
-    float a = 0.f;
-    if (M != -INFINITY) {
-      for (long long c = cf; c <= cl; ++c) {
-        const long long row = (c + b) * hq + h;
-        const float m = __ldcg(p.ws_ml + row * 2);
-        if (m != -INFINITY) a += exp2f(m - M) * __ldcg(p.ws_acc + row * D + d);
-      }
-    }
-    store_elem<T>(p.out, (long long)b * hq * D + i, a * pp.sInv[h]);
-  }
-  return group_sync(pp, gph, lane, p.err);  // sM / sInv free again
 }
 
 // ---- producer warp -----------------------------------------------------------
@@ -580,7 +497,6 @@ __device__ void run_consumer_mma(const Params& p, const Pipe& pp, int warp, int 
           }
         }
       }
-      if (!(flags & kSingle) && !segment_done<__nv_bfloat16, D>(p, pp, b, warp, lane, gph)) return;
     }
 
     __syncwarp();
@@ -814,7 +730,6 @@ __device__ void run_consumer_fma(const Params& p, const Pipe& pp, int warp, int 
           }
         }
       }
-      if (!(flags & kSingle) && !segment_done<T, D>(p, pp, b, warp, lane, gph)) return;
     }
 
     __syncwarp();
@@ -829,6 +744,8 @@ __device__ void run_consumer_fma(const Params& p, const Pipe& pp, int warp, int 
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
+  griddep_wait();
+  griddep_launch_dependents();
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
 
@@ -878,16 +795,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
   const long long W = (total + gridDim.x - 1) / gridDim.x;
   const long long x0 = min(total, (long long)blockIdx.x * W);
   const long long x1 = min(total, x0 + W);
-  pp.cu = s_cu;
-  pp.W = W;
-  pp.flag = reinterpret_cast<volatile int*>(smem + p.off_merge);
-  pp.sM = reinterpret_cast<float*>(smem + p.off_merge + 16);
-  pp.sInv = pp.sM + p.hq;
-  // sequences without tokens (or invalid ones) get an all-zero output row
-  for (int b = blockIdx.x; b < B; b += gridDim.x) {
-    if (s_cu[b + 1] != s_cu[b]) continue;
-    const long long base = (long long)b * p.hq * D;
-    for (int i = tid; i < p.hq * D; i += kThreads) store_elem<T>(p.out, base + i, 0.f);
+  if (blockIdx.x == 0) {
+    for (int b = tid; b <= B; b += kThreads) p.ws_cu[b] = s_cu[b];
+    if (tid == 0) { p.ws_meta[0] = W; p.ws_meta[1] = total; }
   }
   if (x0 >= x1) return;
 
@@ -900,6 +810,67 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
   }
 }
 
+// Merge the partial states of every segment of a sequence, one thread per
+// output element (sequence, q head, d); sequences handled by a single CTA were
+// written by the partial pass already.  Segments are read eight at a time so
+// the loads of a batch are in flight together.  Grid: (ceil(hq*D / 256), batch).
+template <typename T>
+__global__ void __launch_bounds__(256) decode_combine_kernel(const float* __restrict__ ws_acc,
+                                                             const float* __restrict__ ws_ml,
+                                                             const long long* __restrict__ ws_cu,
+                                                             const long long* __restrict__ ws_meta,
+                                                             int hq, int D, T* __restrict__ out) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int b = blockIdx.y;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= hq * D) return;
+  const long long c0 = ws_cu[b], c1 = ws_cu[b + 1];
+  T* o = out + (long long)b * hq * D;
+  if (c1 <= c0) {  // no tokens (or an invalid sequence): zeros
+    o[i] = T(0.f);
+    return;
+  }
+  const long long W = ws_meta[0];
+  const long long cf = c0 / W, cl = (c1 - 1) / W;
+  if (cf == cl) return;
+  const int n = (int)(cl - cf + 1);
+  const int h = i / D, d = i - h * D;
+  const long long ml_stride = (long long)hq * 2, acc_stride = (long long)hq * D;
+  const float* mlp = ws_ml + ((cf + b) * hq + h) * 2;
+  const float* accp = ws_acc + ((cf + b) * hq + h) * D + d;
+  constexpr int U = 8;
+  float M = -INFINITY;
+  for (int k0 = 0; k0 < n; k0 += U) {
+    float mv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) mv[u] = k0 + u < n ? mlp[(k0 + u) * ml_stride] : -INFINITY;
+#pragma unroll
+    for (int u = 0; u < U; ++u) M = fmaxf(M, mv[u]);
+  }
+  float num = 0.f, den = 0.f;
+  if (M != -INFINITY) {
+    for (int k0 = 0; k0 < n; k0 += U) {
+      float mv[U], lv[U], av[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const bool in = k0 + u < n;
+        mv[u] = in ? mlp[(k0 + u) * ml_stride] : -INFINITY;
+        lv[u] = in ? mlp[(k0 + u) * ml_stride + 1] : 0.f;
+        av[u] = in ? accp[(k0 + u) * acc_stride] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (mv[u] == -INFINITY) continue;
+        const float w = exp2f(mv[u] - M);
+        num += w * av[u];
+        den += w * lv[u];
+      }
+    }
+  }
+  o[i] = T(den > 0.f ? num / den : 0.f);
+}
+
 // ---- host side -----------------------------------------------------------------
 
 int stage_tokens(int bs, int row_bytes) {
@@ -909,13 +880,12 @@ int stage_tokens(int bs, int row_bytes) {
 }
 
 struct Layout {
-  int st, rs, stages, smem, off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf, off_merge;
+  int st, rs, stages, smem, off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf;
 };
 
 int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int hq,
-                   int smem_optin) {
+Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int smem_optin) {
   Layout L{};
   L.st = stage_tokens(bs, row_bytes);
   L.rs = row_bytes + kRowPad;
@@ -928,7 +898,6 @@ Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int 
   fixed = align_up(fixed, 16) + 8 * 16;           // scan scratch
   fixed = align_up(fixed, 16) + pbuf;
   if (hkv < kNW) fixed = align_up(fixed, 16) + 4 * kNW * G * (D + 2);
-  fixed = align_up(fixed, 16) + 16 + 8 * hq;      // merge flag, per-head max and 1/sum
   fixed = align_up(fixed, 128);
   int stages = (smem_optin - fixed) / stage_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
@@ -941,16 +910,15 @@ Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int 
   off = align_up(off, 16); L.off_pbuf = off; off += pbuf;
   off = align_up(off, 16); L.off_mbuf = off;
   if (hkv < kNW) off += 4 * kNW * G * (D + 2);
-  off = align_up(off, 16); L.off_merge = off; off += 16 + 8 * hq;
   L.smem = align_up(off, 16);
   return L;
 }
 
-// Workspace carve (bytes): arrival words [batch] (u64) | (m, l) per
-// (segment, q head) | acc per (segment, q head, d); segments are indexed
-// c + b, so grid + batch of them suffice.
+// Workspace carve (bytes): meta [W, total] | cu[batch+1] (int64) |
+// (m, l) per (segment, q head) | acc per (segment, q head, d); segments are
+// indexed c + b, so grid + batch of them suffice.
 struct WsLayout {
-  size_t ctr, ml, acc, total;
+  size_t meta, cu, ml, acc, total;
 };
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
@@ -958,31 +926,12 @@ size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 WsLayout ws_layout(int batch, int hq, int D, int grid) {
   WsLayout w{};
   const size_t parts = (size_t)grid + (size_t)batch;
-  w.ctr = 0;
-  w.ml = round256(8 * (size_t)batch);
+  w.meta = 0;
+  w.cu = 256;
+  w.ml = w.cu + round256(8 * ((size_t)batch + 1));
   w.acc = w.ml + round256(parts * hq * 2 * 4);
   w.total = w.acc + round256(parts * hq * D * 4);
   return w;
-}
-
-// Launch tags for the arrival words: a 40-bit counter from a per-process
-// random start, skipping 0.
-unsigned long long next_epoch() {
-  static std::atomic<unsigned long long> counter{[] {
-    unsigned long long x = (unsigned long long)std::chrono::steady_clock::now()
-                               .time_since_epoch()
-                               .count() ^
-                           (unsigned long long)(uintptr_t)&counter;
-    x += 0x9e3779b97f4a7c15ull;  // splitmix64 finaliser
-    x = (x ^ (x >> 30)) * 0xbf58476d1ce4e5b9ull;
-    x = (x ^ (x >> 27)) * 0x94d049bb133111ebull;
-    return x ^ (x >> 31);
-  }()};
-  unsigned long long e;
-  do {
-    e = counter.fetch_add(1) & ((1ull << 40) - 1);
-  } while (e == 0);
-  return e;
 }
 
 // Dynamic shared memory, configured once per kernel instance and device
@@ -1015,8 +964,8 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   const int grid = a.grid;
   const WsLayout W = ws_layout(a.batch, a.num_q_heads, pv.head_dim, grid);
   char* ws = static_cast<char*>(a.workspace);
-  p.ws_ctr = reinterpret_cast<unsigned long long*>(ws + W.ctr);
-  p.epoch = next_epoch();
+  p.ws_meta = reinterpret_cast<long long*>(ws + W.meta);
+  p.ws_cu = reinterpret_cast<long long*>(ws + W.cu);
   p.ws_ml = reinterpret_cast<float*>(ws + W.ml);
   p.ws_acc = reinterpret_cast<float*>(ws + W.acc);
   p.err = a.err;
@@ -1036,18 +985,22 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   p.off_scan = L.off_scan;
   p.off_pbuf = L.off_pbuf;
   p.off_mbuf = L.off_mbuf;
-  p.off_merge = L.off_merge;
 
   auto kern = decode_partial_kernel<T, D, G>;
   static int configured[64] = {0};
   cudaError_t e = ensure_smem(kern, L.smem, configured);
   if (e != cudaSuccess) return e;
+  // programmatic dependent launches, except when the caller times the partial
+  // pass alone with events (an event between kernels ends the overlap)
+  const bool pdl = a.ev_start == nullptr && a.ev_stop == nullptr;
   if (a.ev_start && (e = cudaEventRecord(a.ev_start, s)) != cudaSuccess) return e;
-  kern<<<grid, kThreads, L.smem, s>>>(p);
-  e = cudaGetLastError();
+  e = launch_kernel(kern, dim3(grid), dim3(kThreads), L.smem, s, pdl, p);
   if (e != cudaSuccess) return e;
   if (a.ev_stop && (e = cudaEventRecord(a.ev_stop, s)) != cudaSuccess) return e;
-  return cudaSuccess;
+  const dim3 cgrid((p.hq * D + 255) / 256, a.batch);
+  return launch_kernel(decode_combine_kernel<T>, cgrid, dim3(256), 0, s, pdl,
+                       (const float*)p.ws_acc, (const float*)p.ws_ml, (const long long*)p.ws_cu,
+                       (const long long*)p.ws_meta, p.hq, D, static_cast<T*>(a.out));
 }
 
 template <typename T, int D>
@@ -1082,7 +1035,7 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s) {
   const PoolView& pv = a.pool;
   const int G = a.num_q_heads / pv.num_kv_heads;
   const Layout L = make_layout(pv.block_size, pv.row_bytes, pv.num_kv_heads, G, pv.head_dim,
-                               a.batch, a.num_q_heads, a.smem_optin);
+                               a.batch, a.smem_optin);
   if (L.stages < 2) return cudaErrorInvalidConfiguration;
   if (pv.elem_size == 2) {
     return pv.head_dim == 128 ? run_g<__nv_bfloat16, 128>(a, L, G, s)

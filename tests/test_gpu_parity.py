@@ -351,3 +351,55 @@ def test_decode_events_hook(dev):
         pkv.set_decode_events(None, None)
     torch.cuda.synchronize()
     assert e0.elapsed_time(e1) > 0
+
+
+def test_cuda_graph_replay_with_changing_inputs(dev):
+    """A decode step captured once in a CUDA graph and replayed with new
+    queries and new token rows each time must match the oracle every time
+    (nothing launch-specific may be baked into the graph)."""
+    w = small_workload(seed=91, num_blocks=256, num_layers=2, block_size=16, num_kv_heads=8,
+                       head_dim=128, dtype="bf16", batch=6, min_len=40, max_len=900,
+                       num_q_heads=32, offsets=True)
+    k, v = make_pools(w, dev)
+    pool = pkv.Pool(k, v)
+    bt, lens, offs, _ = dev_batch(w.batch, dev)
+    B = w.batch.batch
+    # the step appends the last token of every sequence, then attends
+    seq = torch.arange(B, dtype=torch.int32, device=dev)
+    pos = lens - 1
+    q = torch.empty((B, 32, 128), dtype=torch.bfloat16, device=dev)
+    kn = torch.empty((B, 8, 128), dtype=torch.bfloat16, device=dev)
+    vn = torch.empty_like(kn)
+    out = torch.empty_like(q)
+    slots = torch.empty(B, dtype=torch.int64, device=dev)
+    ws = torch.empty(pkv.decode_workspace_size(B, 32, 128, dev), dtype=torch.uint8, device=dev)
+
+    def step():
+        pkv.build_slot_mapping(pool, bt, offs, seq, pos, slots)
+        pkv.write_slots(pool, w.layer, kn, vn, slots)
+        pkv.decode_attention(pool, w.layer, q, w.scale, bt, lens, offs, out, ws)
+
+    q.copy_(rand_rows(q.shape, "bf16", 1, dev)); kn.copy_(rand_rows(kn.shape, "bf16", 2, dev))
+    vn.copy_(rand_rows(vn.shape, "bf16", 3, dev))
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    kh, vh = host_layer(k, w.layer), host_layer(v, w.layer)
+    tokens = TokenStream(np.arange(B, dtype=np.int32), (w.batch.seq_lens - 1).astype(np.int32))
+    sm_ref = oracle.build_slot_mapping(w.batch.block_tables, w.batch.offsets, tokens.token_seq,
+                                       tokens.token_pos, 16)
+    for r in range(4):
+        q.copy_(rand_rows(q.shape, "bf16", 10 + r, dev))
+        kn.copy_(rand_rows(kn.shape, "bf16", 20 + r, dev))
+        vn.copy_(rand_rows(vn.shape, "bf16", 30 + r, dev))
+        graph.replay()
+        torch.cuda.synchronize()
+        oracle.write_slots(kh, vh, 0, to_numpy_bits(kn), to_numpy_bits(vn), sm_ref)
+        ref = oracle.decode_attention(kh, vh, 0, to_numpy_bits(q), w.batch.block_tables,
+                                      w.batch.seq_lens, w.batch.offsets, w.scale)
+        assert max_abs(widen_out(out), ref) <= 2e-2, r
