@@ -114,15 +114,23 @@ def kernel_source_hash() -> str:
 def recorded_traffic():
     """DRAM bytes per launch of the decode partial kernel from the committed
     ncu summary, only if it was taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "decode_partial_traffic.json")
+    p = os.path.join(ROOT, "profiles", "decode_partial_traffic.txt")
+    d = {}
     try:
         with open(p) as f:
-            d = json.load(f)
-    except Exception:
+            for line in f:
+                if line.startswith("#") or ":" not in line:
+                    continue
+                k, v = line.split(":", 1)
+                d[k.strip()] = v.strip()
+    except OSError:
         return None
     if d.get("decode_cu_sha256_16") != kernel_source_hash():
         return None
-    return d.get("dram_bytes_per_launch")
+    try:
+        return int(d["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 class ClockSampler:
@@ -596,6 +604,66 @@ def run_reference(args, rank, world):
     }
 
 
+def decode_sweep(args) -> int:
+    """Decode-attention throughput on every bf16 decode workload (not the
+    bench line): partial-pass kernel alone (library events) and the whole
+    decode call, each over `--steps` launches with the clean L2 flush."""
+    import paged_kv_cache_blk_gb300 as pkv
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    pkv.build()
+    pkv.load()
+    flush = L2Flush(dev)
+    peak, kind = load_peaks()
+    res = {}
+    for name in ("decode_gqa", "long_splitk", "prefix_mix"):
+        w = make_workload(name)
+        k, v = new_pool(w.pool, dev)
+        fill_pool(k, v, w.pool, w.layer, w.seed, w.k_boost_frac, w.k_boost)
+        pool = pkv.Pool(k, v)
+        b = w.batch
+        t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+        bt, lens, offs = (t(b.block_tables, torch.int32), t(b.seq_lens, torch.int32),
+                          t(b.offsets, torch.int32))
+        q = rand_rows((b.batch, w.num_q_heads, w.pool.head_dim), "bf16", 5, dev)
+        out = torch.empty_like(q)
+        ws = torch.empty(pkv.decode_workspace_size(b.batch, w.num_q_heads, w.pool.head_dim, dev),
+                         dtype=torch.uint8, device=dev)
+        call = lambda: pkv.decode_attention(pool, w.layer, q, w.scale, bt, lens, offs, out, ws)
+        for _ in range(args.warmup):
+            call()
+        torch.cuda.synchronize()
+
+        def hook():
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(); e1.record()
+            pkv.set_decode_events(e0, e1)
+            return e0, e1
+
+        times, kev = timed(call, args.steps, flush, hook)
+        pkv.set_decode_events(None, None)
+        call_ms = statistics.mean(times)
+        part_ms = statistics.mean(a.elapsed_time(e) for a, e in kev)
+        db = decode_bytes(b, w.pool.row_bytes, w.num_q_heads, w.pool.head_dim,
+                          w.pool.elem_size, w.pool.block_size)
+        entry = {"kv_read_bytes": db["kv"], "algorithmic_bytes": db["total"],
+                 "partial_ms": round(part_ms, 4), "call_ms": round(call_ms, 4),
+                 "partial_GBps": round(db["total"] / part_ms / 1e6, 1),
+                 "call_kv_GBps": round(db["kv"] / call_ms / 1e6, 1),
+                 "partial_frac_of_" + kind: round(db["total"] / part_ms / 1e6 / peak, 4),
+                 "tokens_per_s": round(b.batch / call_ms * 1e3, 1)}
+        if name == "prefix_mix":
+            prefix = 64 * 16 * w.pool.row_bytes * 2
+            entry["unique_kv_bytes"] = db["kv"] - (b.batch - 1) * prefix + int(
+                (b.offsets.astype(np.int64) * w.pool.row_bytes * 2).sum())
+            entry["call_unique_GBps"] = round(entry["unique_kv_bytes"] / call_ms / 1e6, 1)
+        res[name] = entry
+        del pool, k, v, ws
+        torch.cuda.empty_cache()
+    print(json.dumps({"decode_sweep": res, "peak_GBps": peak, "peak_kind": kind}), flush=True)
+    return 0
+
+
 def ncu_case(kind: str, launches: int = 4) -> int:
     """A small-footprint run of one kernel for ncu: the decode-GQA batch
     (1.27 GB of K/V per launch, larger than L2) over a 1-layer copy of its
@@ -656,9 +724,13 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ncu-case", choices=["decode", "gather", "scatter"],
                     help="run a small-footprint case of one kernel (for ncu) and exit")
+    ap.add_argument("--decode-sweep", action="store_true",
+                    help="decode throughput on every decode workload (not the bench line)")
     args = ap.parse_args(argv)
     if args.ncu_case:
         return ncu_case(args.ncu_case)
+    if args.decode_sweep:
+        return decode_sweep(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, local_rank, world = dist_env()
