@@ -513,9 +513,123 @@ def run_legs(args, dev, rank, flush, pkv):
                      b.total_tokens,
                      "workload": "gather_scatter: pool 16384x32x16x8x128 bf16 layer 0, 32 "
                                  "seqs U[512,4096]"}
-    del pool, k, v, ko, vo
+    # whole-block moves on the same pool: copy-on-write copies (all layers of
+    # 512 block pairs) and swap out / in of 256 blocks to page-locked host memory
+    rng = np.random.default_rng(7 + rank)
+    perm = rng.permutation(w.pool.num_blocks).astype(np.int32)
+    src = torch.from_numpy(perm[:512]).to(dev)
+    dst = torch.from_numpy(perm[512:1024]).to(dev)
+    blk_bytes = w.pool.num_layers * w.pool.block_size * rb            # one block, all layers
+    copy = lambda: pkv.copy_blocks(pool, -1, src, dst)
+    sw = torch.from_numpy(perm[1024:1280]).to(dev)
+    hk = torch.empty((256,) + tuple(k.shape[1:]), dtype=k.dtype, pin_memory=True)
+    hv = torch.empty_like(hk, pin_memory=True)
+    swap_out = lambda: pkv.swap_out(pool, -1, sw, hk, hv)
+    swap_in = lambda: pkv.swap_in(pool, -1, sw, hk, hv)
+    # the same bytes through torch's own page-locked copy, as the link reference
+    dk = torch.empty_like(hk, device=dev)
+    d2h = lambda: hk.copy_(dk, non_blocking=True)
+    h2d = lambda: dk.copy_(hk, non_blocking=True)
+    for _ in range(args.warmup):
+        copy(); swap_out(); swap_in(); d2h(); h2d()
+    torch.cuda.synchronize()
+    for name, fn, nbytes, note in (
+            ("copy_blocks", copy, 512 * blk_bytes * 2 * 2, "512 block pairs, all 32 layers, K+V "
+                                                           "(read + write)"),
+            ("swap_out", swap_out, 256 * blk_bytes * 2, "256 blocks, all layers, K+V to "
+                                                        "page-locked host"),
+            ("swap_in", swap_in, 256 * blk_bytes * 2, "256 blocks, all layers, K+V from "
+                                                      "page-locked host"),
+            ("torch_d2h_same_bytes", d2h, 256 * blk_bytes, "reference: torch copy of one "
+                                                           "256-block buffer to pinned host"),
+            ("torch_h2d_same_bytes", h2d, 256 * blk_bytes, "reference: the reverse")):
+        times, _ = timed(fn, max(5, args.steps // 10), flush)
+        ms = reduce_max(statistics.mean(times))
+        out[name] = {"GB/s": round(nbytes / (ms / 1e3) / 1e9, 1), "ms": round(ms, 4),
+                     "bytes": nbytes, "what": note}
+    del pool, k, v, ko, vo, hk, hv, dk
     torch.cuda.empty_cache()
+    out["allocator"] = allocator_leg()
     return out
+
+
+def allocator_trace(num_blocks: int, bs: int, seed: int):
+    """A serving-shaped operation trace for the block allocator: requests
+    arrive with prompts U[16, 2048], some hit the prefix of a live request
+    (shared blocks) or fork it, every live request appends one token per
+    decode step (copy-on-write where shared), and the oldest leave."""
+    rng = np.random.default_rng(seed)
+    ops = []
+    live, nid = [], 0
+    for step in range(400):
+        if len(live) < 48 or rng.random() < 0.3:
+            sid = nid
+            nid += 1
+            if live and rng.random() < 0.3:
+                ops.append(("fork", int(rng.choice(live)), sid))
+            else:
+                ops.append(("new", sid, int(rng.integers(0, bs))))
+                ops.append(("append", sid, int(rng.integers(16, 2049))))
+            live.append(sid)
+        for sid in live:
+            ops.append(("append", sid, 1))
+        if len(live) > 64:
+            ops.append(("free", live.pop(0), 0))
+    return ops
+
+
+def _run_trace(ops, m):
+    """Replay a trace; the decode appends of a step go in one batched call.
+    Returns the number of sequence operations performed."""
+    n = 0
+    step = []
+
+    def flush_step():
+        nonlocal n
+        if step:
+            try:
+                m.seq_append_batch(step)
+            except Exception:
+                pass
+            n += len(step)
+            step.clear()
+
+    for op, a, b in ops:
+        if op == "append" and b == 1:
+            step.append(a)
+            continue
+        flush_step()
+        try:
+            if op == "new":
+                m.seq_new(a, b)
+            elif op == "append":
+                m.seq_append(a, b)
+            elif op == "fork":
+                m.seq_fork(a, b)
+            else:
+                m.seq_free(a)
+        except Exception:
+            pass
+        n += 1
+    flush_step()
+    return n
+
+
+def allocator_leg():
+    import paged_kv_cache_blk_gb300 as pkv
+    from oracle import allocator as OA
+    N, bs = 16384, 16
+    ops = allocator_trace(N, bs, 11)
+    t0 = time.perf_counter()
+    n = _run_trace(ops, pkv.Allocator(N, bs))
+    lib_s = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    _run_trace(ops, OA.KVCacheManager(N, bs))
+    ora_s = time.perf_counter() - t0
+    return {"ops": n, "lib_ops_per_s": round(n / lib_s, 1), "oracle_ops_per_s": round(n / ora_s, 1),
+            "lib_us_per_decode_step": round(lib_s / 400 * 1e6, 2),
+            "trace": "16384 blocks of 16; 400 decode steps of <=64 live requests (one batched "
+                     "append per step), prompts U[16,2048], 30% forks; through the Python binding"}
 
 
 # ---------------------------------------------------------------------------

@@ -76,7 +76,8 @@ typedef enum {
   PKV_ERR_WORKSPACE = 4,    /* workspace null or smaller than pkv_decode_workspace_size */
   PKV_ERR_INDEX = 5,        /* slot or block id outside the pool, bad packed layout */
   PKV_ERR_CUDA = 6,         /* a CUDA runtime call failed */
-  PKV_ERR_TIMEOUT = 7       /* a bounded device-side wait gave up */
+  PKV_ERR_TIMEOUT = 7,      /* a bounded device-side wait gave up */
+  PKV_ERR_NO_BLOCKS = 8     /* allocator: too few free blocks; nothing was changed */
 } pkv_status;
 
 typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
@@ -213,6 +214,36 @@ PKV_API pkv_status pkv_decode_attention_static(const pkv_pool* pool, int32_t lay
                                                const int32_t* seq_lens, const int32_t* offsets,
                                                int32_t batch, void* out, cudaStream_t stream);
 
+/* Whole-block moves.  `layer` is one layer, or -1 for every layer of the
+ * block (one contiguous run of num_layers * block_size rows).  Block ids
+ * outside [0, num_blocks) are skipped and set the device error word
+ * (PKV_ERR_INDEX in validate mode).
+ *
+ * pkv_copy_blocks: for i < num_pairs, block dst_blocks[i] receives the K and
+ * V contents of block src_blocks[i] (device int32 arrays).  This is the copy
+ * of copy-on-write (mini-runtime "ch.12 Paged KV Cache" §3.1; the allocator's
+ * pkv_seq_append reports the pairs).  Destinations must be distinct and must
+ * not appear among the sources. */
+PKV_API pkv_status pkv_copy_blocks(const pkv_pool* pool, int32_t layer, const int32_t* src_blocks,
+                                   const int32_t* dst_blocks, int32_t num_pairs,
+                                   cudaStream_t stream);
+
+/* pkv_swap_out: the K and V data of blocks[0..n) (device int32 array), in
+ * that order, into host_k / host_v laid out [n, layers, block_size,
+ * num_kv_heads, head_dim] (layers = 1 for a single layer).  pkv_swap_in: the
+ * reverse, host buffers into the listed blocks.  Preemption by swapping
+ * ("vLLM PagedAttention source notes" §2.4).  host_k and host_v must be
+ * page-locked host memory the device can address (cudaHostAlloc or
+ * cudaHostRegister; checked) of at least host_bytes bytes each, and
+ * host_bytes must cover n blocks (checked); the kernel reads and writes them
+ * in place, which on GB300 goes over NVLink-C2C. */
+PKV_API pkv_status pkv_swap_out(const pkv_pool* pool, int32_t layer, const int32_t* blocks,
+                                int32_t n, void* host_k, void* host_v, size_t host_bytes,
+                                cudaStream_t stream);
+PKV_API pkv_status pkv_swap_in(const pkv_pool* pool, int32_t layer, const int32_t* blocks,
+                               int32_t n, const void* host_k, const void* host_v,
+                               size_t host_bytes, cudaStream_t stream);
+
 /* Number of CTAs the decode partial pass uses on the current device; 0 (the
  * default) means one per SM.  A positive value (at most 65536) forces that
  * grid size, which changes how sequences are split (1 = no split).
@@ -236,6 +267,93 @@ PKV_API int32_t pkv_get_validate(void);
  * *status and, if clear != 0, resets it.  Returns PKV_ERR_CUDA if the
  * device cannot be read. */
 PKV_API pkv_status pkv_device_error(pkv_status* status, int32_t clear);
+
+/* ------------------------------------------------------------------------
+ * Host block allocator (block manager).  Plain host memory, no CUDA calls;
+ * one allocator per pool; not thread-safe (the caller serialises calls).
+ *
+ * Restates mini-runtime "ch.12 Paged KV Cache" §2.2 (BlockTable: block ids in
+ * logical order, first-block offset, capacity = blocks * block_size - offset),
+ * §2.3 (FIFO deque of free ids: allocate takes ceil(tokens / block_size) ids
+ * from the front, or fails and changes nothing), §2.4 (ref_count: inc_ref
+ * when a holder shares a block, dec_ref when it lets go, the block returns to
+ * the back of the free deque at zero), §3.1 (copy-on-write + ref_count), and
+ * "vLLM PagedAttention source notes" §2.1 (allocate / free / append_slot) and
+ * §3 (fragmentation ratio).
+ *
+ * Sequences are identified by caller ids (int64).  A sequence's table always
+ * spans exactly ceil((offset + num_tokens) / block_size) blocks.  Appending
+ * fills the last block, then takes fresh blocks in deque order.  If the
+ * block the first appended token lands in is shared (ref_count > 1), it is
+ * first replaced in this sequence by a fresh block (copy-on-write) and the
+ * pair (shared, fresh) is returned for the caller to copy on the device
+ * (pkv_copy_blocks).  Every failing call leaves the allocator unchanged.
+ * ------------------------------------------------------------------------ */
+typedef struct pkv_allocator pkv_allocator;
+
+/* free_order: NULL for ids 0..num_blocks-1 in order, else a host permutation
+ * of them giving the initial deque order.  *out receives the allocator. */
+PKV_API pkv_status pkv_alloc_create(int64_t num_blocks, int32_t block_size,
+                                    const int32_t* free_order, pkv_allocator** out);
+PKV_API pkv_status pkv_alloc_destroy(pkv_allocator* a);
+/* Number of free blocks; -1 for a null allocator. */
+PKV_API int64_t pkv_alloc_num_free(const pkv_allocator* a);
+/* ref_count of a block (0 = free); -1 for a bad block id. */
+PKV_API int32_t pkv_alloc_ref_count(const pkv_allocator* a, int64_t block);
+/* Take n blocks from the front of the deque into out_ids (host, n entries),
+ * each with ref_count 1; PKV_ERR_NO_BLOCKS if fewer than n are free. */
+PKV_API pkv_status pkv_alloc_blocks(pkv_allocator* a, int64_t n, int32_t* out_ids);
+PKV_API pkv_status pkv_alloc_inc_ref(pkv_allocator* a, int32_t block);
+/* At zero the block goes to the back of the deque.  A free block: error. */
+PKV_API pkv_status pkv_alloc_dec_ref(pkv_allocator* a, int32_t block);
+
+/* New empty sequence whose first token will sit at row `offset` of its first
+ * block (0 <= offset < block_size). */
+PKV_API pkv_status pkv_seq_new(pkv_allocator* a, int64_t seq_id, int32_t offset);
+/* Prefix hit: an empty sequence takes n already allocated blocks (inc_ref
+ * each) covering num_tokens tokens; n must equal
+ * ceil((offset + num_tokens) / block_size). */
+PKV_API pkv_status pkv_seq_share(pkv_allocator* a, int64_t seq_id, const int32_t* blocks,
+                                 int32_t n, int64_t num_tokens);
+/* Append num_tokens tokens.  slots_out (nullable, num_tokens entries)
+ * receives their slots (block * block_size + row).  cow_src / cow_dst
+ * (nullable, one entry each) and *n_cow (nullable) receive the copy-on-write
+ * pair, if any (n_cow is 0 or 1).  PKV_ERR_NO_BLOCKS: nothing changed. */
+PKV_API pkv_status pkv_seq_append(pkv_allocator* a, int64_t seq_id, int64_t num_tokens,
+                                  int64_t* slots_out, int32_t* cow_src, int32_t* cow_dst,
+                                  int32_t* n_cow);
+/* One decode step for many sequences: for i < n, append num_tokens[i]
+ * tokens (NULL: one each) to seq_ids[i], in order, as pkv_seq_append would.
+ * slots_out (nullable) receives every appended token's slot, sequence by
+ * sequence (the step's slot_mapping); cow_src / cow_dst (nullable, room for n
+ * entries) and *n_cow receive the copy-on-write pairs.  All or nothing: if
+ * the blocks the whole batch needs (copy-on-write included, in order) are
+ * not free, PKV_ERR_NO_BLOCKS and nothing changes; an unknown id or a repeated
+ * id is PKV_ERR_INVALID_ARG. */
+PKV_API pkv_status pkv_seq_append_batch(pkv_allocator* a, const int64_t* seq_ids, int32_t n,
+                                        const int64_t* num_tokens, int64_t* slots_out,
+                                        int32_t* cow_src, int32_t* cow_dst, int32_t* n_cow);
+
+/* dst (new id) shares every block of src (inc_ref each), same offset and
+ * length. */
+PKV_API pkv_status pkv_seq_fork(pkv_allocator* a, int64_t src, int64_t dst);
+/* Release every block of the sequence (dec_ref) and forget it. */
+PKV_API pkv_status pkv_seq_free(pkv_allocator* a, int64_t seq_id);
+PKV_API pkv_status pkv_seq_info(const pkv_allocator* a, int64_t seq_id, int64_t* num_tokens,
+                                int32_t* offset, int32_t* num_blocks);
+/* Host arrays for the kernels: tables [batch, max_blocks] (row b = blocks of
+ * seq_ids[b], padded with -1), seq_lens [batch], offsets [batch] (both
+ * nullable).  PKV_ERR_CAPACITY if a sequence spans more than max_blocks. */
+PKV_API pkv_status pkv_seq_tables(const pkv_allocator* a, const int64_t* seq_ids, int32_t batch,
+                                  int32_t max_blocks, int32_t* tables, int32_t* seq_lens,
+                                  int32_t* offsets);
+/* Allocated blocks (ref_count > 0), used slots (rows holding a token of some
+ * sequence, each counted once) and the fragmentation ratio
+ * (allocated * block_size - used) / (allocated * block_size), 0 when nothing
+ * is allocated ("vLLM PagedAttention source notes" §3).  Any output may be
+ * NULL. */
+PKV_API pkv_status pkv_alloc_stats(const pkv_allocator* a, int64_t* allocated_blocks,
+                                   int64_t* used_slots, double* fragmentation);
 
 /* Static description of a status code. */
 PKV_API const char* pkv_status_string(pkv_status status);

@@ -50,7 +50,7 @@ __all__ = [
     "slot_of", "build_slot_mapping", "write_slots", "gather_loop",
     "gather_indexed", "gather_batch", "widen", "attention_fp64",
     "decode_attention", "decode_attention_pairs", "split_partials",
-    "combine_partials",
+    "combine_partials", "copy_blocks", "swap_out", "swap_in",
 ]
 
 
@@ -330,3 +330,45 @@ def combine_partials(parts, head_dim: int) -> np.ndarray:
     num = sum(math.exp(m - M) * acc for m, _, acc in parts)
     den = sum(math.exp(m - M) * l for m, l, _ in parts)
     return num / den
+
+
+# ---------------------------------------------------------------------------
+# block copy (copy-on-write) and swap between the pool and host memory
+# ---------------------------------------------------------------------------
+
+def _layers(pool: np.ndarray, layer: int):
+    return slice(None) if layer < 0 else slice(layer, layer + 1)
+
+
+def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, layer: int,
+                src: Sequence[int], dst: Sequence[int]) -> None:
+    """Copy-on-write support (mini-runtime ch.12 §3.1: vLLM shares blocks
+    with copy-on-write plus ref_count): block dst[i] receives the contents of
+    block src[i], in one layer or (layer < 0) in every layer.  The pairs are
+    applied in order; a destination is assumed not to be read as a source by
+    another pair."""
+    ls = _layers(k_cache, layer)
+    for s_, d_ in zip(src, dst):
+        k_cache[int(d_), ls] = k_cache[int(s_), ls]
+        v_cache[int(d_), ls] = v_cache[int(s_), ls]
+
+
+def swap_out(k_cache: np.ndarray, v_cache: np.ndarray, layer: int,
+             blocks: Sequence[int]):
+    """Preemption by swapping ("vLLM PagedAttention source notes" §2.4: move
+    a request's KV from the GPU to the CPU): the listed blocks, in order, as
+    contiguous host arrays [n, layers, bs, Hkv, D]."""
+    ls = _layers(k_cache, layer)
+    ks = np.stack([k_cache[int(b), ls] for b in blocks]) if len(blocks) else None
+    vs = np.stack([v_cache[int(b), ls] for b in blocks]) if len(blocks) else None
+    return ks, vs
+
+
+def swap_in(k_cache: np.ndarray, v_cache: np.ndarray, layer: int,
+            blocks: Sequence[int], host_k: np.ndarray, host_v: np.ndarray) -> None:
+    """The reverse of :func:`swap_out`: host rows i go back into block
+    blocks[i] (any free blocks; the table is updated by the allocator)."""
+    ls = _layers(k_cache, layer)
+    for i, b in enumerate(blocks):
+        k_cache[int(b), ls] = host_k[i]
+        v_cache[int(b), ls] = host_v[i]

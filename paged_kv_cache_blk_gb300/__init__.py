@@ -3,10 +3,12 @@ paged decode attention, as hand-written CUDA kernels behind the C ABI in
 ``include/pkv.h`` (``libpkv.so``), with this thin ctypes binding."""
 
 from ._binding import (  # noqa: F401
+    Allocator,
     Pool,
     PkvError,
     STATUS_CODES,
     build_slot_mapping,
+    copy_blocks,
     decode_attention,
     decode_attention_static,
     decode_workspace_size,
@@ -19,6 +21,8 @@ from ._binding import (  # noqa: F401
     set_decode_events,
     set_validate,
     status_string,
+    swap_in,
+    swap_out,
     version,
     write_slots,
 )

@@ -11,8 +11,9 @@ from __future__ import annotations
 
 import ctypes
 import os
-from typing import Optional
+from typing import List, Optional, Sequence, Tuple
 
+import numpy as np
 import torch
 
 from . import build as _build
@@ -20,6 +21,7 @@ from . import build as _build
 _STATUS = {
     0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_CAPACITY", 3: "PKV_ERR_UNSUPPORTED",
     4: "PKV_ERR_WORKSPACE", 5: "PKV_ERR_INDEX", 6: "PKV_ERR_CUDA", 7: "PKV_ERR_TIMEOUT",
+    8: "PKV_ERR_NO_BLOCKS",
 }
 STATUS_CODES = {v: k for k, v in _STATUS.items()}
 _DTYPE = {torch.float32: 0, torch.bfloat16: 1}
@@ -57,11 +59,30 @@ _SIGS = {
                                     _SZ, _P]),
     "pkv_decode_attention_static": (_I32, [_P, _I32, _P, _I32, _F32, _P, _I32, _P, _P, _I32,
                                            _P, _P]),
+    "pkv_copy_blocks": (_I32, [_P, _I32, _P, _P, _I32, _P]),
+    "pkv_swap_out": (_I32, [_P, _I32, _P, _I32, _P, _P, _SZ, _P]),
+    "pkv_swap_in": (_I32, [_P, _I32, _P, _I32, _P, _P, _SZ, _P]),
     "pkv_set_decode_ctas": (_I32, [_I32]),
     "pkv_set_decode_events": (_I32, [_P, _P]),
     "pkv_set_validate": (_I32, [_I32]),
     "pkv_get_validate": (_I32, []),
     "pkv_device_error": (_I32, [ctypes.POINTER(ctypes.c_int32), _I32]),
+    "pkv_alloc_create": (_I32, [_I64, _I32, _P, ctypes.POINTER(ctypes.c_void_p)]),
+    "pkv_alloc_destroy": (_I32, [_P]),
+    "pkv_alloc_num_free": (_I64, [_P]),
+    "pkv_alloc_ref_count": (_I32, [_P, _I64]),
+    "pkv_alloc_blocks": (_I32, [_P, _I64, _P]),
+    "pkv_alloc_inc_ref": (_I32, [_P, _I32]),
+    "pkv_alloc_dec_ref": (_I32, [_P, _I32]),
+    "pkv_seq_new": (_I32, [_P, _I64, _I32]),
+    "pkv_seq_share": (_I32, [_P, _I64, _P, _I32, _I64]),
+    "pkv_seq_append": (_I32, [_P, _I64, _I64, _P, _P, _P, _P]),
+    "pkv_seq_append_batch": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P]),
+    "pkv_seq_fork": (_I32, [_P, _I64, _I64]),
+    "pkv_seq_free": (_I32, [_P, _I64]),
+    "pkv_seq_info": (_I32, [_P, _I64, _P, _P, _P]),
+    "pkv_seq_tables": (_I32, [_P, _P, _I32, _I32, _P, _P, _P]),
+    "pkv_alloc_stats": (_I32, [_P, _P, _P, _P]),
     "pkv_status_string": (ctypes.c_char_p, [_I32]),
     "pkv_version": (_I32, []),
 }
@@ -226,6 +247,38 @@ def decode_attention_static(pool: Pool, layer: int, q: torch.Tensor, scale: floa
     _check(st, "pkv_decode_attention_static")
 
 
+def copy_blocks(pool: Pool, layer: int, src_blocks: torch.Tensor,
+                dst_blocks: torch.Tensor) -> None:
+    """Block dst[i] <- block src[i] (K and V), one layer or every layer (-1)."""
+    lib = load()
+    with _dev(pool):
+        st = lib.pkv_copy_blocks(pool.ref, layer, _ptr(src_blocks), _ptr(dst_blocks),
+                                 src_blocks.numel(), _stream(pool.device))
+    _check(st, "pkv_copy_blocks")
+
+
+def swap_out(pool: Pool, layer: int, blocks: torch.Tensor, host_k: torch.Tensor,
+             host_v: torch.Tensor) -> None:
+    """Listed blocks -> page-locked host tensors [n, layers, bs, Hkv, D]."""
+    lib = load()
+    nbytes = min(host_k.numel(), host_v.numel()) * host_k.element_size()
+    with _dev(pool):
+        st = lib.pkv_swap_out(pool.ref, layer, _ptr(blocks), blocks.numel(), _ptr(host_k),
+                              _ptr(host_v), nbytes, _stream(pool.device))
+    _check(st, "pkv_swap_out")
+
+
+def swap_in(pool: Pool, layer: int, blocks: torch.Tensor, host_k: torch.Tensor,
+            host_v: torch.Tensor) -> None:
+    """Page-locked host tensors [n, layers, bs, Hkv, D] -> listed blocks."""
+    lib = load()
+    nbytes = min(host_k.numel(), host_v.numel()) * host_k.element_size()
+    with _dev(pool):
+        st = lib.pkv_swap_in(pool.ref, layer, _ptr(blocks), blocks.numel(), _ptr(host_k),
+                             _ptr(host_v), nbytes, _stream(pool.device))
+    _check(st, "pkv_swap_in")
+
+
 def set_decode_ctas(n: int) -> None:
     _check(load().pkv_set_decode_ctas(n), "pkv_set_decode_ctas")
 
@@ -260,3 +313,111 @@ def status_string(status: int) -> str:
 
 def version() -> int:
     return load().pkv_version()
+
+
+class Allocator:
+    """Host block allocator of the library (the allocator section of
+    include/pkv.h): FIFO free deque, reference counts, per-sequence block
+    tables with a first-block offset, copy-on-write on shared blocks."""
+
+    def __init__(self, num_blocks: int, block_size: int,
+                 free_order: Optional[Sequence[int]] = None):
+        lib = load()
+        h = ctypes.c_void_p()
+        order = None
+        if free_order is not None:
+            order = np.ascontiguousarray(np.asarray(free_order, dtype=np.int32))
+        _check(lib.pkv_alloc_create(num_blocks, block_size,
+                                    None if order is None else order.ctypes.data,
+                                    ctypes.byref(h)), "pkv_alloc_create")
+        self._h = h
+        self._lib = lib
+        self.num_blocks, self.block_size = num_blocks, block_size
+
+    def close(self) -> None:
+        if self._h:
+            self._lib.pkv_alloc_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free(self) -> int:
+        return self._lib.pkv_alloc_num_free(self._h)
+
+    def ref_count(self, block: int) -> int:
+        return self._lib.pkv_alloc_ref_count(self._h, block)
+
+    def allocate_blocks(self, n: int) -> List[int]:
+        out = np.empty(max(n, 1), dtype=np.int32)
+        _check(self._lib.pkv_alloc_blocks(self._h, n, out.ctypes.data), "pkv_alloc_blocks")
+        return out[:n].tolist()
+
+    def inc_ref(self, block: int) -> None:
+        _check(self._lib.pkv_alloc_inc_ref(self._h, block), "pkv_alloc_inc_ref")
+
+    def dec_ref(self, block: int) -> None:
+        _check(self._lib.pkv_alloc_dec_ref(self._h, block), "pkv_alloc_dec_ref")
+
+    def seq_new(self, sid: int, offset: int = 0) -> None:
+        _check(self._lib.pkv_seq_new(self._h, sid, offset), "pkv_seq_new")
+
+    def seq_share(self, sid: int, blocks: Sequence[int], num_tokens: int) -> None:
+        arr = np.ascontiguousarray(np.asarray(blocks, dtype=np.int32))
+        _check(self._lib.pkv_seq_share(self._h, sid, arr.ctypes.data if len(arr) else None,
+                                       len(arr), num_tokens), "pkv_seq_share")
+
+    def seq_append(self, sid: int, num_tokens: int) -> Tuple[np.ndarray, List[Tuple[int, int]]]:
+        slots = np.empty(max(num_tokens, 1), dtype=np.int64)
+        src, dst, n = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        _check(self._lib.pkv_seq_append(self._h, sid, num_tokens, slots.ctypes.data,
+                                        ctypes.byref(src), ctypes.byref(dst), ctypes.byref(n)),
+               "pkv_seq_append")
+        return slots[:num_tokens], ([(src.value, dst.value)] if n.value else [])
+
+    def seq_append_batch(self, sids: Sequence[int], counts: Optional[Sequence[int]] = None):
+        ids = np.ascontiguousarray(np.asarray(sids, dtype=np.int64))
+        n = len(ids)
+        cnt = None if counts is None else np.ascontiguousarray(np.asarray(counts, dtype=np.int64))
+        total = n if cnt is None else int(cnt.sum())
+        slots = np.empty(max(total, 1), dtype=np.int64)
+        src = np.empty(max(n, 1), dtype=np.int32)
+        dst = np.empty(max(n, 1), dtype=np.int32)
+        nc = ctypes.c_int32()
+        _check(self._lib.pkv_seq_append_batch(self._h, ids.ctypes.data if n else None, n,
+                                              None if cnt is None else cnt.ctypes.data,
+                                              slots.ctypes.data, src.ctypes.data, dst.ctypes.data,
+                                              ctypes.byref(nc)), "pkv_seq_append_batch")
+        return slots[:total], list(zip(src[:nc.value].tolist(), dst[:nc.value].tolist()))
+
+    def seq_fork(self, src: int, dst: int) -> None:
+        _check(self._lib.pkv_seq_fork(self._h, src, dst), "pkv_seq_fork")
+
+    def seq_free(self, sid: int) -> None:
+        _check(self._lib.pkv_seq_free(self._h, sid), "pkv_seq_free")
+
+    def seq_info(self, sid: int) -> Tuple[int, int, int]:
+        n, off, nb = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        _check(self._lib.pkv_seq_info(self._h, sid, ctypes.byref(n), ctypes.byref(off),
+                                      ctypes.byref(nb)), "pkv_seq_info")
+        return n.value, off.value, nb.value
+
+    def seq_tables(self, sids: Sequence[int], max_blocks: int):
+        ids = np.ascontiguousarray(np.asarray(sids, dtype=np.int64))
+        B = len(ids)
+        tables = np.empty((max(B, 1), max_blocks), dtype=np.int32)
+        lens = np.empty(max(B, 1), dtype=np.int32)
+        offs = np.empty(max(B, 1), dtype=np.int32)
+        _check(self._lib.pkv_seq_tables(self._h, ids.ctypes.data if B else None, B, max_blocks,
+                                        tables.ctypes.data, lens.ctypes.data, offs.ctypes.data),
+               "pkv_seq_tables")
+        return tables[:B], lens[:B], offs[:B]
+
+    def stats(self) -> Tuple[int, int, float]:
+        a, u, f = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_double()
+        _check(self._lib.pkv_alloc_stats(self._h, ctypes.byref(a), ctypes.byref(u),
+                                         ctypes.byref(f)), "pkv_alloc_stats")
+        return a.value, u.value, f.value

@@ -374,6 +374,7 @@ const char* pkv_status_string(pkv_status status) {
     case PKV_ERR_INDEX: return "slot or block id out of range";
     case PKV_ERR_CUDA: return "CUDA error";
     case PKV_ERR_TIMEOUT: return "device wait timed out";
+    case PKV_ERR_NO_BLOCKS: return "too few free blocks (nothing changed)";
   }
   return "unknown status";
 }

@@ -138,3 +138,18 @@ def test_options_and_strings(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         B.load(str(tmp_path / "missing.so"))
+
+
+def test_host_checks_block_moves(lib):
+    p = ctypes.byref(_pool())
+    assert lib.pkv_copy_blocks(p, 0, 16, 16, 0, None) == S["PKV_OK"]
+    assert lib.pkv_copy_blocks(p, 2, 16, 16, 1, None) == S["PKV_ERR_INVALID_ARG"]    # layer
+    assert lib.pkv_copy_blocks(p, -2, 16, 16, 1, None) == S["PKV_ERR_INVALID_ARG"]
+    assert lib.pkv_copy_blocks(p, -1, None, 16, 1, None) == S["PKV_ERR_INVALID_ARG"]
+    assert lib.pkv_copy_blocks(None, 0, 16, 16, 1, None) == S["PKV_ERR_INVALID_ARG"]
+    # host buffers too small for n blocks: refused before any device call
+    run = 16 * 2 * 64 * 2 * 2                                  # all layers: L*bs*Hkv*D*e
+    assert lib.pkv_swap_out(p, -1, 16, 3, 16, 16, 3 * run - 16, None) == S["PKV_ERR_INVALID_ARG"]
+    assert lib.pkv_swap_in(p, 0, 16, 3, 16, 16, 3 * run // 2 - 1, None) == S["PKV_ERR_INVALID_ARG"]
+    assert lib.pkv_swap_out(p, 0, 16, 0, None, None, 0, None) == S["PKV_OK"]
+    assert lib.pkv_swap_out(p, 0, 16, 2, 8, 16, 1 << 20, None) == S["PKV_ERR_INVALID_ARG"]

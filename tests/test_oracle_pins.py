@@ -452,3 +452,60 @@ PLANTED = [
 def test_pins_catch_planted_mistakes(name, run):
     with pytest.raises((AssertionError, IndexError)):
         run()
+
+
+# ---------------------------------------------------------------------------
+# block copy and swap (copy-on-write and preemption by swapping)
+# ---------------------------------------------------------------------------
+
+def test_swap_round_trip_and_copy():
+    rng = np.random.default_rng(13)
+    N, L, bs, H, D = 10, 3, 4, 2, 2
+    k = rng.standard_normal((N, L, bs, H, D)).astype(np.float32)
+    v = rng.standard_normal((N, L, bs, H, D)).astype(np.float32)
+    k0, v0 = k.copy(), v.copy()
+    for layer in (-1, 1):
+        hk, hv = O.swap_out(k, v, layer, [7, 2, 5])
+        assert hk.shape == ((3, L) if layer < 0 else (3, 1)) + (bs, H, D)
+        assert np.array_equal(hk[1], k[2] if layer < 0 else k[2, 1:2])
+        # bring them back into other blocks: those blocks now hold the data
+        O.swap_in(k, v, layer, [0, 1, 3], hk, hv)
+        ls = slice(None) if layer < 0 else slice(1, 2)
+        for src, dst in ((7, 0), (2, 1), (5, 3)):
+            assert np.array_equal(k[dst, ls], k0[src, ls]) and np.array_equal(v[dst, ls], v0[src, ls])
+        k[:], v[:] = k0, v0
+    O.copy_blocks(k, v, 2, [4], [9])
+    assert np.array_equal(k[9, 2], k0[4, 2]) and np.array_equal(k[9, :2], k0[9, :2])
+    O.copy_blocks(k, v, -1, [1, 2], [6, 8])
+    assert np.array_equal(v[6], v0[1]) and np.array_equal(v[8], v0[2])
+
+
+def test_copy_on_write_keeps_shared_prefix():
+    """Fork a sequence, append to the fork: the allocator reports a
+    (shared, fresh) pair; after copying it, the fork reads the same prefix as
+    the original and each writes its new token into its own block."""
+    from oracle import allocator as OA
+    bs, N = 4, 12
+    m = OA.KVCacheManager(N, bs)
+    rng = np.random.default_rng(14)
+    k = np.zeros((N, 1, bs, 1, 2), np.float32)
+    v = np.zeros_like(k)
+    m.seq_new(1, offset=1)
+    slots, _ = m.seq_append(1, 6)
+    kn = rng.standard_normal((6, 1, 2)).astype(np.float32)
+    O.write_slots(k, v, 0, kn, -kn, np.array(slots))
+    m.seq_fork(1, 2)
+    s2, cow = m.seq_append(2, 1)
+    assert len(cow) == 1
+    O.copy_blocks(k, v, -1, [c[0] for c in cow], [c[1] for c in cow])
+    new2 = rng.standard_normal((1, 1, 2)).astype(np.float32)
+    O.write_slots(k, v, 0, new2, -new2, np.array(s2))
+    s1, cow1 = m.seq_append(1, 1)
+    assert cow1 == []
+    new1 = rng.standard_normal((1, 1, 2)).astype(np.float32)
+    O.write_slots(k, v, 0, new1, -new1, np.array(s1))
+    t1, t2 = m.seq_table(1), m.seq_table(2)
+    g1 = O.gather_loop(k, 0, t1.block_ids, t1.num_tokens, t1.offset)
+    g2 = O.gather_loop(k, 0, t2.block_ids, t2.num_tokens, t2.offset)
+    assert np.array_equal(g1[:6], kn) and np.array_equal(g2[:6], kn)
+    assert np.array_equal(g1[6], new1[0]) and np.array_equal(g2[6], new2[0])
