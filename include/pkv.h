@@ -180,6 +180,33 @@ PKV_API pkv_status pkv_decode_attention(const pkv_pool* pool, int32_t layer, con
                                 int32_t batch, void* out, void* workspace,
                                 size_t workspace_bytes, cudaStream_t stream);
 
+/* Paged prefill attention (SURVEY next row; the prefill batch of
+ * "vLLM PagedAttention source notes" §2.4: the prompt tokens' K/V are written
+ * into their blocks, then attention runs over them), on tcgen05 tensor cores.
+ *
+ * For each sequence b, the queries are its LAST n_b = cu_q[b+1] - cu_q[b]
+ * tokens (their K/V must already be in the pool, e.g. by pkv_write_slots):
+ * query i sits at logical position P = seq_lens[b] - n_b + i and attends
+ * causally to the keys 0..P of the sequence, read through the block table
+ * (first-block offset honoured):
+ *     out[cu_q[b] + i][h] = sum_{j <= P} softmax_j(scale * q . K_j[g]) V_j[g],
+ *     g = h / (num_q_heads / num_kv_heads).
+ * q, out: [total_q, num_q_heads, head_dim] bf16 (device); cu_q: int64
+ * [batch + 1] device, cu_q[0] = 0, nondecreasing, cu_q[batch] <= total_q;
+ * max_q_len (host) bounds every n_b (the grid is sized from it; a sequence
+ * with a larger n_b is skipped and sets the device error word).
+ * A sequence with n_b > seq_lens[b] or a bad offset / capacity is skipped and
+ * sets the error word (PKV_ERR_CAPACITY in validate mode).  Supported: bf16
+ * pools with head_dim 128, block_size 8..128 dividing 128, num_q_heads /
+ * num_kv_heads in {1, 2, 4, 8, 16}; others PKV_ERR_UNSUPPORTED.  No
+ * workspace.  fp32 accumulation; P is rounded to bf16 for the P.V product. */
+PKV_API pkv_status pkv_prefill_attention(const pkv_pool* pool, int32_t layer, const void* q,
+                                         int32_t num_q_heads, float scale,
+                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t* seq_lens, const int32_t* offsets,
+                                         const int64_t* cu_q, int32_t batch, int64_t total_q,
+                                         int32_t max_q_len, void* out, cudaStream_t stream);
+
 /* Allocation-free paged decode attention.  The paper has no counterpart:
  * this is a library convenience.  Same computation, arguments, results and
  * error behaviour as pkv_decode_attention, except that the caller passes no

@@ -50,7 +50,7 @@ __all__ = [
     "slot_of", "build_slot_mapping", "write_slots", "gather_loop",
     "gather_indexed", "gather_batch", "widen", "attention_fp64",
     "decode_attention", "decode_attention_pairs", "split_partials",
-    "combine_partials", "copy_blocks", "swap_out", "swap_in",
+    "combine_partials", "copy_blocks", "swap_out", "swap_in", "prefill_attention",
 ]
 
 
@@ -372,3 +372,41 @@ def swap_in(k_cache: np.ndarray, v_cache: np.ndarray, layer: int,
     for i, b in enumerate(blocks):
         k_cache[int(b), ls] = host_k[i]
         v_cache[int(b), ls] = host_v[i]
+
+
+# ---------------------------------------------------------------------------
+# prefill attention (causal, over the paged cache)
+# ---------------------------------------------------------------------------
+
+def prefill_attention(k_cache: np.ndarray, v_cache: np.ndarray, layer: int, q: np.ndarray,
+                      block_tables: np.ndarray, seq_lens: np.ndarray, offsets: np.ndarray,
+                      cu_q: np.ndarray, scale: float) -> np.ndarray:
+    """Prefill attention in fp64, ``[T, Hq, D]``.
+
+    "vLLM PagedAttention source notes" §2.4 (prefill batch): the prompt
+    tokens' K/V are in their blocks; each new token then attends to itself
+    and to every earlier token of its sequence (causal attention; the plain
+    reading, as the pages name no other mask).  The queries of sequence b are
+    its last ``n = cu_q[b+1] - cu_q[b]`` tokens; query i sits at position
+    ``P = seq_len - n + i`` and attends to keys ``0..P``, gathered block by
+    block as in :func:`gather_loop`.  Query head h reads kv head
+    ``h // (Hq // Hkv)``.
+    """
+    T, Hq, D = q.shape
+    group = Hq // k_cache.shape[3]
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    qd = widen(q)
+    for b in range(len(seq_lens)):
+        n = int(cu_q[b + 1] - cu_q[b])
+        if n == 0:
+            continue
+        L = int(seq_lens[b])
+        kb = widen(gather_loop(k_cache, layer, block_tables[b], L, int(offsets[b])))
+        vb = widen(gather_loop(v_cache, layer, block_tables[b], L, int(offsets[b])))
+        for i in range(n):
+            P = L - n + i
+            for h in range(Hq):
+                g = h // group
+                out[int(cu_q[b]) + i, h] = attention_fp64(qd[int(cu_q[b]) + i, h],
+                                                          kb[:P + 1, g], vb[:P + 1, g], scale)
+    return out

@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     get_validate,
     library_path,
     load,
+    prefill_attention,
     set_decode_ctas,
     set_decode_events,
     set_validate,

@@ -62,6 +62,8 @@ _SIGS = {
     "pkv_copy_blocks": (_I32, [_P, _I32, _P, _P, _I32, _P]),
     "pkv_swap_out": (_I32, [_P, _I32, _P, _I32, _P, _P, _SZ, _P]),
     "pkv_swap_in": (_I32, [_P, _I32, _P, _I32, _P, _P, _SZ, _P]),
+    "pkv_prefill_attention": (_I32, [_P, _I32, _P, _I32, _F32, _P, _I32, _P, _P, _P, _I32, _I64,
+                                      _I32, _P, _P]),
     "pkv_set_decode_ctas": (_I32, [_I32]),
     "pkv_set_decode_events": (_I32, [_P, _P]),
     "pkv_set_validate": (_I32, [_I32]),
@@ -277,6 +279,21 @@ def swap_in(pool: Pool, layer: int, blocks: torch.Tensor, host_k: torch.Tensor,
         st = lib.pkv_swap_in(pool.ref, layer, _ptr(blocks), blocks.numel(), _ptr(host_k),
                              _ptr(host_v), nbytes, _stream(pool.device))
     _check(st, "pkv_swap_in")
+
+
+def prefill_attention(pool: Pool, layer: int, q: torch.Tensor, scale: float,
+                      block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                      offsets: Optional[torch.Tensor], cu_q: torch.Tensor, max_q_len: int,
+                      out: torch.Tensor) -> None:
+    """Causal prefill attention of q [T, Hq, D] (the last cu_q[b+1]-cu_q[b]
+    tokens of each sequence) over the paged cache into out [T, Hq, D]."""
+    lib = load()
+    with _dev(pool):
+        st = lib.pkv_prefill_attention(pool.ref, layer, _ptr(q), q.shape[1], float(scale),
+                                       _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+                                       _ptr(offsets), _ptr(cu_q), seq_lens.numel(), q.shape[0],
+                                       max_q_len, _ptr(out), _stream(pool.device))
+    _check(st, "pkv_prefill_attention")
 
 
 def set_decode_ctas(n: int) -> None:

@@ -1,6 +1,7 @@
 // C ABI of libpkv: argument checks, device bookkeeping, validate mode and
 // dispatch to the kernels.  See include/pkv.h for the contract of each call.
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -323,6 +324,44 @@ pkv_status pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void*
     if (e == cudaErrorInvalidConfiguration) return PKV_ERR_UNSUPPORTED;
     if ((st = launched(e)) != PKV_OK) return st;
   }
+  return validate ? read_and_clear(d->err, stream) : PKV_OK;
+}
+
+pkv_status pkv_prefill_attention(const pkv_pool* pool, int32_t layer, const void* q,
+                                 int32_t num_q_heads, float scale, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                 const int32_t* offsets, const int64_t* cu_q, int32_t batch,
+                                 int64_t total_q, int32_t max_q_len, void* out,
+                                 cudaStream_t stream) {
+  pkv::PoolView v;
+  pkv_status st = check_pool(pool, true, &v);
+  if (st != PKV_OK) return st;
+  if (layer < 0 || layer >= pool->num_layers || batch < 0 || num_q_heads <= 0 || total_q < 0 ||
+      max_q_len < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (pkv::prefill_supported(v, num_q_heads) != 0) return PKV_ERR_UNSUPPORTED;
+  if (batch == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
+  if (batch > 65535 || total_q > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  if (!q || !out || !block_tables || !seq_lens || !cu_q || max_blocks_per_seq <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned(cu_q, 8)) return PKV_ERR_INVALID_ARG;
+  DevInfo* d;
+  if ((st = current_device(&d)) != PKV_OK) return st;
+  const bool validate = g_validate.load() != 0;
+  if (validate) {
+    if ((st = clear_word(d->err, stream)) != PKV_OK) return st;
+    if ((st = launched(pkv::launch_validate_tables(v, block_tables, max_blocks_per_seq, seq_lens,
+                                                   offsets, batch, nullptr, 0, d->err,
+                                                   stream))) != PKV_OK)
+      return st;
+    if ((st = read_and_clear(d->err, stream)) != PKV_OK) return st;
+  }
+  if ((st = launched(pkv::launch_prefill(v, layer, q, num_q_heads, scale, block_tables,
+                                         max_blocks_per_seq, seq_lens, offsets, cu_q, batch,
+                                         total_q, max_q_len, out, d->err, stream))) != PKV_OK)
+    return st;
   return validate ? read_and_clear(d->err, stream) : PKV_OK;
 }
 

@@ -1,0 +1,536 @@
+// Paged prefill attention on the 5th-generation tensor cores (tcgen05, TMEM,
+// TMA).
+//
+// What is computed (the prefill batch of "vLLM PagedAttention source notes"
+// §2.4: every prompt token's K/V is computed and written into its blocks, then
+// attention runs over them): the last n_b tokens of sequence b are queries;
+// query i sits at logical position P_i = seq_len_b - n_b + i and attends
+// causally to the keys 0..P_i of the sequence, read in place from the pool
+// through the block table (first-block offset honoured).  GQA: query head h
+// reads kv head h / (Hq / Hkv).
+//
+// One CTA per (query tile, sequence, kv head):
+//  * 128 MMA rows = (128 / G) query tokens x the G query heads of kv head g,
+//    so each K/V tile feeds all G heads (row r = token * G + head).
+//  * Keys in tiles of 128 table positions (128 / bs whole blocks).  Tile t of
+//    K and of V is loaded by TMA (one box per block and 64-column half, 128B
+//    swizzle) into a 2-stage ring; invalid table entries load zeros.
+//  * Warp 5 issues S = Q K^T (M 128, N 128, K 128: 8 tcgen05.mma, fp32 in
+//    TMEM) and O += P V (V is the MN-major operand); S(t+1) is issued as soon
+//    as the softmax has read S(t), so it overlaps the softmax of tile t.
+//  * Warps 0-3 own one row each: they read the S row from TMEM
+//    (tcgen05.ld 32x32b), apply the causal / offset mask, keep the running
+//    max and sum in registers, rescale the O row in TMEM when a warp's max
+//    grows, and write P as bf16 into a K-major 128B-swizzled tile for the
+//    second MMA.
+//  * Epilogue: O row / l -> bf16 -> global (only rows that are real queries).
+// Every wait is bounded; on a timeout the CTA records the error, drains its
+// MMAs and frees its TMEM before returning.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "pkv.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kPfWarps = 6;
+constexpr int kPfThreads = kPfWarps * 32;
+constexpr int kRows = 128;   // MMA M: query rows per CTA
+constexpr int kKeys = 128;   // keys per KV tile (MMA N of Q K^T, K of P V)
+constexpr int kD = 128;      // head_dim
+constexpr int kHalf = 128 * 64 * 2;  // one 128-row x 64-column bf16 half tile (16 KB)
+constexpr int kTileBytes = 2 * kHalf;  // 32 KB
+constexpr uint32_t kTmemCols = 256;    // S: columns [0,128), O: [128,256)
+constexpr float kLog2e = 1.4426950408889634f;
+
+// shared-memory carve, from a 1024-aligned base
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kTileBytes;                  // 2 stages x (K, V)
+constexpr int kOffP = kOffKV + 2 * 2 * kTileBytes;  // P tile
+constexpr int kOffBar = kOffP + kTileBytes;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;    // barriers + TMEM slot + alignment slack
+
+struct PfParams {
+  const int32_t* bt;
+  const int32_t* lens;
+  const int32_t* offs;
+  const long long* cu_q;
+  void* out;
+  int* err;
+  long long total_q;
+  long long blk_coord_limit;  // N * L (coordinate of the combined block/layer dimension)
+  long long num_blocks;
+  int mb, batch, hq, hkv, G, TQ, bs, L, layer;
+  float qscale;
+};
+
+// ---- tcgen05 / TMA helpers ----------------------------------------------------
+
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= 1ull << 46;  // descriptor version for this architecture
+  d |= 2ull << 61;  // 128-byte swizzle
+  return d;
+}
+
+// kind::f16 instruction descriptor: fp32 accumulate, bf16 A and B, M 128, N 128.
+constexpr uint32_t kIdescKK =
+    (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kIdescKMN = kIdescKK | (1u << 16);  // B MN-major
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* m, int x, int y, int z,
+                                       uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"((uint64_t)m), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap* m, int x, int y, int z,
+                                       int w, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"((uint64_t)m), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
+// ---- the kernel ------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, const PfParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  griddep_wait();
+  griddep_launch_dependents();
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // ---- work item -------------------------------------------------------------------
+  const int b = blockIdx.y, g = blockIdx.z;
+  const long long q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
+  const long long nq = q1 - q0;
+  const int TQ = p.TQ, G = p.G;
+  if (nq <= 0) return;
+  const long long ntq = (nq + TQ - 1) / TQ;
+  if (ntq > (long long)gridDim.x) {  // more queries than the host bound allowed for
+    if (blockIdx.x == 0 && tid == 0) set_error(p.err, kErrCapacity);
+    return;
+  }
+  if ((long long)blockIdx.x >= ntq) return;
+  const long long qt = ntq - 1 - blockIdx.x;  // heaviest (latest) query tiles first
+  const long long len = p.lens[b];
+  const int off = p.offs ? p.offs[b] : 0;
+  if (len < nq || off < 0 || off >= p.bs || q1 > p.total_q ||
+      (long long)off + len > (long long)p.mb * p.bs) {
+    if (tid == 0) set_error(p.err, kErrCapacity);
+    return;
+  }
+  const long long first_pos = len - nq;                       // logical position of query 0
+  const long long tq_last = min(nq, (qt + 1) * TQ) - 1;       // last query of this tile
+  const long long p_max = first_pos + tq_last;                // last key any row needs
+  const int n_tiles = (int)((off + p_max) / kKeys) + 1;
+  const int blocks_per_tile = kKeys / p.bs;
+  const long long spanned = ((long long)off + len + p.bs - 1) / p.bs;
+
+  // ---- shared memory, barriers, TMEM --------------------------------------------------
+  unsigned char* sQ = smem + kOffQ;
+  unsigned char* sP = smem + kOffP;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffBar + 128);
+  const uint32_t b_q = smem_addr(&bars[0]);
+  const uint32_t b_kvfull0 = smem_addr(&bars[1]);   // [1], [2]
+  const uint32_t b_kvempty0 = smem_addr(&bars[3]);  // [3], [4]
+  const uint32_t b_sfull = smem_addr(&bars[5]);
+  const uint32_t b_sfree = smem_addr(&bars[6]);
+  const uint32_t b_pfull = smem_addr(&bars[7]);
+  const uint32_t b_pvdone = smem_addr(&bars[8]);
+  const uint32_t b_drain = smem_addr(&bars[9]);
+  auto kv_full = [&](int s) { return b_kvfull0 + 8u * s; };
+  auto kv_empty = [&](int s) { return b_kvempty0 + 8u * s; };
+  auto sK = [&](int s) { return smem + kOffKV + s * 2 * kTileBytes; };
+  auto sV = [&](int s) { return smem + kOffKV + s * 2 * kTileBytes + kTileBytes; };
+
+  if (tid == 0) {
+    mbar_init(b_q, 1);
+    mbar_init(kv_full(0), 1);
+    mbar_init(kv_full(1), 1);
+    mbar_init(kv_empty(0), 1);
+    mbar_init(kv_empty(1), 1);
+    mbar_init(b_sfull, 1);
+    mbar_init(b_sfree, 4);
+    mbar_init(b_pfull, 4);
+    mbar_init(b_pvdone, 1);
+    mbar_init(b_drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tslot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t tS = tmem, tO = tmem + 128;
+  bool ok = true;
+
+  if (warp == 4) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      mbar_arrive_expect_tx(b_q, kTileBytes);
+      const int z = (int)(q0 + qt * TQ);
+      for (int h = 0; h < 2; ++h) tma_3d(smem_addr(sQ + h * kHalf), &tq, h * 64, g * G, z, b_q);
+    }
+    const int boxes = 2 * 2 * blocks_per_tile;  // (K, V) x halves x blocks
+    const int box_bytes = p.bs * 128;
+    for (int t = 0; t < n_tiles && ok; ++t) {
+      const int s = t & 1;
+      if (t >= 2 && !mbar_wait(kv_empty(s), ((t >> 1) - 1) & 1, p.err)) { ok = false; break; }
+      if (lane == 0) mbar_arrive_expect_tx(kv_full(s), 2 * kTileBytes);
+      __syncwarp();
+      for (int i = lane; i < boxes; i += 32) {
+        const int is_v = i / (2 * blocks_per_tile);
+        const int h = (i / blocks_per_tile) & 1;
+        const int k = i % blocks_per_tile;
+        const long long lb = (long long)t * blocks_per_tile + k;  // logical block
+        long long coord = p.blk_coord_limit;                       // out of range: zeros
+        if (lb < spanned) {
+          const int blk = p.bt[(long long)b * p.mb + lb];
+          if (blk >= 0 && blk < p.num_blocks) {
+            coord = (long long)blk * p.L + p.layer;
+          } else {
+            set_error(p.err, kErrIndex);
+          }
+        }
+        unsigned char* base = is_v ? sV(s) : sK(s);
+        tma_4d(smem_addr(base + h * kHalf + k * box_bytes), is_v ? &tv : &tk, h * 64, g, 0,
+               (int)coord, kv_full(s));
+      }
+      __syncwarp();
+    }
+  } else if (warp == 5) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      const uint32_t q_addr = smem_addr(sQ), p_addr = smem_addr(sP);
+      auto issue_s = [&](int t) {
+        const uint32_t k_addr = smem_addr(sK(t & 1));
+        tc_fence_after();
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t a = desc_sw128(q_addr + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
+          const uint64_t bd = desc_sw128(k_addr + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
+          umma(tS, a, bd, kIdescKK, k > 0);
+        }
+        umma_commit(b_sfull);
+      };
+      ok = mbar_wait(b_q, 0, p.err) && mbar_wait(kv_full(0), 0, p.err);
+      if (ok) issue_s(0);
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        if (t + 1 < n_tiles) {
+          if (!mbar_wait(kv_full((t + 1) & 1), ((t + 1) >> 1) & 1, p.err) ||
+              !mbar_wait(b_sfree, t & 1, p.err)) {
+            ok = false;
+            break;
+          }
+          issue_s(t + 1);
+        }
+        if (!mbar_wait(b_pfull, t & 1, p.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t v_addr = smem_addr(sV(t & 1));
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t a = desc_sw128(p_addr + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
+          const uint64_t bd = desc_sw128(v_addr + k * 2048, kHalf, 1024);
+          umma(tO, a, bd, kIdescKMN, (t > 0 || k > 0) ? 1u : 0u);
+        }
+        umma_commit(b_pvdone);
+        umma_commit(kv_empty(t & 1));
+      }
+      umma_commit(b_drain);  // arrives once every MMA issued above has completed
+    }
+  } else {
+    // ================= softmax warps 0-3: one row per thread =================
+    const int r = tid;                        // MMA row = TMEM lane
+    const int qtok = r / G, hh = r - qtok * G;
+    const long long qi = qt * TQ + qtok;      // query index within the sequence
+    const bool row_ok = qi < nq;
+    const long long pos = first_pos + qi;     // its logical position
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float m = -INFINITY, l = 0.f;
+    for (int t = 0; t < n_tiles && ok; ++t) {
+      if (!mbar_wait(b_sfull, t & 1, p.err)) { ok = false; break; }
+      tc_fence_after();
+      float sreg[kKeys];
+#pragma unroll
+      for (int c0 = 0; c0 < kKeys; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tS + lane_base + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sreg[c0 + j] = __uint_as_float(v[j]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_sfree);
+      // mask: the key in column c sits at table position t*128 + c, i.e. logical
+      // j = t*128 + c - off; it is valid for 0 <= j <= pos
+      const long long tp0 = (long long)t * kKeys;
+      const int c_lo = (int)max(0ll, (long long)off - tp0);
+      const int c_hi = row_ok ? (int)min((long long)kKeys - 1, pos + off - tp0) : -1;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kKeys; ++c) {
+        const bool valid = c >= c_lo && c <= c_hi;
+        sreg[c] = valid ? sreg[c] * p.qscale : -INFINITY;
+        mt = fmaxf(mt, sreg[c]);
+      }
+      const float m_new = fmaxf(m, mt);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = m == -INFINITY ? 0.f : exp2f(m - m_use);
+      if (t > 0) {
+        // O must hold P(t-1) V(t-1) before it is rescaled or P is rewritten
+        if (!mbar_wait(b_pvdone, (t - 1) & 1, p.err)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c0 = 0; c0 < kD; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tO + lane_base + c0, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+            tmem_st32(tO + lane_base + c0, v);
+          }
+          tmem_wait_st();
+        }
+      }
+      float psum = 0.f;
+      // P row (bf16) into the K-major 128B-swizzled P tile: 16-byte chunk ch of
+      // row r at (r/8)*1024 + (r%8)*128 + ((ch ^ (r%8)) * 16), per 64-column half
+#pragma unroll
+      for (int c = 0; c < kKeys; c += 8) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a0 = exp2f(sreg[c + 2 * e] - m_use);
+          const float a1 = exp2f(sreg[c + 2 * e + 1] - m_use);
+          psum += a0 + a1;
+          w[e] = pack_bf16x2(a0, a1);
+        }
+        const int half = c >> 6, chunk = (c & 63) >> 3;
+        unsigned char* dst =
+            sP + half * kHalf + (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      l = l * alpha + psum;
+      m = m_new;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_pfull);
+    }
+    // epilogue: O row / l -> bf16 -> out
+    if (ok && mbar_wait(b_pvdone, (n_tiles - 1) & 1, p.err)) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
+                            ((q0 + qi) * p.hq + (long long)g * G + hh) * kD;
+#pragma unroll
+      for (int c0 = 0; c0 < kD; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tO + lane_base + c0, v);
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(v[j]) * inv, __uint_as_float(v[j + 1]) * inv);
+            o.y = pack_bf16x2(__uint_as_float(v[j + 2]) * inv, __uint_as_float(v[j + 3]) * inv);
+            o.z = pack_bf16x2(__uint_as_float(v[j + 4]) * inv, __uint_as_float(v[j + 5]) * inv);
+            o.w = pack_bf16x2(__uint_as_float(v[j + 6]) * inv, __uint_as_float(v[j + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c0 + j) = o;
+          }
+        }
+      }
+    }
+  }
+
+  // ---- teardown: every MMA this CTA issued has completed before TMEM is freed ----
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    mbar_wait(b_drain, 0, p.err);
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---- host side ------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+bool encode(CUtensorMap* m, int rank, void* base, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int prefill_supported(const PoolView& pv, int num_q_heads) {
+  if (pv.elem_size != 2 || pv.head_dim != kD) return 1;
+  if (pv.block_size < 8 || pv.block_size > kKeys || kKeys % pv.block_size) return 1;
+  if (num_q_heads % pv.num_kv_heads) return 1;
+  const int G = num_q_heads / pv.num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return 1;
+  return 0;
+}
+
+cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num_q_heads,
+                           float scale, const int32_t* bt, int mb, const int32_t* lens,
+                           const int32_t* offs, const int64_t* cu_q, int batch, long long total_q,
+                           int max_q_len, void* out, int* err, cudaStream_t s) {
+  if (batch == 0 || total_q == 0 || max_q_len == 0) return cudaSuccess;
+  const int G = num_q_heads / pv.num_kv_heads;
+  const int TQ = kRows / G;
+  CUtensorMap tq, tk, tv;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)num_q_heads * kD * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)TQ};
+    if (!encode(&tq, 3, const_cast<void*>(q), dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  const long long nl = pv.num_blocks * pv.num_layers;
+  {
+    cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)pv.num_kv_heads, (cuuint64_t)pv.block_size,
+                          (cuuint64_t)nl};
+    cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)pv.row_bytes,
+                             (cuuint64_t)pv.row_bytes * pv.block_size};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)pv.block_size, 1};
+    if (!encode(&tk, 4, const_cast<char*>(pv.k), dims, strides, box) ||
+        !encode(&tv, 4, const_cast<char*>(pv.v), dims, strides, box))
+      return cudaErrorInvalidValue;
+  }
+  PfParams p{};
+  p.bt = bt;
+  p.lens = lens;
+  p.offs = offs;
+  p.cu_q = reinterpret_cast<const long long*>(cu_q);
+  p.out = out;
+  p.err = err;
+  p.total_q = total_q;
+  p.blk_coord_limit = nl;
+  p.num_blocks = pv.num_blocks;
+  p.mb = mb;
+  p.batch = batch;
+  p.hq = num_q_heads;
+  p.hkv = pv.num_kv_heads;
+  p.G = G;
+  p.TQ = TQ;
+  p.bs = pv.block_size;
+  p.L = pv.num_layers;
+  p.layer = layer;
+  p.qscale = scale * kLog2e;
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && configured[dev] == 0) {
+    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  const dim3 grid((unsigned)((max_q_len + TQ - 1) / TQ), (unsigned)batch,
+                  (unsigned)pv.num_kv_heads);
+  return launch_kernel(prefill_kernel, grid, dim3(kPfThreads), (size_t)kSmemBytes, s, true, tq, tk,
+                       tv, p);
+}
+
+}  // namespace pkv

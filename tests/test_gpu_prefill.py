@@ -1,0 +1,113 @@
+"""GPU parity for paged prefill attention (tcgen05 kernel) against the oracle:
+causal attention of each sequence's last n_b tokens over its paged K/V."""
+
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_blk_gb300 as pkv
+from paged_kv_cache_blk_gb300 import PkvError
+from workloads import PoolSpec, rand_rows, to_numpy_bits
+from workloads.gen import FreeList, _pack
+
+from gpu_util import max_abs, need_gpu, widen_out
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    d = need_gpu()
+    pkv.set_validate(False)
+    pkv.device_error(clear=True)
+    return d
+
+
+def _case(dev, seed, lens, nq, G, bs=16, hkv=2, offsets=True, num_blocks=None, layer=1):
+    rng = np.random.default_rng(seed)
+    lens = np.asarray(lens, np.int64)
+    B = len(lens)
+    offs = rng.integers(0, bs, size=B) if offsets else np.zeros(B, np.int64)
+    need = sum(-(-(int(o) + int(L)) // bs) for o, L in zip(offs, lens))
+    N = num_blocks or max(16, need + 8)
+    spec = PoolSpec(N, 2, bs, hkv, 128, "bf16")
+    free = FreeList(rng.permutation(N))
+    tables = [free.pop(-(-(int(o) + int(L)) // bs)) for o, L in zip(offs, lens)]
+    batch = _pack(tables, lens, offs)
+    nq = np.asarray(nq, np.int64)
+    cu = np.concatenate([[0], np.cumsum(nq)]).astype(np.int64)
+    k = rand_rows(spec.shape, "bf16", seed + 1, dev)
+    v = rand_rows(spec.shape, "bf16", seed + 2, dev)
+    q = rand_rows((int(cu[-1]), hkv * G, 128), "bf16", seed + 3, dev)
+    return spec, batch, cu, k, v, q, layer
+
+
+def _run(dev, spec, batch, cu, k, v, q, layer, scale=128 ** -0.5):
+    pool = pkv.Pool(k, v)
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+    out = torch.full_like(q, float("nan"))
+    nq = np.diff(cu)
+    pkv.prefill_attention(pool, layer, q, scale, t(batch.block_tables, torch.int32),
+                          t(batch.seq_lens, torch.int32), t(batch.offsets, torch.int32),
+                          t(cu, torch.int64), int(nq.max()) if len(nq) else 0, out)
+    torch.cuda.synchronize()
+    ref = oracle.prefill_attention(to_numpy_bits(k), to_numpy_bits(v), layer, to_numpy_bits(q),
+                                   batch.block_tables, batch.seq_lens, batch.offsets, cu, scale)
+    return out, ref
+
+
+CASES = [
+    # G, bs, lens, nq (queries = last nq tokens of each sequence)
+    (4, 16, [100], [100]),                         # whole prompt, one query tile + tail
+    (4, 16, [300, 37, 129], [300, 37, 129]),       # several tiles, ragged
+    (4, 16, [700, 260], [40, 260]),                # cached prefix then new tokens
+    (1, 16, [200, 130], [200, 5]),
+    (2, 32, [333, 64], [100, 64]),
+    (8, 16, [400, 17], [33, 17]),
+    (16, 16, [150, 90], [150, 8]),
+    (4, 8, [250], [250]),
+    (4, 128, [600, 1], [300, 1]),
+    (4, 64, [513, 128, 129], [513, 1, 2]),
+]
+
+
+@pytest.mark.parametrize("G,bs,lens,nq", CASES, ids=[f"G{c[0]}-bs{c[1]}-{c[2]}-{c[3]}" for c in CASES])
+def test_prefill_matches_oracle(dev, G, bs, lens, nq):
+    seed = zlib.crc32(repr((G, bs, lens, nq)).encode()) % 10000
+    spec, batch, cu, k, v, q, layer = _case(dev, seed, lens, nq, G, bs=bs)
+    out, ref = _run(dev, spec, batch, cu, k, v, q, layer)
+    assert torch.isfinite(out.float()).all()
+    assert max_abs(widen_out(out), ref) <= 2e-2
+    assert pkv.device_error() == "PKV_OK"
+
+
+def test_prefill_long_context_sampled(dev):
+    """Long cached prefix and a chunk of new tokens: the K/V ring cycles many
+    times.  Checked on every query of the chunk for all heads."""
+    spec, batch, cu, k, v, q, layer = _case(dev, 77, [3000, 2100], [256, 300], 4, hkv=2)
+    out, ref = _run(dev, spec, batch, cu, k, v, q, layer)
+    assert max_abs(widen_out(out), ref) <= 2e-2
+
+
+def test_prefill_empty_and_bounds(dev):
+    spec, batch, cu, k, v, q, layer = _case(dev, 88, [50, 60], [0, 60], 4)
+    out, ref = _run(dev, spec, batch, cu, k, v, q, layer)
+    assert max_abs(widen_out(out), ref) <= 2e-2
+    pool = pkv.Pool(k, v)
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+    # more queries than the host bound: that sequence is skipped and flagged
+    out2 = torch.zeros_like(q)
+    pkv.prefill_attention(pool, layer, q, 0.1, t(batch.block_tables, torch.int32),
+                          t(batch.seq_lens, torch.int32), t(batch.offsets, torch.int32),
+                          t(cu, torch.int64), 16, out2)
+    assert pkv.device_error() == "PKV_ERR_CAPACITY"
+    assert torch.count_nonzero(out2) == 0
+    with pytest.raises(PkvError) as e:
+        bad = torch.zeros((4, 3, 128), dtype=torch.bfloat16, device=dev)   # 3 heads: group 1.5
+        pkv.prefill_attention(pool, layer, bad, 0.1, t(batch.block_tables, torch.int32),
+                              t(batch.seq_lens, torch.int32), None, t(cu, torch.int64), 4,
+                              torch.zeros_like(bad))
+    assert e.value.name == "PKV_ERR_INVALID_ARG"

@@ -509,3 +509,64 @@ def test_copy_on_write_keeps_shared_prefix():
     g2 = O.gather_loop(k, 0, t2.block_ids, t2.num_tokens, t2.offset)
     assert np.array_equal(g1[:6], kn) and np.array_equal(g2[:6], kn)
     assert np.array_equal(g1[6], new1[0]) and np.array_equal(g2[6], new2[0])
+
+
+# ---------------------------------------------------------------------------
+# prefill attention
+# ---------------------------------------------------------------------------
+
+def _prefill_case(rng, group=2, B=3, maxlen=40):
+    k, v, _, bt, lens, offs = _rand_case(rng, group=group, B=B, maxlen=maxlen)
+    n = np.array([rng.integers(0, L + 1) for L in lens], np.int64)
+    cu = np.concatenate([[0], np.cumsum(n)]).astype(np.int64)
+    q = rng.standard_normal((int(cu[-1]), k.shape[3] * group, k.shape[4])).astype(np.float32)
+    return k, v, q, bt, lens, offs, cu
+
+
+def test_prefill_vs_sdpa_with_explicit_causal_mask():
+    rng = np.random.default_rng(15)
+    for group in (1, 2, 4):
+        k, v, q, bt, lens, offs, cu = _prefill_case(rng, group=group)
+        got = O.prefill_attention(k, v, 1, q, bt, lens, offs, cu, 0.31)
+        for b in range(len(lens)):
+            n, L = int(cu[b + 1] - cu[b]), int(lens[b])
+            if n == 0:
+                continue
+            kb = O.gather_indexed(k, 1, bt[b], L, int(offs[b])).astype(np.float64)
+            vb = O.gather_indexed(v, 1, bt[b], L, int(offs[b])).astype(np.float64)
+            qt = torch.from_numpy(q[cu[b]:cu[b + 1]].astype(np.float64)).permute(1, 0, 2)
+            kt = torch.from_numpy(kb).permute(1, 0, 2).repeat_interleave(group, 0)
+            vt = torch.from_numpy(vb).permute(1, 0, 2).repeat_interleave(group, 0)
+            # query i (position L-n+i) sees keys 0..L-n+i: a bottom-right aligned mask
+            mask = torch.arange(L)[None, :] <= (L - n + torch.arange(n))[:, None]
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qt, kt, vt, attn_mask=mask, scale=0.31).permute(1, 0, 2).numpy()
+            np.testing.assert_allclose(got[cu[b]:cu[b + 1]], ref, rtol=0, atol=1e-12)
+
+
+def test_prefill_whole_prompt_is_plain_causal_and_last_row_is_decode():
+    rng = np.random.default_rng(16)
+    k, v, _, bt, lens, offs = _rand_case(rng, group=2, B=2, maxlen=30)
+    lens = np.maximum(lens, 1).astype(np.int32)
+    for b in range(2):
+        nb = O.blocks_needed(int(lens[b]), 4, int(offs[b]))
+        bt[b, :nb] = np.arange(b * 10, b * 10 + nb)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    q = rng.standard_normal((int(cu[-1]), 4, 8)).astype(np.float32)
+    got = O.prefill_attention(k, v, 0, q, bt, lens, offs, cu, 0.5)
+    for b in range(2):
+        L = int(lens[b])
+        kb = O.gather_indexed(k, 0, bt[b], L, int(offs[b])).astype(np.float64)
+        vb = O.gather_indexed(v, 0, bt[b], L, int(offs[b])).astype(np.float64)
+        qt = torch.from_numpy(q[cu[b]:cu[b + 1]].astype(np.float64)).permute(1, 0, 2)
+        kt = torch.from_numpy(kb).permute(1, 0, 2).repeat_interleave(2, 0)
+        vt = torch.from_numpy(vb).permute(1, 0, 2).repeat_interleave(2, 0)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qt, kt, vt, is_causal=True, scale=0.5).permute(1, 0, 2).numpy()
+        np.testing.assert_allclose(got[cu[b]:cu[b + 1]], ref, atol=1e-12)
+        # the last prompt token attends to the whole sequence: a decode step
+        dec = O.decode_attention(k, v, 0, q[cu[b + 1] - 1][None], bt[b:b + 1], lens[b:b + 1],
+                                 offs[b:b + 1], 0.5)
+        np.testing.assert_allclose(got[cu[b + 1] - 1], dec[0], atol=1e-12)
+        # the first token attends only to itself: its V row
+        np.testing.assert_allclose(got[cu[b]], np.repeat(vb[0], 2, axis=0), atol=1e-14)
