@@ -550,6 +550,64 @@ def run_legs(args, dev, rank, flush, pkv):
     del pool, k, v, ko, vo, hk, hv, dk
     torch.cuda.empty_cache()
     out["allocator"] = allocator_leg()
+    out["prefill"] = prefill_leg(args, dev, flush, pkv)
+    return out
+
+
+def prefill_case(dev, kind: str, seed: int = 0):
+    """Prefill workloads on the decode-GQA head geometry (Hkv 8, Hq 32, D 128,
+    bf16, block 16) over a 1-layer pool: 'prompts' = 16 prompts of 2048 tokens,
+    all of them queries; 'chunk' = 16 sequences of 4096 tokens whose last 512
+    are the queries (chunked prefill after a cached prefix)."""
+    from workloads.gen import FreeList, PoolSpec, _pack
+    B, L, nq = (16, 2048, 2048) if kind == "prompts" else (16, 4096, 512)
+    bs, Hkv, G, D = 16, 8, 4, 128
+    spec = PoolSpec(B * L // bs + 64, 1, bs, Hkv, D, "bf16")
+    rng = np.random.default_rng(seed)
+    free = FreeList(rng.permutation(spec.num_blocks))
+    batch = _pack([free.pop(L // bs) for _ in range(B)], [L] * B, [0] * B)
+    cu = np.arange(B + 1, dtype=np.int64) * nq
+    k, v = new_pool(spec, dev)
+    fill_pool(k, v, spec, 0, seed)
+    q = rand_rows((B * nq, Hkv * G, D), "bf16", seed + 9, dev)
+    # algorithmic flops: 2 matmuls x 2 flops per (query, attended key, head, d)
+    keys = sum((L - nq + i + 1) for i in range(nq)) * B
+    flops = 4 * D * Hkv * G * keys
+    return spec, batch, cu, nq, k, v, q, flops
+
+
+def prefill_leg(args, dev, flush, pkv):
+    out = {}
+    for kind in ("prompts", "chunk"):
+        spec, batch, cu, nq, k, v, q, flops = prefill_case(dev, kind)
+        pool = pkv.Pool(k, v)
+        t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+        bt, lens, offs, cuq = (t(batch.block_tables, torch.int32), t(batch.seq_lens, torch.int32),
+                               t(batch.offsets, torch.int32), t(cu, torch.int64))
+        o = torch.empty_like(q)
+        fn = lambda: pkv.prefill_attention(pool, 0, q, 128 ** -0.5, bt, lens, offs, cuq, nq, o)
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        times, _ = timed(fn, max(10, args.steps // 10), flush)
+        ms = reduce_max(statistics.mean(times))
+        out[kind] = {"TFLOP/s": round(flops / (ms / 1e3) / 1e12, 1), "ms": round(ms, 4),
+                     "flops": flops, "queries": int(cu[-1]),
+                     "what": ("16 prompts x 2048 tokens, causal, Hq 32 / Hkv 8, D 128, bf16"
+                              if kind == "prompts" else
+                              "16 x (3584 cached + 512 new) tokens, causal, Hq 32 / Hkv 8")}
+        del pool, k, v, q, o
+        torch.cuda.empty_cache()
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        peaks = {"bf16_tflops": d["bf16_tflops"], "kind": "measured"}
+    except Exception:
+        peaks = {"bf16_tflops": 1900.0, "kind": "fallback"}
+    for kind in ("prompts", "chunk"):
+        out[kind]["frac_of_bf16_peak"] = round(out[kind]["TFLOP/s"] / peaks["bf16_tflops"], 4)
+    out["peak"] = peaks
     return out
 
 
@@ -788,6 +846,18 @@ def ncu_case(kind: str, launches: int = 4) -> int:
     torch.cuda.set_device(dev)
     pkv.build()
     pkv.load()
+    if kind == "prefill":
+        spec, batch, cu, nq, k, v, q, flops = prefill_case(dev, "prompts")
+        pool = pkv.Pool(k, v)
+        t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+        bt, lens, offs, cuq = (t(batch.block_tables, torch.int32), t(batch.seq_lens, torch.int32),
+                               t(batch.offsets, torch.int32), t(cu, torch.int64))
+        o = torch.empty_like(q)
+        for _ in range(launches):
+            pkv.prefill_attention(pool, 0, q, 128 ** -0.5, bt, lens, offs, cuq, nq, o)
+        torch.cuda.synchronize()
+        print(f"ncu case prefill: {launches} launches done")
+        return 0
     name = WORKLOAD if kind == "decode" else LEG_WORKLOAD
     w = make_workload(name)
     sp = w.pool
@@ -836,7 +906,7 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true",
                     help="time the step from eager API calls only (no CUDA graph replay)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--ncu-case", choices=["decode", "gather", "scatter"],
+    ap.add_argument("--ncu-case", choices=["decode", "gather", "scatter", "prefill"],
                     help="run a small-footprint case of one kernel (for ncu) and exit")
     ap.add_argument("--decode-sweep", action="store_true",
                     help="decode throughput on every decode workload (not the bench line)")
