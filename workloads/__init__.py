@@ -15,6 +15,7 @@ from .gen import (  # noqa: F401
     make_workload,
     small_workload,
     fill_pool,
+    fill_pool_i8,
     new_pool,
     rand_rows,
     to_numpy_bits,

@@ -28,19 +28,21 @@ from typing import Optional
 import numpy as np
 import torch
 
-DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
+DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "i8": torch.uint8}
 
 
 @dataclass(frozen=True)
 class PoolSpec:
-    """Shape of one K (or V) pool tensor ``[N, L, bs, Hkv, D]``."""
+    """Shape of one K (or V) pool tensor ``[N, L, bs, Hkv, D]``; an ``"i8"``
+    pool is bytes ``[N, L, bs, row_bytes]`` whose token rows hold Hkv * D int8
+    codes, then Hkv fp32 scales, then padding to a multiple of 16 bytes."""
 
     num_blocks: int
     num_layers: int
     block_size: int
     num_kv_heads: int
     head_dim: int
-    dtype: str  # "f32" | "bf16"
+    dtype: str  # "f32" | "bf16" | "i8"
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -48,7 +50,7 @@ class PoolSpec:
 
     @property
     def elem_size(self) -> int:
-        return 4 if self.dtype == "f32" else 2
+        return {"f32": 4, "bf16": 2, "i8": 1}[self.dtype]
 
     @property
     def row_elems(self) -> int:
@@ -57,10 +59,14 @@ class PoolSpec:
 
     @property
     def row_bytes(self) -> int:
+        if self.dtype == "i8":
+            return self.row_elems + (4 * self.num_kv_heads + 15) // 16 * 16
         return self.row_elems * self.elem_size
 
     @property
     def shape(self):
+        if self.dtype == "i8":
+            return (self.num_blocks, self.num_layers, self.block_size, self.row_bytes)
         return (self.num_blocks, self.num_layers, self.block_size,
                 self.num_kv_heads, self.head_dim)
 
@@ -395,6 +401,44 @@ def fill_pool(k_cache: torch.Tensor, v_cache: torch.Tensor, spec: PoolSpec,
         v_cache[lo:hi, layer].copy_(vv.to(spec.torch_dtype))
 
 
+def fill_pool_i8(k_cache: torch.Tensor, v_cache: torch.Tensor, spec: PoolSpec,
+                 layer: int, seed: int, k_boost_frac: float = 0.0,
+                 k_boost: float = 3.0) -> None:
+    """Fill one layer of two int8 pools with seeded random rows: codes are
+    N(0,1) * 42 rounded and clipped to [-127, 127] (the spread of absmax-coded
+    Gaussian rows), scales are uniform in [0.01, 0.04] (a Gaussian head's
+    absmax / 127), padding bytes are random.  With ``k_boost_frac`` > 0 the
+    K scales of that fraction of token rows are multiplied by ``k_boost``.
+    Drawn on the pool's device in fixed chunks of blocks."""
+    dev = k_cache.device
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed * 7919 + 29)
+    N, bs, H, D = spec.num_blocks, spec.block_size, spec.num_kv_heads, spec.head_dim
+    R = spec.row_bytes
+    boost = None
+    if k_boost_frac > 0:
+        rng = np.random.default_rng(seed * 104729 + 5)
+        nrows = N * bs
+        pick = rng.permutation(nrows)[:int(round(k_boost_frac * nrows))]
+        mask = np.zeros(nrows, dtype=bool)
+        mask[pick] = True
+        boost = torch.from_numpy(mask.reshape(N, bs)).to(dev)
+    for lo in range(0, N, _CHUNK_BLOCKS):
+        hi = min(N, lo + _CHUNK_BLOCKS)
+        for which, pool in ((0, k_cache), (1, v_cache)):
+            rows = torch.randint(0, 256, (hi - lo, bs, R), generator=g, device=dev,
+                                 dtype=torch.uint8)
+            codes = torch.randn((hi - lo, bs, H * D), generator=g, device=dev) * 42.0
+            codes = codes.round().clamp_(-127, 127).to(torch.int8)
+            sc = torch.rand((hi - lo, bs, H), generator=g, device=dev) * 0.03 + 0.01
+            if which == 0 and boost is not None:
+                sc = torch.where(boost[lo:hi, :, None], sc * k_boost, sc)
+            rows[:, :, :H * D] = codes.view(torch.uint8)
+            rows[:, :, H * D:H * D + 4 * H] = sc.contiguous().view(torch.uint8).view(
+                hi - lo, bs, 4 * H)
+            pool[lo:hi, layer].copy_(rows)
+
+
 def rand_rows(shape, dtype: str, seed: int, device) -> torch.Tensor:
     """N(0,1) drawn in fp32 on ``device`` and rounded once to ``dtype``."""
     g = torch.Generator(device=device)
@@ -408,6 +452,6 @@ def to_numpy_bits(t: torch.Tensor) -> np.ndarray:
     t = t.detach().cpu().contiguous()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
-    if t.dtype == torch.float32:
+    if t.dtype in (torch.float32, torch.uint8):
         return t.numpy()
     raise TypeError(f"unsupported dtype {t.dtype}")
