@@ -214,17 +214,32 @@ def preload(fn, clocks: "ClockSampler", min_s: float = 0.6, max_s: float = 5.0):
 # ---------------------------------------------------------------------------
 
 class DecodeStep:
-    """Device state of one decode-GQA replica and its step."""
+    """Device state of one decode-GQA replica and its step.  With ``quant``
+    the pool is an int8 pool of the same geometry (token rows of codes plus
+    one fp32 scale per kv head) and the scatter quantises the new rows."""
 
-    def __init__(self, dev, seed_shift: int):
+    def __init__(self, dev, seed_shift: int, quant: bool = False):
         import paged_kv_cache_blk_gb300 as pkv
+        from workloads import fill_pool_i8
+        from workloads.gen import PoolSpec
         self.pkv = pkv
         w = make_workload(WORKLOAD)
         self.w = w
         self.dev = dev
-        k, v = new_pool(w.pool, dev)
-        fill_pool(k, v, w.pool, w.layer, w.seed + seed_shift)
-        self.pool = pkv.Pool(k, v)
+        sp = w.pool
+        if quant:
+            spec = PoolSpec(sp.num_blocks, sp.num_layers, sp.block_size, sp.num_kv_heads,
+                            sp.head_dim, "i8")
+            k = torch.empty(spec.shape, dtype=torch.uint8, device=dev)
+            v = torch.empty_like(k)
+            fill_pool_i8(k, v, spec, w.layer, w.seed + seed_shift)
+            self.pool = pkv.Pool(k, v, spec.num_kv_heads, spec.head_dim)
+        else:
+            spec = sp
+            k, v = new_pool(sp, dev)
+            fill_pool(k, v, sp, w.layer, w.seed + seed_shift)
+            self.pool = pkv.Pool(k, v)
+        self.spec = spec
         t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
         b = w.batch
         self.host = {
@@ -251,8 +266,7 @@ class DecodeStep:
         for name in ("q", "k_new", "v_new"):
             self.host[name] = getattr(self, name).cpu().pin_memory()
         self.host_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        self.bytes = decode_bytes(b, w.pool.row_bytes, hq, D, w.pool.elem_size,
-                                  w.pool.block_size)
+        self.bytes = decode_bytes(b, spec.row_bytes, hq, D, 2, spec.block_size)
         self.launches_per_step = 4  # slot mapping, scatter, decode partial, combine
 
     def step(self):
@@ -477,6 +491,74 @@ def run_ours(args, rank, local_rank, world):
     return result
 
 
+def decode_events_hook(pkv):
+    """Events the library records around the decode partial kernel."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(); e1.record()
+    pkv.set_decode_events(e0, e1)
+    return e0, e1
+
+
+def graph_step_ms(step, steps: int, warmup: int, flush, dev) -> float:
+    """Mean device time of `step` replayed from a CUDA graph."""
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    times, _ = timed(graph.replay, steps, flush)
+    del graph
+    return statistics.mean(times)
+
+
+def int8_leg(args, dev, rank, flush, pkv) -> dict:
+    """The decode step of the decode-GQA workload over an int8 pool of the
+    same geometry: slot mapping, quantising scatter of the 64 new bf16 rows,
+    decode attention.  Step time from a CUDA graph, the partial kernel alone
+    from the library's events, and its roofline over the int8 bytes."""
+    st = DecodeStep(dev, seed_shift=rank, quant=True)
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+    times, kev = timed(st.step, args.steps, flush, lambda: decode_events_hook(pkv))
+    pkv.set_decode_events(None, None)
+    eager_ms = reduce_max(statistics.mean(times))
+    part_ms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    graph_ms = None if args.no_graph else reduce_max(
+        graph_step_ms(st.step, args.steps, args.warmup, flush, dev))
+    ms = graph_ms if graph_ms is not None else eager_ms
+    peak, kind = load_peaks()
+    db = st.bytes
+    out = {
+        "what": "decode_gqa step over an int8 pool 16384x32x16x(8x128 codes + 8 fp32 scales) "
+                "(1056-byte token rows): slot mapping + quantising scatter of 64 tokens + "
+                "paged decode attention (bf16 q / out)",
+        "ms_per_step": round(ms, 4),
+        "step_mode": "cuda_graph" if graph_ms is not None else "eager",
+        "eager_ms_per_step": round(eager_ms, 4),
+        "kv_read_bytes_per_step": db["kv"],
+        "GB/s": round(db["kv"] / (ms / 1e3) / 1e9, 1),
+        "tokens_per_s": round(st.w.batch.batch / (ms / 1e3), 1),
+        "decode_partial": {
+            "kernel": "decode_partial_kernel<int8,128,4>",
+            "avg_launch_ms": round(part_ms, 4),
+            "algorithmic_bytes_per_launch": db["total"],
+            "achieved_GBps": round(db["total"] / (part_ms / 1e3) / 1e9, 1),
+            "frac": round(db["total"] / (part_ms / 1e3) / 1e9 / peak, 4),
+            "peak": peak, "peak_kind": kind,
+        },
+    }
+    del st
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_legs(args, dev, rank, flush, pkv):
     w = make_workload(LEG_WORKLOAD)
     k, v = new_pool(w.pool, dev)
@@ -551,6 +633,7 @@ def run_legs(args, dev, rank, flush, pkv):
     torch.cuda.empty_cache()
     out["allocator"] = allocator_leg()
     out["prefill"] = prefill_leg(args, dev, flush, pkv)
+    out["int8_decode"] = int8_leg(args, dev, rank, flush, pkv)
     return out
 
 
@@ -858,19 +941,27 @@ def ncu_case(kind: str, launches: int = 4) -> int:
         torch.cuda.synchronize()
         print(f"ncu case prefill: {launches} launches done")
         return 0
-    name = WORKLOAD if kind == "decode" else LEG_WORKLOAD
+    name = WORKLOAD if kind.startswith("decode") else LEG_WORKLOAD
     w = make_workload(name)
     sp = w.pool
-    one = PoolSpec(sp.num_blocks, 1, sp.block_size, sp.num_kv_heads, sp.head_dim, sp.dtype)
-    k, v = new_pool(one, dev)
-    fill_pool(k, v, one, 0, w.seed)
-    pool = pkv.Pool(k, v)
+    if kind == "decode_i8":
+        from workloads import fill_pool_i8
+        one = PoolSpec(sp.num_blocks, 1, sp.block_size, sp.num_kv_heads, sp.head_dim, "i8")
+        k = torch.empty(one.shape, dtype=torch.uint8, device=dev)
+        v = torch.empty_like(k)
+        fill_pool_i8(k, v, one, 0, w.seed)
+        pool = pkv.Pool(k, v, one.num_kv_heads, one.head_dim)
+    else:
+        one = PoolSpec(sp.num_blocks, 1, sp.block_size, sp.num_kv_heads, sp.head_dim, sp.dtype)
+        k, v = new_pool(one, dev)
+        fill_pool(k, v, one, 0, w.seed)
+        pool = pkv.Pool(k, v)
     b = w.batch
     t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
     bt, lens, offs, cu = (t(b.block_tables, torch.int32), t(b.seq_lens, torch.int32),
                           t(b.offsets, torch.int32), t(b.cu_seqlens, torch.int64))
     row = (sp.num_kv_heads, sp.head_dim)
-    if kind == "decode":
+    if kind.startswith("decode"):
         q = rand_rows((b.batch, w.num_q_heads, sp.head_dim), "bf16", 1, dev)
         out = torch.empty_like(q)
         ws = torch.empty(pkv.decode_workspace_size(b.batch, w.num_q_heads, sp.head_dim, dev),
@@ -906,7 +997,8 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true",
                     help="time the step from eager API calls only (no CUDA graph replay)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--ncu-case", choices=["decode", "gather", "scatter", "prefill"],
+    ap.add_argument("--ncu-case", choices=["decode", "decode_i8", "gather", "scatter",
+                                           "prefill"],
                     help="run a small-footprint case of one kernel (for ncu) and exit")
     ap.add_argument("--decode-sweep", action="store_true",
                     help="decode throughput on every decode workload (not the bench line)")

@@ -80,10 +80,18 @@ typedef enum {
   PKV_ERR_NO_BLOCKS = 8     /* allocator: too few free blocks; nothing was changed */
 } pkv_status;
 
-typedef enum { PKV_F32 = 0, PKV_BF16 = 1 } pkv_dtype;
+/* PKV_I8 is the quantised pool ([ch12] §6 Evolution names int8 KV as the
+ * next step of paged caches; the scheme below is this library's reading).
+ * Its token row (all kv heads of one token) is a byte row of
+ *     R = num_kv_heads * head_dim + pad16(4 * num_kv_heads)
+ * bytes: the num_kv_heads * head_dim int8 codes (head-major), then one fp32
+ * scale per kv head (little-endian), then padding to a multiple of 16 bytes.
+ * The stored value of element d of head g is code[g][d] * scale[g]. */
+typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_I8 = 2 } pkv_dtype;
 
 /* Pool descriptor: two device tensors [num_blocks, num_layers, block_size,
- * num_kv_heads, head_dim] of `dtype`.  block_size must be a power of two in
+ * num_kv_heads, head_dim] of `dtype` (PKV_I8: bytes [num_blocks, num_layers,
+ * block_size, R], R as above).  block_size must be a power of two in
  * [1, 1024]; num_kv_heads * head_dim * element size must be a multiple of 16
  * bytes.  ([vllm-notes] §2.2 layout; [ch12] §4.2 uses block_size 16.) */
 typedef struct {
@@ -121,7 +129,13 @@ PKV_API pkv_status pkv_build_slot_mapping(const pkv_pool* pool, const int32_t* b
  *
  * For t < num_tokens with s = slot_mapping[t] >= 0:
  *     k_cache[s / bs][layer][s % bs] = k_new[t],  v_cache[...] = v_new[t].
- * k_new, v_new: [num_tokens, Hkv, D] in the pool dtype, contiguous.  Entries
+ * k_new, v_new: [num_tokens, Hkv, D] in the pool dtype, contiguous.
+ * PKV_I8 pools take bf16 k_new / v_new and quantise each (token, kv head)
+ * row of D values x on the way in: scale = absmax(x) / 127 and
+ * code = round_half_even(x / scale) clamped to [-127, 127], both divisions
+ * IEEE fp32 round-to-nearest (subnormals kept); a row of zeros stores scale
+ * 0 and codes 0.  The padding bytes of the row are not written.  For int8
+ * pools head_dim must be 32, 64, 128 or 256 (else PKV_ERR_UNSUPPORTED).  Entries
  * equal to -1 are skipped and their rows untouched.  Other negative entries
  * and entries >= num_blocks * bs are skipped and set the device error word
  * (PKV_ERR_INDEX in validate mode).  Non-negative slots must be distinct; a
@@ -136,7 +150,7 @@ PKV_API pkv_status pkv_write_slots(const pkv_pool* pool, int32_t layer, const vo
  * For every sequence b and i < seq_lens[b], with p = offsets[b] + i:
  *     k_out[cu_seqlens[b] + i] = k_cache[block_tables[b][p / bs]][layer][p % bs]
  * and the same for V.  k_out, v_out: [total_tokens, Hkv, D] contiguous, pool
- * dtype.  cu_seqlens: int64 [batch + 1], the packed output layout, with
+ * dtype (PKV_I8: the byte rows as stored, [total_tokens, R]).  cu_seqlens: int64 [batch + 1], the packed output layout, with
  * cu_seqlens[0] = 0, cu_seqlens[b+1] - cu_seqlens[b] = seq_lens[b] and
  * cu_seqlens[batch] = total_tokens (validate mode checks all three).
  * total_tokens is the number of output rows the caller allocated.  A row
@@ -162,13 +176,17 @@ PKV_API size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int
  *     out[b][h] = sum_i softmax(s)_i * V_i[g].
  * q, out: [batch, num_q_heads, head_dim] contiguous in the pool dtype.
  * seq_lens[b] == 0 gives an all-zero row.  Accumulation is fp32.
+ * For PKV_I8 pools q and out are bf16 and K_i, V_i are the dequantised
+ * rows (code * scale; the kernel computes q . codes on fp16 tensor cores
+ * with q scaled by a power of two, and folds the V scales into the softmax
+ * weights, which are rounded to bf16 for the P.V product).
  * The work is split along the sequence across the GPU; partial softmax
  * states go to `workspace` (>= pkv_decode_workspace_size bytes, contents
  * need no initialisation and are overwritten) and a second kernel combines
  * them.  Both kernels are launched as programmatic dependents of the work
  * before them on the stream and wait for it before reading any input, so the
  * call may be captured in a CUDA graph and replayed.  Supported: head_dim 64 or 128; num_kv_heads 1, 2, 4 or 8;
- * num_q_heads / num_kv_heads 1, 2, 4 or 8; either dtype; any block_size the
+ * num_q_heads / num_kv_heads 1, 2, 4 or 8; any pool dtype; any block_size the
  * pool allows.  Others return PKV_ERR_UNSUPPORTED.  A sequence whose offset
  * is out of range or whose length exceeds its table row's capacity is
  * treated as empty and sets the device error word (PKV_ERR_CAPACITY in
@@ -180,7 +198,7 @@ PKV_API pkv_status pkv_decode_attention(const pkv_pool* pool, int32_t layer, con
                                 int32_t batch, void* out, void* workspace,
                                 size_t workspace_bytes, cudaStream_t stream);
 
-/* Paged prefill attention (SURVEY next row; the prefill batch of
+/* Paged prefill attention (the prefill batch of
  * "vLLM PagedAttention source notes" §2.4: the prompt tokens' K/V are written
  * into their blocks, then attention runs over them), on tcgen05 tensor cores.
  *
@@ -257,7 +275,8 @@ PKV_API pkv_status pkv_copy_blocks(const pkv_pool* pool, int32_t layer, const in
 
 /* pkv_swap_out: the K and V data of blocks[0..n) (device int32 array), in
  * that order, into host_k / host_v laid out [n, layers, block_size,
- * num_kv_heads, head_dim] (layers = 1 for a single layer).  pkv_swap_in: the
+ * num_kv_heads, head_dim] (layers = 1 for a single layer; PKV_I8 pools:
+ * [n, layers, block_size, R] bytes, codes and scales together).  pkv_swap_in: the
  * reverse, host buffers into the listed blocks.  Preemption by swapping
  * ("vLLM PagedAttention source notes" §2.4).  host_k and host_v must be
  * page-locked host memory the device can address (cudaHostAlloc or

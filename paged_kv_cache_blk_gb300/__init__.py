@@ -1,6 +1,8 @@
 """GB300 paged KV cache hot path: slot mapping, scatter, gather and fused
-paged decode attention, as hand-written CUDA kernels behind the C ABI in
-``include/pkv.h`` (``libpkv.so``), with this thin ctypes binding."""
+paged decode attention (bf16, fp32 and int8 pools), paged prefill attention,
+block copy / swap and the host block allocator, as hand-written CUDA and C++
+behind the C ABI in ``include/pkv.h`` (``libpkv.so``), with this thin ctypes
+binding."""
 
 from ._binding import (  # noqa: F401
     Allocator,
@@ -15,6 +17,7 @@ from ._binding import (  # noqa: F401
     device_error,
     gather,
     get_validate,
+    int8_row_bytes,
     library_path,
     load,
     prefill_attention,

@@ -24,7 +24,7 @@ _STATUS = {
     8: "PKV_ERR_NO_BLOCKS",
 }
 STATUS_CODES = {v: k for k, v in _STATUS.items()}
-_DTYPE = {torch.float32: 0, torch.bfloat16: 1}
+_DTYPE = {torch.float32: 0, torch.bfloat16: 1, torch.uint8: 2}
 
 
 class PkvError(RuntimeError):
@@ -127,19 +127,38 @@ def _stream(dev: torch.device) -> int:
     return torch.cuda.current_stream(dev).cuda_stream
 
 
+def int8_row_bytes(num_kv_heads: int, head_dim: int) -> int:
+    """Bytes of one token row of an int8 pool (PKV_I8 in include/pkv.h)."""
+    return num_kv_heads * head_dim + (4 * num_kv_heads + 15) // 16 * 16
+
+
 class Pool:
     """K and V block pools ``[num_blocks, num_layers, block_size, num_kv_heads,
-    head_dim]`` on one CUDA device, as the library's pool descriptor."""
+    head_dim]`` on one CUDA device, as the library's pool descriptor.  An int8
+    pool is a pair of uint8 tensors ``[num_blocks, num_layers, block_size, R]``
+    (R = :func:`int8_row_bytes`) with ``num_kv_heads`` and ``head_dim`` given."""
 
-    def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor):
+    def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                 num_kv_heads: Optional[int] = None, head_dim: Optional[int] = None):
         if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
             raise ValueError("k_cache and v_cache must have the same shape and dtype")
-        if k_cache.dim() != 5 or not k_cache.is_contiguous() or not v_cache.is_contiguous():
-            raise ValueError("pools must be contiguous [N, L, bs, Hkv, D] tensors")
+        if not k_cache.is_contiguous() or not v_cache.is_contiguous():
+            raise ValueError("pools must be contiguous tensors")
         if k_cache.dtype not in _DTYPE:
             raise ValueError(f"unsupported pool dtype {k_cache.dtype}")
+        if k_cache.dtype == torch.uint8:
+            if k_cache.dim() != 4 or num_kv_heads is None or head_dim is None:
+                raise ValueError("int8 pools are [N, L, bs, R] uint8 tensors with "
+                                 "num_kv_heads and head_dim given")
+            if k_cache.shape[3] != int8_row_bytes(num_kv_heads, head_dim):
+                raise ValueError("int8 pool rows do not match num_kv_heads and head_dim")
+            N, L, bs = k_cache.shape[:3]
+            H, D = num_kv_heads, head_dim
+        else:
+            if k_cache.dim() != 5:
+                raise ValueError("pools must be contiguous [N, L, bs, Hkv, D] tensors")
+            N, L, bs, H, D = k_cache.shape
         self.k_cache, self.v_cache = k_cache, v_cache
-        N, L, bs, H, D = k_cache.shape
         self.struct = _PoolStruct(k_cache.data_ptr(), v_cache.data_ptr(), N, L, bs, H, D,
                                   _DTYPE[k_cache.dtype])
         self.device = k_cache.device

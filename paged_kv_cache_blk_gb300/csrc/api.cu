@@ -66,7 +66,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
-int elem_size(int32_t dtype) { return dtype == PKV_F32 ? 4 : dtype == PKV_BF16 ? 2 : 0; }
+int elem_size(int32_t dtype) {
+  return dtype == PKV_F32 ? 4 : dtype == PKV_BF16 ? 2 : dtype == PKV_I8 ? 1 : 0;
+}
 
 // Geometry checks shared by every call; `need_ptrs` also checks the tensors.
 pkv_status check_pool(const pkv_pool* p, bool need_ptrs, pkv::PoolView* v) {
@@ -76,8 +78,13 @@ pkv_status check_pool(const pkv_pool* p, bool need_ptrs, pkv::PoolView* v) {
   if (p->num_blocks <= 0 || p->num_layers <= 0 || p->num_kv_heads <= 0 || p->head_dim <= 0)
     return PKV_ERR_INVALID_ARG;
   if (!pow2(p->block_size) || p->block_size > 1024) return PKV_ERR_INVALID_ARG;
-  const long long row = (long long)p->num_kv_heads * p->head_dim * es;
-  if (row % 16 != 0 || row > (1ll << 30)) return PKV_ERR_UNSUPPORTED;
+  const long long elems = (long long)p->num_kv_heads * p->head_dim;
+  if (elems > (1ll << 28)) return PKV_ERR_UNSUPPORTED;
+  const bool quant = p->dtype == PKV_I8;
+  // int8 rows: codes, then one fp32 scale per kv head padded to 16 bytes
+  const long long row =
+      quant ? elems + (4ll * p->num_kv_heads + 15) / 16 * 16 : elems * es;
+  if ((elems * es) % 16 != 0) return PKV_ERR_UNSUPPORTED;
   if (need_ptrs) {
     if (!p->k_cache || !p->v_cache) return PKV_ERR_INVALID_ARG;
     if (!aligned16(p->k_cache) || !aligned16(p->v_cache)) return PKV_ERR_INVALID_ARG;
@@ -93,6 +100,9 @@ pkv_status check_pool(const pkv_pool* p, bool need_ptrs, pkv::PoolView* v) {
   v->head_dim = p->head_dim;
   v->elem_size = es;
   v->row_bytes = (int)row;
+  v->quant = quant ? 1 : 0;
+  v->io_size = quant ? 2 : es;
+  v->scale_off = quant ? (int)elems : 0;
   return PKV_OK;
 }
 
@@ -145,6 +155,10 @@ int decode_grid(const DevInfo& d) {
 }  // namespace
 
 namespace pkv {
+
+int pool_view(const pkv_pool* p, bool need_ptrs, PoolView* v) {
+  return check_pool(p, need_ptrs, v);
+}
 
 int device_facts(int* smem_optin, int** err_word, int* grid, int* validate) {
   DevInfo* d;
@@ -205,6 +219,8 @@ pkv_status pkv_write_slots(const pkv_pool* pool, int32_t layer, const void* k_ne
   if (st != PKV_OK) return st;
   if (layer < 0 || layer >= pool->num_layers || num_tokens < 0) return PKV_ERR_INVALID_ARG;
   if (num_tokens == 0) return PKV_OK;
+  if (v.quant && v.head_dim != 32 && v.head_dim != 64 && v.head_dim != 128 && v.head_dim != 256)
+    return PKV_ERR_UNSUPPORTED;
   if (!k_new || !v_new || !slot_mapping) return PKV_ERR_INVALID_ARG;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned(slot_mapping, 8))
     return PKV_ERR_INVALID_ARG;
@@ -305,8 +321,8 @@ pkv_status pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void*
     pkv::DecodeLaunch a;
     a.pool = v;
     a.layer = layer;
-    a.q = static_cast<const char*>(q) + b0 * row_elems * v.elem_size;
-    a.out = static_cast<char*>(out) + b0 * row_elems * v.elem_size;
+    a.q = static_cast<const char*>(q) + b0 * row_elems * v.io_size;
+    a.out = static_cast<char*>(out) + b0 * row_elems * v.io_size;
     a.num_q_heads = num_q_heads;
     a.scale = scale;
     a.bt = block_tables + (size_t)b0 * max_blocks_per_seq;

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
+#include "pkv.h"
+
 namespace pkv {
 
 // Bits of the sticky device error word.
@@ -161,9 +163,16 @@ struct PoolView {
   int block_size;
   int num_kv_heads;
   int head_dim;
-  int elem_size;
-  int row_bytes;  // num_kv_heads * head_dim * elem_size
+  int elem_size;  // bytes of one stored element (1 for the int8 codes)
+  int row_bytes;  // bytes of one token row (int8 pools: codes, scales, padding)
+  int quant;      // 1 for int8 pools
+  int io_size;    // element size of q, out, k_new, v_new (bf16 for int8 pools)
+  int scale_off;  // int8 pools: byte offset of the fp32 scales in a row
 };
+
+// Geometry and pointer checks of a pool descriptor (pkv_status value); fills
+// `v` when it returns PKV_OK.  `need_ptrs` also checks the two tensors.
+int pool_view(const pkv_pool* p, bool need_ptrs, PoolView* v);
 
 cudaError_t launch_slot_mapping(const PoolView& p, const int32_t* bt, int mb, const int32_t* offs,
                                 int batch, const int32_t* tok_seq, const int32_t* tok_pos,

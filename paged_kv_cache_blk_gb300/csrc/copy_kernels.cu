@@ -119,6 +119,110 @@ __global__ void __launch_bounds__(kCopyThreads) write_slots_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// quantising scatter (int8 pools): one warp per (token, kv head), K and V.
+// The D bf16 values of the head are spread D/32 per lane; the absmax is a
+// warp max over |x| bit patterns (the order of non-negative IEEE numbers),
+// scale = absmax / 127 and code = round_half_even(x / scale), both quotients
+// IEEE fp32 with subnormals kept (div.rn.f32 without .ftz, whatever the
+// fast-math flags), codes clamped to [-127, 127].  A zero absmax stores
+// scale 0 and codes 0.  The padding bytes of the row are not written.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float div_ieee(float a, float b) {
+  float r;
+  asm("div.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+template <int VPL>
+__device__ __forceinline__ void load_bf16(const __nv_bfloat16* src, float (&x)[VPL]) {
+  if constexpr (VPL == 8) {
+    const uint4 r = *reinterpret_cast<const uint4*>(src);
+    x[0] = bf16_lo(r.x); x[1] = bf16_hi(r.x); x[2] = bf16_lo(r.y); x[3] = bf16_hi(r.y);
+    x[4] = bf16_lo(r.z); x[5] = bf16_hi(r.z); x[6] = bf16_lo(r.w); x[7] = bf16_hi(r.w);
+  } else if constexpr (VPL == 4) {
+    const uint2 r = *reinterpret_cast<const uint2*>(src);
+    x[0] = bf16_lo(r.x); x[1] = bf16_hi(r.x); x[2] = bf16_lo(r.y); x[3] = bf16_hi(r.y);
+  } else if constexpr (VPL == 2) {
+    const uint32_t r = *reinterpret_cast<const uint32_t*>(src);
+    x[0] = bf16_lo(r); x[1] = bf16_hi(r);
+  } else {
+    x[0] = __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(src)) << 16);
+  }
+}
+
+// Quantise one head (VPL values per lane); returns the scale, codes in c.
+template <int VPL>
+__device__ __forceinline__ float quantise_head(const float (&x)[VPL], int (&c)[VPL]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) m = max(m, __float_as_uint(x[i]) & 0x7FFFFFFFu);
+  m = __reduce_max_sync(0xffffffffu, m);
+  const float scale = div_ieee(__uint_as_float(m), 127.f);
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    c[i] = m == 0 ? 0 : min(127, max(-127, __float2int_rn(div_ieee(x[i], scale))));
+  return scale;
+}
+
+template <int VPL>
+__device__ __forceinline__ void store_codes(char* dst, const int (&c)[VPL]) {
+  uint32_t w[(VPL + 3) / 4] = {};
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) w[i / 4] |= (uint32_t)(c[i] & 0xFF) << (8 * (i % 4));
+  if constexpr (VPL == 8) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+  } else if constexpr (VPL == 4) {
+    *reinterpret_cast<uint32_t*>(dst) = w[0];
+  } else if constexpr (VPL == 2) {
+    *reinterpret_cast<uint16_t*>(dst) = (uint16_t)w[0];
+  } else {
+    *reinterpret_cast<uint8_t*>(dst) = (uint8_t)w[0];
+  }
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(kCopyThreads) quant_write_slots_kernel(
+    char* __restrict__ kc, char* __restrict__ vc, const __nv_bfloat16* __restrict__ k_new,
+    const __nv_bfloat16* __restrict__ v_new, const int64_t* __restrict__ slots, long long n,
+    long long num_blocks, int L, int layer, int bs, int row_bytes, int hkv, int scale_off,
+    int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
+  constexpr int D = 32 * VPL;
+  const int lane = threadIdx.x & 31;
+  const long long tasks = n * hkv;
+  const long long warps = (long long)gridDim.x * kCopyWarps;
+  for (long long w = blockIdx.x * (long long)kCopyWarps + (threadIdx.x >> 5); w < tasks;
+       w += warps) {
+    const long long t = w / hkv;
+    const int g = (int)(w - t * hkv);
+    const int64_t s = slots[t];
+    if (s < 0) {
+      if (s != -1 && lane == 0 && g == 0) set_error(err, kErrIndex);
+      continue;  // -1 is padding: that row is not written
+    }
+    if (s >= num_blocks * bs) {
+      if (lane == 0 && g == 0) set_error(err, kErrIndex);
+      continue;
+    }
+    const long long row = row_offset(s / bs, layer, (int)(s % bs), L, bs, row_bytes);
+    const long long src = (t * hkv + g) * D + lane * VPL;
+    float xk[VPL], xv[VPL];
+    load_bf16<VPL>(k_new + src, xk);
+    load_bf16<VPL>(v_new + src, xv);
+    int ck[VPL], cv[VPL];
+    const float sk = quantise_head<VPL>(xk, ck);
+    const float sv = quantise_head<VPL>(xv, cv);
+    store_codes<VPL>(kc + row + g * D + lane * VPL, ck);
+    store_codes<VPL>(vc + row + g * D + lane * VPL, cv);
+    if (lane == 0) {
+      *reinterpret_cast<float*>(kc + row + scale_off + 4 * g) = sk;
+      *reinterpret_cast<float*>(vc + row + scale_off + 4 * g) = sv;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // gather: one warp per output row; the owning sequence is found by binary
 // search in the packed layout cu_seqlens (small and cache-resident)
 // ---------------------------------------------------------------------------
@@ -251,6 +355,23 @@ cudaError_t launch_write_slots(const PoolView& p, int layer, const void* k_new, 
                                cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   (void)sm_count;
+  if (p.quant) {
+    const dim3 grid(grid_for(n * p.num_kv_heads, kCopyWarps, 1 << 24));
+    const auto* kn = static_cast<const __nv_bfloat16*>(k_new);
+    const auto* vn = static_cast<const __nv_bfloat16*>(v_new);
+#define PKV_QUANT_LAUNCH(VPL)                                                                  \
+  launch_kernel(quant_write_slots_kernel<VPL>, grid, dim3(kCopyThreads), 0, s, true, p.k_mut,  \
+                p.v_mut, kn, vn, slots, n, p.num_blocks, p.num_layers, layer, p.block_size,    \
+                p.row_bytes, p.num_kv_heads, p.scale_off, err)
+    switch (p.head_dim) {
+      case 32: return PKV_QUANT_LAUNCH(1);
+      case 64: return PKV_QUANT_LAUNCH(2);
+      case 128: return PKV_QUANT_LAUNCH(4);
+      case 256: return PKV_QUANT_LAUNCH(8);
+    }
+#undef PKV_QUANT_LAUNCH
+    return cudaErrorInvalidValue;
+  }
   return launch_kernel(write_slots_kernel, dim3(grid_for(n, kCopyWarps, 1 << 24)),
                        dim3(kCopyThreads), 0, s, true, p.k_mut, p.v_mut,
                        static_cast<const char*>(k_new), static_cast<const char*>(v_new), slots, n,

@@ -42,6 +42,9 @@
 //    error word and the warp leaves after the producer has drained its copies.
 #include <cfloat>
 #include <cmath>
+#include <type_traits>
+
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 
@@ -75,9 +78,11 @@ struct Params {
   long long* ws_meta;
   int* err;
   int mb, batch, hq, hkv, bs, row_bytes, rs, st, stages;
+  int scale_off;  // int8 pools: byte offset of the fp32 scales in a token row
+  int vrs;        // int8 pools: row pitch of a warp's bf16 V tile
   float qscale;
   // shared-memory carve (bytes from the start of dynamic smem)
-  int off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf;
+  int off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf, off_vbuf;
 };
 
 // ---- small helpers ----------------------------------------------------------
@@ -303,6 +308,123 @@ __device__ void run_producer(const Params& p, const Pipe& pp, const long long* s
   }
 }
 
+// Output index of accumulator row `pos`: the int8 path stores each group of
+// four V codes as (d0, d2, d1, d3) in its bf16 tile, so rows 1 and 2 of every
+// group of four swap back; the bf16 path keeps d in order.
+template <bool PERM>
+__device__ __forceinline__ int out_d(int pos) {
+  if constexpr (PERM) return (pos & ~3) | ((pos & 1) << 1) | ((pos >> 1) & 1);
+  else return pos;
+}
+
+// End of a segment for the tensor-core consumers: sum the row shares of l,
+// merge the warps that served the same kv head (when Hkv < 8), then write the
+// normalised output (sequence inside one CTA) or the partial state (m, l, acc)
+// to the workspace.  False when a bounded wait gave up.
+template <int D, int G, bool PERM>
+__device__ __forceinline__ bool mma_segment_end(const Params& p, const Pipe& pp, uint32_t& gph,
+                                                float (&o)[D / 16][4], float m0, float m1,
+                                                float l0, float l1, bool mv, int b, int seg,
+                                                int flags, int warp, int lane) {
+  constexpr int KS = D / 16;
+  const int hkv = p.hkv;
+  const int g = warp % hkv;
+  const int wsub = warp / hkv;
+  const int wph = kNW / hkv;
+  const int gl = lane >> 2;
+  const int qi = lane & 3;
+  float* mbuf = reinterpret_cast<float*>(pp.smem + p.off_mbuf);
+  // row sums: each thread held the share of its token rows
+  float L0 = l0, L1 = l1;
+#pragma unroll
+  for (int o2 = 4; o2 < 32; o2 <<= 1) {
+    L0 += __shfl_xor_sync(kFull, L0, o2);
+    L1 += __shfl_xor_sync(kFull, L1, o2);
+  }
+  float M0 = mv ? m0 : -INFINITY, M1 = mv ? m1 : -INFINITY;
+  const int h0 = 2 * qi, h1 = h0 + 1;
+  if (wph > 1) {
+    // merge the token shares of the warps serving the same kv head
+    float* mw = mbuf + warp * G * (D + 2);
+#pragma unroll
+    for (int kt = 0; kt < KS; ++kt) {
+      const int d0 = kt * 16 + gl, d1 = d0 + 8;
+      if (h0 < G) { mw[h0 * (D + 2) + d0] = o[kt][0]; mw[h0 * (D + 2) + d1] = o[kt][2]; }
+      if (h1 < G) { mw[h1 * (D + 2) + d0] = o[kt][1]; mw[h1 * (D + 2) + d1] = o[kt][3]; }
+    }
+    if (gl == 0) {
+      if (h0 < G) { mw[h0 * (D + 2) + D] = M0; mw[h0 * (D + 2) + D + 1] = L0; }
+      if (h1 < G) { mw[h1 * (D + 2) + D] = M1; mw[h1 * (D + 2) + D + 1] = L1; }
+    }
+    if (!group_sync(pp, gph, lane, p.err)) return false;
+    if (wsub == 0) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int h = h0 + hh;
+        if (h >= G) continue;
+        float Mx = -INFINITY;
+        for (int w2 = g; w2 < kNW; w2 += hkv) Mx = fmaxf(Mx, mbuf[(w2 * G + h) * (D + 2) + D]);
+        float Ls = 0.f;
+        float acc[KS][2];
+#pragma unroll
+        for (int kt = 0; kt < KS; ++kt) acc[kt][0] = acc[kt][1] = 0.f;
+        if (Mx != -INFINITY) {
+          for (int w2 = g; w2 < kNW; w2 += hkv) {
+            const float* src = mbuf + (w2 * G + h) * (D + 2);
+            if (src[D] == -INFINITY) continue;
+            const float wgt = exp2f(src[D] - Mx);
+            Ls += wgt * src[D + 1];
+#pragma unroll
+            for (int kt = 0; kt < KS; ++kt) {
+              acc[kt][0] += wgt * src[kt * 16 + gl];
+              acc[kt][1] += wgt * src[kt * 16 + gl + 8];
+            }
+          }
+        }
+#pragma unroll
+        for (int kt = 0; kt < KS; ++kt) {
+          o[kt][hh] = acc[kt][0];
+          o[kt][2 + hh] = acc[kt][1];
+        }
+        if (hh == 0) { M0 = Mx; L0 = Ls; } else { M1 = Mx; L1 = Ls; }
+      }
+    }
+    if (!group_sync(pp, gph, lane, p.err)) return false;
+  }
+  if (wsub == 0) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int h = h0 + hh;
+      if (h >= G) continue;
+      const float Lh = hh == 0 ? L0 : L1;
+      const float Mh = hh == 0 ? M0 : M1;
+      const long long row_out = (long long)b * p.hq + g * G + h;
+      const long long row_ws = (long long)seg * p.hq + g * G + h;
+      if (flags & kSingle) {
+        const float inv = Lh > 0.f ? 1.f / Lh : 0.f;
+#pragma unroll
+        for (int kt = 0; kt < KS; ++kt) {
+          store_elem<__nv_bfloat16>(p.out, row_out * D + out_d<PERM>(kt * 16 + gl),
+                                    o[kt][hh] * inv);
+          store_elem<__nv_bfloat16>(p.out, row_out * D + out_d<PERM>(kt * 16 + gl + 8),
+                                    o[kt][2 + hh] * inv);
+        }
+      } else {
+#pragma unroll
+        for (int kt = 0; kt < KS; ++kt) {
+          p.ws_acc[row_ws * D + out_d<PERM>(kt * 16 + gl)] = o[kt][hh];
+          p.ws_acc[row_ws * D + out_d<PERM>(kt * 16 + gl + 8)] = o[kt][2 + hh];
+        }
+        if (gl == 0) {
+          p.ws_ml[row_ws * 2] = Mh;
+          p.ws_ml[row_ws * 2 + 1] = Lh;
+        }
+      }
+    }
+  }
+  return true;
+}
+
 // ---- bf16 consumer: tensor cores ---------------------------------------------
 
 template <int D, int G>
@@ -323,7 +445,6 @@ __device__ void run_consumer_mma(const Params& p, const Pipe& pp, int warp, int 
   const int pv_c = (lane >> 3) & 1;
   unsigned char* ptile = pp.smem + p.off_pbuf + warp * 256;  // P^T [16 t][8 h] bf16
   const uint32_t pt_addr = smem_addr(ptile);
-  float* mbuf = reinterpret_cast<float*>(pp.smem + p.off_mbuf);
   const float qs = p.qscale;
 
   uint32_t qb[KS][2];
@@ -410,93 +531,239 @@ __device__ void run_consumer_mma(const Params& p, const Pipe& pp, int warp, int 
     }
 
     if (flags & kEnd) {
-      // row sums: each thread held the share of its token rows
-      float L0 = l0, L1 = l1;
+      if (!mma_segment_end<D, G, false>(p, pp, gph, o, m0, m1, l0, l1, mv, b, seg, flags, warp,
+                                        lane))
+        return;
+    }
+
+    __syncwarp();
+    if (lane == 0) mbar_arrive(pp.empty(s));
+    if (++s == pp.stages) { s = 0; ph ^= 1; }
+    if (flags & kLast) break;
+  }
+}
+
+// ---- int8 consumer: tensor cores on converted codes ----------------------------
+//
+// K side.  q . (code * scale) = scale * (q . code): the 16 x 16 A fragments of
+// S^T are the raw codes of K converted to fp16 (exact, |code| <= 127), the B
+// fragments are q scaled by a power of two 2^e into fp16 (exact except for
+// values below 2^-14 of fp16's range, i.e. 2^-28 of the head's absmax), and
+// the fp32 accumulator is multiplied by scale_k * 2^-e per (token, head).  A
+// lane takes its A values from one contiguous run of D/4 codes per row: the
+// k index of the mma is a fixed permutation of d applied to both operands
+// (lane qi, k-step j, slots 2qi, 2qi+1, 2qi+8, 2qi+9 <-> d = (D/4) qi + 4j +
+// 0..3), which leaves every dot product unchanged.
+// V side.  sum_t p_t (code_t * scale_t) = sum_t (p_t scale_t) code_t: the V
+// scales are folded into the softmax weights before they are rounded to bf16,
+// and the codes of the 16 tokens of a tile are converted to a bf16 tile in
+// the warp's shared memory so the ldmatrix.trans path of the bf16 consumer
+// serves unchanged.  Each word of four codes becomes (d0, d2) and (d1, d3)
+// pairs (two masks, no byte shuffle), so the tile holds d in the order
+// 0, 2, 1, 3 within groups of four; out_d<true> undoes that at the end.
+
+// Four int8 codes -> two fp16x2 (codes 0,1 and 2,3): the codes, offset by
+// 128, become the low mantissa byte of 1024 + u; subtracting 1152 is exact.
+__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(x), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(x), "r"(0x64646464u));
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+  asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
+// Four int8 codes -> bf16x2 (codes 0, 2) and (codes 1, 3).  For a code c with
+// bits s:m (sign bit s, low seven bits m), bf16 128 + m minus bf16 128 (s = 0)
+// or 256 (s = 1) is c exactly.
+__device__ __forceinline__ void i8x4_to_bf16(uint32_t w, uint32_t& even, uint32_t& odd) {
+  const uint32_t w8 = w >> 8;
+  const uint32_t me = (w & 0x007F007Fu) | 0x43004300u, se = (w & 0x00800080u) | 0x43004300u;
+  const uint32_t mo = (w8 & 0x007F007Fu) | 0x43004300u, so = (w8 & 0x00800080u) | 0x43004300u;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(even) : "r"(me), "r"(se));
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(odd) : "r"(mo), "r"(so));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// D[16x8] += A[16x16] * B[16x8], fp16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int D, int G>
+__device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int lane) {
+  constexpr int KS = D / 16;  // k-steps of Q.K = m-tiles of P.V
+  constexpr int QW = D / 4;   // codes (bytes) of one K row a lane reads
+  const int hkv = p.hkv;
+  const int g = warp % hkv;
+  const int wsub = warp / hkv;
+  const int wph = kNW / hkv;
+  const int gl = lane >> 2;  // mma group row
+  const int qi = lane & 3;   // mma thread in group
+  const int rs = p.rs;
+  const int ST = p.st;
+  const int k_off = g * D + QW * qi;      // this lane's K codes within a row
+  const int s_off = p.scale_off + 4 * g;  // this head's scale within a row
+  const int vt = lane & 15, vh = lane >> 4;  // V conversion: token row, half of the head
+  const int pv_t = (lane & 7) + (lane >> 4) * 8;  // V rows (A of P.V, trans)
+  const int pv_c = (lane >> 3) & 1;
+  unsigned char* ptile = pp.smem + p.off_pbuf + warp * 256;  // P^T [16 t][8 h] bf16
+  const uint32_t pt_addr = smem_addr(ptile);
+  const int vrs = p.vrs;
+  unsigned char* vtile = pp.smem + p.off_vbuf + warp * 16 * vrs;  // [16 t][D] bf16
+  const uint32_t vt_addr = smem_addr(vtile);
+
+  uint32_t qb[KS][2];
+  float qs0 = 0.f, qs1 = 0.f;  // score factors of this lane's head columns 2qi, 2qi+1
+  float o[KS][4];
+  float m0 = 0.f, m1 = 0.f, l0 = 0.f, l1 = 0.f;
+  bool mv = false;
+
+  int s = 0;
+  uint32_t ph = 0, gph = 0;
+  while (true) {
+    if (!mbar_wait(pp.full(s), ph, p.err)) return;
+    const int4 dsc = pp.desc[s];
+    const int b = dsc.x, n = dsc.y, flags = dsc.z, seg = dsc.w;
+    const unsigned char* sK = pp.smem + (size_t)s * pp.stage_bytes;
+    const unsigned char* sV = sK + ST * rs;
+
+    if (flags & kStart) {
+      mv = false;
+      m0 = m1 = l0 = l1 = 0.f;
+#pragma unroll
+      for (int kt = 0; kt < KS; ++kt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[kt][c] = 0.f;
+      // this lane's QW query values of head g*G + gl (zero for padding columns)
+      uint4 raw[QW / 8];
+      const uint4* qrow = reinterpret_cast<const uint4*>(
+          static_cast<const char*>(p.q) + (((long long)b * p.hq + g * G + gl) * D + QW * qi) * 2);
+#pragma unroll
+      for (int i = 0; i < QW / 8; ++i) raw[i] = gl < G ? __ldg(qrow + i) : make_uint4(0, 0, 0, 0);
+      // |q| maximum of the head, compared as bf16 bit patterns
+      uint32_t mx = 0;
+#pragma unroll
+      for (int i = 0; i < QW / 8; ++i) {
+        const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mx = max(mx, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+      }
+      mx = max(mx, __shfl_xor_sync(kFull, mx, 1));
+      mx = max(mx, __shfl_xor_sync(kFull, mx, 2));
+      // 2^e brings the absmax into [2^14, 2^15): fp16 holds every bf16 value
+      // down to 2^-28 of it exactly
+      int e = 0;
+      if (mx != 0) e = min(126, max(-126, 141 - (int)((mx >> 7) & 0xFF)));
+      const float up = __uint_as_float((uint32_t)(127 + e) << 23);
+      const float down = __uint_as_float((uint32_t)(127 - e) << 23);
+#pragma unroll
+      for (int j = 0; j < KS; ++j) {
+        const uint4& r = raw[j >> 1];
+        const uint32_t w0 = (j & 1) ? r.z : r.x, w1 = (j & 1) ? r.w : r.y;
+        qb[j][0] = pack_f16x2(bf16_lo(w0) * up, bf16_hi(w0) * up);
+        qb[j][1] = pack_f16x2(bf16_lo(w1) * up, bf16_hi(w1) * up);
+      }
+      qs0 = p.qscale * __shfl_sync(kFull, down, (2 * qi) * 4);
+      qs1 = p.qscale * __shfl_sync(kFull, down, (2 * qi + 1) * 4);
+    }
+
+    for (int mt = wsub; mt * 16 < n; mt += wph) {
+      const int t_lo = mt * 16;
+      const int t0 = t_lo + gl, t1 = t0 + 8;
+      // rows past n hold stale data: read a valid row instead (it is masked)
+      const unsigned char* k0 = sK + min(t0, n - 1) * rs;
+      const unsigned char* k1 = sK + min(t1, n - 1) * rs;
+      uint32_t w0[KS], w1[KS];
+#pragma unroll
+      for (int i = 0; i < QW / 16; ++i) {
+        const uint4 a = *reinterpret_cast<const uint4*>(k0 + k_off + 16 * i);
+        const uint4 c = *reinterpret_cast<const uint4*>(k1 + k_off + 16 * i);
+        w0[4 * i] = a.x; w0[4 * i + 1] = a.y; w0[4 * i + 2] = a.z; w0[4 * i + 3] = a.w;
+        w1[4 * i] = c.x; w1[4 * i + 1] = c.y; w1[4 * i + 2] = c.z; w1[4 * i + 3] = c.w;
+      }
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < KS; ++j) {
+        uint32_t a[4];
+        i8x4_to_f16(w0[j], a[0], a[2]);
+        i8x4_to_f16(w1[j], a[1], a[3]);
+        mma_f16(sc, a, qb[j][0], qb[j][1]);
+      }
+      const float sk0 = *reinterpret_cast<const float*>(k0 + s_off);
+      const float sk1 = *reinterpret_cast<const float*>(k1 + s_off);
+      sc[0] = t0 < n ? sc[0] * qs0 * sk0 : -INFINITY;
+      sc[1] = t0 < n ? sc[1] * qs1 * sk0 : -INFINITY;
+      sc[2] = t1 < n ? sc[2] * qs0 * sk1 : -INFINITY;
+      sc[3] = t1 < n ? sc[3] * qs1 * sk1 : -INFINITY;
+      float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
       for (int o2 = 4; o2 < 32; o2 <<= 1) {
-        L0 += __shfl_xor_sync(kFull, L0, o2);
-        L1 += __shfl_xor_sync(kFull, L1, o2);
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o2));
       }
-      float M0 = mv ? m0 : -INFINITY, M1 = mv ? m1 : -INFINITY;
-      const int h0 = 2 * qi, h1 = h0 + 1;
-      if (wph > 1) {
-        // merge the token shares of the warps serving the same kv head
-        float* mw = mbuf + warp * G * (D + 2);
+      const float n0 = mv ? fmaxf(m0, mx0) : mx0;
+      const float n1 = mv ? fmaxf(m1, mx1) : mx1;
+      const float a0 = mv ? exp2f(m0 - n0) : 0.f;
+      const float a1 = mv ? exp2f(m1 - n1) : 0.f;
+      const float p0 = exp2f(sc[0] - n0), p1 = exp2f(sc[1] - n1);
+      const float p2 = exp2f(sc[2] - n0), p3 = exp2f(sc[3] - n1);
+      l0 = l0 * a0 + p0 + p2;  // this thread's share; summed over rows at the end
+      l1 = l1 * a1 + p1 + p3;
+      m0 = n0;
+      m1 = n1;
+      mv = true;
 #pragma unroll
-        for (int kt = 0; kt < KS; ++kt) {
-          const int d0 = kt * 16 + gl, d1 = d0 + 8;
-          if (h0 < G) { mw[h0 * (D + 2) + d0] = o[kt][0]; mw[h0 * (D + 2) + d1] = o[kt][2]; }
-          if (h1 < G) { mw[h1 * (D + 2) + d0] = o[kt][1]; mw[h1 * (D + 2) + d1] = o[kt][3]; }
-        }
-        if (gl == 0) {
-          if (h0 < G) { mw[h0 * (D + 2) + D] = M0; mw[h0 * (D + 2) + D + 1] = L0; }
-          if (h1 < G) { mw[h1 * (D + 2) + D] = M1; mw[h1 * (D + 2) + D + 1] = L1; }
-        }
-        if (!group_sync(pp, gph, lane, p.err)) return;
-        if (wsub == 0) {
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int h = h0 + hh;
-            if (h >= G) continue;
-            float Mx = -INFINITY;
-            for (int w2 = g; w2 < kNW; w2 += hkv) Mx = fmaxf(Mx, mbuf[(w2 * G + h) * (D + 2) + D]);
-            float Ls = 0.f;
-            float acc[KS][2];
-#pragma unroll
-            for (int kt = 0; kt < KS; ++kt) acc[kt][0] = acc[kt][1] = 0.f;
-            if (Mx != -INFINITY) {
-              for (int w2 = g; w2 < kNW; w2 += hkv) {
-                const float* src = mbuf + (w2 * G + h) * (D + 2);
-                if (src[D] == -INFINITY) continue;
-                const float wgt = exp2f(src[D] - Mx);
-                Ls += wgt * src[D + 1];
-#pragma unroll
-                for (int kt = 0; kt < KS; ++kt) {
-                  acc[kt][0] += wgt * src[kt * 16 + gl];
-                  acc[kt][1] += wgt * src[kt * 16 + gl + 8];
-                }
-              }
-            }
-#pragma unroll
-            for (int kt = 0; kt < KS; ++kt) {
-              o[kt][hh] = acc[kt][0];
-              o[kt][2 + hh] = acc[kt][1];
-            }
-            if (hh == 0) { M0 = Mx; L0 = Ls; } else { M1 = Mx; L1 = Ls; }
-          }
-        }
-        if (!group_sync(pp, gph, lane, p.err)) return;
+      for (int kt = 0; kt < KS; ++kt) {
+        o[kt][0] *= a0; o[kt][1] *= a1; o[kt][2] *= a0; o[kt][3] *= a1;
       }
-      if (wsub == 0) {
+      // weights times the V scales of their tokens
+      const float sv0 = *reinterpret_cast<const float*>(sV + min(t0, n - 1) * rs + s_off);
+      const float sv1 = *reinterpret_cast<const float*>(sV + min(t1, n - 1) * rs + s_off);
+      *reinterpret_cast<uint32_t*>(ptile + gl * 16 + qi * 4) = pack_bf16x2(p0 * sv0, p1 * sv0);
+      *reinterpret_cast<uint32_t*>(ptile + (gl + 8) * 16 + qi * 4) =
+          pack_bf16x2(p2 * sv1, p3 * sv1);
+      // V codes of the 16 tokens -> bf16 tile (lane: token vt, half vh of the head)
+      {
+        const unsigned char* src = sV + min(t_lo + vt, n - 1) * rs + g * D + vh * (D / 2);
+        unsigned char* dst = vtile + vt * vrs + vh * D;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int h = h0 + hh;
-          if (h >= G) continue;
-          const float Lh = hh == 0 ? L0 : L1;
-          const float Mh = hh == 0 ? M0 : M1;
-          const long long row_out = (long long)b * p.hq + g * G + h;
-          const long long row_ws = (long long)seg * p.hq + g * G + h;
-          if (flags & kSingle) {
-            const float inv = Lh > 0.f ? 1.f / Lh : 0.f;
-#pragma unroll
-            for (int kt = 0; kt < KS; ++kt) {
-              store_elem<__nv_bfloat16>(p.out, row_out * D + kt * 16 + gl, o[kt][hh] * inv);
-              store_elem<__nv_bfloat16>(p.out, row_out * D + kt * 16 + gl + 8,
-                                        o[kt][2 + hh] * inv);
-            }
-          } else {
-#pragma unroll
-            for (int kt = 0; kt < KS; ++kt) {
-              p.ws_acc[row_ws * D + kt * 16 + gl] = o[kt][hh];
-              p.ws_acc[row_ws * D + kt * 16 + gl + 8] = o[kt][2 + hh];
-            }
-            if (gl == 0) {
-              p.ws_ml[row_ws * 2] = Mh;
-              p.ws_ml[row_ws * 2 + 1] = Lh;
-            }
-          }
+        for (int c = 0; c < D / 32; ++c) {
+          const uint4 w = *reinterpret_cast<const uint4*>(src + 16 * c);
+          uint4 lo, hi;
+          i8x4_to_bf16(w.x, lo.x, lo.y);
+          i8x4_to_bf16(w.y, lo.z, lo.w);
+          i8x4_to_bf16(w.z, hi.x, hi.y);
+          i8x4_to_bf16(w.w, hi.z, hi.w);
+          *reinterpret_cast<uint4*>(dst + 32 * c) = lo;
+          *reinterpret_cast<uint4*>(dst + 32 * c + 16) = hi;
         }
       }
+      __syncwarp();
+      uint32_t pb[2];
+      ldsm_x2_t(pb, pt_addr + (lane & 15) * 16);
+#pragma unroll
+      for (int kt = 0; kt < KS; ++kt) {
+        uint32_t a[4];
+        ldsm_x4_t(a, vt_addr + pv_t * vrs + (2 * kt + pv_c) * 16);
+        mma_bf16(o[kt], a, pb[0], pb[1]);
+      }
+      __syncwarp();
+    }
+
+    if (flags & kEnd) {
+      if (!mma_segment_end<D, G, true>(p, pp, gph, o, m0, m1, l0, l1, mv, b, seg, flags, warp,
+                                       lane))
+        return;
     }
 
     __syncwarp();
@@ -803,6 +1070,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
 
   if (warp == kNW) {
     run_producer(p, pp, s_cu, lane, x0, x1);
+  } else if constexpr (sizeof(T) == 1) {
+    run_consumer_i8<D, G>(p, pp, warp, lane);
   } else if constexpr (sizeof(T) == 2) {
     run_consumer_mma<D, G>(p, pp, warp, lane);
   } else {
@@ -880,15 +1149,19 @@ int stage_tokens(int bs, int row_bytes) {
 }
 
 struct Layout {
-  int st, rs, stages, smem, off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf;
+  int st, rs, vrs, stages, smem, off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf,
+      off_vbuf;
 };
 
 int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int smem_optin) {
+Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int smem_optin,
+                   bool quant) {
   Layout L{};
   L.st = stage_tokens(bs, row_bytes);
   L.rs = row_bytes + kRowPad;
+  L.vrs = quant ? 2 * D + 16 : 0;  // bf16 V tile rows, padded like the stage rows
+  const int vbuf = kNW * 16 * L.vrs;
   const int stage_bytes = 2 * L.st * L.rs;
   const int pbuf = kNW * (L.st * G * 4 > 256 ? L.st * G * 4 : 256);
   int fixed = 0;
@@ -898,6 +1171,7 @@ Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int 
   fixed = align_up(fixed, 16) + 8 * 16;           // scan scratch
   fixed = align_up(fixed, 16) + pbuf;
   if (hkv < kNW) fixed = align_up(fixed, 16) + 4 * kNW * G * (D + 2);
+  fixed = align_up(fixed, 16) + vbuf;
   fixed = align_up(fixed, 128);
   int stages = (smem_optin - fixed) / stage_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
@@ -910,6 +1184,7 @@ Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int 
   off = align_up(off, 16); L.off_pbuf = off; off += pbuf;
   off = align_up(off, 16); L.off_mbuf = off;
   if (hkv < kNW) off += 4 * kNW * G * (D + 2);
+  off = align_up(off, 16); L.off_vbuf = off; off += vbuf;
   L.smem = align_up(off, 16);
   return L;
 }
@@ -978,6 +1253,8 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   p.rs = L.rs;
   p.st = L.st;
   p.stages = L.stages;
+  p.scale_off = pv.scale_off;
+  p.vrs = L.vrs;
   p.qscale = a.scale * kLog2e;
   p.off_bar = L.off_bar;
   p.off_desc = L.off_desc;
@@ -985,6 +1262,7 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   p.off_scan = L.off_scan;
   p.off_pbuf = L.off_pbuf;
   p.off_mbuf = L.off_mbuf;
+  p.off_vbuf = L.off_vbuf;
 
   auto kern = decode_partial_kernel<T, D, G>;
   static int configured[64] = {0};
@@ -997,10 +1275,12 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   e = launch_kernel(kern, dim3(grid), dim3(kThreads), L.smem, s, pdl, p);
   if (e != cudaSuccess) return e;
   if (a.ev_stop && (e = cudaEventRecord(a.ev_stop, s)) != cudaSuccess) return e;
+  // int8 pools take and return bf16
+  using OutT = std::conditional_t<sizeof(T) == 1, __nv_bfloat16, T>;
   const dim3 cgrid((p.hq * D + 255) / 256, a.batch);
-  return launch_kernel(decode_combine_kernel<T>, cgrid, dim3(256), 0, s, pdl,
+  return launch_kernel(decode_combine_kernel<OutT>, cgrid, dim3(256), 0, s, pdl,
                        (const float*)p.ws_acc, (const float*)p.ws_ml, (const long long*)p.ws_cu,
-                       (const long long*)p.ws_meta, p.hq, D, static_cast<T*>(a.out));
+                       (const long long*)p.ws_meta, p.hq, D, static_cast<OutT*>(a.out));
 }
 
 template <typename T, int D>
@@ -1035,8 +1315,11 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s) {
   const PoolView& pv = a.pool;
   const int G = a.num_q_heads / pv.num_kv_heads;
   const Layout L = make_layout(pv.block_size, pv.row_bytes, pv.num_kv_heads, G, pv.head_dim,
-                               a.batch, a.smem_optin);
+                               a.batch, a.smem_optin, pv.quant != 0);
   if (L.stages < 2) return cudaErrorInvalidConfiguration;
+  if (pv.quant) {
+    return pv.head_dim == 128 ? run_g<int8_t, 128>(a, L, G, s) : run_g<int8_t, 64>(a, L, G, s);
+  }
   if (pv.elem_size == 2) {
     return pv.head_dim == 128 ? run_g<__nv_bfloat16, 128>(a, L, G, s)
                               : run_g<__nv_bfloat16, 64>(a, L, G, s);

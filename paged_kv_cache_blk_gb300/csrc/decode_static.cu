@@ -68,8 +68,6 @@ pkv_status scratch_address(void** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int elem_size(int32_t dtype) { return dtype == PKV_F32 ? 4 : dtype == PKV_BF16 ? 2 : 0; }
-
 }  // namespace
 
 extern "C" pkv_status pkv_decode_attention_static(const pkv_pool* pool, int32_t layer,
@@ -79,30 +77,9 @@ extern "C" pkv_status pkv_decode_attention_static(const pkv_pool* pool, int32_t 
                                                   const int32_t* seq_lens, const int32_t* offsets,
                                                   int32_t batch, void* out, cudaStream_t stream) {
   // ---- host-visible argument checks (same rules as pkv_decode_attention) ----
-  if (!pool) return PKV_ERR_INVALID_ARG;
-  const int es = elem_size(pool->dtype);
-  if (es == 0) return PKV_ERR_UNSUPPORTED;
-  if (pool->num_blocks <= 0 || pool->num_layers <= 0 || pool->num_kv_heads <= 0 ||
-      pool->head_dim <= 0)
-    return PKV_ERR_INVALID_ARG;
-  const int bs = pool->block_size;
-  if (bs <= 0 || (bs & (bs - 1)) != 0 || bs > 1024) return PKV_ERR_INVALID_ARG;
-  const long long row = (long long)pool->num_kv_heads * pool->head_dim * es;
-  if (row % 16 != 0 || row > (1ll << 30)) return PKV_ERR_UNSUPPORTED;
-  if (!pool->k_cache || !pool->v_cache || !aligned16(pool->k_cache) || !aligned16(pool->v_cache))
-    return PKV_ERR_INVALID_ARG;
   pkv::PoolView v;
-  v.k = static_cast<const char*>(pool->k_cache);
-  v.v = static_cast<const char*>(pool->v_cache);
-  v.k_mut = static_cast<char*>(pool->k_cache);
-  v.v_mut = static_cast<char*>(pool->v_cache);
-  v.num_blocks = pool->num_blocks;
-  v.num_layers = pool->num_layers;
-  v.block_size = bs;
-  v.num_kv_heads = pool->num_kv_heads;
-  v.head_dim = pool->head_dim;
-  v.elem_size = es;
-  v.row_bytes = (int)row;
+  pkv_status st = static_cast<pkv_status>(pkv::pool_view(pool, true, &v));
+  if (st != PKV_OK) return st;
   if (layer < 0 || layer >= pool->num_layers || batch < 0 || num_q_heads <= 0)
     return PKV_ERR_INVALID_ARG;
   if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
@@ -115,8 +92,7 @@ extern "C" pkv_status pkv_decode_attention_static(const pkv_pool* pool, int32_t 
 
   int smem_optin = 0, grid = 0, validate = 0;
   int* err = nullptr;
-  pkv_status st =
-      static_cast<pkv_status>(pkv::device_facts(&smem_optin, &err, &grid, &validate));
+  st = static_cast<pkv_status>(pkv::device_facts(&smem_optin, &err, &grid, &validate));
   if (st != PKV_OK) return st;
   // the fixed array bounds the shape: refuse what does not fit
   if (pkv::decode_workspace_bytes(batch, num_q_heads, v.head_dim, grid) >
@@ -141,8 +117,8 @@ extern "C" pkv_status pkv_decode_attention_static(const pkv_pool* pool, int32_t 
     pkv::DecodeLaunch a;
     a.pool = v;
     a.layer = layer;
-    a.q = static_cast<const char*>(q) + b0 * row_elems * v.elem_size;
-    a.out = static_cast<char*>(out) + b0 * row_elems * v.elem_size;
+    a.q = static_cast<const char*>(q) + b0 * row_elems * v.io_size;
+    a.out = static_cast<char*>(out) + b0 * row_elems * v.io_size;
     a.num_q_heads = num_q_heads;
     a.scale = scale;
     a.bt = block_tables + (size_t)b0 * max_blocks_per_seq;

@@ -122,6 +122,23 @@ def test_host_checks_decode(lib):
     assert lib.pkv_decode_attention(p, *nan) == S["PKV_ERR_INVALID_ARG"]
 
 
+def test_host_checks_int8_pools(lib):
+    # int8 pools: codes must fill 16-byte multiples, the quantising scatter
+    # takes head sizes 32..256 (powers of two), prefill takes bf16 pools only
+    p8 = ctypes.byref(_pool(dtype=2, num_kv_heads=1, head_dim=8))
+    assert lib.pkv_write_slots(p8, 0, 16, 16, 8, 1, None) == S["PKV_ERR_UNSUPPORTED"]
+    p96 = ctypes.byref(_pool(dtype=2, num_kv_heads=2, head_dim=96))
+    assert lib.pkv_write_slots(p96, 0, 16, 16, 8, 1, None) == S["PKV_ERR_UNSUPPORTED"]
+    p = ctypes.byref(_pool(dtype=2))
+    assert lib.pkv_write_slots(p, 0, 16, 16, 8, 0, None) == S["PKV_OK"]
+    assert lib.pkv_write_slots(p, 0, 24, 16, 8, 1, None) == S["PKV_ERR_INVALID_ARG"]
+    dec = [0, 16, 8, 0.1, 16, 4, 16, None, 2, 16, 16, 1 << 20, None]
+    assert lib.pkv_decode_attention(p96, *dec) == S["PKV_ERR_UNSUPPORTED"]
+    pre = [0, 16, 8, 0.1, 16, 4, 16, None, 16, 2, 4, 4, 16, None]
+    assert lib.pkv_prefill_attention(p, *pre) == S["PKV_ERR_UNSUPPORTED"]
+    assert B.int8_row_bytes(8, 128) == 1056 and B.int8_row_bytes(3, 32) == 112
+
+
 def test_options_and_strings(lib):
     assert lib.pkv_set_decode_ctas(-1) == S["PKV_ERR_INVALID_ARG"]
     assert lib.pkv_set_decode_ctas(0) == S["PKV_OK"]
