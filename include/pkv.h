@@ -177,9 +177,10 @@ PKV_API size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int
  * q, out: [batch, num_q_heads, head_dim] contiguous in the pool dtype.
  * seq_lens[b] == 0 gives an all-zero row.  Accumulation is fp32.
  * For PKV_I8 pools q and out are bf16 and K_i, V_i are the dequantised
- * rows (code * scale; the kernel computes q . codes on fp16 tensor cores
- * with q scaled by a power of two, and folds the V scales into the softmax
- * weights, which are rounded to bf16 for the P.V product).
+ * rows (code * scale).  Both products run on fp16 tensor cores over the
+ * exact codes: q is scaled by a power of two into fp16, and the V scales
+ * are folded into the softmax weights (normalised by a running power of
+ * two), which are rounded to fp16 for the P.V product.
  * The work is split along the sequence across the GPU; partial softmax
  * states go to `workspace` (>= pkv_decode_workspace_size bytes, contents
  * need no initialisation and are overwritten) and a second kernel combines

@@ -76,17 +76,11 @@ struct Runs {
 };
 
 int pool_runs(const pkv_pool* p, int32_t layer, Runs* r) {
-  const int es = p->dtype == PKV_F32 ? 4 : p->dtype == PKV_BF16 ? 2 : 0;
-  if (es == 0) return PKV_ERR_UNSUPPORTED;
-  if (p->num_blocks <= 0 || p->num_layers <= 0 || p->num_kv_heads <= 0 || p->head_dim <= 0 ||
-      p->block_size <= 0 || (p->block_size & (p->block_size - 1)) || p->block_size > 1024)
-    return PKV_ERR_INVALID_ARG;
-  if (!p->k_cache || !p->v_cache || !aligned16(p->k_cache) || !aligned16(p->v_cache))
-    return PKV_ERR_INVALID_ARG;
-  const long long row = (long long)p->num_kv_heads * p->head_dim * es;
-  if (row % 16) return PKV_ERR_UNSUPPORTED;
+  PoolView v;
+  const int st = pool_view(p, true, &v);  // geometry, tensors, row bytes of any dtype
+  if (st != PKV_OK) return st;
   if (layer < -1 || layer >= p->num_layers) return PKV_ERR_INVALID_ARG;
-  const long long layer_run = (long long)p->block_size * row;
+  const long long layer_run = (long long)p->block_size * v.row_bytes;
   r->stride = layer_run * p->num_layers;
   r->base = layer < 0 ? 0 : layer * layer_run;
   r->run = layer < 0 ? r->stride : layer_run;

@@ -308,20 +308,11 @@ __device__ void run_producer(const Params& p, const Pipe& pp, const long long* s
   }
 }
 
-// Output index of accumulator row `pos`: the int8 path stores each group of
-// four V codes as (d0, d2, d1, d3) in its bf16 tile, so rows 1 and 2 of every
-// group of four swap back; the bf16 path keeps d in order.
-template <bool PERM>
-__device__ __forceinline__ int out_d(int pos) {
-  if constexpr (PERM) return (pos & ~3) | ((pos & 1) << 1) | ((pos >> 1) & 1);
-  else return pos;
-}
-
 // End of a segment for the tensor-core consumers: sum the row shares of l,
 // merge the warps that served the same kv head (when Hkv < 8), then write the
 // normalised output (sequence inside one CTA) or the partial state (m, l, acc)
 // to the workspace.  False when a bounded wait gave up.
-template <int D, int G, bool PERM>
+template <int D, int G>
 __device__ __forceinline__ bool mma_segment_end(const Params& p, const Pipe& pp, uint32_t& gph,
                                                 float (&o)[D / 16][4], float m0, float m1,
                                                 float l0, float l1, bool mv, int b, int seg,
@@ -404,16 +395,16 @@ __device__ __forceinline__ bool mma_segment_end(const Params& p, const Pipe& pp,
         const float inv = Lh > 0.f ? 1.f / Lh : 0.f;
 #pragma unroll
         for (int kt = 0; kt < KS; ++kt) {
-          store_elem<__nv_bfloat16>(p.out, row_out * D + out_d<PERM>(kt * 16 + gl),
+          store_elem<__nv_bfloat16>(p.out, row_out * D + kt * 16 + gl,
                                     o[kt][hh] * inv);
-          store_elem<__nv_bfloat16>(p.out, row_out * D + out_d<PERM>(kt * 16 + gl + 8),
+          store_elem<__nv_bfloat16>(p.out, row_out * D + kt * 16 + gl + 8,
                                     o[kt][2 + hh] * inv);
         }
       } else {
 #pragma unroll
         for (int kt = 0; kt < KS; ++kt) {
-          p.ws_acc[row_ws * D + out_d<PERM>(kt * 16 + gl)] = o[kt][hh];
-          p.ws_acc[row_ws * D + out_d<PERM>(kt * 16 + gl + 8)] = o[kt][2 + hh];
+          p.ws_acc[row_ws * D + kt * 16 + gl] = o[kt][hh];
+          p.ws_acc[row_ws * D + kt * 16 + gl + 8] = o[kt][2 + hh];
         }
         if (gl == 0) {
           p.ws_ml[row_ws * 2] = Mh;
@@ -531,7 +522,7 @@ __device__ void run_consumer_mma(const Params& p, const Pipe& pp, int warp, int 
     }
 
     if (flags & kEnd) {
-      if (!mma_segment_end<D, G, false>(p, pp, gph, o, m0, m1, l0, l1, mv, b, seg, flags, warp,
+      if (!mma_segment_end<D, G>(p, pp, gph, o, m0, m1, l0, l1, mv, b, seg, flags, warp,
                                         lane))
         return;
     }
@@ -545,22 +536,24 @@ __device__ void run_consumer_mma(const Params& p, const Pipe& pp, int warp, int 
 
 // ---- int8 consumer: tensor cores on converted codes ----------------------------
 //
-// K side.  q . (code * scale) = scale * (q . code): the 16 x 16 A fragments of
-// S^T are the raw codes of K converted to fp16 (exact, |code| <= 127), the B
-// fragments are q scaled by a power of two 2^e into fp16 (exact except for
-// values below 2^-14 of fp16's range, i.e. 2^-28 of the head's absmax), and
-// the fp32 accumulator is multiplied by scale_k * 2^-e per (token, head).  A
-// lane takes its A values from one contiguous run of D/4 codes per row: the
-// k index of the mma is a fixed permutation of d applied to both operands
+// Both products run on fp16 tensor cores with fp32 accumulators; every int8
+// code is exact in fp16 (|code| <= 127).
+// K side.  q . (code * scale) = scale * (q . code): the A fragments of S^T
+// are K's codes, the B fragments are q scaled by a power of two 2^e into
+// fp16 (exact except for values below 2^-28 of the head's absmax), and the
+// fp32 accumulator is multiplied by scale_k * 2^-e per (token, head).  A lane
+// takes its A values from one contiguous run of D/4 codes per row: the k
+// index of the mma is a fixed permutation of d applied to both operands
 // (lane qi, k-step j, slots 2qi, 2qi+1, 2qi+8, 2qi+9 <-> d = (D/4) qi + 4j +
 // 0..3), which leaves every dot product unchanged.
 // V side.  sum_t p_t (code_t * scale_t) = sum_t (p_t scale_t) code_t: the V
-// scales are folded into the softmax weights before they are rounded to bf16,
-// and the codes of the 16 tokens of a tile are converted to a bf16 tile in
-// the warp's shared memory so the ldmatrix.trans path of the bf16 consumer
-// serves unchanged.  Each word of four codes becomes (d0, d2) and (d1, d3)
-// pairs (two masks, no byte shuffle), so the tile holds d in the order
-// 0, 2, 1, 3 within groups of four; out_d<true> undoes that at the end.
+// scales are folded into the softmax weights, normalised by a running power
+// of two 2^E (E = the largest scale exponent seen in the segment, raised like
+// the softmax maximum, with an exact power-of-two rescale of O) so that the
+// fp16 weights p * scale * 2^-E stay in [0, 2); O is multiplied back by 2^E
+// at the segment end.  The codes of the 16 tokens of a tile are converted to
+// an fp16 tile in the warp's shared memory so the ldmatrix.trans path of the
+// bf16 consumer serves unchanged.
 
 // Four int8 codes -> two fp16x2 (codes 0,1 and 2,3): the codes, offset by
 // 128, become the low mantissa byte of 1024 + u; subtracting 1152 is exact.
@@ -571,17 +564,6 @@ __device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& 
   asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(x), "r"(0x64646464u));
   asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
   asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
-}
-
-// Four int8 codes -> bf16x2 (codes 0, 2) and (codes 1, 3).  For a code c with
-// bits s:m (sign bit s, low seven bits m), bf16 128 + m minus bf16 128 (s = 0)
-// or 256 (s = 1) is c exactly.
-__device__ __forceinline__ void i8x4_to_bf16(uint32_t w, uint32_t& even, uint32_t& odd) {
-  const uint32_t w8 = w >> 8;
-  const uint32_t me = (w & 0x007F007Fu) | 0x43004300u, se = (w & 0x00800080u) | 0x43004300u;
-  const uint32_t mo = (w8 & 0x007F007Fu) | 0x43004300u, so = (w8 & 0x00800080u) | 0x43004300u;
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(even) : "r"(me), "r"(se));
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(odd) : "r"(mo), "r"(so));
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -627,6 +609,7 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
   float o[KS][4];
   float m0 = 0.f, m1 = 0.f, l0 = 0.f, l1 = 0.f;
   bool mv = false;
+  int ev = 0;  // biased exponent E of the V-weight normaliser 2^(E-127)
 
   int s = 0;
   uint32_t ph = 0, gph = 0;
@@ -640,6 +623,7 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
     if (flags & kStart) {
       mv = false;
       m0 = m1 = l0 = l1 = 0.f;
+      ev = 0;
 #pragma unroll
       for (int kt = 0; kt < KS; ++kt)
 #pragma unroll
@@ -722,17 +706,31 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
       m0 = n0;
       m1 = n1;
       mv = true;
-#pragma unroll
-      for (int kt = 0; kt < KS; ++kt) {
-        o[kt][0] *= a0; o[kt][1] *= a1; o[kt][2] *= a0; o[kt][3] *= a1;
-      }
-      // weights times the V scales of their tokens
+      // V scales of the tile's tokens and the running power-of-two normaliser
       const float sv0 = *reinterpret_cast<const float*>(sV + min(t0, n - 1) * rs + s_off);
       const float sv1 = *reinterpret_cast<const float*>(sV + min(t1, n - 1) * rs + s_off);
-      *reinterpret_cast<uint32_t*>(ptile + gl * 16 + qi * 4) = pack_bf16x2(p0 * sv0, p1 * sv0);
+      int et = max((int)((__float_as_uint(sv0) >> 23) & 0xFF),
+                   (int)((__float_as_uint(sv1) >> 23) & 0xFF));
+      et = max(et, __shfl_xor_sync(kFull, et, 4));
+      et = max(et, __shfl_xor_sync(kFull, et, 8));
+      et = max(et, __shfl_xor_sync(kFull, et, 16));
+      const int en = min(253, max(ev, et));
+      // O in units of 2^(ev-127) -> 2^(en-127): an exact power of two (or 0
+      // when the old terms are below 2^-126 of the new scale)
+      const float rescale = ev - en >= -126 ? __uint_as_float((uint32_t)(127 + ev - en) << 23)
+                                            : 0.f;
+      const float f = __uint_as_float((uint32_t)(254 - en) << 23);  // 2^(127-en)
+      ev = en;
+      const float r0 = a0 * rescale, r1 = a1 * rescale;
+#pragma unroll
+      for (int kt = 0; kt < KS; ++kt) {
+        o[kt][0] *= r0; o[kt][1] *= r1; o[kt][2] *= r0; o[kt][3] *= r1;
+      }
+      const float vw0 = sv0 * f, vw1 = sv1 * f;
+      *reinterpret_cast<uint32_t*>(ptile + gl * 16 + qi * 4) = pack_f16x2(p0 * vw0, p1 * vw0);
       *reinterpret_cast<uint32_t*>(ptile + (gl + 8) * 16 + qi * 4) =
-          pack_bf16x2(p2 * sv1, p3 * sv1);
-      // V codes of the 16 tokens -> bf16 tile (lane: token vt, half vh of the head)
+          pack_f16x2(p2 * vw1, p3 * vw1);
+      // V codes of the 16 tokens -> fp16 tile (lane: token vt, half vh of the head)
       {
         const unsigned char* src = sV + min(t_lo + vt, n - 1) * rs + g * D + vh * (D / 2);
         unsigned char* dst = vtile + vt * vrs + vh * D;
@@ -740,10 +738,10 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
         for (int c = 0; c < D / 32; ++c) {
           const uint4 w = *reinterpret_cast<const uint4*>(src + 16 * c);
           uint4 lo, hi;
-          i8x4_to_bf16(w.x, lo.x, lo.y);
-          i8x4_to_bf16(w.y, lo.z, lo.w);
-          i8x4_to_bf16(w.z, hi.x, hi.y);
-          i8x4_to_bf16(w.w, hi.z, hi.w);
+          i8x4_to_f16(w.x, lo.x, lo.y);
+          i8x4_to_f16(w.y, lo.z, lo.w);
+          i8x4_to_f16(w.z, hi.x, hi.y);
+          i8x4_to_f16(w.w, hi.z, hi.w);
           *reinterpret_cast<uint4*>(dst + 32 * c) = lo;
           *reinterpret_cast<uint4*>(dst + 32 * c + 16) = hi;
         }
@@ -755,13 +753,20 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
       for (int kt = 0; kt < KS; ++kt) {
         uint32_t a[4];
         ldsm_x4_t(a, vt_addr + pv_t * vrs + (2 * kt + pv_c) * 16);
-        mma_bf16(o[kt], a, pb[0], pb[1]);
+        mma_f16(o[kt], a, pb[0], pb[1]);
       }
       __syncwarp();
     }
 
     if (flags & kEnd) {
-      if (!mma_segment_end<D, G, true>(p, pp, gph, o, m0, m1, l0, l1, mv, b, seg, flags, warp,
+      // back to true units: O * 2^(E-127) (0 when every V scale was 0 or
+      // subnormal, where the true terms are below 2^-126)
+      const float back = ev >= 1 ? __uint_as_float((uint32_t)ev << 23) : 0.f;
+#pragma unroll
+      for (int kt = 0; kt < KS; ++kt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[kt][c] *= back;
+      if (!mma_segment_end<D, G>(p, pp, gph, o, m0, m1, l0, l1, mv, b, seg, flags, warp,
                                        lane))
         return;
     }
