@@ -42,17 +42,23 @@
 //    error word and the warp leaves after the producer has drained its copies.
 #include <cfloat>
 #include <cmath>
+#include <cstring>
 #include <type_traits>
 
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace pkv {
 namespace {
 
-constexpr int kNW = 8;                    // consumer warps
-constexpr int kThreads = (kNW + 1) * 32;  // + one producer warp
+constexpr int kNW = 8;     // consumer warps (bf16 / fp32 pools)
+constexpr int kNWI8 = 8;   // consumer warps (int8 pools)
+
+// consumer warps of the kernel instance for element type T
+template <typename T>
+__host__ __device__ constexpr int consumer_warps() { return sizeof(T) == 1 ? kNWI8 : kNW; }
 constexpr int kMaxStageTokens = 16;       // rows per stage (one mma M tile)
 constexpr int kMaxPW = kMaxStageTokens / 4;
 constexpr int kMaxStages = 8;
@@ -78,11 +84,25 @@ struct Params {
   long long* ws_meta;
   int* err;
   int mb, batch, hq, hkv, bs, row_bytes, rs, st, stages;
-  int scale_off;  // int8 pools: byte offset of the fp32 scales in a token row
-  int vrs;        // int8 pools: row pitch of a warp's bf16 V tile
+  int nw;       // consumer warps (the producer is warp nw)
+  int mstride;  // floats between two warps' merge buffers
+  int stage_bytes;  // bytes of one pipeline stage (a multiple of 1024)
+  // int8 pools: stage carve (K codes, V codes, K scales, V scales), the bytes
+  // the four tensor copies of a stage deliver, the scale bytes of a row, the
+  // pitch of a warp's fp16 V tile, and the token-row coordinate of a block
+  int off_kc, off_vc, off_ks, off_vs, tx_bytes, sbytes, vrs;
+  long long rows_per_block;  // num_layers * block_size
+  int layer_row;             // layer * block_size
   float qscale;
   // shared-memory carve (bytes from the start of dynamic smem)
   int off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf, off_vbuf;
+};
+
+// Tensor maps of an int8 pool (unused for bf16 / fp32 pools): K and V codes
+// as (d, token row, kv head) boxes of (D, stage tokens, Hkv) bytes with the
+// D-byte swizzle, and the scale bytes as (byte, token row) boxes.
+struct I8Maps {
+  CUtensorMap kc, vc, ks, vs;
 };
 
 // ---- small helpers ----------------------------------------------------------
@@ -211,7 +231,7 @@ struct Pipe {
   __device__ uint32_t group() const { return bar0 + 8u * (2 * stages); }
 };
 
-// Reusable barrier over the consumer warps (mbarrier with kNW arrivals),
+// Reusable barrier over the consumer warps (mbarrier with nw arrivals),
 // bounded like every other wait.
 __device__ __forceinline__ bool group_sync(const Pipe& pp, uint32_t& gph, int lane, int* err) {
   __syncwarp();
@@ -223,8 +243,9 @@ __device__ __forceinline__ bool group_sync(const Pipe& pp, uint32_t& gph, int la
 
 // ---- producer warp -----------------------------------------------------------
 
-__device__ void run_producer(const Params& p, const Pipe& pp, const long long* s_cu, int lane,
-                             long long x0, long long x1) {
+template <bool TMA>
+__device__ void run_producer(const Params& p, const Pipe& pp, const I8Maps& maps,
+                             const long long* s_cu, int lane, long long x0, long long x1) {
   const int B = p.batch;
   const int ST = p.st;
   int lo = 0, hi = B;  // sequence holding block x0: largest b with s_cu[b] <= x0
@@ -279,6 +300,27 @@ __device__ void run_producer(const Params& p, const Pipe& pp, const long long* s
         if (kx == x1 - 1 && re == kr1) flags |= kLast;
         if (single) flags |= kSingle;
         if (!mbar_wait(pp.empty(s), ph, p.err)) { ok = false; break; }
+        if constexpr (TMA) {
+          // int8 pools: four tensor copies per stage (K and V codes, K and V
+          // scales), always whole boxes of st rows starting at row rs0; rows
+          // past n are never read (past the pool they arrive as zeros)
+          if (lane == 0) {
+            pp.desc[s] = make_int4(kb, blk_ok ? n : 0, flags, (int)blockIdx.x + kb);
+            if (blk_ok) {
+              const uint32_t full = pp.full(s);
+              mbar_arrive_expect_tx(full, (uint32_t)p.tx_bytes);
+              const int row = (int)(kblk * p.rows_per_block + p.layer_row + rs0);
+              const uint32_t base = smem_addr(pp.smem + (size_t)s * pp.stage_bytes);
+              tma_3d(base + p.off_kc, &maps.kc, 0, row, 0, full);
+              tma_3d(base + p.off_vc, &maps.vc, 0, row, 0, full);
+              tma_2d(base + p.off_ks, &maps.ks, 0, row, full);
+              tma_2d(base + p.off_vs, &maps.vs, 0, row, full);
+            } else {
+              mbar_arrive(pp.full(s));
+            }
+          }
+          __syncwarp();
+        } else {
         if (lane == 0) {
           pp.desc[s] = make_int4(kb, blk_ok ? n : 0, flags, (int)blockIdx.x + kb);
           if (blk_ok) mbar_arrive_expect_tx(pp.full(s), 2u * n * p.row_bytes);
@@ -292,6 +334,7 @@ __device__ void run_producer(const Params& p, const Pipe& pp, const long long* s
           bulk_g2s(dst, (v_lane ? p.v_base : p.k_base) + src, p.row_bytes, pp.full(s));
         }
         __syncwarp();
+        }
         filled |= 1u << s;
         fill_par = (fill_par & ~(1u << s)) | (((ph ^ 1u) & 1u) << s);
         if (++s == pp.stages) { s = 0; ph ^= 1; }
@@ -321,7 +364,7 @@ __device__ __forceinline__ bool mma_segment_end(const Params& p, const Pipe& pp,
   const int hkv = p.hkv;
   const int g = warp % hkv;
   const int wsub = warp / hkv;
-  const int wph = kNW / hkv;
+  const int wph = p.nw / hkv;
   const int gl = lane >> 2;
   const int qi = lane & 3;
   float* mbuf = reinterpret_cast<float*>(pp.smem + p.off_mbuf);
@@ -336,7 +379,7 @@ __device__ __forceinline__ bool mma_segment_end(const Params& p, const Pipe& pp,
   const int h0 = 2 * qi, h1 = h0 + 1;
   if (wph > 1) {
     // merge the token shares of the warps serving the same kv head
-    float* mw = mbuf + warp * G * (D + 2);
+    float* mw = mbuf + warp * p.mstride;
 #pragma unroll
     for (int kt = 0; kt < KS; ++kt) {
       const int d0 = kt * 16 + gl, d1 = d0 + 8;
@@ -354,14 +397,15 @@ __device__ __forceinline__ bool mma_segment_end(const Params& p, const Pipe& pp,
         const int h = h0 + hh;
         if (h >= G) continue;
         float Mx = -INFINITY;
-        for (int w2 = g; w2 < kNW; w2 += hkv) Mx = fmaxf(Mx, mbuf[(w2 * G + h) * (D + 2) + D]);
+        for (int w2 = g; w2 < p.nw; w2 += hkv)
+          Mx = fmaxf(Mx, mbuf[w2 * p.mstride + h * (D + 2) + D]);
         float Ls = 0.f;
         float acc[KS][2];
 #pragma unroll
         for (int kt = 0; kt < KS; ++kt) acc[kt][0] = acc[kt][1] = 0.f;
         if (Mx != -INFINITY) {
-          for (int w2 = g; w2 < kNW; w2 += hkv) {
-            const float* src = mbuf + (w2 * G + h) * (D + 2);
+          for (int w2 = g; w2 < p.nw; w2 += hkv) {
+            const float* src = mbuf + w2 * p.mstride + h * (D + 2);
             if (src[D] == -INFINITY) continue;
             const float wgt = exp2f(src[D] - Mx);
             Ls += wgt * src[D + 1];
@@ -424,7 +468,7 @@ __device__ void run_consumer_mma(const Params& p, const Pipe& pp, int warp, int 
   const int hkv = p.hkv;
   const int g = warp % hkv;
   const int wsub = warp / hkv;
-  const int wph = kNW / hkv;
+  const int wph = p.nw / hkv;
   const int gl = lane >> 2;  // mma group row
   const int qi = lane & 3;   // mma thread in group
   const int rs = p.rs;
@@ -555,15 +599,54 @@ __device__ void run_consumer_mma(const Params& p, const Pipe& pp, int warp, int 
 // an fp16 tile in the warp's shared memory so the ldmatrix.trans path of the
 // bf16 consumer serves unchanged.
 
-// Four int8 codes -> two fp16x2 (codes 0,1 and 2,3): the codes, offset by
-// 128, become the low mantissa byte of 1024 + u; subtracting 1152 is exact.
-__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+// Four int8 codes -> two fp16x2 holding code + 1152 (codes 0,1 and 2,3):
+// each code, offset by 128, becomes the low mantissa byte of 1024 + u.  The
+// bias is removed after the products (kBias times the sum of the other
+// operand), so the conversion is one XOR and two byte permutes.
+constexpr float kBias = 1152.f;
+constexpr uint32_t kBiasF16x2 = 0x64806480u;  // (1152, 1152) in fp16
+__device__ __forceinline__ void i8x4_to_f16b(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t x = w ^ 0x80808080u;
-  uint32_t a, b;
-  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(x), "r"(0x64646464u));
-  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(x), "r"(0x64646464u));
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
-  asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(x), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(x), "r"(0x64646464u));
+}
+
+// Address of 16-byte unit u of line `line` of a code tile written by a tensor
+// copy with the D-byte swizzle (tile 1024-byte aligned, D-byte lines): the
+// unit index is XORed with address bits 7.. of the line (three bits for the
+// 128-byte swizzle, two for the 64-byte one).
+template <int D>
+__device__ __forceinline__ uint32_t code_unit(uint32_t tile, int line, int u) {
+  constexpr int kMask = D == 128 ? 7 : 3;
+  const int x = ((line * D) >> 7) & kMask;
+  return tile + line * D + ((u ^ x) << 4);
+}
+
+// Shared-memory accesses by 32-bit shared-window address (the compiler
+// cannot always prove a generic pointer is shared and would then issue
+// generic loads, which wait on the long scoreboard).
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(a));
+  return r;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float r;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(r) : "r"(a));
+  return r;
+}
+
+__device__ __forceinline__ void sts128(uint32_t a, const uint4& v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -588,42 +671,93 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
   const int hkv = p.hkv;
   const int g = warp % hkv;
   const int wsub = warp / hkv;
-  const int wph = kNW / hkv;
+  const int wph = p.nw / hkv;
   const int gl = lane >> 2;  // mma group row
   const int qi = lane & 3;   // mma thread in group
-  const int rs = p.rs;
   const int ST = p.st;
-  const int k_off = g * D + QW * qi;      // this lane's K codes within a row
-  const int s_off = p.scale_off + 4 * g;  // this head's scale within a row
-  const int vt = lane & 15, vh = lane >> 4;  // V conversion: token row, half of the head
+  const int sb = p.sbytes;
+  const int vt_row = lane & 15, vh = lane >> 4;  // V conversion: token row, half of the head
   const int pv_t = (lane & 7) + (lane >> 4) * 8;  // V rows (A of P.V, trans)
   const int pv_c = (lane >> 3) & 1;
-  unsigned char* ptile = pp.smem + p.off_pbuf + warp * 256;  // P^T [16 t][8 h] bf16
-  const uint32_t pt_addr = smem_addr(ptile);
+  // two P^T tiles [16 t][8 h] and two fp16 V tiles [16 t][D] per warp: the
+  // P.V product of a tile runs one tile late, overlapping the next tile's
+  // Q.K chain
+  const uint32_t pt_addr = smem_addr(pp.smem + p.off_pbuf + warp * 512);
   const int vrs = p.vrs;
-  unsigned char* vtile = pp.smem + p.off_vbuf + warp * 16 * vrs;  // [16 t][D] bf16
-  const uint32_t vt_addr = smem_addr(vtile);
+  const uint32_t vt_addr = smem_addr(pp.smem + p.off_vbuf + warp * 32 * vrs);
+  const uint32_t smem0 = smem_addr(pp.smem);
 
   uint32_t qb[KS][2];
   float qs0 = 0.f, qs1 = 0.f;  // score factors of this lane's head columns 2qi, 2qi+1
+  float kb0 = 0.f, kb1 = 0.f;  // K-code bias terms of those columns: 1152 * sum(q)
   float o[KS][4];
+  float vb0 = 0.f, vb1 = 0.f;  // V-code bias terms of O: 1152 * sum(weights)
   float m0 = 0.f, m1 = 0.f, l0 = 0.f, l1 = 0.f;
   bool mv = false;
   int ev = 0;  // biased exponent E of the V-weight normaliser 2^(E-127)
+  // Offsets of this lane's code units within a stage's code tile: every row
+  // of a tile holds real data (a tensor copy always fills all ST rows, past
+  // the pool with zeros), so rows past n are read unclamped; their scores are
+  // masked and their weights are zero.
+  uint32_t koff[2][QW / 16], voff[D / 32];
+#pragma unroll
+  for (int i = 0; i < QW / 16; ++i) {
+    koff[0][i] = code_unit<D>(0, g * ST + gl, (QW / 16) * qi + i);
+    koff[1][i] = code_unit<D>(0, g * ST + gl + 8, (QW / 16) * qi + i);
+  }
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) voff[c] = code_unit<D>(0, g * ST + vt_row, vh * (D / 32) + c);
+  int pend = -1;                 // buffer of the tile whose P.V is pending
+  float pa0 = 1.f, pa1 = 1.f;    // O scale factors to apply before that P.V
+
+  // O <- O * (pa0, pa1) + P^T V of buffer `buf` (and the same for the bias sums)
+  auto pv_step = [&](int buf) {
+    if (__any_sync(kFull, pa0 != 1.f || pa1 != 1.f)) {
+#pragma unroll
+      for (int kt = 0; kt < KS; ++kt) {
+        o[kt][0] *= pa0; o[kt][1] *= pa1; o[kt][2] *= pa0; o[kt][3] *= pa1;
+      }
+      vb0 *= pa0;
+      vb1 *= pa1;
+    }
+    uint32_t pb[2];
+    ldsm_x2_t(pb, pt_addr + buf * 256 + (lane & 15) * 16);
+    const uint32_t vt = vt_addr + buf * 16 * vrs;
+#pragma unroll
+    for (int kt = 0; kt < KS; ++kt) {
+      uint32_t a[4];
+      ldsm_x4_t(a, vt + pv_t * vrs + (2 * kt + pv_c) * 16);
+      mma_f16(o[kt], a, pb[0], pb[1]);
+    }
+    // the bias part of the products: every A row 1152
+    const uint32_t ab[4] = {kBiasF16x2, kBiasF16x2, kBiasF16x2, kBiasF16x2};
+    float vb[4] = {vb0, vb1, vb0, vb1};
+    mma_f16(vb, ab, pb[0], pb[1]);
+    vb0 = vb[0];
+    vb1 = vb[1];
+  };
 
   int s = 0;
   uint32_t ph = 0, gph = 0;
+  int turn = 0;  // the wph warps of a kv head take the stages in turn
   while (true) {
     if (!mbar_wait(pp.full(s), ph, p.err)) return;
     const int4 dsc = pp.desc[s];
-    const int b = dsc.x, n = dsc.y, flags = dsc.z, seg = dsc.w;
-    const unsigned char* sK = pp.smem + (size_t)s * pp.stage_bytes;
-    const unsigned char* sV = sK + ST * rs;
+    const int b = dsc.x, flags = dsc.z, seg = dsc.w;
+    const int n = turn == wsub ? dsc.y : 0;  // rows this warp processes
+    if (++turn == wph) turn = 0;
+    // stage: code tiles [Hkv][ST rows][D bytes] with the D-byte swizzle,
+    // scales [ST rows][sb bytes]
+    const uint32_t base = smem0 + s * pp.stage_bytes;
+    const uint32_t sKc = base + p.off_kc, sVc = base + p.off_vc;
+    const uint32_t sKs = base + p.off_ks + 4 * g, sVs = base + p.off_vs + 4 * g;
 
     if (flags & kStart) {
       mv = false;
       m0 = m1 = l0 = l1 = 0.f;
+      vb0 = vb1 = 0.f;
       ev = 0;
+      pend = -1;
 #pragma unroll
       for (int kt = 0; kt < KS; ++kt)
 #pragma unroll
@@ -657,38 +791,71 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
         qb[j][0] = pack_f16x2(bf16_lo(w0) * up, bf16_hi(w0) * up);
         qb[j][1] = pack_f16x2(bf16_lo(w1) * up, bf16_hi(w1) * up);
       }
+      // sum of the fp16 query values of the head (for the K-code bias)
+      float qsum = 0.f;
+#pragma unroll
+      for (int j = 0; j < KS; ++j) {
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&qb[j][0]));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&qb[j][1]));
+        qsum += (f0.x + f0.y) + (f1.x + f1.y);
+      }
+      qsum += __shfl_xor_sync(kFull, qsum, 1);
+      qsum += __shfl_xor_sync(kFull, qsum, 2);
+      kb0 = kBias * __shfl_sync(kFull, qsum, (2 * qi) * 4);
+      kb1 = kBias * __shfl_sync(kFull, qsum, (2 * qi + 1) * 4);
       qs0 = p.qscale * __shfl_sync(kFull, down, (2 * qi) * 4);
       qs1 = p.qscale * __shfl_sync(kFull, down, (2 * qi + 1) * 4);
     }
 
-    for (int mt = wsub; mt * 16 < n; mt += wph) {
-      const int t_lo = mt * 16;
-      const int t0 = t_lo + gl, t1 = t0 + 8;
-      // rows past n hold stale data: read a valid row instead (it is masked)
-      const unsigned char* k0 = sK + min(t0, n - 1) * rs;
-      const unsigned char* k1 = sK + min(t1, n - 1) * rs;
+    if (n > 0) {  // one 16-row tile (stages never hold more rows)
+      const int cur = pend < 0 ? 0 : pend ^ 1;
+      const uint32_t vt = vt_addr + cur * 16 * vrs, pt = pt_addr + cur * 256;
+      const int t0 = gl, t1 = gl + 8;
+      // V codes of the 16 tokens -> fp16 tile (lane: token vt, half vh of the
+      // head); independent of the scores, so issued first to overlap them
+      {
+        const uint32_t dst = vt + vt_row * vrs + vh * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          const uint4 w = lds128(sVc + voff[c]);
+          uint4 lo, hi;
+          i8x4_to_f16b(w.x, lo.x, lo.y);
+          i8x4_to_f16b(w.y, lo.z, lo.w);
+          i8x4_to_f16b(w.z, hi.x, hi.y);
+          i8x4_to_f16b(w.w, hi.z, hi.w);
+          sts128(dst + 32 * c, lo);
+          sts128(dst + 32 * c + 16, hi);
+        }
+      }
       uint32_t w0[KS], w1[KS];
 #pragma unroll
       for (int i = 0; i < QW / 16; ++i) {
-        const uint4 a = *reinterpret_cast<const uint4*>(k0 + k_off + 16 * i);
-        const uint4 c = *reinterpret_cast<const uint4*>(k1 + k_off + 16 * i);
+        const uint4 a = lds128(sKc + koff[0][i]);
+        const uint4 c = lds128(sKc + koff[1][i]);
         w0[4 * i] = a.x; w0[4 * i + 1] = a.y; w0[4 * i + 2] = a.z; w0[4 * i + 3] = a.w;
         w1[4 * i] = c.x; w1[4 * i + 1] = c.y; w1[4 * i + 2] = c.z; w1[4 * i + 3] = c.w;
       }
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      // scales of rows past n may be anything (rows of other blocks): their
+      // scores are masked below and their V scales replaced by 0
+      const float sk0 = lds_f32(sKs + t0 * sb), sk1 = lds_f32(sKs + t1 * sb);
+      const float sv0 = t0 < n ? lds_f32(sVs + t0 * sb) : 0.f;
+      const float sv1 = t1 < n ? lds_f32(sVs + t1 * sb) : 0.f;
+      // two independent accumulation chains over the k-steps
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < KS; ++j) {
         uint32_t a[4];
-        i8x4_to_f16(w0[j], a[0], a[2]);
-        i8x4_to_f16(w1[j], a[1], a[3]);
-        mma_f16(sc, a, qb[j][0], qb[j][1]);
+        i8x4_to_f16b(w0[j], a[0], a[2]);
+        i8x4_to_f16b(w1[j], a[1], a[3]);
+        mma_f16((j & 1) ? sq : sa, a, qb[j][0], qb[j][1]);
       }
-      const float sk0 = *reinterpret_cast<const float*>(k0 + s_off);
-      const float sk1 = *reinterpret_cast<const float*>(k1 + s_off);
-      sc[0] = t0 < n ? sc[0] * qs0 * sk0 : -INFINITY;
-      sc[1] = t0 < n ? sc[1] * qs1 * sk0 : -INFINITY;
-      sc[2] = t1 < n ? sc[2] * qs0 * sk1 : -INFINITY;
-      sc[3] = t1 < n ? sc[3] * qs1 * sk1 : -INFINITY;
+      // the previous tile's P.V: independent of this tile's scores
+      if (pend >= 0) pv_step(pend);
+      float sc[4];
+      sc[0] = t0 < n ? ((sa[0] + sq[0]) - kb0) * qs0 * sk0 : -INFINITY;
+      sc[1] = t0 < n ? ((sa[1] + sq[1]) - kb1) * qs1 * sk0 : -INFINITY;
+      sc[2] = t1 < n ? ((sa[2] + sq[2]) - kb0) * qs0 * sk1 : -INFINITY;
+      sc[3] = t1 < n ? ((sa[3] + sq[3]) - kb1) * qs1 * sk1 : -INFINITY;
       float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
 #pragma unroll
       for (int o2 = 4; o2 < 32; o2 <<= 1) {
@@ -706,9 +873,7 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
       m0 = n0;
       m1 = n1;
       mv = true;
-      // V scales of the tile's tokens and the running power-of-two normaliser
-      const float sv0 = *reinterpret_cast<const float*>(sV + min(t0, n - 1) * rs + s_off);
-      const float sv1 = *reinterpret_cast<const float*>(sV + min(t1, n - 1) * rs + s_off);
+      // running power-of-two normaliser of the V-scaled weights
       int et = max((int)((__float_as_uint(sv0) >> 23) & 0xFF),
                    (int)((__float_as_uint(sv1) >> 23) & 0xFF));
       et = max(et, __shfl_xor_sync(kFull, et, 4));
@@ -721,51 +886,31 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
                                             : 0.f;
       const float f = __uint_as_float((uint32_t)(254 - en) << 23);  // 2^(127-en)
       ev = en;
-      const float r0 = a0 * rescale, r1 = a1 * rescale;
-#pragma unroll
-      for (int kt = 0; kt < KS; ++kt) {
-        o[kt][0] *= r0; o[kt][1] *= r1; o[kt][2] *= r0; o[kt][3] *= r1;
-      }
+      // this tile's factors, applied to O right before its own P.V
+      pa0 = a0 * rescale;
+      pa1 = a1 * rescale;
       const float vw0 = sv0 * f, vw1 = sv1 * f;
-      *reinterpret_cast<uint32_t*>(ptile + gl * 16 + qi * 4) = pack_f16x2(p0 * vw0, p1 * vw0);
-      *reinterpret_cast<uint32_t*>(ptile + (gl + 8) * 16 + qi * 4) =
-          pack_f16x2(p2 * vw1, p3 * vw1);
-      // V codes of the 16 tokens -> fp16 tile (lane: token vt, half vh of the head)
-      {
-        const unsigned char* src = sV + min(t_lo + vt, n - 1) * rs + g * D + vh * (D / 2);
-        unsigned char* dst = vtile + vt * vrs + vh * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          const uint4 w = *reinterpret_cast<const uint4*>(src + 16 * c);
-          uint4 lo, hi;
-          i8x4_to_f16(w.x, lo.x, lo.y);
-          i8x4_to_f16(w.y, lo.z, lo.w);
-          i8x4_to_f16(w.z, hi.x, hi.y);
-          i8x4_to_f16(w.w, hi.z, hi.w);
-          *reinterpret_cast<uint4*>(dst + 32 * c) = lo;
-          *reinterpret_cast<uint4*>(dst + 32 * c + 16) = hi;
-        }
-      }
-      __syncwarp();
-      uint32_t pb[2];
-      ldsm_x2_t(pb, pt_addr + (lane & 15) * 16);
-#pragma unroll
-      for (int kt = 0; kt < KS; ++kt) {
-        uint32_t a[4];
-        ldsm_x4_t(a, vt_addr + pv_t * vrs + (2 * kt + pv_c) * 16);
-        mma_f16(o[kt], a, pb[0], pb[1]);
-      }
+      sts32(pt + gl * 16 + qi * 4, pack_f16x2(p0 * vw0, p1 * vw0));
+      sts32(pt + (gl + 8) * 16 + qi * 4, pack_f16x2(p2 * vw1, p3 * vw1));
+      pend = cur;
       __syncwarp();
     }
 
     if (flags & kEnd) {
-      // back to true units: O * 2^(E-127) (0 when every V scale was 0 or
-      // subnormal, where the true terms are below 2^-126)
+      if (pend >= 0) {  // drain the pending P.V
+        pv_step(pend);
+        pend = -1;
+      }
+      // remove the V-code bias, then back to true units: O * 2^(E-127) (0
+      // when every V scale was 0 or subnormal: true terms below 2^-126)
       const float back = ev >= 1 ? __uint_as_float((uint32_t)ev << 23) : 0.f;
 #pragma unroll
-      for (int kt = 0; kt < KS; ++kt)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) o[kt][c] *= back;
+      for (int kt = 0; kt < KS; ++kt) {
+        o[kt][0] = (o[kt][0] - vb0) * back;
+        o[kt][1] = (o[kt][1] - vb1) * back;
+        o[kt][2] = (o[kt][2] - vb0) * back;
+        o[kt][3] = (o[kt][3] - vb1) * back;
+      }
       if (!mma_segment_end<D, G>(p, pp, gph, o, m0, m1, l0, l1, mv, b, seg, flags, warp,
                                        lane))
         return;
@@ -798,7 +943,7 @@ __device__ void run_consumer_fma(const Params& p, const Pipe& pp, int warp, int 
   const int hkv = p.hkv;
   const int g = warp % hkv;
   const int wsub = warp / hkv;
-  const int wph = kNW / hkv;
+  const int wph = p.nw / hkv;
   const int jg = lane >> 3;  // token slot within a pass
   const int il = lane & 7;   // lane within the token group
   const int hs = il >> C::HSHIFT;
@@ -947,7 +1092,7 @@ __device__ void run_consumer_fma(const Params& p, const Pipe& pp, int warp, int 
         mh[hh] = __shfl_sync(kFull, m_valid ? m_run : -INFINITY, hh << C::HSHIFT);
       }
       if (wph > 1) {
-        float* mw = mbuf + warp * G * (D + 2);
+        float* mw = mbuf + warp * p.mstride;
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
 #pragma unroll
@@ -959,13 +1104,14 @@ __device__ void run_consumer_fma(const Params& p, const Pipe& pp, int warp, int 
 #pragma unroll
           for (int hh = 0; hh < G; ++hh) {
             float M = -INFINITY;
-            for (int w2 = g; w2 < kNW; w2 += hkv) M = fmaxf(M, mbuf[(w2 * G + hh) * (D + 2) + D]);
+            for (int w2 = g; w2 < p.nw; w2 += hkv)
+              M = fmaxf(M, mbuf[w2 * p.mstride + hh * (D + 2) + D]);
             float l = 0.f, a[C::PVE];
 #pragma unroll
             for (int e = 0; e < C::PVE; ++e) a[e] = 0.f;
             if (M != -INFINITY) {
-              for (int w2 = g; w2 < kNW; w2 += hkv) {
-                const float* src = mbuf + (w2 * G + hh) * (D + 2);
+              for (int w2 = g; w2 < p.nw; w2 += hkv) {
+                const float* src = mbuf + w2 * p.mstride + hh * (D + 2);
                 const float mm = src[D];
                 if (mm == -INFINITY) continue;
                 const float wgt = exp2f(mm - M);
@@ -1014,8 +1160,11 @@ __device__ void run_consumer_fma(const Params& p, const Pipe& pp, int warp, int 
 // ---- the partial-pass kernel -------------------------------------------------
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Params p) {
-  extern __shared__ __align__(128) unsigned char smem[];
+__global__ void __launch_bounds__((consumer_warps<T>() + 1) * 32, 1)
+    decode_partial_kernel(const Params p, const __grid_constant__ I8Maps maps) {
+  constexpr int NW = consumer_warps<T>();
+  constexpr int kThreads = (NW + 1) * 32;
+  extern __shared__ __align__(1024) unsigned char smem[];
   griddep_wait();
   griddep_launch_dependents();
   const int tid = threadIdx.x;
@@ -1028,7 +1177,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
   pp.desc = reinterpret_cast<int4*>(smem + p.off_desc);
   pp.bar0 = smem_addr(smem + p.off_bar);
   pp.stages = p.stages;
-  pp.stage_bytes = 2 * p.st * p.rs;
+  pp.stage_bytes = p.stage_bytes;
 
   // ---- block counts and their exclusive scan (every CTA, same result) ----
   const int B = p.batch;
@@ -1047,9 +1196,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(pp.full(s), 1);
-      mbar_init(pp.empty(s), kNW);
+      mbar_init(pp.empty(s), NW);
     }
-    mbar_init(pp.group(), kNW);
+    mbar_init(pp.group(), NW);
     fence_mbar_init();
   }
   __syncthreads();
@@ -1073,8 +1222,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_partial_kernel(const Param
   }
   if (x0 >= x1) return;
 
-  if (warp == kNW) {
-    run_producer(p, pp, s_cu, lane, x0, x1);
+  if (warp == NW) {
+    run_producer<sizeof(T) == 1>(p, pp, maps, s_cu, lane, x0, x1);
   } else if constexpr (sizeof(T) == 1) {
     run_consumer_i8<D, G>(p, pp, warp, lane);
   } else if constexpr (sizeof(T) == 2) {
@@ -1156,28 +1305,49 @@ int stage_tokens(int bs, int row_bytes) {
 struct Layout {
   int st, rs, vrs, stages, smem, off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf,
       off_vbuf;
+  int stage_bytes, off_kc, off_vc, off_ks, off_vs, tx_bytes, sbytes;  // see Params
 };
 
 int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int smem_optin,
-                   bool quant) {
+                   bool quant, int nw) {
   Layout L{};
   L.st = stage_tokens(bs, row_bytes);
   L.rs = row_bytes + kRowPad;
-  L.vrs = quant ? 2 * D + 16 : 0;  // bf16 V tile rows, padded like the stage rows
-  const int vbuf = kNW * 16 * L.vrs;
-  const int stage_bytes = 2 * L.st * L.rs;
-  const int pbuf = kNW * (L.st * G * 4 > 256 ? L.st * G * 4 : 256);
+  L.vrs = quant ? 2 * D + 16 : 0;  // fp16 V tile rows, padded for ldmatrix
+  const int vbuf = nw * 32 * L.vrs;  // two V tiles per warp (int8 pools)
+  if (quant) {
+    // [K codes (Hkv, st, D) | V codes | K scales (st, sbytes) | V scales]:
+    // every tensor-copy destination 128-byte aligned, the swizzled code
+    // tiles 1024-byte aligned
+    const int codes = hkv * L.st * D;
+    L.sbytes = (4 * hkv + 15) / 16 * 16;
+    L.off_kc = 0;
+    L.off_vc = align_up(codes, 1024);
+    L.off_ks = 2 * align_up(codes, 1024);
+    L.off_vs = align_up(L.off_ks + L.st * L.sbytes, 128);
+    L.stage_bytes = align_up(L.off_vs + L.st * L.sbytes, 1024);
+    L.tx_bytes = 2 * codes + 2 * L.st * L.sbytes;
+  } else {
+    L.stage_bytes = 2 * L.st * L.rs;
+  }
+  const int stage_bytes = L.stage_bytes;
+  const int pbuf = nw * (quant ? 512 : (L.st * G * 4 > 256 ? L.st * G * 4 : 256));
+  // merge buffers of warps sharing a kv head: their own region, or (int8)
+  // each warp's V tile, idle while segments are merged
+  const int mbuf = (!quant && hkv < nw) ? 4 * nw * G * (D + 2) : 0;
   int fixed = 0;
   fixed += 8 * (2 * kMaxStages + 1);              // barriers
   fixed = align_up(fixed, 16) + 16 * kMaxStages;  // descriptors
   fixed = align_up(fixed, 16) + 8 * (batch + 1);  // cu
-  fixed = align_up(fixed, 16) + 8 * 16;           // scan scratch
+  fixed = align_up(fixed, 16) + 8 * 32;           // scan scratch
   fixed = align_up(fixed, 16) + pbuf;
-  if (hkv < kNW) fixed = align_up(fixed, 16) + 4 * kNW * G * (D + 2);
+  fixed = align_up(fixed, 16) + mbuf;
   fixed = align_up(fixed, 16) + vbuf;
   fixed = align_up(fixed, 128);
+  if (quant && (L.off_vc % 1024 || L.off_ks % 128 || L.off_vs % 128 || stage_bytes % 1024))
+    return L;  // stages 0: refused (every tensor copy needs an aligned destination)
   int stages = (smem_optin - fixed) / stage_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
   L.stages = stages;
@@ -1185,11 +1355,11 @@ Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int 
   L.off_bar = off;   off += 8 * (2 * stages + 1);
   off = align_up(off, 16); L.off_desc = off; off += 16 * stages;
   off = align_up(off, 16); L.off_cu = off;   off += 8 * (batch + 1);
-  off = align_up(off, 16); L.off_scan = off; off += 8 * 16;
+  off = align_up(off, 16); L.off_scan = off; off += 8 * 32;
   off = align_up(off, 16); L.off_pbuf = off; off += pbuf;
-  off = align_up(off, 16); L.off_mbuf = off;
-  if (hkv < kNW) off += 4 * kNW * G * (D + 2);
+  off = align_up(off, 16); L.off_mbuf = off; off += mbuf;
   off = align_up(off, 16); L.off_vbuf = off; off += vbuf;
+  if (quant) L.off_mbuf = L.off_vbuf;
   L.smem = align_up(off, 16);
   return L;
 }
@@ -1258,8 +1428,18 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   p.rs = L.rs;
   p.st = L.st;
   p.stages = L.stages;
-  p.scale_off = pv.scale_off;
   p.vrs = L.vrs;
+  p.stage_bytes = L.stage_bytes;
+  p.nw = consumer_warps<T>();
+  p.mstride = sizeof(T) == 1 ? 32 * L.vrs / 4 : G * (D + 2);
+  p.off_kc = L.off_kc;
+  p.off_vc = L.off_vc;
+  p.off_ks = L.off_ks;
+  p.off_vs = L.off_vs;
+  p.tx_bytes = L.tx_bytes;
+  p.sbytes = L.sbytes;
+  p.rows_per_block = (long long)pv.num_layers * pv.block_size;
+  p.layer_row = a.layer * pv.block_size;
   p.qscale = a.scale * kLog2e;
   p.off_bar = L.off_bar;
   p.off_desc = L.off_desc;
@@ -1269,6 +1449,26 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   p.off_mbuf = L.off_mbuf;
   p.off_vbuf = L.off_vbuf;
 
+  I8Maps maps;
+  memset(&maps, 0, sizeof(maps));
+  if constexpr (sizeof(T) == 1) {
+    const int H = pv.num_kv_heads;
+    const cuuint64_t rows = (cuuint64_t)pv.num_blocks * pv.num_layers * pv.block_size;
+    const cuuint64_t cdims[3] = {(cuuint64_t)D, rows, (cuuint64_t)H};
+    const cuuint64_t cstrides[2] = {(cuuint64_t)pv.row_bytes, (cuuint64_t)D};
+    const cuuint32_t cbox[3] = {(cuuint32_t)D, (cuuint32_t)L.st, (cuuint32_t)H};
+    const CUtensorMapSwizzle sw = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const cuuint64_t sdims[2] = {(cuuint64_t)L.sbytes, rows};
+    const cuuint64_t sstrides[1] = {(cuuint64_t)pv.row_bytes};
+    const cuuint32_t sbox[2] = {(cuuint32_t)L.sbytes, (cuuint32_t)L.st};
+    if (!encode_tiled(&maps.kc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, pv.k, cdims, cstrides, cbox, sw) ||
+        !encode_tiled(&maps.vc, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, pv.v, cdims, cstrides, cbox, sw) ||
+        !encode_tiled(&maps.ks, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, pv.k + pv.scale_off, sdims,
+                      sstrides, sbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tiled(&maps.vs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, pv.v + pv.scale_off, sdims,
+                      sstrides, sbox, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  }
   auto kern = decode_partial_kernel<T, D, G>;
   static int configured[64] = {0};
   cudaError_t e = ensure_smem(kern, L.smem, configured);
@@ -1277,7 +1477,8 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   // pass alone with events (an event between kernels ends the overlap)
   const bool pdl = a.ev_start == nullptr && a.ev_stop == nullptr;
   if (a.ev_start && (e = cudaEventRecord(a.ev_start, s)) != cudaSuccess) return e;
-  e = launch_kernel(kern, dim3(grid), dim3(kThreads), L.smem, s, pdl, p);
+  e = launch_kernel(kern, dim3(grid), dim3((consumer_warps<T>() + 1) * 32), L.smem, s, pdl, p,
+                    maps);
   if (e != cudaSuccess) return e;
   if (a.ev_stop && (e = cudaEventRecord(a.ev_stop, s)) != cudaSuccess) return e;
   // int8 pools take and return bf16
@@ -1320,9 +1521,14 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s) {
   const PoolView& pv = a.pool;
   const int G = a.num_q_heads / pv.num_kv_heads;
   const Layout L = make_layout(pv.block_size, pv.row_bytes, pv.num_kv_heads, G, pv.head_dim,
-                               a.batch, a.smem_optin, pv.quant != 0);
+                               a.batch, a.smem_optin, pv.quant != 0, pv.quant ? kNWI8 : kNW);
   if (L.stages < 2) return cudaErrorInvalidConfiguration;
   if (pv.quant) {
+    // the merge buffer of a warp lives in its V tile
+    if (G * (pv.head_dim + 2) * 4 > 32 * L.vrs) return cudaErrorInvalidConfiguration;
+    // tensor-copy row coordinates are 32-bit
+    if ((long long)pv.num_blocks * pv.num_layers * pv.block_size >= (1ll << 31))
+      return cudaErrorInvalidConfiguration;
     return pv.head_dim == 128 ? run_g<int8_t, 128>(a, L, G, s) : run_g<int8_t, 64>(a, L, G, s);
   }
   if (pv.elem_size == 2) {

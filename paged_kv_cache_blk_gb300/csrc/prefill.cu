@@ -34,6 +34,7 @@
 
 #include "common.cuh"
 #include "pkv.h"
+#include "tma.cuh"
 
 namespace pkv {
 namespace {
@@ -137,24 +138,6 @@ __device__ __forceinline__ void tmem_wait_ld() {
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* m, int x, int y, int z,
-                                       uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
-      "[%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"((uint64_t)m), "r"(x), "r"(y), "r"(z), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap* m, int x, int y, int z,
-                                       int w, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
-      "[%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-      "l"((uint64_t)m), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
-      : "memory");
 }
 
 // ---- the kernel ------------------------------------------------------------------
@@ -434,33 +417,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
 // ---- host side ------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    else
-      cudaGetLastError();
-  });
-  return fn;
-}
-
-bool encode(CUtensorMap* m, int rank, void* base, const cuuint64_t* dims,
-            const cuuint64_t* strides, const cuuint32_t* box) {
-  auto fn = tensor_map_encoder();
-  if (!fn) return false;
-  cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
-}
-
 }  // namespace
 
 int prefill_supported(const PoolView& pv, int num_q_heads) {
@@ -484,7 +440,9 @@ cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num
     cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
     cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)num_q_heads * kD * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)TQ};
-    if (!encode(&tq, 3, const_cast<void*>(q), dims, strides, box)) return cudaErrorInvalidValue;
+    if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
   }
   const long long nl = pv.num_blocks * pv.num_layers;
   {
@@ -493,8 +451,10 @@ cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num
     cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)pv.row_bytes,
                              (cuuint64_t)pv.row_bytes * pv.block_size};
     cuuint32_t box[4] = {64, 1, (cuuint32_t)pv.block_size, 1};
-    if (!encode(&tk, 4, const_cast<char*>(pv.k), dims, strides, box) ||
-        !encode(&tv, 4, const_cast<char*>(pv.v), dims, strides, box))
+    if (!encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pv.k, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pv.v, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   PfParams p{};
