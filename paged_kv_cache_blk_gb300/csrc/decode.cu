@@ -169,6 +169,16 @@ __device__ __forceinline__ void ldsm_x2_t(uint32_t (&r)[2], uint32_t addr) {
                : "memory");
 }
 
+// Transposing load of a 16 x 16 byte matrix (rows addressed by lanes 0-15):
+// lane l receives column l/4 (r0) and column l/4 + 8 (r1) of rows
+// 4 (l % 4) .. 4 (l % 4) + 3, one byte per row, lowest row in the low byte.
+__device__ __forceinline__ void ldsm_b8_t(uint32_t& r0, uint32_t& r1, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m16n16.x1.trans.shared.b8 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr)
+               : "memory");
+}
+
 // D[16x8] += A[16x16] * B[16x8], bf16 inputs, fp32 accumulate.
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
@@ -676,15 +686,8 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
   const int qi = lane & 3;   // mma thread in group
   const int ST = p.st;
   const int sb = p.sbytes;
-  const int vt_row = lane & 15, vh = lane >> 4;  // V conversion: token row, half of the head
-  const int pv_t = (lane & 7) + (lane >> 4) * 8;  // V rows (A of P.V, trans)
-  const int pv_c = (lane >> 3) & 1;
-  // two P^T tiles [16 t][8 h] and two fp16 V tiles [16 t][D] per warp: the
-  // P.V product of a tile runs one tile late, overlapping the next tile's
-  // Q.K chain
-  const uint32_t pt_addr = smem_addr(pp.smem + p.off_pbuf + warp * 512);
-  const int vrs = p.vrs;
-  const uint32_t vt_addr = smem_addr(pp.smem + p.off_vbuf + warp * 32 * vrs);
+  // P^T tile [16 rows][8 heads] fp16; token t goes to row prow(t) (see below)
+  const uint32_t pt_addr = smem_addr(pp.smem + p.off_pbuf + warp * 256);
   const uint32_t smem0 = smem_addr(pp.smem);
 
   uint32_t qb[KS][2];
@@ -695,47 +698,29 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
   float m0 = 0.f, m1 = 0.f, l0 = 0.f, l1 = 0.f;
   bool mv = false;
   int ev = 0;  // biased exponent E of the V-weight normaliser 2^(E-127)
-  // Offsets of this lane's code units within a stage's code tile: every row
+  // Offsets of this lane's code units within a stage's code tile.  Every row
   // of a tile holds real data (a tensor copy always fills all ST rows, past
-  // the pool with zeros), so rows past n are read unclamped; their scores are
-  // masked and their weights are zero.
-  uint32_t koff[2][QW / 16], voff[D / 32];
+  // the pool with zeros), so rows past n are read as they are: their scores
+  // are masked and their weights are zero.
+  //  K: rows gl and gl + 8, the lane's QW-byte run of d.
+  //  V: the 16-byte unit kt of token row (lane & 15), the row address of
+  //     a transposing 16 x 16 byte ldmatrix.  That load hands lane (gl, qi)
+  //     bytes d = 16 kt + gl (and + 8) of tokens 4 qi .. 4 qi + 3, which
+  //     after conversion are the A fragment of V^T when the k index of the
+  //     P.V mma maps k = 2qi + {0, 1} to token 4qi + {0, 1} and k = 2qi + 8 +
+  //     {0, 1} to token 4qi + 2 + {0, 1}; P^T is stored with the same map.
+  uint32_t koff[2][QW / 16], voff[KS];
 #pragma unroll
   for (int i = 0; i < QW / 16; ++i) {
     koff[0][i] = code_unit<D>(0, g * ST + gl, (QW / 16) * qi + i);
     koff[1][i] = code_unit<D>(0, g * ST + gl + 8, (QW / 16) * qi + i);
   }
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) voff[c] = code_unit<D>(0, g * ST + vt_row, vh * (D / 32) + c);
-  int pend = -1;                 // buffer of the tile whose P.V is pending
-  float pa0 = 1.f, pa1 = 1.f;    // O scale factors to apply before that P.V
-
-  // O <- O * (pa0, pa1) + P^T V of buffer `buf` (and the same for the bias sums)
-  auto pv_step = [&](int buf) {
-    if (__any_sync(kFull, pa0 != 1.f || pa1 != 1.f)) {
-#pragma unroll
-      for (int kt = 0; kt < KS; ++kt) {
-        o[kt][0] *= pa0; o[kt][1] *= pa1; o[kt][2] *= pa0; o[kt][3] *= pa1;
-      }
-      vb0 *= pa0;
-      vb1 *= pa1;
-    }
-    uint32_t pb[2];
-    ldsm_x2_t(pb, pt_addr + buf * 256 + (lane & 15) * 16);
-    const uint32_t vt = vt_addr + buf * 16 * vrs;
-#pragma unroll
-    for (int kt = 0; kt < KS; ++kt) {
-      uint32_t a[4];
-      ldsm_x4_t(a, vt + pv_t * vrs + (2 * kt + pv_c) * 16);
-      mma_f16(o[kt], a, pb[0], pb[1]);
-    }
-    // the bias part of the products: every A row 1152
-    const uint32_t ab[4] = {kBiasF16x2, kBiasF16x2, kBiasF16x2, kBiasF16x2};
-    float vb[4] = {vb0, vb1, vb0, vb1};
-    mma_f16(vb, ab, pb[0], pb[1]);
-    vb0 = vb[0];
-    vb1 = vb[1];
-  };
+  for (int kt = 0; kt < KS; ++kt) voff[kt] = code_unit<D>(0, g * ST + (lane & 15), kt);
+  // P^T rows of this lane's tokens gl and gl + 8 under that map
+  auto prow = [](int t) { return (t & 2) ? 2 * (t >> 2) + 8 + (t & 1) : 2 * (t >> 2) + (t & 1); };
+  const uint32_t p_st0 = pt_addr + prow(gl) * 16 + qi * 4;
+  const uint32_t p_st1 = pt_addr + prow(gl + 8) * 16 + qi * 4;
 
   int s = 0;
   uint32_t ph = 0, gph = 0;
@@ -757,7 +742,6 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
       m0 = m1 = l0 = l1 = 0.f;
       vb0 = vb1 = 0.f;
       ev = 0;
-      pend = -1;
 #pragma unroll
       for (int kt = 0; kt < KS; ++kt)
 #pragma unroll
@@ -808,25 +792,7 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
     }
 
     if (n > 0) {  // one 16-row tile (stages never hold more rows)
-      const int cur = pend < 0 ? 0 : pend ^ 1;
-      const uint32_t vt = vt_addr + cur * 16 * vrs, pt = pt_addr + cur * 256;
       const int t0 = gl, t1 = gl + 8;
-      // V codes of the 16 tokens -> fp16 tile (lane: token vt, half vh of the
-      // head); independent of the scores, so issued first to overlap them
-      {
-        const uint32_t dst = vt + vt_row * vrs + vh * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          const uint4 w = lds128(sVc + voff[c]);
-          uint4 lo, hi;
-          i8x4_to_f16b(w.x, lo.x, lo.y);
-          i8x4_to_f16b(w.y, lo.z, lo.w);
-          i8x4_to_f16b(w.z, hi.x, hi.y);
-          i8x4_to_f16b(w.w, hi.z, hi.w);
-          sts128(dst + 32 * c, lo);
-          sts128(dst + 32 * c + 16, hi);
-        }
-      }
       uint32_t w0[KS], w1[KS];
 #pragma unroll
       for (int i = 0; i < QW / 16; ++i) {
@@ -849,8 +815,6 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
         i8x4_to_f16b(w1[j], a[1], a[3]);
         mma_f16((j & 1) ? sq : sa, a, qb[j][0], qb[j][1]);
       }
-      // the previous tile's P.V: independent of this tile's scores
-      if (pend >= 0) pv_step(pend);
       float sc[4];
       sc[0] = t0 < n ? ((sa[0] + sq[0]) - kb0) * qs0 * sk0 : -INFINITY;
       sc[1] = t0 < n ? ((sa[1] + sq[1]) - kb1) * qs1 * sk0 : -INFINITY;
@@ -886,21 +850,43 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
                                             : 0.f;
       const float f = __uint_as_float((uint32_t)(254 - en) << 23);  // 2^(127-en)
       ev = en;
-      // this tile's factors, applied to O right before its own P.V
-      pa0 = a0 * rescale;
-      pa1 = a1 * rescale;
+      const float ra0 = a0 * rescale, ra1 = a1 * rescale;
+      // O only changes scale when a running maximum moved (rare after the
+      // first tiles): skip the multiplies when no column of the warp moved
+      if (__any_sync(kFull, ra0 != 1.f || ra1 != 1.f)) {
+#pragma unroll
+        for (int kt = 0; kt < KS; ++kt) {
+          o[kt][0] *= ra0; o[kt][1] *= ra1; o[kt][2] *= ra0; o[kt][3] *= ra1;
+        }
+        vb0 *= ra0;
+        vb1 *= ra1;
+      }
       const float vw0 = sv0 * f, vw1 = sv1 * f;
-      sts32(pt + gl * 16 + qi * 4, pack_f16x2(p0 * vw0, p1 * vw0));
-      sts32(pt + (gl + 8) * 16 + qi * 4, pack_f16x2(p2 * vw1, p3 * vw1));
-      pend = cur;
+      sts32(p_st0, pack_f16x2(p0 * vw0, p1 * vw0));
+      sts32(p_st1, pack_f16x2(p2 * vw1, p3 * vw1));
+      __syncwarp();
+      uint32_t pb[2];
+      ldsm_x2_t(pb, pt_addr + (lane & 15) * 16);
+#pragma unroll
+      for (int kt = 0; kt < KS; ++kt) {
+        uint32_t r0, r1, a[4];
+        ldsm_b8_t(r0, r1, sVc + voff[kt]);
+        i8x4_to_f16b(r0, a[0], a[2]);
+        i8x4_to_f16b(r1, a[1], a[3]);
+        mma_f16(o[kt], a, pb[0], pb[1]);
+      }
+      {
+        // the bias part of the products: every A row 1152
+        const uint32_t ab[4] = {kBiasF16x2, kBiasF16x2, kBiasF16x2, kBiasF16x2};
+        float vb[4] = {vb0, vb1, vb0, vb1};
+        mma_f16(vb, ab, pb[0], pb[1]);
+        vb0 = vb[0];
+        vb1 = vb[1];
+      }
       __syncwarp();
     }
 
     if (flags & kEnd) {
-      if (pend >= 0) {  // drain the pending P.V
-        pv_step(pend);
-        pend = -1;
-      }
       // remove the V-code bias, then back to true units: O * 2^(E-127) (0
       // when every V scale was 0 or subnormal: true terms below 2^-126)
       const float back = ev >= 1 ? __uint_as_float((uint32_t)ev << 23) : 0.f;
@@ -912,7 +898,7 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
         o[kt][3] = (o[kt][3] - vb1) * back;
       }
       if (!mma_segment_end<D, G>(p, pp, gph, o, m0, m1, l0, l1, mv, b, seg, flags, warp,
-                                       lane))
+                                 lane))
         return;
     }
 
@@ -1315,8 +1301,8 @@ Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int 
   Layout L{};
   L.st = stage_tokens(bs, row_bytes);
   L.rs = row_bytes + kRowPad;
-  L.vrs = quant ? 2 * D + 16 : 0;  // fp16 V tile rows, padded for ldmatrix
-  const int vbuf = nw * 32 * L.vrs;  // two V tiles per warp (int8 pools)
+  L.vrs = 0;
+  const int vbuf = 0;
   if (quant) {
     // [K codes (Hkv, st, D) | V codes | K scales (st, sbytes) | V scales]:
     // every tensor-copy destination 128-byte aligned, the swizzled code
@@ -1333,10 +1319,9 @@ Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int 
     L.stage_bytes = 2 * L.st * L.rs;
   }
   const int stage_bytes = L.stage_bytes;
-  const int pbuf = nw * (quant ? 512 : (L.st * G * 4 > 256 ? L.st * G * 4 : 256));
-  // merge buffers of warps sharing a kv head: their own region, or (int8)
-  // each warp's V tile, idle while segments are merged
-  const int mbuf = (!quant && hkv < nw) ? 4 * nw * G * (D + 2) : 0;
+  const int pbuf = nw * (quant ? 256 : (L.st * G * 4 > 256 ? L.st * G * 4 : 256));
+  // merge buffers of warps sharing a kv head
+  const int mbuf = hkv < nw ? 4 * nw * G * (D + 2) : 0;
   int fixed = 0;
   fixed += 8 * (2 * kMaxStages + 1);              // barriers
   fixed = align_up(fixed, 16) + 16 * kMaxStages;  // descriptors
@@ -1359,7 +1344,6 @@ Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int 
   off = align_up(off, 16); L.off_pbuf = off; off += pbuf;
   off = align_up(off, 16); L.off_mbuf = off; off += mbuf;
   off = align_up(off, 16); L.off_vbuf = off; off += vbuf;
-  if (quant) L.off_mbuf = L.off_vbuf;
   L.smem = align_up(off, 16);
   return L;
 }
@@ -1431,7 +1415,7 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   p.vrs = L.vrs;
   p.stage_bytes = L.stage_bytes;
   p.nw = consumer_warps<T>();
-  p.mstride = sizeof(T) == 1 ? 32 * L.vrs / 4 : G * (D + 2);
+  p.mstride = G * (D + 2);
   p.off_kc = L.off_kc;
   p.off_vc = L.off_vc;
   p.off_ks = L.off_ks;
@@ -1524,8 +1508,6 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s) {
                                a.batch, a.smem_optin, pv.quant != 0, pv.quant ? kNWI8 : kNW);
   if (L.stages < 2) return cudaErrorInvalidConfiguration;
   if (pv.quant) {
-    // the merge buffer of a warp lives in its V tile
-    if (G * (pv.head_dim + 2) * 4 > 32 * L.vrs) return cudaErrorInvalidConfiguration;
     // tensor-copy row coordinates are 32-bit
     if ((long long)pv.num_blocks * pv.num_layers * pv.block_size >= (1ll << 31))
       return cudaErrorInvalidConfiguration;
