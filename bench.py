@@ -111,10 +111,10 @@ def kernel_source_hash() -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per launch of the decode partial kernel from the committed
-    ncu summary, only if it was taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "decode_partial_traffic.txt")
+def recorded_traffic(name: str = "decode_partial_traffic.txt"):
+    """DRAM bytes per launch of a decode partial kernel from a committed ncu
+    summary, only if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", name)
     d = {}
     try:
         with open(p) as f:
@@ -552,6 +552,7 @@ def int8_leg(args, dev, rank, flush, pkv) -> dict:
             "achieved_GBps": round(db["total"] / (part_ms / 1e3) / 1e9, 1),
             "frac": round(db["total"] / (part_ms / 1e3) / 1e9 / peak, 4),
             "peak": peak, "peak_kind": kind,
+            "traffic": recorded_traffic("decode_partial_i8_traffic.txt"),
         },
     }
     del st
