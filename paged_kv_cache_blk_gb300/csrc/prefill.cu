@@ -9,20 +9,23 @@
 // through the block table (first-block offset honoured).  GQA: query head h
 // reads kv head h / (Hq / Hkv).
 //
-// One CTA per (query tile, sequence, kv head):
-//  * 128 MMA rows = (128 / G) query tokens x the G query heads of kv head g,
-//    so each K/V tile feeds all G heads (row r = token * G + head).
-//  * Keys in tiles of 128 table positions (128 / bs whole blocks).  Tile t of
-//    K and of V is loaded by TMA (one box per block and 64-column half, 128B
-//    swizzle) into a 2-stage ring; invalid table entries load zeros.
-//  * Warp 5 issues S = Q K^T (M 128, N 128, K 128: 8 tcgen05.mma, fp32 in
-//    TMEM) and O += P V (V is the MN-major operand); S(t+1) is issued as soon
-//    as the softmax has read S(t), so it overlaps the softmax of tile t.
-//  * Warps 0-3 own one row each: they read the S row from TMEM
-//    (tcgen05.ld 32x32b), apply the causal / offset mask, keep the running
-//    max and sum in registers, rescale the O row in TMEM when a warp's max
-//    grows, and write P as bf16 into a K-major 128B-swizzled tile for the
-//    second MMA.
+// One CTA per (pair of query tiles, sequence, kv head):
+//  * A query tile is 128 MMA rows = (128 / G) query tokens x the G query
+//    heads of kv head g, so each K/V tile feeds all G heads (row r = token *
+//    G + head).  The CTA owns two tiles, A and B, that share the K/V stream.
+//  * Keys in tiles of 128 table positions (128 / bs whole blocks).  K(t) and
+//    V(t) are loaded by TMA (one box per block and 64-column half, 128B
+//    swizzle) into a 3-slot ring in the order K0 V0 K1 V1 ...; invalid table
+//    entries load zeros.
+//  * Warp 9 issues S_x = Q_x K^T (M 128, N 128, K 128: 8 tcgen05.mma, fp32
+//    in TMEM) and O_x += P_x V (V is the MN-major operand) in the order
+//    S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ..., so the softmax
+//    of one tile runs while the tensor cores work on the other.
+//  * Warps 0-3 (tile A) and 4-7 (tile B) own one row each: they read the S
+//    row from TMEM (tcgen05.ld 32x32b), mask only the tiles that need it, keep
+//    the running sum and a maximum that moves only when a score exceeds it by
+//    more than 2^8 (then the O row is rescaled in TMEM), and write P as bf16
+//    into a K-major 128B-swizzled tile for the second MMA.
 //  * Epilogue: O row / l -> bf16 -> global (only rows that are real queries).
 // Every wait is bounded; on a timeout the CTA records the error, drains its
 // MMAs and frees its TMEM before returning.
@@ -39,22 +42,25 @@
 namespace pkv {
 namespace {
 
-constexpr int kPfWarps = 6;
+constexpr int kPfWarps = 10;  // 0-3 softmax A, 4-7 softmax B, 8 TMA, 9 MMA
+constexpr int kWarpTma = 8;
+constexpr int kWarpMma = 9;
 constexpr int kPfThreads = kPfWarps * 32;
-constexpr int kRows = 128;   // MMA M: query rows per CTA
+constexpr int kRows = 128;   // MMA M: query rows per tile
 constexpr int kKeys = 128;   // keys per KV tile (MMA N of Q K^T, K of P V)
 constexpr int kD = 128;      // head_dim
 constexpr int kHalf = 128 * 64 * 2;  // one 128-row x 64-column bf16 half tile (16 KB)
 constexpr int kTileBytes = 2 * kHalf;  // 32 KB
-constexpr uint32_t kTmemCols = 256;    // S: columns [0,128), O: [128,256)
+constexpr int kSlots = 3;              // K / V ring: K(t), V(t), K(t+1) in flight
+constexpr uint32_t kTmemCols = 512;    // S_A, S_B, O_A, O_B
 constexpr float kLog2e = 1.4426950408889634f;
 
 // shared-memory carve, from a 1024-aligned base
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kTileBytes;                  // 2 stages x (K, V)
-constexpr int kOffP = kOffKV + 2 * 2 * kTileBytes;  // P tile
-constexpr int kOffBar = kOffP + kTileBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;    // barriers + TMEM slot + alignment slack
+constexpr int kOffQ = 0;                              // Q_A, Q_B
+constexpr int kOffKV = 2 * kTileBytes;                // ring of kSlots tiles
+constexpr int kOffP = kOffKV + kSlots * kTileBytes;   // P_A, P_B
+constexpr int kOffBar = kOffP + 2 * kTileBytes;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;      // barriers + TMEM slot + alignment slack
 
 struct PfParams {
   const int32_t* bt;
@@ -66,7 +72,7 @@ struct PfParams {
   long long total_q;
   long long blk_coord_limit;  // N * L (coordinate of the combined block/layer dimension)
   long long num_blocks;
-  int mb, batch, hq, hkv, G, TQ, bs, L, layer;
+  int mb, batch, hq, hkv, G, TQ, bs, L, layer, max_q_len;
   float qscale;
 };
 
@@ -142,6 +148,105 @@ __device__ __forceinline__ void tmem_wait_st() {
 
 // ---- the kernel ------------------------------------------------------------------
 
+// Rows of the S / P tile per thread of a softmax warpgroup (one row per
+// thread), and the state a warpgroup keeps for its query tile.
+struct RowState {
+  float m_used;  // the maximum P is taken against (raised only by more than 8)
+  float l;       // running sum of P
+};
+
+// Softmax of one S tile for one row: reads the row from TMEM, masks it,
+// updates the running state, rescales the O row when the maximum moved, and
+// writes the bf16 P row into the 128B-swizzled K-major P tile.  Returns false
+// when a bounded wait gave up.
+__device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t lane_base,
+                                             unsigned char* sP, int r, int t, int c_lo, int c_hi,
+                                             bool full_tile, float qs, RowState& st,
+                                             uint32_t b_pvdone, int* err) {
+  // With a positive scale the maximum is taken on the raw scores and the scale
+  // goes into the exponent's FMA; otherwise each score is scaled first.
+  const bool pre = qs <= 0.f;
+  const float qe = pre ? 1.f : qs;
+  // one 32-column chunk of the S row, scaled when needed and masked (the key
+  // in column c is valid for c_lo <= c <= c_hi)
+  auto load_chunk = [&](int c0, float (&x)[32]) {
+    uint32_t v[32];
+    tmem_ld32(tS + lane_base + c0, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      float f = __uint_as_float(v[j]);
+      if (pre) f *= qs;
+      if (!full_tile) f = (c0 + j >= c_lo && c0 + j <= c_hi) ? f : -INFINITY;
+      x[j] = f;
+    }
+  };
+  // pass 1: the row maximum (the S row is read twice from TMEM instead of
+  // being held in 128 registers)
+  float mt = -INFINITY;
+#pragma unroll 1
+  for (int c0 = 0; c0 < kKeys; c0 += 32) {
+    float x[32];
+    load_chunk(c0, x);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) mt = fmaxf(mt, x[j]);
+  }
+  const float mt_s = mt * qe;
+  float alpha = 1.f;
+  if (st.m_used == -INFINITY) {
+    if (mt_s != -INFINITY) st.m_used = mt_s;
+    alpha = 0.f;  // nothing accumulated yet
+  } else if (mt_s > st.m_used + 8.f) {
+    // P would exceed 2^8 against the old maximum: move it
+    alpha = exp2f(st.m_used - mt_s);
+    st.m_used = mt_s;
+  }
+  const float mu = st.m_used == -INFINITY ? 0.f : st.m_used;
+  if (t > 0) {
+    // O must hold P(t-1) V(t-1) before it is rescaled or P is rewritten
+    if (!mbar_wait(b_pvdone, (t - 1) & 1, err)) return false;
+    tc_fence_after();
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+      for (int c0 = 0; c0 < kD; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tO + lane_base + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+        tmem_st32(tO + lane_base + c0, v);
+      }
+      tmem_wait_st();
+    }
+  }
+  // pass 2: P row (bf16) into the K-major 128B-swizzled P tile: 16-byte chunk
+  // ch of row r at (r/8)*1024 + (r%8)*128 + ((ch ^ (r%8)) * 16), per 64-column half
+  float psum = 0.f;
+#pragma unroll 1
+  for (int c0 = 0; c0 < kKeys; c0 += 32) {
+    float x[32];
+    load_chunk(c0, x);
+#pragma unroll
+    for (int c = 0; c < 32; c += 8) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float a0 = exp2f(fmaf(x[c + 2 * e], qe, -mu));
+        const float a1 = exp2f(fmaf(x[c + 2 * e + 1], qe, -mu));
+        psum += a0 + a1;
+        w[e] = pack_bf16x2(a0, a1);
+      }
+      const int col = c0 + c;
+      const int half = col >> 6, chunk = (col & 63) >> 3;
+      unsigned char* dst =
+          sP + half * kHalf + (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  st.l = st.l * alpha + psum;
+  return true;
+}
+
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const PfParams p) {
@@ -152,19 +257,19 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // ---- work item -------------------------------------------------------------------
+  // ---- work item: two query tiles of one (sequence, kv head) ------------------------
   const int b = blockIdx.y, g = blockIdx.z;
   const long long q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
   const long long nq = q1 - q0;
   const int TQ = p.TQ, G = p.G;
   if (nq <= 0) return;
   const long long ntq = (nq + TQ - 1) / TQ;
-  if (ntq > (long long)gridDim.x) {  // more queries than the host bound allowed for
+  const long long npairs = (ntq + 1) / 2;
+  if (nq > p.max_q_len) {  // more queries than the host bound allowed for
     if (blockIdx.x == 0 && tid == 0) set_error(p.err, kErrCapacity);
     return;
   }
-  if ((long long)blockIdx.x >= ntq) return;
-  const long long qt = ntq - 1 - blockIdx.x;  // heaviest (latest) query tiles first
+  if ((long long)blockIdx.x >= npairs) return;
   const long long len = p.lens[b];
   const int off = p.offs ? p.offs[b] : 0;
   if (len < nq || off < 0 || off >= p.bs || q1 > p.total_q ||
@@ -172,41 +277,47 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (tid == 0) set_error(p.err, kErrCapacity);
     return;
   }
-  const long long first_pos = len - nq;                       // logical position of query 0
-  const long long tq_last = min(nq, (qt + 1) * TQ) - 1;       // last query of this tile
-  const long long p_max = first_pos + tq_last;                // last key any row needs
-  const int n_tiles = (int)((off + p_max) / kKeys) + 1;
+  // heaviest (latest) tiles first: pair x holds tiles ntq-1-2x (B) and
+  // ntq-2-2x (A, absent when negative); B needs at least as many keys as A
+  const long long qtB = ntq - 1 - 2 * (long long)blockIdx.x;
+  const long long qtA = qtB - 1;
+  const long long first_pos = len - nq;  // logical position of query 0
+  auto tiles_for = [&](long long qt) -> int {
+    if (qt < 0) return 0;
+    const long long last = min(nq, (qt + 1) * TQ) - 1;
+    return (int)((off + first_pos + last) / kKeys) + 1;
+  };
+  const int nA = tiles_for(qtA), nB = tiles_for(qtB);
   const int blocks_per_tile = kKeys / p.bs;
   const long long spanned = ((long long)off + len + p.bs - 1) / p.bs;
 
   // ---- shared memory, barriers, TMEM --------------------------------------------------
-  unsigned char* sQ = smem + kOffQ;
-  unsigned char* sP = smem + kOffP;
+  unsigned char* sQ = smem + kOffQ;  // [A | B]
+  unsigned char* sP = smem + kOffP;  // [A | B]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffBar + 128);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffBar + 192);
   const uint32_t b_q = smem_addr(&bars[0]);
-  const uint32_t b_kvfull0 = smem_addr(&bars[1]);   // [1], [2]
-  const uint32_t b_kvempty0 = smem_addr(&bars[3]);  // [3], [4]
-  const uint32_t b_sfull = smem_addr(&bars[5]);
-  const uint32_t b_sfree = smem_addr(&bars[6]);
-  const uint32_t b_pfull = smem_addr(&bars[7]);
-  const uint32_t b_pvdone = smem_addr(&bars[8]);
-  const uint32_t b_drain = smem_addr(&bars[9]);
-  auto kv_full = [&](int s) { return b_kvfull0 + 8u * s; };
-  auto kv_empty = [&](int s) { return b_kvempty0 + 8u * s; };
-  auto sK = [&](int s) { return smem + kOffKV + s * 2 * kTileBytes; };
-  auto sV = [&](int s) { return smem + kOffKV + s * 2 * kTileBytes + kTileBytes; };
+  const uint32_t b_full0 = smem_addr(&bars[1]);    // [1..3]  ring slot filled
+  const uint32_t b_empty0 = smem_addr(&bars[4]);   // [4..6]  ring slot consumed
+  const uint32_t b_sfull0 = smem_addr(&bars[7]);   // [7, 8]  S of tile A / B ready
+  const uint32_t b_pfull0 = smem_addr(&bars[9]);   // [9, 10] P of tile A / B written
+  const uint32_t b_pvdone0 = smem_addr(&bars[11]); // [11, 12] O += P V of A / B done
+  const uint32_t b_drain = smem_addr(&bars[13]);
+  auto slot_full = [&](int i) { return b_full0 + 8u * i; };
+  auto slot_empty = [&](int i) { return b_empty0 + 8u * i; };
+  auto slot_ptr = [&](int i) { return smem + kOffKV + i * kTileBytes; };
 
   if (tid == 0) {
     mbar_init(b_q, 1);
-    mbar_init(kv_full(0), 1);
-    mbar_init(kv_full(1), 1);
-    mbar_init(kv_empty(0), 1);
-    mbar_init(kv_empty(1), 1);
-    mbar_init(b_sfull, 1);
-    mbar_init(b_sfree, 4);
-    mbar_init(b_pfull, 4);
-    mbar_init(b_pvdone, 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(slot_full(i), 1);
+      mbar_init(slot_empty(i), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(b_sfull0 + 8u * x, 1);
+      mbar_init(b_pfull0 + 8u * x, 4);
+      mbar_init(b_pvdone0 + 8u * x, 1);
+    }
     mbar_init(b_drain, 1);
     fence_mbar_init();
   }
@@ -221,26 +332,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t tS = tmem, tO = tmem + 128;
+  // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512)
+  auto tS = [&](int x) { return tmem + 128u * x; };
+  auto tO = [&](int x) { return tmem + 256u + 128u * x; };
   bool ok = true;
 
-  if (warp == 4) {
-    // ================= TMA producer =================
+  if (warp == kWarpTma) {
+    // ================= TMA producer: Q tiles, then K(0) V(0) K(1) V(1) ... =================
     if (lane == 0) {
-      mbar_arrive_expect_tx(b_q, kTileBytes);
-      const int z = (int)(q0 + qt * TQ);
-      for (int h = 0; h < 2; ++h) tma_3d(smem_addr(sQ + h * kHalf), &tq, h * 64, g * G, z, b_q);
+      mbar_arrive_expect_tx(b_q, (nA > 0 ? 2 : 1) * kTileBytes);
+      for (int x = (nA > 0 ? 0 : 1); x < 2; ++x) {
+        const int z = (int)(q0 + (x == 0 ? qtA : qtB) * TQ);
+        for (int h = 0; h < 2; ++h)
+          tma_3d(smem_addr(sQ + x * kTileBytes + h * kHalf), &tq, h * 64, g * G, z, b_q);
+      }
     }
-    const int boxes = 2 * 2 * blocks_per_tile;  // (K, V) x halves x blocks
     const int box_bytes = p.bs * 128;
-    for (int t = 0; t < n_tiles && ok; ++t) {
-      const int s = t & 1;
-      if (t >= 2 && !mbar_wait(kv_empty(s), ((t >> 1) - 1) & 1, p.err)) { ok = false; break; }
-      if (lane == 0) mbar_arrive_expect_tx(kv_full(s), 2 * kTileBytes);
+    for (int li = 0; li < 2 * nB && ok; ++li) {
+      const int slot = li % kSlots, use = li / kSlots;
+      if (use > 0 && !mbar_wait(slot_empty(slot), (use - 1) & 1, p.err)) { ok = false; break; }
+      const int t = li >> 1, is_v = li & 1;
+      if (lane == 0) mbar_arrive_expect_tx(slot_full(slot), kTileBytes);
       __syncwarp();
-      for (int i = lane; i < boxes; i += 32) {
-        const int is_v = i / (2 * blocks_per_tile);
-        const int h = (i / blocks_per_tile) & 1;
+      for (int i = lane; i < 2 * blocks_per_tile; i += 32) {
+        const int h = i / blocks_per_tile;
         const int k = i % blocks_per_tile;
         const long long lb = (long long)t * blocks_per_tile + k;  // logical block
         long long coord = p.blk_coord_limit;                       // out of range: zeros
@@ -252,141 +367,126 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             set_error(p.err, kErrIndex);
           }
         }
-        unsigned char* base = is_v ? sV(s) : sK(s);
-        tma_4d(smem_addr(base + h * kHalf + k * box_bytes), is_v ? &tv : &tk, h * 64, g, 0,
-               (int)coord, kv_full(s));
+        tma_4d(smem_addr(slot_ptr(slot) + h * kHalf + k * box_bytes), is_v ? &tv : &tk, h * 64,
+               g, 0, (int)coord, slot_full(slot));
       }
       __syncwarp();
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ================= MMA issuer =================
+    // order: S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ...  so that
+    // each warpgroup's softmax overlaps the other tile's products
     if (lane == 0) {
       const uint32_t q_addr = smem_addr(sQ), p_addr = smem_addr(sP);
-      auto issue_s = [&](int t) {
-        const uint32_t k_addr = smem_addr(sK(t & 1));
-        tc_fence_after();
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t a = desc_sw128(q_addr + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = desc_sw128(k_addr + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
-          umma(tS, a, bd, kIdescKK, k > 0);
-        }
-        umma_commit(b_sfull);
+      auto k_slot = [&](int t) { return (2 * t) % kSlots; };
+      auto v_slot = [&](int t) { return (2 * t + 1) % kSlots; };
+      auto k_ready = [&](int t) {
+        return mbar_wait(slot_full(k_slot(t)), ((2 * t) / kSlots) & 1, p.err);
       };
-      ok = mbar_wait(b_q, 0, p.err) && mbar_wait(kv_full(0), 0, p.err);
-      if (ok) issue_s(0);
-      for (int t = 0; t < n_tiles && ok; ++t) {
-        if (t + 1 < n_tiles) {
-          if (!mbar_wait(kv_full((t + 1) & 1), ((t + 1) >> 1) & 1, p.err) ||
-              !mbar_wait(b_sfree, t & 1, p.err)) {
-            ok = false;
-            break;
-          }
-          issue_s(t + 1);
-        }
-        if (!mbar_wait(b_pfull, t & 1, p.err)) { ok = false; break; }
+      auto v_ready = [&](int t) {
+        return mbar_wait(slot_full(v_slot(t)), ((2 * t + 1) / kSlots) & 1, p.err);
+      };
+      auto issue_s = [&](int x, int t) {
+        const uint32_t k_addr = smem_addr(slot_ptr(k_slot(t)));
+        const uint32_t qa = q_addr + x * kTileBytes;
         tc_fence_after();
-        const uint32_t v_addr = smem_addr(sV(t & 1));
         for (int k = 0; k < 8; ++k) {
-          const uint64_t a = desc_sw128(p_addr + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = desc_sw128(v_addr + k * 2048, kHalf, 1024);
-          umma(tO, a, bd, kIdescKMN, (t > 0 || k > 0) ? 1u : 0u);
+          const uint64_t a = desc_sw128(qa + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
+          const uint64_t bd = desc_sw128(k_addr + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
+          umma(tS(x), a, bd, kIdescKK, k > 0);
         }
-        umma_commit(b_pvdone);
-        umma_commit(kv_empty(t & 1));
+        umma_commit(b_sfull0 + 8u * x);
+      };
+      auto issue_pv = [&](int x, int t) {
+        const uint32_t v_addr = smem_addr(slot_ptr(v_slot(t)));
+        const uint32_t pa = p_addr + x * kTileBytes;
+        tc_fence_after();
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t a = desc_sw128(pa + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
+          const uint64_t bd = desc_sw128(v_addr + k * 2048, kHalf, 1024);
+          umma(tO(x), a, bd, kIdescKMN, (t > 0 || k > 0) ? 1u : 0u);
+        }
+        umma_commit(b_pvdone0 + 8u * x);
+      };
+      ok = mbar_wait(b_q, 0, p.err) && k_ready(0);
+      if (ok) {
+        if (nA > 0) issue_s(0, 0);
+        issue_s(1, 0);
+        if (nB == 1 || nA <= 1) {
+          // K(0) is not needed again once both products are issued
+        }
+      }
+      for (int t = 0; t < nB && ok; ++t) {
+        const bool more = t + 1 < nB;
+        // K(t) is released after the last S product that reads it
+        umma_commit(slot_empty(k_slot(t)));
+        if (!v_ready(t)) { ok = false; break; }
+        if (t < nA) {
+          if (!mbar_wait(b_pfull0, t & 1, p.err)) { ok = false; break; }
+          issue_pv(0, t);
+          if (t + 1 < nA) {
+            if (!k_ready(t + 1)) { ok = false; break; }
+            issue_s(0, t + 1);
+          }
+        }
+        if (!mbar_wait(b_pfull0 + 8u, t & 1, p.err)) { ok = false; break; }
+        issue_pv(1, t);
+        umma_commit(slot_empty(v_slot(t)));
+        if (more) {
+          if (!(t + 1 < nA) && !k_ready(t + 1)) { ok = false; break; }
+          issue_s(1, t + 1);
+        }
       }
       umma_commit(b_drain);  // arrives once every MMA issued above has completed
     }
   } else {
-    // ================= softmax warps 0-3: one row per thread =================
-    const int r = tid;                        // MMA row = TMEM lane
+    // ================= softmax: warpgroup x = 0 (tile A) or 1 (tile B), one row per thread ======
+    const int x = warp >> 2;
+    const int nX = x == 0 ? nA : nB;
+    const long long qt = x == 0 ? qtA : qtB;
+    const int r = tid & 127;                 // MMA row = TMEM lane
     const int qtok = r / G, hh = r - qtok * G;
-    const long long qi = qt * TQ + qtok;      // query index within the sequence
-    const bool row_ok = qi < nq;
-    const long long pos = first_pos + qi;     // its logical position
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float m = -INFINITY, l = 0.f;
-    for (int t = 0; t < n_tiles && ok; ++t) {
+    const long long qi = qt * TQ + qtok;     // query index within the sequence
+    const bool row_ok = nX > 0 && qi < nq;
+    const long long pos = first_pos + qi;    // its logical position
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t b_sfull = b_sfull0 + 8u * x, b_pfull = b_pfull0 + 8u * x;
+    const uint32_t b_pvdone = b_pvdone0 + 8u * x;
+    unsigned char* sPx = sP + x * kTileBytes;
+    // first and last key tiles where some row of this warpgroup is masked
+    const long long tq_first = qt * TQ;
+    const int t_mask_lo = (int)((off + first_pos + tq_first) / kKeys);
+    const bool rows_full = (qt + 1) * TQ <= nq;
+    RowState st{-INFINITY, 0.f};
+    for (int t = 0; t < nX && ok; ++t) {
       if (!mbar_wait(b_sfull, t & 1, p.err)) { ok = false; break; }
       tc_fence_after();
-      float sreg[kKeys];
-#pragma unroll
-      for (int c0 = 0; c0 < kKeys; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tS + lane_base + c0, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sreg[c0 + j] = __uint_as_float(v[j]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_sfree);
-      // mask: the key in column c sits at table position t*128 + c, i.e. logical
-      // j = t*128 + c - off; it is valid for 0 <= j <= pos
       const long long tp0 = (long long)t * kKeys;
       const int c_lo = (int)max(0ll, (long long)off - tp0);
       const int c_hi = row_ok ? (int)min((long long)kKeys - 1, pos + off - tp0) : -1;
-      float mt = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kKeys; ++c) {
-        const bool valid = c >= c_lo && c <= c_hi;
-        sreg[c] = valid ? sreg[c] * p.qscale : -INFINITY;
-        mt = fmaxf(mt, sreg[c]);
+      // tiles before the first diagonal tile are full for every row when the
+      // tile has no padding rows (and t = 0 only without a first-block offset)
+      const bool full_tile = (t > 0 || off == 0) && t < t_mask_lo && rows_full;
+      if (!softmax_tile(tS(x), tO(x), lane_base, sPx, r, t, c_lo, c_hi, full_tile, p.qscale, st,
+                        b_pvdone, p.err)) {
+        ok = false;
+        break;
       }
-      const float m_new = fmaxf(m, mt);
-      const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = m == -INFINITY ? 0.f : exp2f(m - m_use);
-      if (t > 0) {
-        // O must hold P(t-1) V(t-1) before it is rescaled or P is rewritten
-        if (!mbar_wait(b_pvdone, (t - 1) & 1, p.err)) { ok = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-          for (int c0 = 0; c0 < kD; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tO + lane_base + c0, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-            tmem_st32(tO + lane_base + c0, v);
-          }
-          tmem_wait_st();
-        }
-      }
-      float psum = 0.f;
-      // P row (bf16) into the K-major 128B-swizzled P tile: 16-byte chunk ch of
-      // row r at (r/8)*1024 + (r%8)*128 + ((ch ^ (r%8)) * 16), per 64-column half
-#pragma unroll
-      for (int c = 0; c < kKeys; c += 8) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float a0 = exp2f(sreg[c + 2 * e] - m_use);
-          const float a1 = exp2f(sreg[c + 2 * e + 1] - m_use);
-          psum += a0 + a1;
-          w[e] = pack_bf16x2(a0, a1);
-        }
-        const int half = c >> 6, chunk = (c & 63) >> 3;
-        unsigned char* dst =
-            sP + half * kHalf + (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      l = l * alpha + psum;
-      m = m_new;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_pfull);
     }
     // epilogue: O row / l -> bf16 -> out
-    if (ok && mbar_wait(b_pvdone, (n_tiles - 1) & 1, p.err)) {
+    if (ok && nX > 0 && mbar_wait(b_pvdone, (nX - 1) & 1, p.err)) {
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
                             ((q0 + qi) * p.hq + (long long)g * G + hh) * kD;
 #pragma unroll
       for (int c0 = 0; c0 < kD; c0 += 32) {
         uint32_t v[32];
-        tmem_ld32(tO + lane_base + c0, v);
+        tmem_ld32(tO(x) + lane_base + c0, v);
         tmem_wait_ld();
         if (row_ok) {
 #pragma unroll
@@ -476,6 +576,7 @@ cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num
   p.bs = pv.block_size;
   p.L = pv.num_layers;
   p.layer = layer;
+  p.max_q_len = max_q_len;
   p.qscale = scale * kLog2e;
   static int configured[64] = {0};
   int dev = 0;
@@ -487,8 +588,8 @@ cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  const dim3 grid((unsigned)((max_q_len + TQ - 1) / TQ), (unsigned)batch,
-                  (unsigned)pv.num_kv_heads);
+  const long long ntq = (max_q_len + TQ - 1) / TQ;
+  const dim3 grid((unsigned)((ntq + 1) / 2), (unsigned)batch, (unsigned)pv.num_kv_heads);
   return launch_kernel(prefill_kernel, grid, dim3(kPfThreads), (size_t)kSmemBytes, s, true, tq, tk,
                        tv, p);
 }
