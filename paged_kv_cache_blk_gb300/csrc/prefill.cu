@@ -159,6 +159,12 @@ struct RowState {
 // updates the running state, rescales the O row when the maximum moved, and
 // writes the bf16 P row into the 128B-swizzled K-major P tile.  Returns false
 // when a bounded wait gave up.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t lane_base,
                                              unsigned char* sP, int r, int t, int c_lo, int c_hi,
                                              bool full_tile, float qs, RowState& st,
@@ -181,51 +187,11 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
       x[j] = f;
     }
   };
-  // pass 1: the row maximum (the S row is read twice from TMEM instead of
-  // being held in 128 registers)
-  float mt = -INFINITY;
-#pragma unroll 1
-  for (int c0 = 0; c0 < kKeys; c0 += 32) {
-    float x[32];
-    load_chunk(c0, x);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) mt = fmaxf(mt, x[j]);
-  }
-  const float mt_s = mt * qe;
-  float alpha = 1.f;
-  if (st.m_used == -INFINITY) {
-    if (mt_s != -INFINITY) st.m_used = mt_s;
-    alpha = 0.f;  // nothing accumulated yet
-  } else if (mt_s > st.m_used + 8.f) {
-    // P would exceed 2^8 against the old maximum: move it
-    alpha = exp2f(st.m_used - mt_s);
-    st.m_used = mt_s;
-  }
-  const float mu = st.m_used == -INFINITY ? 0.f : st.m_used;
-  if (t > 0) {
-    // O must hold P(t-1) V(t-1) before it is rescaled or P is rewritten
-    if (!mbar_wait(b_pvdone, (t - 1) & 1, err)) return false;
-    tc_fence_after();
-    if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-      for (int c0 = 0; c0 < kD; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tO + lane_base + c0, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
-        tmem_st32(tO + lane_base + c0, v);
-      }
-      tmem_wait_st();
-    }
-  }
-  // pass 2: P row (bf16) into the K-major 128B-swizzled P tile: 16-byte chunk
-  // ch of row r at (r/8)*1024 + (r%8)*128 + ((ch ^ (r%8)) * 16), per 64-column half
-  float psum = 0.f;
-#pragma unroll 1
-  for (int c0 = 0; c0 < kKeys; c0 += 32) {
-    float x[32];
-    load_chunk(c0, x);
+  // P row (bf16) of one chunk against the maximum mu into the K-major
+  // 128B-swizzled P tile: 16-byte chunk ch of row r at (r/8)*1024 + (r%8)*128
+  // + ((ch ^ (r%8)) * 16), per 64-column half; returns the chunk's sum
+  auto write_p = [&](int c0, const float (&x)[32], float mu) {
+    float psum = 0.f;
 #pragma unroll
     for (int c = 0; c < 32; c += 8) {
       uint32_t w[4];
@@ -242,6 +208,80 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
           sP + half * kHalf + (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4);
       *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
     }
+    return psum;
+  };
+  auto chunk_max = [&](const float (&x)[32], float m) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) m = max3(m, x[j], x[j + 1]);
+    return m;
+  };
+  // Every tcgen05.ld / st below is a warp-wide instruction, so all control
+  // flow around them is warp-uniform: per-row decisions only select data.
+  // O must hold P(t-1) V(t-1) before P is rewritten or O rescaled (by the
+  // time S(t) is ready that product has normally finished).
+  if (t > 0) {
+    const bool waited = mbar_wait(b_pvdone, (t - 1) & 1, err);
+    if (!__all_sync(0xffffffffu, waited)) return false;
+    tc_fence_after();
+  }
+  float psum = 0.f, alpha = 1.f;
+  const bool first = st.m_used == -INFINITY;  // this row has no maximum yet
+  const bool any_first = __any_sync(0xffffffffu, first);
+  float mt = -INFINITY;
+  if (!any_first) {
+    // one pass against the current maximum, tracking this tile's maximum
+#pragma unroll 1
+    for (int c0 = 0; c0 < kKeys; c0 += 32) {
+      float x[32];
+      load_chunk(c0, x);
+      mt = chunk_max(x, mt);
+      psum += write_p(c0, x, st.m_used);
+    }
+  } else {
+    // some row still needs its first maximum: find the maxima first
+#pragma unroll 1
+    for (int c0 = 0; c0 < kKeys; c0 += 32) {
+      float x[32];
+      load_chunk(c0, x);
+      mt = chunk_max(x, mt);
+    }
+  }
+  const float mt_s = mt * qe;
+  bool rewrite = any_first;  // P not written yet in this warp
+  if (first) {
+    // a real row finds its first keys in tile 0 (nothing accumulated yet); a
+    // padding row (all keys masked) keeps P = 0 and is never written out
+    if (mt_s != -INFINITY) {
+      st.m_used = mt_s;
+      alpha = 0.f;
+    }
+  } else if (mt_s > st.m_used + 8.f) {
+    // P would exceed 2^8 against the old maximum: move it and write P again
+    alpha = exp2f(st.m_used - mt_s);
+    st.m_used = mt_s;
+    rewrite = true;
+  }
+  if (__any_sync(0xffffffffu, rewrite)) {
+    const float mu = st.m_used == -INFINITY ? 0.f : st.m_used;
+    psum = 0.f;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kKeys; c0 += 32) {
+      float x[32];
+      load_chunk(c0, x);
+      psum += write_p(c0, x, mu);
+    }
+  }
+  if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < kD; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(tO + lane_base + c0, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
+      tmem_st32(tO + lane_base + c0, v);
+    }
+    tmem_wait_st();
   }
   st.l = st.l * alpha + psum;
   return true;
@@ -459,7 +499,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const bool rows_full = (qt + 1) * TQ <= nq;
     RowState st{-INFINITY, 0.f};
     for (int t = 0; t < nX && ok; ++t) {
-      if (!mbar_wait(b_sfull, t & 1, p.err)) { ok = false; break; }
+      const bool waited = mbar_wait(b_sfull, t & 1, p.err);
+      if (!__all_sync(0xffffffffu, waited)) { ok = false; break; }
       tc_fence_after();
       const long long tp0 = (long long)t * kKeys;
       const int c_lo = (int)max(0ll, (long long)off - tp0);
@@ -478,7 +519,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (lane == 0) mbar_arrive(b_pfull);
     }
     // epilogue: O row / l -> bf16 -> out
-    if (ok && nX > 0 && mbar_wait(b_pvdone, (nX - 1) & 1, p.err)) {
+    bool done = ok && nX > 0;
+    if (done) done = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (nX - 1) & 1, p.err));
+    if (done) {
       tc_fence_after();
       const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
@@ -508,6 +551,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   __syncthreads();
   if (warp == 0) {
     mbar_wait(b_drain, 0, p.err);
+    __syncwarp();  // the dealloc below is warp-wide
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
