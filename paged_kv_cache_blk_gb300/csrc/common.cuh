@@ -66,15 +66,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same with an explicit suspend-time hint: the waiting thread sleeps until
+// the phase completes or about `hint_ns` pass, instead of polling, so a waiting
+// warp takes no issue slots from the warps that work beside it.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of parity `parity` to complete, giving up after
 // kWaitTimeoutNs (or 2^30 polls): on giving up, set kErrTimeout and return
-// false so the caller can leave cleanly.
+// false so the caller can leave cleanly.  Polls: for the short waits of the
+// streaming kernels.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) break;
+  }
+  set_error(err, kErrTimeout);
+  return false;
+}
+
+// The same bound, sleeping between checks (suspend-time hint): for waits that
+// last as long as a tensor-core product, where a polling warp would take issue
+// slots from the warp working beside it.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1; it < (1u << 26); ++it) {
+    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
   }
   set_error(err, kErrTimeout);
   return false;

@@ -220,7 +220,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
   // O must hold P(t-1) V(t-1) before P is rewritten or O rescaled (by the
   // time S(t) is ready that product has normally finished).
   if (t > 0) {
-    const bool waited = mbar_wait(b_pvdone, (t - 1) & 1, err);
+    const bool waited = mbar_wait_sleep(b_pvdone, (t - 1) & 1, err);
     if (!__all_sync(0xffffffffu, waited)) return false;
     tc_fence_after();
   }
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int box_bytes = p.bs * 128;
     for (int li = 0; li < 2 * nB && ok; ++li) {
       const int slot = li % kSlots, use = li / kSlots;
-      if (use > 0 && !mbar_wait(slot_empty(slot), (use - 1) & 1, p.err)) { ok = false; break; }
+      if (use > 0 && !mbar_wait_sleep(slot_empty(slot), (use - 1) & 1, p.err)) { ok = false; break; }
       const int t = li >> 1, is_v = li & 1;
       if (lane == 0) mbar_arrive_expect_tx(slot_full(slot), kTileBytes);
       __syncwarp();
@@ -421,10 +421,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       auto k_slot = [&](int t) { return (2 * t) % kSlots; };
       auto v_slot = [&](int t) { return (2 * t + 1) % kSlots; };
       auto k_ready = [&](int t) {
-        return mbar_wait(slot_full(k_slot(t)), ((2 * t) / kSlots) & 1, p.err);
+        return mbar_wait_sleep(slot_full(k_slot(t)), ((2 * t) / kSlots) & 1, p.err);
       };
       auto v_ready = [&](int t) {
-        return mbar_wait(slot_full(v_slot(t)), ((2 * t + 1) / kSlots) & 1, p.err);
+        return mbar_wait_sleep(slot_full(v_slot(t)), ((2 * t + 1) / kSlots) & 1, p.err);
       };
       auto issue_s = [&](int x, int t) {
         const uint32_t k_addr = smem_addr(slot_ptr(k_slot(t)));
@@ -448,7 +448,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         umma_commit(b_pvdone0 + 8u * x);
       };
-      ok = mbar_wait(b_q, 0, p.err) && k_ready(0);
+      ok = mbar_wait_sleep(b_q, 0, p.err) && k_ready(0);
       if (ok) {
         if (nA > 0) issue_s(0, 0);
         issue_s(1, 0);
@@ -462,14 +462,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         umma_commit(slot_empty(k_slot(t)));
         if (!v_ready(t)) { ok = false; break; }
         if (t < nA) {
-          if (!mbar_wait(b_pfull0, t & 1, p.err)) { ok = false; break; }
+          if (!mbar_wait_sleep(b_pfull0, t & 1, p.err)) { ok = false; break; }
           issue_pv(0, t);
           if (t + 1 < nA) {
             if (!k_ready(t + 1)) { ok = false; break; }
             issue_s(0, t + 1);
           }
         }
-        if (!mbar_wait(b_pfull0 + 8u, t & 1, p.err)) { ok = false; break; }
+        if (!mbar_wait_sleep(b_pfull0 + 8u, t & 1, p.err)) { ok = false; break; }
         issue_pv(1, t);
         umma_commit(slot_empty(v_slot(t)));
         if (more) {
@@ -499,7 +499,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const bool rows_full = (qt + 1) * TQ <= nq;
     RowState st{-INFINITY, 0.f};
     for (int t = 0; t < nX && ok; ++t) {
-      const bool waited = mbar_wait(b_sfull, t & 1, p.err);
+      const bool waited = mbar_wait_sleep(b_sfull, t & 1, p.err);
       if (!__all_sync(0xffffffffu, waited)) { ok = false; break; }
       tc_fence_after();
       const long long tp0 = (long long)t * kKeys;
@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     // epilogue: O row / l -> bf16 -> out
     bool done = ok && nX > 0;
-    if (done) done = __all_sync(0xffffffffu, mbar_wait(b_pvdone, (nX - 1) & 1, p.err));
+    if (done) done = __all_sync(0xffffffffu, mbar_wait_sleep(b_pvdone, (nX - 1) & 1, p.err));
     if (done) {
       tc_fence_after();
       const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
@@ -550,7 +550,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
-    mbar_wait(b_drain, 0, p.err);
+    mbar_wait_sleep(b_drain, 0, p.err);
     __syncwarp();  // the dealloc below is warp-wide
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
