@@ -376,7 +376,7 @@ pkv_status pkv_prefill_attention(const pkv_pool* pool, int32_t layer, const void
   }
   if ((st = launched(pkv::launch_prefill(v, layer, q, num_q_heads, scale, block_tables,
                                          max_blocks_per_seq, seq_lens, offsets, cu_q, batch,
-                                         total_q, max_q_len, out, d->err, stream))) != PKV_OK)
+                                         total_q, max_q_len, out, d->err, d->sm_count, stream))) != PKV_OK)
     return st;
   return validate ? read_and_clear(d->err, stream) : PKV_OK;
 }

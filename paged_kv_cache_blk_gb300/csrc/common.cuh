@@ -260,7 +260,7 @@ int prefill_supported(const PoolView& pv, int num_q_heads);
 cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num_q_heads,
                            float scale, const int32_t* bt, int mb, const int32_t* lens,
                            const int32_t* offs, const int64_t* cu_q, int batch, long long total_q,
-                           int max_q_len, void* out, int* err, cudaStream_t s);
+                           int max_q_len, void* out, int* err, int sm_count, cudaStream_t s);
 
 // Current-device facts for entry points defined outside api.cu: dynamic
 // shared memory limit, the sticky error word, the decode grid size and the

@@ -72,6 +72,7 @@ struct PfParams {
   long long total_q;
   long long blk_coord_limit;  // N * L (coordinate of the combined block/layer dimension)
   long long num_blocks;
+  long long n_items;  // pairs x batch x kv heads
   int mb, batch, hq, hkv, G, TQ, bs, L, layer, max_q_len;
   float qscale;
 };
@@ -168,7 +169,7 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t lane_base,
                                              unsigned char* sP, int r, int t, int c_lo, int c_hi,
                                              bool full_tile, float qs, RowState& st,
-                                             uint32_t b_pvdone, int* err) {
+                                             uint32_t b_pvdone, uint32_t pv_parity, int* err) {
   // With a positive scale the maximum is taken on the raw scores and the scale
   // goes into the exponent's FMA; otherwise each score is scaled first.
   const bool pre = qs <= 0.f;
@@ -220,7 +221,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
   // O must hold P(t-1) V(t-1) before P is rewritten or O rescaled (by the
   // time S(t) is ready that product has normally finished).
   if (t > 0) {
-    const bool waited = mbar_wait_sleep(b_pvdone, (t - 1) & 1, err);
+    const bool waited = mbar_wait_sleep(b_pvdone, pv_parity, err);
     if (!__all_sync(0xffffffffu, waited)) return false;
     tc_fence_after();
   }
@@ -287,6 +288,58 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
   return true;
 }
 
+// One work item: a pair of query tiles of one (sequence, kv head).  All roles
+// of a CTA derive the same values from the same inputs, so they skip the same
+// items and agree on every barrier phase.
+struct Item {
+  bool valid;
+  int b, g, nA, nB;
+  long long q0, nq, qtA, qtB, first_pos, spanned;
+  int off;
+};
+
+__device__ __forceinline__ Item make_item(const PfParams& p, long long i, int tid) {
+  Item it{};
+  const long long per = (long long)p.batch * p.hkv;
+  const long long px = i / per;  // pair rank: 0 = the latest (heaviest) pair
+  const long long rem = i - px * per;
+  it.b = (int)(rem / p.hkv);
+  it.g = (int)(rem - (long long)it.b * p.hkv);
+  it.q0 = p.cu_q[it.b];
+  const long long q1 = p.cu_q[it.b + 1];
+  it.nq = q1 - it.q0;
+  if (it.nq <= 0) return it;
+  const int TQ = p.TQ;
+  const long long ntq = (it.nq + TQ - 1) / TQ;
+  if (px >= (ntq + 1) / 2) return it;
+  const long long len = p.lens[it.b];
+  it.off = p.offs ? p.offs[it.b] : 0;
+  if (it.nq > p.max_q_len || len < it.nq || it.off < 0 || it.off >= p.bs || q1 > p.total_q ||
+      (long long)it.off + len > (long long)p.mb * p.bs) {
+    // reported once, by the item of the sequence's first pair and head
+    if (px == 0 && it.g == 0 && tid == 0) set_error(p.err, kErrCapacity);
+    return it;
+  }
+  it.qtB = ntq - 1 - 2 * px;
+  it.qtA = it.qtB - 1;
+  it.first_pos = len - it.nq;
+  auto tiles_for = [&](long long qt) -> int {
+    if (qt < 0) return 0;
+    const long long last = min(it.nq, (qt + 1) * TQ) - 1;
+    return (int)((it.off + it.first_pos + last) / kKeys) + 1;
+  };
+  it.nA = tiles_for(it.qtA);
+  it.nB = tiles_for(it.qtB);
+  it.spanned = ((long long)it.off + len + p.bs - 1) / p.bs;
+  it.valid = true;
+  return it;
+}
+
+// Persistent: one CTA per SM walks the items c, c + grid, c + 2 grid, ...
+// (pairs of every sequence and head in order of decreasing key count).  The
+// K/V ring, the barrier phases and the TMEM allocation carry over from item
+// to item, so the next item's loads and first products overlap the previous
+// item's epilogue.
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const PfParams p) {
@@ -296,59 +349,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  // ---- work item: two query tiles of one (sequence, kv head) ------------------------
-  const int b = blockIdx.y, g = blockIdx.z;
-  const long long q0 = p.cu_q[b], q1 = p.cu_q[b + 1];
-  const long long nq = q1 - q0;
   const int TQ = p.TQ, G = p.G;
-  if (nq <= 0) return;
-  const long long ntq = (nq + TQ - 1) / TQ;
-  const long long npairs = (ntq + 1) / 2;
-  if (nq > p.max_q_len) {  // more queries than the host bound allowed for
-    if (blockIdx.x == 0 && tid == 0) set_error(p.err, kErrCapacity);
-    return;
-  }
-  if ((long long)blockIdx.x >= npairs) return;
-  const long long len = p.lens[b];
-  const int off = p.offs ? p.offs[b] : 0;
-  if (len < nq || off < 0 || off >= p.bs || q1 > p.total_q ||
-      (long long)off + len > (long long)p.mb * p.bs) {
-    if (tid == 0) set_error(p.err, kErrCapacity);
-    return;
-  }
-  // heaviest (latest) tiles first: pair x holds tiles ntq-1-2x (B) and
-  // ntq-2-2x (A, absent when negative); B needs at least as many keys as A
-  const long long qtB = ntq - 1 - 2 * (long long)blockIdx.x;
-  const long long qtA = qtB - 1;
-  const long long first_pos = len - nq;  // logical position of query 0
-  auto tiles_for = [&](long long qt) -> int {
-    if (qt < 0) return 0;
-    const long long last = min(nq, (qt + 1) * TQ) - 1;
-    return (int)((off + first_pos + last) / kKeys) + 1;
-  };
-  const int nA = tiles_for(qtA), nB = tiles_for(qtB);
   const int blocks_per_tile = kKeys / p.bs;
-  const long long spanned = ((long long)off + len + p.bs - 1) / p.bs;
 
   // ---- shared memory, barriers, TMEM --------------------------------------------------
   unsigned char* sQ = smem + kOffQ;  // [A | B]
   unsigned char* sP = smem + kOffP;  // [A | B]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffBar + 192);
-  const uint32_t b_q = smem_addr(&bars[0]);
-  const uint32_t b_full0 = smem_addr(&bars[1]);    // [1..3]  ring slot filled
-  const uint32_t b_empty0 = smem_addr(&bars[4]);   // [4..6]  ring slot consumed
-  const uint32_t b_sfull0 = smem_addr(&bars[7]);   // [7, 8]  S of tile A / B ready
-  const uint32_t b_pfull0 = smem_addr(&bars[9]);   // [9, 10] P of tile A / B written
-  const uint32_t b_pvdone0 = smem_addr(&bars[11]); // [11, 12] O += P V of A / B done
+  const uint32_t b_qfull = smem_addr(&bars[0]);
+  const uint32_t b_full0 = smem_addr(&bars[1]);     // [1..3]  ring slot filled
+  const uint32_t b_empty0 = smem_addr(&bars[4]);    // [4..6]  ring slot consumed
+  const uint32_t b_sfull0 = smem_addr(&bars[7]);    // [7, 8]  S of tile A / B ready
+  const uint32_t b_pfull0 = smem_addr(&bars[9]);    // [9, 10] P of tile A / B written
+  const uint32_t b_pvdone0 = smem_addr(&bars[11]);  // [11, 12] O += P V of A / B done
   const uint32_t b_drain = smem_addr(&bars[13]);
+  const uint32_t b_qempty = smem_addr(&bars[14]);   // the S products of an item have read Q
+  const uint32_t b_ofree0 = smem_addr(&bars[15]);   // [15, 16] O of A / B read by the epilogue
   auto slot_full = [&](int i) { return b_full0 + 8u * i; };
   auto slot_empty = [&](int i) { return b_empty0 + 8u * i; };
   auto slot_ptr = [&](int i) { return smem + kOffKV + i * kTileBytes; };
 
   if (tid == 0) {
-    mbar_init(b_q, 1);
+    mbar_init(b_qfull, 1);
+    mbar_init(b_qempty, 1);
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(slot_full(i), 1);
       mbar_init(slot_empty(i), 1);
@@ -357,6 +381,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(b_sfull0 + 8u * x, 1);
       mbar_init(b_pfull0 + 8u * x, 4);
       mbar_init(b_pvdone0 + 8u * x, 1);
+      mbar_init(b_ofree0 + 8u * x, 4);
     }
     mbar_init(b_drain, 1);
     fence_mbar_init();
@@ -375,59 +400,73 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512)
   auto tS = [&](int x) { return tmem + 128u * x; };
   auto tO = [&](int x) { return tmem + 256u + 128u * x; };
+  const long long n_items = p.n_items;
   bool ok = true;
 
   if (warp == kWarpTma) {
-    // ================= TMA producer: Q tiles, then K(0) V(0) K(1) V(1) ... =================
-    if (lane == 0) {
-      mbar_arrive_expect_tx(b_q, (nA > 0 ? 2 : 1) * kTileBytes);
-      for (int x = (nA > 0 ? 0 : 1); x < 2; ++x) {
-        const int z = (int)(q0 + (x == 0 ? qtA : qtB) * TQ);
-        for (int h = 0; h < 2; ++h)
-          tma_3d(smem_addr(sQ + x * kTileBytes + h * kHalf), &tq, h * 64, g * G, z, b_q);
-      }
-    }
+    // ================= TMA producer: per item Q, then K(0) V(0) K(1) V(1) ... =================
     const int box_bytes = p.bs * 128;
-    for (int li = 0; li < 2 * nB && ok; ++li) {
-      const int slot = li % kSlots, use = li / kSlots;
-      if (use > 0 && !mbar_wait_sleep(slot_empty(slot), (use - 1) & 1, p.err)) { ok = false; break; }
-      const int t = li >> 1, is_v = li & 1;
-      if (lane == 0) mbar_arrive_expect_tx(slot_full(slot), kTileBytes);
-      __syncwarp();
-      for (int i = lane; i < 2 * blocks_per_tile; i += 32) {
-        const int h = i / blocks_per_tile;
-        const int k = i % blocks_per_tile;
-        const long long lb = (long long)t * blocks_per_tile + k;  // logical block
-        long long coord = p.blk_coord_limit;                       // out of range: zeros
-        if (lb < spanned) {
-          const int blk = p.bt[(long long)b * p.mb + lb];
-          if (blk >= 0 && blk < p.num_blocks) {
-            coord = (long long)blk * p.L + p.layer;
-          } else {
-            set_error(p.err, kErrIndex);
-          }
+    long long ld = 0;  // K / V loads issued so far (ring position)
+    int jq = 0;        // items whose Q was loaded
+    for (long long i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      const Item it = make_item(p, i, tid);
+      if (!it.valid) continue;
+      // Q of this item once the previous item's S products have read the old one
+      if (jq > 0 && !mbar_wait_sleep(b_qempty, (jq - 1) & 1, p.err)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(b_qfull, (it.nA > 0 ? 2 : 1) * kTileBytes);
+        for (int x = (it.nA > 0 ? 0 : 1); x < 2; ++x) {
+          const int z = (int)(it.q0 + (x == 0 ? it.qtA : it.qtB) * TQ);
+          for (int h = 0; h < 2; ++h)
+            tma_3d(smem_addr(sQ + x * kTileBytes + h * kHalf), &tq, h * 64, it.g * G, z, b_qfull);
         }
-        tma_4d(smem_addr(slot_ptr(slot) + h * kHalf + k * box_bytes), is_v ? &tv : &tk, h * 64,
-               g, 0, (int)coord, slot_full(slot));
       }
-      __syncwarp();
+      ++jq;
+      for (int li = 0; li < 2 * it.nB && ok; ++li, ++ld) {
+        const int slot = (int)(ld % kSlots);
+        const long long use = ld / kSlots;
+        if (use > 0 && !mbar_wait_sleep(slot_empty(slot), (uint32_t)((use - 1) & 1), p.err)) {
+          ok = false;
+          break;
+        }
+        const int t = li >> 1, is_v = li & 1;
+        if (lane == 0) mbar_arrive_expect_tx(slot_full(slot), kTileBytes);
+        __syncwarp();
+        for (int k2 = lane; k2 < 2 * blocks_per_tile; k2 += 32) {
+          const int h = k2 / blocks_per_tile;
+          const int k = k2 % blocks_per_tile;
+          const long long lb = (long long)t * blocks_per_tile + k;  // logical block
+          long long coord = p.blk_coord_limit;                       // out of range: zeros
+          if (lb < it.spanned) {
+            const int blk = p.bt[(long long)it.b * p.mb + lb];
+            if (blk >= 0 && blk < p.num_blocks) {
+              coord = (long long)blk * p.L + p.layer;
+            } else {
+              set_error(p.err, kErrIndex);
+            }
+          }
+          tma_4d(smem_addr(slot_ptr(slot) + h * kHalf + k * box_bytes), is_v ? &tv : &tk, h * 64,
+                 it.g, 0, (int)coord, slot_full(slot));
+        }
+        __syncwarp();
+      }
     }
   } else if (warp == kWarpMma) {
     // ================= MMA issuer =================
-    // order: S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ...  so that
+    // per item: S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ..., so
     // each warpgroup's softmax overlaps the other tile's products
     if (lane == 0) {
       const uint32_t q_addr = smem_addr(sQ), p_addr = smem_addr(sP);
-      auto k_slot = [&](int t) { return (2 * t) % kSlots; };
-      auto v_slot = [&](int t) { return (2 * t + 1) % kSlots; };
-      auto k_ready = [&](int t) {
-        return mbar_wait_sleep(slot_full(k_slot(t)), ((2 * t) / kSlots) & 1, p.err);
+      long long ld = 0;            // K / V loads consumed so far
+      int jq = 0;                  // items started
+      long long nt[2] = {0, 0};    // tiles of A / B across items (barrier phases)
+      int ne[2] = {0, 0};          // epilogues of A / B across items
+      auto slot_of = [&](long long idx) { return (int)(idx % kSlots); };
+      auto ready = [&](long long idx) {
+        return mbar_wait_sleep(slot_full(slot_of(idx)), (uint32_t)((idx / kSlots) & 1), p.err);
       };
-      auto v_ready = [&](int t) {
-        return mbar_wait_sleep(slot_full(v_slot(t)), ((2 * t + 1) / kSlots) & 1, p.err);
-      };
-      auto issue_s = [&](int x, int t) {
-        const uint32_t k_addr = smem_addr(slot_ptr(k_slot(t)));
+      auto issue_s = [&](int x, long long k_idx) {
+        const uint32_t k_addr = smem_addr(slot_ptr(slot_of(k_idx)));
         const uint32_t qa = q_addr + x * kTileBytes;
         tc_fence_after();
         for (int k = 0; k < 8; ++k) {
@@ -437,96 +476,120 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         umma_commit(b_sfull0 + 8u * x);
       };
-      auto issue_pv = [&](int x, int t) {
-        const uint32_t v_addr = smem_addr(slot_ptr(v_slot(t)));
+      auto issue_pv = [&](int x, long long v_idx, bool first) {
+        const uint32_t v_addr = smem_addr(slot_ptr(slot_of(v_idx)));
         const uint32_t pa = p_addr + x * kTileBytes;
         tc_fence_after();
         for (int k = 0; k < 8; ++k) {
           const uint64_t a = desc_sw128(pa + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
           const uint64_t bd = desc_sw128(v_addr + k * 2048, kHalf, 1024);
-          umma(tO(x), a, bd, kIdescKMN, (t > 0 || k > 0) ? 1u : 0u);
+          umma(tO(x), a, bd, kIdescKMN, (!first || k > 0) ? 1u : 0u);
         }
         umma_commit(b_pvdone0 + 8u * x);
       };
-      ok = mbar_wait_sleep(b_q, 0, p.err) && k_ready(0);
-      if (ok) {
-        if (nA > 0) issue_s(0, 0);
-        issue_s(1, 0);
-        if (nB == 1 || nA <= 1) {
-          // K(0) is not needed again once both products are issued
-        }
-      }
-      for (int t = 0; t < nB && ok; ++t) {
-        const bool more = t + 1 < nB;
-        // K(t) is released after the last S product that reads it
-        umma_commit(slot_empty(k_slot(t)));
-        if (!v_ready(t)) { ok = false; break; }
-        if (t < nA) {
-          if (!mbar_wait_sleep(b_pfull0, t & 1, p.err)) { ok = false; break; }
-          issue_pv(0, t);
-          if (t + 1 < nA) {
-            if (!k_ready(t + 1)) { ok = false; break; }
-            issue_s(0, t + 1);
+      for (long long i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+        const Item it = make_item(p, i, tid);
+        if (!it.valid) continue;
+        const int nA = it.nA, nB = it.nB;
+        const long long base = ld;  // load index of K(0) of this item
+        if (!mbar_wait_sleep(b_qfull, jq & 1, p.err) || !ready(base)) { ok = false; break; }
+        ++jq;
+        if (nA > 0) issue_s(0, base);
+        issue_s(1, base);
+        // Q may be replaced once the last S product of the item completes: the
+        // next item's loads then overlap this item's last products and epilogue
+        if (nB == 1) umma_commit(b_qempty);
+        for (int t = 0; t < nB && ok; ++t) {
+          const long long ki = base + 2 * t, vi = ki + 1;
+          // K(t) is released after the S products that read it
+          umma_commit(slot_empty(slot_of(ki)));
+          if (!ready(vi)) { ok = false; break; }
+          if (t < nA) {
+            // O_A is overwritten by the first product: the previous epilogue
+            // must have read it
+            if (t == 0 && ne[0] > 0 && !mbar_wait_sleep(b_ofree0, (ne[0] - 1) & 1, p.err)) {
+              ok = false;
+              break;
+            }
+            if (!mbar_wait_sleep(b_pfull0, (uint32_t)(nt[0] & 1), p.err)) { ok = false; break; }
+            ++nt[0];
+            issue_pv(0, vi, t == 0);
+            if (t + 1 < nA) {
+              if (!ready(ki + 2)) { ok = false; break; }
+              issue_s(0, ki + 2);
+            }
+          }
+          if (t == 0 && ne[1] > 0 && !mbar_wait_sleep(b_ofree0 + 8u, (ne[1] - 1) & 1, p.err)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait_sleep(b_pfull0 + 8u, (uint32_t)(nt[1] & 1), p.err)) { ok = false; break; }
+          ++nt[1];
+          issue_pv(1, vi, t == 0);
+          umma_commit(slot_empty(slot_of(vi)));
+          if (t + 1 < nB) {
+            if (!(t + 1 < nA) && !ready(ki + 2)) { ok = false; break; }
+            issue_s(1, ki + 2);
+            if (t + 2 == nB) umma_commit(b_qempty);
           }
         }
-        if (!mbar_wait_sleep(b_pfull0 + 8u, t & 1, p.err)) { ok = false; break; }
-        issue_pv(1, t);
-        umma_commit(slot_empty(v_slot(t)));
-        if (more) {
-          if (!(t + 1 < nA) && !k_ready(t + 1)) { ok = false; break; }
-          issue_s(1, t + 1);
-        }
+        ld = base + 2 * nB;
+        if (nA > 0) ++ne[0];
+        ++ne[1];
       }
       umma_commit(b_drain);  // arrives once every MMA issued above has completed
     }
   } else {
     // ================= softmax: warpgroup x = 0 (tile A) or 1 (tile B), one row per thread ======
     const int x = warp >> 2;
-    const int nX = x == 0 ? nA : nB;
-    const long long qt = x == 0 ? qtA : qtB;
     const int r = tid & 127;                 // MMA row = TMEM lane
     const int qtok = r / G, hh = r - qtok * G;
-    const long long qi = qt * TQ + qtok;     // query index within the sequence
-    const bool row_ok = nX > 0 && qi < nq;
-    const long long pos = first_pos + qi;    // its logical position
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t b_sfull = b_sfull0 + 8u * x, b_pfull = b_pfull0 + 8u * x;
-    const uint32_t b_pvdone = b_pvdone0 + 8u * x;
+    const uint32_t b_pvdone = b_pvdone0 + 8u * x, b_ofree = b_ofree0 + 8u * x;
     unsigned char* sPx = sP + x * kTileBytes;
-    // first and last key tiles where some row of this warpgroup is masked
-    const long long tq_first = qt * TQ;
-    const int t_mask_lo = (int)((off + first_pos + tq_first) / kKeys);
-    const bool rows_full = (qt + 1) * TQ <= nq;
-    RowState st{-INFINITY, 0.f};
-    for (int t = 0; t < nX && ok; ++t) {
-      const bool waited = mbar_wait_sleep(b_sfull, t & 1, p.err);
-      if (!__all_sync(0xffffffffu, waited)) { ok = false; break; }
-      tc_fence_after();
-      const long long tp0 = (long long)t * kKeys;
-      const int c_lo = (int)max(0ll, (long long)off - tp0);
-      const int c_hi = row_ok ? (int)min((long long)kKeys - 1, pos + off - tp0) : -1;
+    long long nt = 0;  // tiles of this warpgroup across items (barrier phases)
+    for (long long i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      const Item it = make_item(p, i, tid);
+      if (!it.valid) continue;
+      const int nX = x == 0 ? it.nA : it.nB;
+      if (nX == 0) continue;
+      const long long qt = x == 0 ? it.qtA : it.qtB;
+      const long long qi = qt * TQ + qtok;   // query index within the sequence
+      const bool row_ok = qi < it.nq;
+      const long long pos = it.first_pos + qi;  // its logical position
       // tiles before the first diagonal tile are full for every row when the
       // tile has no padding rows (and t = 0 only without a first-block offset)
-      const bool full_tile = (t > 0 || off == 0) && t < t_mask_lo && rows_full;
-      if (!softmax_tile(tS(x), tO(x), lane_base, sPx, r, t, c_lo, c_hi, full_tile, p.qscale, st,
-                        b_pvdone, p.err)) {
-        ok = false;
-        break;
+      const int t_mask_lo = (int)((it.off + it.first_pos + qt * TQ) / kKeys);
+      const bool rows_full = (qt + 1) * TQ <= it.nq;
+      RowState st{-INFINITY, 0.f};
+      for (int t = 0; t < nX && ok; ++t, ++nt) {
+        const bool waited = mbar_wait_sleep(b_sfull, (uint32_t)(nt & 1), p.err);
+        if (!__all_sync(0xffffffffu, waited)) { ok = false; break; }
+        tc_fence_after();
+        const long long tp0 = (long long)t * kKeys;
+        const int c_lo = (int)max(0ll, (long long)it.off - tp0);
+        const int c_hi = row_ok ? (int)min((long long)kKeys - 1, pos + it.off - tp0) : -1;
+        const bool full_tile = (t > 0 || it.off == 0) && t < t_mask_lo && rows_full;
+        if (!softmax_tile(tS(x), tO(x), lane_base, sPx, r, t, c_lo, c_hi, full_tile, p.qscale,
+                          st, b_pvdone, (uint32_t)((nt - 1) & 1), p.err)) {
+          ok = false;
+          break;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_pfull);
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_pfull);
-    }
-    // epilogue: O row / l -> bf16 -> out
-    bool done = ok && nX > 0;
-    if (done) done = __all_sync(0xffffffffu, mbar_wait_sleep(b_pvdone, (nX - 1) & 1, p.err));
-    if (done) {
+      if (!ok) break;
+      // epilogue: O row / l -> bf16 -> out, then hand O back to the MMA warp
+      const bool waited = mbar_wait_sleep(b_pvdone, (uint32_t)((nt - 1) & 1), p.err);
+      if (!__all_sync(0xffffffffu, waited)) { ok = false; break; }
       tc_fence_after();
       const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
-                            ((q0 + qi) * p.hq + (long long)g * G + hh) * kD;
-#pragma unroll
+                            ((it.q0 + qi) * p.hq + (long long)it.g * G + hh) * kD;
+#pragma unroll 1
       for (int c0 = 0; c0 < kD; c0 += 32) {
         uint32_t v[32];
         tmem_ld32(tO(x) + lane_base + c0, v);
@@ -543,6 +606,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_ofree);
     }
   }
 
@@ -575,7 +641,7 @@ int prefill_supported(const PoolView& pv, int num_q_heads) {
 cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num_q_heads,
                            float scale, const int32_t* bt, int mb, const int32_t* lens,
                            const int32_t* offs, const int64_t* cu_q, int batch, long long total_q,
-                           int max_q_len, void* out, int* err, cudaStream_t s) {
+                           int max_q_len, void* out, int* err, int sm_count, cudaStream_t s) {
   if (batch == 0 || total_q == 0 || max_q_len == 0) return cudaSuccess;
   const int G = num_q_heads / pv.num_kv_heads;
   const int TQ = kRows / G;
@@ -633,9 +699,10 @@ cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num
     configured[dev] = 1;
   }
   const long long ntq = (max_q_len + TQ - 1) / TQ;
-  const dim3 grid((unsigned)((ntq + 1) / 2), (unsigned)batch, (unsigned)pv.num_kv_heads);
-  return launch_kernel(prefill_kernel, grid, dim3(kPfThreads), (size_t)kSmemBytes, s, true, tq, tk,
-                       tv, p);
+  p.n_items = (ntq + 1) / 2 * (long long)batch * pv.num_kv_heads;
+  const long long grid = p.n_items < sm_count ? p.n_items : sm_count;
+  return launch_kernel(prefill_kernel, dim3((unsigned)grid), dim3(kPfThreads), (size_t)kSmemBytes,
+                       s, true, tq, tk, tv, p);
 }
 
 }  // namespace pkv
