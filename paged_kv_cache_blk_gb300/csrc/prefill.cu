@@ -51,15 +51,14 @@ constexpr int kKeys = 128;   // keys per KV tile (MMA N of Q K^T, K of P V)
 constexpr int kD = 128;      // head_dim
 constexpr int kHalf = 128 * 64 * 2;  // one 128-row x 64-column bf16 half tile (16 KB)
 constexpr int kTileBytes = 2 * kHalf;  // 32 KB
-constexpr int kSlots = 3;              // K / V ring: K(t), V(t), K(t+1) in flight
+constexpr int kSlots = 5;              // K / V ring: K(t) V(t) .. two tiles ahead
 constexpr uint32_t kTmemCols = 512;    // S_A, S_B, O_A, O_B
 constexpr float kLog2e = 1.4426950408889634f;
 
 // shared-memory carve, from a 1024-aligned base
 constexpr int kOffQ = 0;                              // Q_A, Q_B
 constexpr int kOffKV = 2 * kTileBytes;                // ring of kSlots tiles
-constexpr int kOffP = kOffKV + kSlots * kTileBytes;   // P_A, P_B
-constexpr int kOffBar = kOffP + 2 * kTileBytes;
+constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;      // barriers + TMEM slot + alignment slack
 
 struct PfParams {
@@ -103,6 +102,17 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
       : "memory");
 }
 
+// The same with the A operand in TMEM (M rows = lanes; column c holds the
+// bf16 pair of k = 2c (low half) and 2c + 1; a K = 16 step spans 8 columns).
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -140,6 +150,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -167,9 +187,9 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 }
 
 __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t lane_base,
-                                             unsigned char* sP, int r, int t, int c_lo, int c_hi,
-                                             bool full_tile, float qs, RowState& st,
-                                             uint32_t b_pvdone, uint32_t pv_parity, int* err) {
+                                             int t, int c_lo, int c_hi, bool full_tile, float qs,
+                                             RowState& st, uint32_t b_pvdone, uint32_t pv_parity,
+                                             int* err) {
   // With a positive scale the maximum is taken on the raw scores and the scale
   // goes into the exponent's FMA; otherwise each score is scaled first.
   const bool pre = qs <= 0.f;
@@ -188,27 +208,20 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
       x[j] = f;
     }
   };
-  // P row (bf16) of one chunk against the maximum mu into the K-major
-  // 128B-swizzled P tile: 16-byte chunk ch of row r at (r/8)*1024 + (r%8)*128
-  // + ((ch ^ (r%8)) * 16), per 64-column half; returns the chunk's sum
+  // P (bf16 pairs) of one chunk against the maximum mu, into TMEM columns
+  // c0/2 .. c0/2 + 15 of the S region, the A operand of O += P V.  Those
+  // columns hold S values of this chunk or of earlier ones, all read before.
   auto write_p = [&](int c0, const float (&x)[32], float mu) {
     float psum = 0.f;
+    uint32_t w[16];
 #pragma unroll
-    for (int c = 0; c < 32; c += 8) {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float a0 = exp2f(fmaf(x[c + 2 * e], qe, -mu));
-        const float a1 = exp2f(fmaf(x[c + 2 * e + 1], qe, -mu));
-        psum += a0 + a1;
-        w[e] = pack_bf16x2(a0, a1);
-      }
-      const int col = c0 + c;
-      const int half = col >> 6, chunk = (col & 63) >> 3;
-      unsigned char* dst =
-          sP + half * kHalf + (r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4);
-      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int e = 0; e < 16; ++e) {
+      const float a0 = exp2f(fmaf(x[2 * e], qe, -mu));
+      const float a1 = exp2f(fmaf(x[2 * e + 1], qe, -mu));
+      psum += a0 + a1;
+      w[e] = pack_bf16x2(a0, a1);
     }
+    tmem_st16(tS + lane_base + (c0 >> 1), w);
     return psum;
   };
   auto chunk_max = [&](const float (&x)[32], float m) {
@@ -218,8 +231,8 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
   };
   // Every tcgen05.ld / st below is a warp-wide instruction, so all control
   // flow around them is warp-uniform: per-row decisions only select data.
-  // O must hold P(t-1) V(t-1) before P is rewritten or O rescaled (by the
-  // time S(t) is ready that product has normally finished).
+  // O must hold P(t-1) V(t-1) before O is rescaled (by the time S(t) is
+  // ready that product has normally finished).
   if (t > 0) {
     const bool waited = mbar_wait_sleep(b_pvdone, pv_parity, err);
     if (!__all_sync(0xffffffffu, waited)) return false;
@@ -227,10 +240,9 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
   }
   float psum = 0.f, alpha = 1.f;
   const bool first = st.m_used == -INFINITY;  // this row has no maximum yet
-  const bool any_first = __any_sync(0xffffffffu, first);
-  float mt = -INFINITY;
-  if (!any_first) {
+  if (!__any_sync(0xffffffffu, first)) {
     // one pass against the current maximum, tracking this tile's maximum
+    float mt = -INFINITY;
 #pragma unroll 1
     for (int c0 = 0; c0 < kKeys; c0 += 32) {
       float x[32];
@@ -238,33 +250,50 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
       mt = chunk_max(x, mt);
       psum += write_p(c0, x, st.m_used);
     }
+    const float mt_s = mt * qe;
+    float beta = 1.f;  // correction of the P just written
+    if (mt_s > st.m_used + 8.f) {
+      // P would exceed 2^8 against the old maximum: move it, and scale the
+      // P already written (bf16, in place) and its sum to the new maximum
+      beta = exp2f(st.m_used - mt_s);
+      alpha = beta;
+      st.m_used = mt_s;
+      psum *= beta;
+    }
+    if (__any_sync(0xffffffffu, beta != 1.f)) {
+      tmem_wait_st();  // the P just stored, before it is read back
+#pragma unroll 1
+      for (int c0 = 0; c0 < kKeys / 2; c0 += 32) {  // the 64 P columns
+        uint32_t v[32];
+        tmem_ld32(tS + lane_base + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = pack_bf16x2(bf16_lo(v[j]) * beta, bf16_hi(v[j]) * beta);
+        tmem_st32(tS + lane_base + c0, v);
+      }
+    }
   } else {
-    // some row still needs its first maximum: find the maxima first
+    // some row still needs its first maximum: find the maxima first, then P
+    float mt = -INFINITY;
 #pragma unroll 1
     for (int c0 = 0; c0 < kKeys; c0 += 32) {
       float x[32];
       load_chunk(c0, x);
       mt = chunk_max(x, mt);
     }
-  }
-  const float mt_s = mt * qe;
-  bool rewrite = any_first;  // P not written yet in this warp
-  if (first) {
-    // a real row finds its first keys in tile 0 (nothing accumulated yet); a
-    // padding row (all keys masked) keeps P = 0 and is never written out
-    if (mt_s != -INFINITY) {
+    const float mt_s = mt * qe;
+    if (first) {
+      // a real row finds its first keys in tile 0 (nothing accumulated yet); a
+      // padding row (all keys masked) keeps P = 0 and is never written out
+      if (mt_s != -INFINITY) {
+        st.m_used = mt_s;
+        alpha = 0.f;
+      }
+    } else if (mt_s > st.m_used + 8.f) {
+      alpha = exp2f(st.m_used - mt_s);
       st.m_used = mt_s;
-      alpha = 0.f;
     }
-  } else if (mt_s > st.m_used + 8.f) {
-    // P would exceed 2^8 against the old maximum: move it and write P again
-    alpha = exp2f(st.m_used - mt_s);
-    st.m_used = mt_s;
-    rewrite = true;
-  }
-  if (__any_sync(0xffffffffu, rewrite)) {
     const float mu = st.m_used == -INFINITY ? 0.f : st.m_used;
-    psum = 0.f;
 #pragma unroll 1
     for (int c0 = 0; c0 < kKeys; c0 += 32) {
       float x[32];
@@ -284,6 +313,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
     }
     tmem_wait_st();
   }
+  tmem_wait_st();
   st.l = st.l * alpha + psum;
   return true;
 }
@@ -354,18 +384,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   // ---- shared memory, barriers, TMEM --------------------------------------------------
   unsigned char* sQ = smem + kOffQ;  // [A | B]
-  unsigned char* sP = smem + kOffP;  // [A | B]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffBar + 192);
+  // barriers: Q full, ring full[kSlots], ring empty[kSlots], then per tile
+  // A / B: S ready, P written, O += P V done, O read by the epilogue
+  static_assert((2 * kSlots + 12) * 8 <= 192, "barriers overlap the TMEM address slot");
   const uint32_t b_qfull = smem_addr(&bars[0]);
-  const uint32_t b_full0 = smem_addr(&bars[1]);     // [1..3]  ring slot filled
-  const uint32_t b_empty0 = smem_addr(&bars[4]);    // [4..6]  ring slot consumed
-  const uint32_t b_sfull0 = smem_addr(&bars[7]);    // [7, 8]  S of tile A / B ready
-  const uint32_t b_pfull0 = smem_addr(&bars[9]);    // [9, 10] P of tile A / B written
-  const uint32_t b_pvdone0 = smem_addr(&bars[11]);  // [11, 12] O += P V of A / B done
-  const uint32_t b_drain = smem_addr(&bars[13]);
-  const uint32_t b_qempty = smem_addr(&bars[14]);   // the S products of an item have read Q
-  const uint32_t b_ofree0 = smem_addr(&bars[15]);   // [15, 16] O of A / B read by the epilogue
+  const uint32_t b_full0 = smem_addr(&bars[1]);                // ring slot filled
+  const uint32_t b_empty0 = smem_addr(&bars[1 + kSlots]);      // ring slot consumed
+  const uint32_t b_sfull0 = smem_addr(&bars[1 + 2 * kSlots]);  // S of tile A / B ready
+  const uint32_t b_pfull0 = smem_addr(&bars[3 + 2 * kSlots]);  // P of tile A / B written
+  const uint32_t b_pvdone0 = smem_addr(&bars[5 + 2 * kSlots]); // O += P V of A / B done
+  const uint32_t b_ofree0 = smem_addr(&bars[7 + 2 * kSlots]);  // O of A / B read by the epilogue
+  const uint32_t b_drain = smem_addr(&bars[9 + 2 * kSlots]);
+  const uint32_t b_qempty = smem_addr(&bars[10 + 2 * kSlots]);  // an item's S products read Q
   auto slot_full = [&](int i) { return b_full0 + 8u * i; };
   auto slot_empty = [&](int i) { return b_empty0 + 8u * i; };
   auto slot_ptr = [&](int i) { return smem + kOffKV + i * kTileBytes; };
@@ -456,7 +488,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // per item: S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ..., so
     // each warpgroup's softmax overlaps the other tile's products
     if (lane == 0) {
-      const uint32_t q_addr = smem_addr(sQ), p_addr = smem_addr(sP);
+      const uint32_t q_addr = smem_addr(sQ);
       long long ld = 0;            // K / V loads consumed so far
       int jq = 0;                  // items started
       long long nt[2] = {0, 0};    // tiles of A / B across items (barrier phases)
@@ -478,12 +510,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       };
       auto issue_pv = [&](int x, long long v_idx, bool first) {
         const uint32_t v_addr = smem_addr(slot_ptr(slot_of(v_idx)));
-        const uint32_t pa = p_addr + x * kTileBytes;
         tc_fence_after();
         for (int k = 0; k < 8; ++k) {
-          const uint64_t a = desc_sw128(pa + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
+          // A = P from TMEM (S columns of tile x), B = V MN-major
           const uint64_t bd = desc_sw128(v_addr + k * 2048, kHalf, 1024);
-          umma(tO(x), a, bd, kIdescKMN, (!first || k > 0) ? 1u : 0u);
+          umma_ts(tO(x), tS(x) + 8u * k, bd, kIdescKMN, (!first || k > 0) ? 1u : 0u);
         }
         umma_commit(b_pvdone0 + 8u * x);
       };
@@ -547,7 +578,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t b_sfull = b_sfull0 + 8u * x, b_pfull = b_pfull0 + 8u * x;
     const uint32_t b_pvdone = b_pvdone0 + 8u * x, b_ofree = b_ofree0 + 8u * x;
-    unsigned char* sPx = sP + x * kTileBytes;
     long long nt = 0;  // tiles of this warpgroup across items (barrier phases)
     for (long long i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       const Item it = make_item(p, i, tid);
@@ -571,12 +601,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int c_lo = (int)max(0ll, (long long)it.off - tp0);
         const int c_hi = row_ok ? (int)min((long long)kKeys - 1, pos + it.off - tp0) : -1;
         const bool full_tile = (t > 0 || it.off == 0) && t < t_mask_lo && rows_full;
-        if (!softmax_tile(tS(x), tO(x), lane_base, sPx, r, t, c_lo, c_hi, full_tile, p.qscale,
-                          st, b_pvdone, (uint32_t)((nt - 1) & 1), p.err)) {
+        if (!softmax_tile(tS(x), tO(x), lane_base, t, c_lo, c_hi, full_tile, p.qscale, st,
+                          b_pvdone, (uint32_t)((nt - 1) & 1), p.err)) {
           ok = false;
           break;
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_pfull);
