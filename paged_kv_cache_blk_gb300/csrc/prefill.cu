@@ -243,12 +243,27 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
   if (!__any_sync(0xffffffffu, first)) {
     // one pass against the current maximum, tracking this tile's maximum
     float mt = -INFINITY;
+    if (full_tile && !pre) {
+      // the common case, kept free of masking and scaling code
 #pragma unroll 1
-    for (int c0 = 0; c0 < kKeys; c0 += 32) {
-      float x[32];
-      load_chunk(c0, x);
-      mt = chunk_max(x, mt);
-      psum += write_p(c0, x, st.m_used);
+      for (int c0 = 0; c0 < kKeys; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tS + lane_base + c0, v);
+        tmem_wait_ld();
+        float x[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
+        mt = chunk_max(x, mt);
+        psum += write_p(c0, x, st.m_used);
+      }
+    } else {
+#pragma unroll 1
+      for (int c0 = 0; c0 < kKeys; c0 += 32) {
+        float x[32];
+        load_chunk(c0, x);
+        mt = chunk_max(x, mt);
+        psum += write_p(c0, x, st.m_used);
+      }
     }
     const float mt_s = mt * qe;
     float beta = 1.f;  // correction of the P just written
