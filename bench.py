@@ -267,12 +267,14 @@ class DecodeStep:
             self.host[name] = getattr(self, name).cpu().pin_memory()
         self.host_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
         self.bytes = decode_bytes(b, spec.row_bytes, hq, D, 2, spec.block_size)
-        self.launches_per_step = 4  # slot mapping, scatter, decode partial, combine
+        self.launches_per_step = 3  # slot mapping + scatter (one kernel), decode partial, combine
 
     def step(self):
         pkv = self.pkv
-        pkv.build_slot_mapping(self.pool, self.bt, self.offs, self.seq, self.pos, self.slots)
-        pkv.write_slots(self.pool, self.w.layer, self.k_new, self.v_new, self.slots)
+        # slot mapping and scatter of the new tokens in one kernel (the slots
+        # are also written out), then decode attention
+        pkv.append_tokens(self.pool, self.w.layer, self.bt, self.offs, self.seq, self.pos,
+                          self.k_new, self.v_new, self.slots)
         pkv.decode_attention(self.pool, self.w.layer, self.q, self.w.scale, self.bt, self.lens,
                              self.offs, self.out, self.ws)
 
@@ -332,19 +334,18 @@ def timed(fn, steps: int, flush, events_hook=None):
 def step_breakdown(st: "DecodeStep", flush: torch.Tensor, steps: int) -> dict:
     """Eager per-call device times of the step (events between the calls)."""
     pkv = st.pkv
-    names = ("slot_mapping", "scatter", "decode_attention")
+    names = ("append_tokens", "decode_attention")
     acc = {n: 0.0 for n in names}
     for _ in range(steps):
         flush.zero_()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         ev[0].record()
-        pkv.build_slot_mapping(st.pool, st.bt, st.offs, st.seq, st.pos, st.slots)
+        pkv.append_tokens(st.pool, st.w.layer, st.bt, st.offs, st.seq, st.pos, st.k_new,
+                          st.v_new, st.slots)
         ev[1].record()
-        pkv.write_slots(st.pool, st.w.layer, st.k_new, st.v_new, st.slots)
-        ev[2].record()
         pkv.decode_attention(st.pool, st.w.layer, st.q, st.w.scale, st.bt, st.lens, st.offs,
                              st.out, st.ws)
-        ev[3].record()
+        ev[2].record()
         torch.cuda.synchronize()
         for i, n in enumerate(names):
             acc[n] += ev[i].elapsed_time(ev[i + 1])
@@ -455,7 +456,8 @@ def run_ours(args, rank, local_rank, world):
         "config": {
             "workload": "decode_gqa: pool 16384x32x16x8x128 bf16 (layer 7), Hq 32 (GQA 4), "
                         "batch 64, seq_len U[1024,8192], random non-contiguous tables; step = "
-                        "slot mapping + scatter of 64 new tokens + paged decode attention",
+                        "slot mapping + scatter of 64 new tokens (one fused kernel) + paged "
+                        "decode attention",
             "batch": int(w.batch.batch),
             "kv_read_bytes_per_step": kv,
             "l2": "flushed between steps outside the events (512 MiB write, then a 512 MiB read "
@@ -537,7 +539,8 @@ def int8_leg(args, dev, rank, flush, pkv) -> dict:
     db = st.bytes
     out = {
         "what": "decode_gqa step over an int8 pool 16384x32x16x(8x128 codes + 8 fp32 scales) "
-                "(1056-byte token rows): slot mapping + quantising scatter of 64 tokens + "
+                "(1056-byte token rows): slot mapping + quantising scatter of 64 tokens (one "
+                "fused kernel) + "
                 "paged decode attention (bf16 q / out)",
         "ms_per_step": round(ms, 4),
         "step_mode": "cuda_graph" if graph_ms is not None else "eager",

@@ -144,6 +144,23 @@ PKV_API pkv_status pkv_write_slots(const pkv_pool* pool, int32_t layer, const vo
                            const void* v_new, const int64_t* slot_mapping,
                            int64_t num_tokens, cudaStream_t stream);
 
+/* Slot mapping and scatter in one call: the new rows of a decode step (or a
+ * prompt) go straight from (sequence, position) pairs into their slots.  The
+ * result is that of pkv_build_slot_mapping followed by pkv_write_slots with
+ * its output, in one kernel: for each token t, the slot is computed as in
+ * pkv_build_slot_mapping (padding and out-of-range tokens get -1 and are not
+ * written; out-of-range ones set the device error word, PKV_ERR_INDEX /
+ * PKV_ERR_CAPACITY in validate mode) and row t of k_new / v_new is written
+ * there as in pkv_write_slots (quantised for PKV_I8 pools).  slot_mapping
+ * (int64 [num_tokens], device) receives the slots when not NULL.  Arguments
+ * and their rules are those of the two calls. */
+PKV_API pkv_status pkv_append_tokens(const pkv_pool* pool, int32_t layer,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t* offsets, int32_t batch,
+                                     const int32_t* token_seq, const int32_t* token_pos,
+                                     int64_t num_tokens, const void* k_new, const void* v_new,
+                                     int64_t* slot_mapping, cudaStream_t stream);
+
 /* Gather ([step14_2] "Problem" and "Solution"; [vllm-notes] §2.3
  * gather_kv_for_attention; [ch12] §2.2 offset, §2.5 read_layer).
  *

@@ -6,6 +6,7 @@ binding."""
 
 from ._binding import (  # noqa: F401
     Allocator,
+    append_tokens,
     Pool,
     PkvError,
     STATUS_CODES,

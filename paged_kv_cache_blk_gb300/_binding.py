@@ -53,6 +53,7 @@ _P, _I32, _I64, _F32, _SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ct
 _SIGS = {
     "pkv_build_slot_mapping": (_I32, [_P, _P, _I32, _P, _I32, _P, _P, _I64, _P, _P]),
     "pkv_write_slots": (_I32, [_P, _I32, _P, _P, _P, _I64, _P]),
+    "pkv_append_tokens": (_I32, [_P, _I32, _P, _I32, _P, _I32, _P, _P, _I64, _P, _P, _P, _P]),
     "pkv_gather": (_I32, [_P, _I32, _P, _I32, _P, _P, _I32, _P, _I64, _P, _P, _P]),
     "pkv_decode_workspace_size": (_SZ, [_I32, _I32, _I32]),
     "pkv_decode_attention": (_I32, [_P, _I32, _P, _I32, _F32, _P, _I32, _P, _P, _I32, _P, _P,
@@ -213,6 +214,22 @@ def write_slots(pool: Pool, layer: int, k_new: torch.Tensor, v_new: torch.Tensor
         st = lib.pkv_write_slots(pool.ref, layer, _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
                                  slot_mapping.numel(), _stream(pool.device))
     _check(st, "pkv_write_slots")
+
+
+def append_tokens(pool: Pool, layer: int, block_tables: torch.Tensor,
+                  offsets: Optional[torch.Tensor], token_seq: torch.Tensor,
+                  token_pos: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                  slot_mapping: Optional[torch.Tensor] = None) -> None:
+    """Slot mapping and scatter in one call: rows of ``k_new``/``v_new``
+    ([T, Hkv, D]) go to the slots of (token_seq, token_pos); the slots are
+    also written to ``slot_mapping`` (int64 [T]) when given."""
+    lib = load()
+    with _dev(pool):
+        st = lib.pkv_append_tokens(pool.ref, layer, _ptr(block_tables), block_tables.shape[1],
+                                   _ptr(offsets), block_tables.shape[0], _ptr(token_seq),
+                                   _ptr(token_pos), token_seq.numel(), _ptr(k_new), _ptr(v_new),
+                                   _ptr(slot_mapping), _stream(pool.device))
+    _check(st, "pkv_append_tokens")
 
 
 def gather(pool: Pool, layer: int, block_tables: torch.Tensor, seq_lens: torch.Tensor,

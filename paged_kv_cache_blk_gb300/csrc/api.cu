@@ -240,6 +240,42 @@ pkv_status pkv_write_slots(const pkv_pool* pool, int32_t layer, const void* k_ne
   return validate ? read_and_clear(d->err, stream) : PKV_OK;
 }
 
+pkv_status pkv_append_tokens(const pkv_pool* pool, int32_t layer, const int32_t* block_tables,
+                             int32_t max_blocks_per_seq, const int32_t* offsets, int32_t batch,
+                             const int32_t* token_seq, const int32_t* token_pos,
+                             int64_t num_tokens, const void* k_new, const void* v_new,
+                             int64_t* slot_mapping, cudaStream_t stream) {
+  pkv::PoolView v;
+  pkv_status st = check_pool(pool, true, &v);
+  if (st != PKV_OK) return st;
+  if (layer < 0 || layer >= pool->num_layers || num_tokens < 0 || batch < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (v.quant && v.head_dim != 32 && v.head_dim != 64 && v.head_dim != 128 && v.head_dim != 256)
+    return PKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!token_seq || !token_pos || !k_new || !v_new) return PKV_ERR_INVALID_ARG;
+  if (!aligned(token_seq, 4) || !aligned(token_pos, 4) || !aligned16(k_new) || !aligned16(v_new))
+    return PKV_ERR_INVALID_ARG;
+  if (slot_mapping && !aligned(slot_mapping, 8)) return PKV_ERR_INVALID_ARG;
+  if (batch > 0 && (!block_tables || max_blocks_per_seq <= 0)) return PKV_ERR_INVALID_ARG;
+  DevInfo* d;
+  if ((st = current_device(&d)) != PKV_OK) return st;
+  const bool validate = g_validate.load() != 0;
+  if (validate) {
+    if ((st = clear_word(d->err, stream)) != PKV_OK) return st;
+    if ((st = launched(pkv::launch_validate_tokens(v, block_tables, max_blocks_per_seq, offsets,
+                                                   batch, token_seq, token_pos, num_tokens,
+                                                   d->err, stream))) != PKV_OK)
+      return st;
+    if ((st = read_and_clear(d->err, stream)) != PKV_OK) return st;
+  }
+  if ((st = launched(pkv::launch_append(v, layer, block_tables, max_blocks_per_seq, offsets,
+                                        batch, token_seq, token_pos, num_tokens, k_new, v_new,
+                                        slot_mapping, d->err, stream))) != PKV_OK)
+    return st;
+  return validate ? read_and_clear(d->err, stream) : PKV_OK;
+}
+
 pkv_status pkv_gather(const pkv_pool* pool, int32_t layer, const int32_t* block_tables,
                       int32_t max_blocks_per_seq, const int32_t* seq_lens,
                       const int32_t* offsets, int32_t batch, const int64_t* cu_seqlens,

@@ -213,6 +213,12 @@ cudaError_t launch_write_slots(const PoolView& p, int layer, const void* k_new, 
                                const int64_t* slots, long long n, int* err, int sm_count,
                                cudaStream_t s);
 
+// Slot mapping and scatter in one kernel (pkv_append_tokens); slots_out may be null.
+cudaError_t launch_append(const PoolView& p, int layer, const int32_t* bt, int mb,
+                          const int32_t* offs, int batch, const int32_t* tok_seq,
+                          const int32_t* tok_pos, long long n, const void* k_new,
+                          const void* v_new, int64_t* slots_out, int* err, cudaStream_t s);
+
 cudaError_t launch_gather(const PoolView& p, int layer, const int32_t* bt, int mb,
                           const int32_t* offs, int batch, const int64_t* cu, long long total,
                           void* k_out, void* v_out, int* err, cudaStream_t s);

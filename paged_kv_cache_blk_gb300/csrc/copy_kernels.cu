@@ -58,52 +58,86 @@ __device__ __forceinline__ long long row_offset(long long blk, int layer, int j,
 // ---------------------------------------------------------------------------
 // slot mapping: one thread per token
 // ---------------------------------------------------------------------------
-__global__ void slot_mapping_kernel(const int32_t* __restrict__ bt, int mb,
-                                    const int32_t* __restrict__ offs, int batch,
-                                    const int32_t* __restrict__ tok_seq,
-                                    const int32_t* __restrict__ tok_pos, long long n,
-                                    long long num_blocks, int bs, int64_t* __restrict__ slots,
+// Where the slots of a scatter come from: read from slot_mapping, or (the
+// fused append) computed from (sequence, position) pairs through the tables.
+struct SlotSrc {
+  const int64_t* slots;  // read when not fused
+  const int32_t* bt;
+  const int32_t* offs;
+  const int32_t* tok_seq;
+  const int32_t* tok_pos;
+  int64_t* slots_out;  // fused: also written here when not null
+  int mb, batch;
+};
+
+// Slot of token t from its (sequence, position): -1 for padding (negative
+// sequence) and for anything out of range (recorded in the error word when
+// `report`).
+__device__ __forceinline__ int64_t token_slot(const SlotSrc& ss, long long t, long long num_blocks,
+                                              int bs, int* err, bool report) {
+  const int b = ss.tok_seq[t];
+  if (b < 0) return -1;
+  if (b >= ss.batch) {
+    if (report) set_error(err, kErrIndex);
+    return -1;
+  }
+  const int off = ss.offs ? ss.offs[b] : 0;
+  const long long p = (long long)off + ss.tok_pos[t];
+  if (off < 0 || off >= bs || ss.tok_pos[t] < 0 || p >= (long long)ss.mb * bs) {
+    if (report) set_error(err, kErrCapacity);
+    return -1;
+  }
+  const int blk = ss.bt[(long long)b * ss.mb + p / bs];
+  if (blk < 0 || blk >= num_blocks) {
+    if (report) set_error(err, kErrIndex);
+    return -1;
+  }
+  return (int64_t)blk * bs + p % bs;
+}
+
+__global__ void slot_mapping_kernel(const SlotSrc ss, long long n, long long num_blocks, int bs,
                                     int* err) {
   griddep_wait();
   griddep_launch_dependents();
   for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < n;
-       t += (long long)gridDim.x * blockDim.x) {
-    const int b = tok_seq[t];
-    int64_t slot = -1;
-    if (b >= batch) {
-      set_error(err, kErrIndex);
-    } else if (b >= 0) {
-      const int off = offs ? offs[b] : 0;
-      const long long p = (long long)off + tok_pos[t];
-      if (off < 0 || off >= bs || tok_pos[t] < 0 || p >= (long long)mb * bs) {
-        set_error(err, kErrCapacity);
-      } else {
-        const int blk = bt[(long long)b * mb + p / bs];
-        if (blk < 0 || blk >= num_blocks) {
-          set_error(err, kErrIndex);
-        } else {
-          slot = (int64_t)blk * bs + p % bs;
-        }
-      }
+       t += (long long)gridDim.x * blockDim.x)
+    ss.slots_out[t] = token_slot(ss, t, num_blocks, bs, err, true);
+}
+
+// The slot of token t for a scatter: read, or computed (fused append) by
+// lane 0 and broadcast to the warp; the warp that `reports` also writes the
+// slot out and records errors.
+template <bool FUSED>
+__device__ __forceinline__ int64_t scatter_slot(const SlotSrc& ss, long long t,
+                                                long long num_blocks, int bs, int* err,
+                                                bool report, int lane) {
+  if constexpr (!FUSED) {
+    return ss.slots[t];
+  } else {
+    int64_t s = 0;
+    if (lane == 0) {
+      s = token_slot(ss, t, num_blocks, bs, err, report);
+      if (report && ss.slots_out) ss.slots_out[t] = s;
     }
-    slots[t] = slot;
+    return __shfl_sync(0xffffffffu, s, 0);
   }
 }
 
 // ---------------------------------------------------------------------------
 // scatter: one warp per token (K row + V row)
 // ---------------------------------------------------------------------------
+template <bool FUSED>
 __global__ void __launch_bounds__(kCopyThreads) write_slots_kernel(
     char* __restrict__ kc, char* __restrict__ vc, const char* __restrict__ k_new,
-    const char* __restrict__ v_new, const int64_t* __restrict__ slots, long long n,
-    long long num_blocks, int L, int layer, int bs, int row_bytes, int* err) {
+    const char* __restrict__ v_new, const SlotSrc ss, long long n, long long num_blocks, int L,
+    int layer, int bs, int row_bytes, int* err) {
   griddep_wait();
   griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long warps = (long long)gridDim.x * kCopyWarps;
   const int row_vecs = row_bytes >> 4;
   for (long long t = blockIdx.x * (long long)kCopyWarps + (threadIdx.x >> 5); t < n; t += warps) {
-    const int64_t s = slots[t];
+    const int64_t s = scatter_slot<FUSED>(ss, t, num_blocks, bs, err, true, lane);
     if (s < 0) {
       if (s != -1 && lane == 0) set_error(err, kErrIndex);
       continue;  // -1 is padding: that row is not written
@@ -180,12 +214,11 @@ __device__ __forceinline__ void store_codes(char* dst, const int (&c)[VPL]) {
   }
 }
 
-template <int VPL>
+template <int VPL, bool FUSED>
 __global__ void __launch_bounds__(kCopyThreads) quant_write_slots_kernel(
     char* __restrict__ kc, char* __restrict__ vc, const __nv_bfloat16* __restrict__ k_new,
-    const __nv_bfloat16* __restrict__ v_new, const int64_t* __restrict__ slots, long long n,
-    long long num_blocks, int L, int layer, int bs, int row_bytes, int hkv, int scale_off,
-    int* err) {
+    const __nv_bfloat16* __restrict__ v_new, const SlotSrc ss, long long n, long long num_blocks,
+    int L, int layer, int bs, int row_bytes, int hkv, int scale_off, int* err) {
   griddep_wait();
   griddep_launch_dependents();
   constexpr int D = 32 * VPL;
@@ -196,7 +229,7 @@ __global__ void __launch_bounds__(kCopyThreads) quant_write_slots_kernel(
        w += warps) {
     const long long t = w / hkv;
     const int g = (int)(w - t * hkv);
-    const int64_t s = slots[t];
+    const int64_t s = scatter_slot<FUSED>(ss, t, num_blocks, bs, err, g == 0, lane);
     if (s < 0) {
       if (s != -1 && lane == 0 && g == 0) set_error(err, kErrIndex);
       continue;  // -1 is padding: that row is not written
@@ -345,24 +378,26 @@ cudaError_t launch_slot_mapping(const PoolView& p, const int32_t* bt, int mb, co
                                 int batch, const int32_t* tok_seq, const int32_t* tok_pos,
                                 long long n, int64_t* slots, int* err, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
+  SlotSrc ss{nullptr, bt, offs, tok_seq, tok_pos, slots, mb, batch};
   return launch_kernel(slot_mapping_kernel, dim3(grid_for(n, 256, 1 << 20)), dim3(256), 0, s, true,
-                       bt, mb, offs, batch, tok_seq, tok_pos, n, p.num_blocks, p.block_size, slots,
-                       err);
+                       ss, n, p.num_blocks, p.block_size, err);
 }
 
-cudaError_t launch_write_slots(const PoolView& p, int layer, const void* k_new, const void* v_new,
-                               const int64_t* slots, long long n, int* err, int sm_count,
-                               cudaStream_t s) {
+namespace {
+
+// The scatter, with slots read (FUSED false) or computed from the tokens.
+template <bool FUSED>
+cudaError_t launch_scatter(const PoolView& p, int layer, const void* k_new, const void* v_new,
+                           const SlotSrc& ss, long long n, int* err, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  (void)sm_count;
   if (p.quant) {
     const dim3 grid(grid_for(n * p.num_kv_heads, kCopyWarps, 1 << 24));
     const auto* kn = static_cast<const __nv_bfloat16*>(k_new);
     const auto* vn = static_cast<const __nv_bfloat16*>(v_new);
 #define PKV_QUANT_LAUNCH(VPL)                                                                  \
-  launch_kernel(quant_write_slots_kernel<VPL>, grid, dim3(kCopyThreads), 0, s, true, p.k_mut,  \
-                p.v_mut, kn, vn, slots, n, p.num_blocks, p.num_layers, layer, p.block_size,    \
-                p.row_bytes, p.num_kv_heads, p.scale_off, err)
+  launch_kernel(quant_write_slots_kernel<VPL, FUSED>, grid, dim3(kCopyThreads), 0, s, true,    \
+                p.k_mut, p.v_mut, kn, vn, ss, n, p.num_blocks, p.num_layers, layer,            \
+                p.block_size, p.row_bytes, p.num_kv_heads, p.scale_off, err)
     switch (p.head_dim) {
       case 32: return PKV_QUANT_LAUNCH(1);
       case 64: return PKV_QUANT_LAUNCH(2);
@@ -372,10 +407,28 @@ cudaError_t launch_write_slots(const PoolView& p, int layer, const void* k_new, 
 #undef PKV_QUANT_LAUNCH
     return cudaErrorInvalidValue;
   }
-  return launch_kernel(write_slots_kernel, dim3(grid_for(n, kCopyWarps, 1 << 24)),
+  return launch_kernel(write_slots_kernel<FUSED>, dim3(grid_for(n, kCopyWarps, 1 << 24)),
                        dim3(kCopyThreads), 0, s, true, p.k_mut, p.v_mut,
-                       static_cast<const char*>(k_new), static_cast<const char*>(v_new), slots, n,
+                       static_cast<const char*>(k_new), static_cast<const char*>(v_new), ss, n,
                        p.num_blocks, p.num_layers, layer, p.block_size, p.row_bytes, err);
+}
+
+}  // namespace
+
+cudaError_t launch_write_slots(const PoolView& p, int layer, const void* k_new, const void* v_new,
+                               const int64_t* slots, long long n, int* err, int sm_count,
+                               cudaStream_t s) {
+  (void)sm_count;
+  SlotSrc ss{slots, nullptr, nullptr, nullptr, nullptr, nullptr, 0, 0};
+  return launch_scatter<false>(p, layer, k_new, v_new, ss, n, err, s);
+}
+
+cudaError_t launch_append(const PoolView& p, int layer, const int32_t* bt, int mb,
+                          const int32_t* offs, int batch, const int32_t* tok_seq,
+                          const int32_t* tok_pos, long long n, const void* k_new,
+                          const void* v_new, int64_t* slots_out, int* err, cudaStream_t s) {
+  SlotSrc ss{nullptr, bt, offs, tok_seq, tok_pos, slots_out, mb, batch};
+  return launch_scatter<true>(p, layer, k_new, v_new, ss, n, err, s);
 }
 
 cudaError_t launch_gather(const PoolView& p, int layer, const int32_t* bt, int mb,

@@ -122,6 +122,20 @@ def test_host_checks_decode(lib):
     assert lib.pkv_decode_attention(p, *nan) == S["PKV_ERR_INVALID_ARG"]
 
 
+def test_host_checks_append(lib):
+    p = ctypes.byref(_pool())
+    args = lambda **kw: [kw.get("layer", 0), kw.get("bt", 16), 4, None, kw.get("batch", 2),
+                         kw.get("seq", 16), kw.get("pos", 16), kw.get("n", 3),
+                         kw.get("k", 16), kw.get("v", 16), kw.get("sm", None), None]
+    assert lib.pkv_append_tokens(p, *args(n=0)) == S["PKV_OK"]
+    assert lib.pkv_append_tokens(p, *args(layer=2)) == S["PKV_ERR_INVALID_ARG"]
+    assert lib.pkv_append_tokens(p, *args(n=-1)) == S["PKV_ERR_INVALID_ARG"]
+    assert lib.pkv_append_tokens(p, *args(k=24)) == S["PKV_ERR_INVALID_ARG"]   # align
+    assert lib.pkv_append_tokens(p, *args(seq=0)) == S["PKV_ERR_INVALID_ARG"]
+    assert lib.pkv_append_tokens(p, *args(sm=12)) == S["PKV_ERR_INVALID_ARG"]  # slot align
+    assert lib.pkv_append_tokens(p, *args(bt=0)) == S["PKV_ERR_INVALID_ARG"]
+
+
 def test_host_checks_int8_pools(lib):
     # int8 pools: codes must fill 16-byte multiples, the quantising scatter
     # takes head sizes 32..256 (powers of two), prefill takes bf16 pools only
