@@ -9,13 +9,14 @@
 // through the block table (first-block offset honoured).  GQA: query head h
 // reads kv head h / (Hq / Hkv).
 //
-// One CTA per (pair of query tiles, sequence, kv head):
+// Work items are (pair of query tiles, sequence, kv head), taken in turn by a
+// persistent grid of one CTA per SM:
 //  * A query tile is 128 MMA rows = (128 / G) query tokens x the G query
 //    heads of kv head g, so each K/V tile feeds all G heads (row r = token *
 //    G + head).  The CTA owns two tiles, A and B, that share the K/V stream.
 //  * Keys in tiles of 128 table positions (128 / bs whole blocks).  K(t) and
 //    V(t) are loaded by TMA (one box per block and 64-column half, 128B
-//    swizzle) into a 3-slot ring in the order K0 V0 K1 V1 ...; invalid table
+//    swizzle) into a 5-slot ring in the order K0 V0 K1 V1 ...; invalid table
 //    entries load zeros.
 //  * Warp 9 issues S_x = Q_x K^T (M 128, N 128, K 128: 8 tcgen05.mma, fp32
 //    in TMEM) and O_x += P_x V (V is the MN-major operand) in the order
@@ -24,8 +25,9 @@
 //  * Warps 0-3 (tile A) and 4-7 (tile B) own one row each: they read the S
 //    row from TMEM (tcgen05.ld 32x32b), mask only the tiles that need it, keep
 //    the running sum and a maximum that moves only when a score exceeds it by
-//    more than 2^8 (then the O row is rescaled in TMEM), and write P as bf16
-//    into a K-major 128B-swizzled tile for the second MMA.
+//    more than 8 in log2 units (checked per 32-key chunk before that chunk's
+//    P is stored; the O row is then rescaled in TMEM), and write P as bf16
+//    pairs over the S columns in TMEM, the A operand of the second MMA.
 //  * Epilogue: O row / l -> bf16 -> global (only rows that are real queries).
 // Every wait is bounded; on a timeout the CTA records the error, drains its
 // MMAs and frees its TMEM before returning.
@@ -138,6 +140,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
       : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -176,10 +188,6 @@ struct RowState {
   float l;       // running sum of P
 };
 
-// Softmax of one S tile for one row: reads the row from TMEM, masks it,
-// updates the running state, rescales the O row when the maximum moved, and
-// writes the bf16 P row into the 128B-swizzled K-major P tile.  Returns false
-// when a bounded wait gave up.
 // 2^x for x <= 2^8 on the FMA pipe, to take part of the exponentials off the
 // multi-function unit (which runs one warp instruction per 8 cycles).  Range
 // reduction x = n + f with n = round(x) (by the 1.5 * 2^23 rounding constant)
@@ -202,10 +210,13 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return r;
 }
 
-__device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t lane_base,
-                                             int t, int c_lo, int c_hi, bool full_tile, float qs,
-                                             RowState& st, uint32_t b_pvdone, uint32_t pv_parity,
-                                             int* err) {
+// Softmax of one S tile for one row: reads the row from TMEM, masks it,
+// updates the running state, rescales the O row when the maximum moved, and
+// writes the row's P as bf16 pairs back into TMEM, where the P V product reads
+// it as its A operand.
+__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, uint32_t lane_base, int t,
+                                             int c_lo, int c_hi, bool full_tile, float qs,
+                                             RowState& st) {
   // With a positive scale the maximum is taken on the raw scores and the scale
   // goes into the exponent's FMA; otherwise each score is scaled first.
   const bool pre = qs <= 0.f;
@@ -224,12 +235,9 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
       x[j] = f;
     }
   };
-  // P (bf16 pairs) of one chunk against the maximum mu, into TMEM columns
-  // c0/2 .. c0/2 + 15 of the S region, the A operand of O += P V.  Those
-  // columns hold S values of this chunk or of earlier ones, all read before.
-  auto write_p = [&](int c0, const float (&x)[32], float mu) {
+  // P of one chunk against the maximum mu as bf16 pairs, and their sum
+  auto p_chunk = [&](const float (&x)[32], float mu, uint32_t (&w)[16]) {
     float psum = 0.f;
-    uint32_t w[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
       // one pair in four on the FMA pipe (see exp2_poly), the rest on the MUFU
@@ -239,72 +247,81 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
       psum += a0 + a1;
       w[e] = pack_bf16x2(a0, a1);
     }
-    tmem_st16(tS + lane_base + (c0 >> 1), w);
     return psum;
   };
-  auto chunk_max = [&](const float (&x)[32], float m) {
+  // maximum of a chunk as four independent chains, so its latency is short
+  auto chunk_max = [&](const float (&x)[32]) {
+    float m[4];
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) m = max3(m, x[j], x[j + 1]);
-    return m;
+    for (int k = 0; k < 4; ++k) {
+      const float* y = x + 8 * k;
+      m[k] = fmaxf(max3(max3(max3(y[0], y[1], y[2]), y[3], y[4]), y[5], y[6]), y[7]);
+    }
+    return fmaxf(max3(m[0], m[1], m[2]), m[3]);
   };
+  // P (bf16 pairs) of chunk c0 goes to TMEM columns c0/2 .. c0/2 + 15 of the S
+  // region, the A operand of O += P V.  Those columns hold S values of this
+  // chunk or of earlier ones, all read before.
+  //
   // Every tcgen05.ld / st below is a warp-wide instruction, so all control
   // flow around them is warp-uniform: per-row decisions only select data.
-  // O must hold P(t-1) V(t-1) before O is rescaled (by the time S(t) is
-  // ready that product has normally finished).
-  if (t > 0) {
-    const bool waited = mbar_wait_sleep(b_pvdone, pv_parity, err);
-    if (!__all_sync(0xffffffffu, waited)) return false;
-    tc_fence_after();
-  }
+  // The O rescale needs P(t-1) V(t-1) to have completed; it has, because
+  // S(t) was issued after it and its commit (the "S ready" barrier) covers
+  // every earlier product.
   float psum = 0.f, alpha = 1.f;
   const bool first = st.m_used == -INFINITY;  // this row has no maximum yet
   if (!__any_sync(0xffffffffu, first)) {
-    // one pass against the current maximum, tracking this tile's maximum
-    float mt = -INFINITY;
-    if (full_tile && !pre) {
-      // the common case, kept free of masking and scaling code
+    // One pass against the maximum in use.  Each chunk's maximum is checked
+    // before its P is stored: a row whose chunk maximum lies more than 8
+    // above the maximum in use raises it to that chunk maximum, scales the P
+    // it stored for earlier chunks (bf16, in place) and their sum by
+    // 2^(old - new), and recomputes the chunk's P.  So no stored P exceeds
+    // 2^8 and no exponential overflows, however far a later score jumps.
+    float mu = st.m_used;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kKeys; c0 += 32) {
+    for (int c0 = 0; c0 < kKeys; c0 += 32) {
+      float x[32];
+      if (full_tile && !pre) {
+        // the common case, kept free of masking and scaling code
         uint32_t v[32];
         tmem_ld32(tS + lane_base + c0, v);
         tmem_wait_ld();
-        float x[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
-        mt = chunk_max(x, mt);
-        psum += write_p(c0, x, st.m_used);
-      }
-    } else {
-#pragma unroll 1
-      for (int c0 = 0; c0 < kKeys; c0 += 32) {
-        float x[32];
+      } else {
         load_chunk(c0, x);
-        mt = chunk_max(x, mt);
-        psum += write_p(c0, x, st.m_used);
       }
-    }
-    const float mt_s = mt * qe;
-    float beta = 1.f;  // correction of the P just written
-    if (mt_s > st.m_used + 8.f) {
-      // P would exceed 2^8 against the old maximum: move it, and scale the
-      // P already written (bf16, in place) and its sum to the new maximum
-      beta = exp2f(st.m_used - mt_s);
-      alpha = beta;
-      st.m_used = mt_s;
-      psum *= beta;
-    }
-    if (__any_sync(0xffffffffu, beta != 1.f)) {
-      tmem_wait_st();  // the P just stored, before it is read back
+      const float cm = chunk_max(x) * qe;
+      uint32_t w[16];
+      float ps = p_chunk(x, mu, w);
+      // stored before the check so the store does not wait for the maximum;
+      // a row that raises its maximum overwrites it below
+      tmem_st16(tS + lane_base + (c0 >> 1), w);
+      if (__any_sync(0xffffffffu, cm > mu + 8.f)) {
+        const float nm = cm > mu + 8.f ? cm : mu;
+        const float beta = exp2f(mu - nm);  // 1 for rows that keep their maximum
+        mu = nm;
+        psum *= beta;
+        alpha *= beta;
+        tmem_wait_st();  // the P stored so far, before it is read back or replaced
+        if (c0 > 0) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < kKeys / 2; c0 += 32) {  // the 64 P columns
-        uint32_t v[32];
-        tmem_ld32(tS + lane_base + c0, v);
-        tmem_wait_ld();
+          for (int cc = 0; cc < (c0 >> 1); cc += 16) {
+            uint32_t pv[16];
+            tmem_ld16(tS + lane_base + cc, pv);
+            tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = pack_bf16x2(bf16_lo(v[j]) * beta, bf16_hi(v[j]) * beta);
-        tmem_st32(tS + lane_base + c0, v);
+            for (int j = 0; j < 16; ++j)
+              pv[j] = pack_bf16x2(bf16_lo(pv[j]) * beta, bf16_hi(pv[j]) * beta);
+            tmem_st16(tS + lane_base + cc, pv);
+          }
+        }
+        ps = p_chunk(x, mu, w);
+        tmem_st16(tS + lane_base + (c0 >> 1), w);
       }
+      psum += ps;
     }
+    st.m_used = mu;
   } else {
     // some row still needs its first maximum: find the maxima first, then P
     float mt = -INFINITY;
@@ -312,7 +329,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
     for (int c0 = 0; c0 < kKeys; c0 += 32) {
       float x[32];
       load_chunk(c0, x);
-      mt = chunk_max(x, mt);
+      mt = fmaxf(mt, chunk_max(x));
     }
     const float mt_s = mt * qe;
     if (first) {
@@ -331,7 +348,9 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
     for (int c0 = 0; c0 < kKeys; c0 += 32) {
       float x[32];
       load_chunk(c0, x);
-      psum += write_p(c0, x, mu);
+      uint32_t w[16];
+      psum += p_chunk(x, mu, w);
+      tmem_st16(tS + lane_base + (c0 >> 1), w);
     }
   }
   if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -344,11 +363,9 @@ __device__ __forceinline__ bool softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
       for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
       tmem_st32(tO + lane_base + c0, v);
     }
-    tmem_wait_st();
   }
   tmem_wait_st();
   st.l = st.l * alpha + psum;
-  return true;
 }
 
 // One work item: a pair of query tiles of one (sequence, kv head).  All roles
@@ -634,11 +651,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int c_lo = (int)max(0ll, (long long)it.off - tp0);
         const int c_hi = row_ok ? (int)min((long long)kKeys - 1, pos + it.off - tp0) : -1;
         const bool full_tile = (t > 0 || it.off == 0) && t < t_mask_lo && rows_full;
-        if (!softmax_tile(tS(x), tO(x), lane_base, t, c_lo, c_hi, full_tile, p.qscale, st,
-                          b_pvdone, (uint32_t)((nt - 1) & 1), p.err)) {
-          ok = false;
-          break;
-        }
+        softmax_tile(tS(x), tO(x), lane_base, t, c_lo, c_hi, full_tile, p.qscale, st);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_pfull);

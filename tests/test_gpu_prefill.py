@@ -111,3 +111,38 @@ def test_prefill_empty_and_bounds(dev):
                               t(batch.seq_lens, torch.int32), None, t(cu, torch.int64), 4,
                               torch.zeros_like(bad))
     assert e.value.name == "PKV_ERR_INVALID_ARG"
+
+
+JUMPS = [
+    # (scale sign, planted key positions and magnitudes, queries): a query
+    # that reaches a planted key sees its score jump far above every score of
+    # the earlier key tiles (by 100 to 300 in log2 units)
+    (1, [(300, 16.0)], 600),
+    (1, [(150, 8.0), (300, 16.0), (470, 24.0)], 600),
+    (1, [(70, 16.0)], 600),             # inside the first key tile
+    (-1, [(300, 16.0)], 600),           # negative scale: the planted key is -c
+    (1, [(1000, 16.0)], 200),           # cached prefix: every query tile is past it
+]
+
+
+@pytest.mark.parametrize("sign,plants,nq", JUMPS, ids=[f"s{j[0]}-{len(j[1])}keys-nq{j[2]}" for j in JUMPS])
+def test_prefill_score_jumps(dev, sign, plants, nq):
+    """Scores of a later key tile far above the running maximum: the kernel
+    raises the maximum before such a score reaches an exponential, so P never
+    overflows.  Queries are |N(0,1)| (all positive) and each planted key row
+    is the constant c (or -c with a negative scale), so every query that
+    reaches it scores about 13 c against it in log2 units."""
+    L = 1200 if nq == 200 else 600
+    spec, batch, cu, k, v, q, layer = _case(dev, 91 + len(plants), [L], [nq], 4, hkv=2,
+                                            offsets=True)
+    q.abs_()
+    bs = spec.block_size
+    off = int(batch.offsets[0])
+    for pos, c in plants:
+        p = off + pos
+        blk = int(batch.block_tables[0][p // bs])
+        k[blk, layer, p % bs] = sign * c
+    out, ref = _run(dev, spec, batch, cu, k, v, q, layer, scale=sign * 128 ** -0.5)
+    assert torch.isfinite(out.float()).all()
+    assert max_abs(widen_out(out), ref) <= 2e-2
+    assert pkv.device_error() == "PKV_OK"
