@@ -1033,7 +1033,9 @@ def decode_sweep(args) -> int:
 def ncu_case(kind: str, launches: int = 4) -> int:
     """A small-footprint run of one kernel for ncu: the decode-GQA batch
     (1.27 GB of K/V per launch, larger than L2) over a 1-layer copy of its
-    pool (1 GB), or the gather/scatter legs over a 1-layer pool."""
+    pool (1 GB), the long split-K or prefix-mix decode batches over 1-layer
+    copies of theirs (4.3 / 2.1 GB), or the gather/scatter legs over a
+    1-layer pool.  Each launch reads the same bytes as on the full pool."""
     import paged_kv_cache_blk_gb300 as pkv
     from workloads.gen import PoolSpec
     dev = torch.device("cuda", 0)
@@ -1052,7 +1054,8 @@ def ncu_case(kind: str, launches: int = 4) -> int:
         torch.cuda.synchronize()
         print(f"ncu case prefill: {launches} launches done")
         return 0
-    name = WORKLOAD if kind.startswith("decode") else LEG_WORKLOAD
+    name = {"decode_long": "long_splitk", "decode_prefix": "prefix_mix"}.get(
+        kind, WORKLOAD if kind.startswith("decode") else LEG_WORKLOAD)
     w = make_workload(name)
     sp = w.pool
     if kind == "decode_i8":
@@ -1108,7 +1111,8 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true",
                     help="time the step from eager API calls only (no CUDA graph replay)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--ncu-case", choices=["decode", "decode_i8", "gather", "scatter",
+    ap.add_argument("--ncu-case", choices=["decode", "decode_i8", "decode_long", "decode_prefix",
+                                           "gather", "scatter",
                                            "prefill"],
                     help="run a small-footprint case of one kernel (for ncu) and exit")
     ap.add_argument("--decode-sweep", action="store_true",
