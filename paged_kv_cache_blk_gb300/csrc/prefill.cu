@@ -188,22 +188,6 @@ struct RowState {
   float l;       // running sum of P
 };
 
-// 2^x for x <= 2^8 on the FMA pipe, to take part of the exponentials off the
-// multi-function unit (which runs one warp instruction per 8 cycles).  Range
-// reduction x = n + f with n = round(x) (by the 1.5 * 2^23 rounding constant)
-// and f in [-1/2, 1/2], a degree-3 polynomial for 2^f (coefficients fitted
-// here for relative error: at most 7.7e-5, below bf16's 2^-9 rounding), and
-// n added to the exponent field.  Inputs below -126 give 2^-126 (P of such a
-// key is below bf16's smallest normal and contributes nothing visible).
-__device__ __forceinline__ float exp2_poly(float x) {
-  x = fmaxf(x, -126.f);
-  const float t = __fadd_rn(x, 12582912.f);
-  const float f = __fsub_rn(x, __fsub_rn(t, 12582912.f));
-  const float p = fmaf(fmaf(fmaf(0.05518098f, f, 0.24263459f), f, 0.69326133f), f, 0.99992621f);
-  const int n = __float_as_int(t) - 0x4B400000;
-  return __int_as_float(__float_as_int(p) + (n << 23));
-}
-
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -240,10 +224,8 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
     float psum = 0.f;
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      // one pair in four on the FMA pipe (see exp2_poly), the rest on the MUFU
       const float y0 = fmaf(x[2 * e], qe, -mu), y1 = fmaf(x[2 * e + 1], qe, -mu);
-      const float a0 = (e & 3) == 3 ? exp2_poly(y0) : exp2f(y0);
-      const float a1 = (e & 3) == 3 ? exp2_poly(y1) : exp2f(y1);
+      const float a0 = exp2f(y0), a1 = exp2f(y1);
       psum += a0 + a1;
       w[e] = pack_bf16x2(a0, a1);
     }
