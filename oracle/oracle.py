@@ -51,6 +51,7 @@ __all__ = [
     "gather_indexed", "gather_batch", "widen", "attention_fp64",
     "decode_attention", "decode_attention_pairs", "split_partials",
     "combine_partials", "copy_blocks", "swap_out", "swap_in", "prefill_attention",
+    "prefill_attention_rows",
 ]
 
 
@@ -410,3 +411,25 @@ def prefill_attention(k_cache: np.ndarray, v_cache: np.ndarray, layer: int, q: n
                 out[int(cu_q[b]) + i, h] = attention_fp64(qd[int(cu_q[b]) + i, h],
                                                           kb[:P + 1, g], vb[:P + 1, g], scale)
     return out
+
+
+def prefill_attention_rows(k_cache: np.ndarray, v_cache: np.ndarray, layer: int, q: np.ndarray,
+                           block_tables: np.ndarray, seq_lens: np.ndarray, offsets: np.ndarray,
+                           cu_q: np.ndarray, scale: float, rows: Iterable) -> dict:
+    """:func:`prefill_attention` for selected ``(t, h)`` pairs only (``t`` a
+    row of ``q``, ``h`` a query head): the same definition, evaluated where a
+    full-size check samples it."""
+    Hq = q.shape[1]
+    group = Hq // k_cache.shape[3]
+    out = {}
+    for t, h in rows:
+        b = int(np.searchsorted(cu_q, t, side="right") - 1)
+        n = int(cu_q[b + 1] - cu_q[b])
+        L = int(seq_lens[b])
+        P = L - n + (t - int(cu_q[b]))
+        g = h // group
+        kb = widen(gather_loop(k_cache, layer, block_tables[b], P + 1, int(offsets[b])))
+        vb = widen(gather_loop(v_cache, layer, block_tables[b], P + 1, int(offsets[b])))
+        out[(t, h)] = attention_fp64(widen(q[t, h]), kb[:, g], vb[:, g], scale)
+    return out
+

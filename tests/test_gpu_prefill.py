@@ -146,3 +146,41 @@ def test_prefill_score_jumps(dev, sign, plants, nq):
     assert torch.isfinite(out.float()).all()
     assert max_abs(widen_out(out), ref) <= 2e-2
     assert pkv.device_error() == "PKV_OK"
+
+
+@pytest.mark.parametrize("kind", ["prompts", "chunk"])
+def test_prefill_bench_workloads_sampled(dev, kind):
+    """The benchmark's own prefill launches (16 x 2048-token prompts; 16 x 512
+    new tokens after 3584 cached ones), checked on sampled (query, head)
+    rows: the first and last query of every sequence, rows at key-tile
+    boundaries, and random rows."""
+    import bench
+    spec, batch, cu, nq, k, v, q, _ = bench.prefill_case(dev, kind)
+    pool = pkv.Pool(k, v)
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+    out = torch.full_like(q, float("nan"))
+    scale = 128 ** -0.5
+    pkv.prefill_attention(pool, 0, q, scale, t(batch.block_tables, torch.int32),
+                          t(batch.seq_lens, torch.int32), t(batch.offsets, torch.int32),
+                          t(cu, torch.int64), nq, out)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
+    rng = np.random.default_rng(5)
+    Hq = q.shape[1]
+    rows = set()
+    for b in range(len(cu) - 1):
+        lo, hi = int(cu[b]), int(cu[b + 1])
+        rows.add((lo, int(rng.integers(Hq))))
+        rows.add((hi - 1, int(rng.integers(Hq))))
+        for i in (127, 128, 255, 256):
+            if lo + i < hi:
+                rows.add((lo + i, int(rng.integers(Hq))))
+    for _ in range(32):
+        rows.add((int(rng.integers(int(cu[-1]))), int(rng.integers(Hq))))
+    ref = oracle.prefill_attention_rows(to_numpy_bits(k), to_numpy_bits(v), 0, to_numpy_bits(q),
+                                        batch.block_tables, batch.seq_lens, batch.offsets, cu,
+                                        scale, sorted(rows))
+    got = widen_out(out)
+    err = max(float(np.max(np.abs(got[t_, h] - r))) for (t_, h), r in ref.items())
+    assert err <= 2e-2, err
+    assert pkv.device_error() == "PKV_OK"

@@ -544,6 +544,33 @@ def test_prefill_vs_sdpa_with_explicit_causal_mask():
             np.testing.assert_allclose(got[cu[b]:cu[b + 1]], ref, rtol=0, atol=1e-12)
 
 
+def test_prefill_rows_vs_sdpa():
+    """The sampled-rows form, checked row by row against SDPA with the
+    bottom-right causal mask (including sequences with no queries)."""
+    rng = np.random.default_rng(17)
+    for group in (1, 4):
+        k, v, q, bt, lens, offs, cu = _prefill_case(rng, group=group, B=4)
+        Hq = q.shape[1]
+        rows = [(t, h) for t in range(int(cu[-1])) for h in range(Hq)]
+        got = O.prefill_attention_rows(k, v, 1, q, bt, lens, offs, cu, 0.27, rows)
+        for b in range(len(lens)):
+            n, L = int(cu[b + 1] - cu[b]), int(lens[b])
+            if n == 0:
+                continue
+            kb = O.gather_indexed(k, 1, bt[b], L, int(offs[b])).astype(np.float64)
+            vb = O.gather_indexed(v, 1, bt[b], L, int(offs[b])).astype(np.float64)
+            qt = torch.from_numpy(q[cu[b]:cu[b + 1]].astype(np.float64)).permute(1, 0, 2)
+            kt = torch.from_numpy(kb).permute(1, 0, 2).repeat_interleave(group, 0)
+            vt = torch.from_numpy(vb).permute(1, 0, 2).repeat_interleave(group, 0)
+            mask = torch.arange(L)[None, :] <= (L - n + torch.arange(n))[:, None]
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                qt, kt, vt, attn_mask=mask, scale=0.27).permute(1, 0, 2).numpy()
+            for i in range(n):
+                for h in range(Hq):
+                    np.testing.assert_allclose(got[(int(cu[b]) + i, h)], ref[i, h], rtol=0,
+                                               atol=1e-12)
+
+
 def test_prefill_whole_prompt_is_plain_causal_and_last_row_is_decode():
     rng = np.random.default_rng(16)
     k, v, _, bt, lens, offs = _rand_case(rng, group=2, B=2, maxlen=30)
