@@ -2,9 +2,10 @@
 
 A step is one decode iteration of the decode-GQA workload (pool
 16384x32x16x8x128 bf16, layer 7, 32 query heads, batch 64, seq_len
-U[1024, 8192]): build the slots of the 64 new tokens, scatter their K/V rows
-into the pool, then run fused paged decode attention (partial pass + combine)
-over every sequence.  `value` is the KV bytes the attention reads per step
+U[1024, 8192]): each of the 64 new tokens' K/V rows goes to its slot (the
+table lookup of position seq_len - 1) and paged decode attention runs over
+every sequence, in one fused pass over the pool (pkv_decode_step), followed
+by the split-K combine.  `value` is the KV bytes the attention reads per step
 (sum of seq_len x 2 x row bytes) divided by the step time, in GB/s.  The
 gather and scatter bandwidths are measured on the gather/scatter workload
 (pool 16384x32x16x8x128 bf16, 32 sequences, seq_len U[512, 4096]) and
@@ -266,20 +267,29 @@ class DecodeStep:
         for name in ("q", "k_new", "v_new"):
             self.host[name] = getattr(self, name).cpu().pin_memory()
         self.host_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        self._pack_inputs()
         self.bytes = decode_bytes(b, spec.row_bytes, hq, D, 2, spec.block_size)
-        self.launches_per_step = 3  # slot mapping + scatter (one kernel), decode partial, combine
+        self.quant = quant
+        # bf16: one fused decode step (new rows stored, attention) + combine;
+        # int8: slot mapping + quantising scatter, decode partial, combine
+        self.launches_per_step = 3 if quant else 2
+        self._INPUTS = (("bt", "lens", "offs", "seq", "pos", "q", "k_new", "v_new") if quant
+                        else ("bt", "lens", "offs", "q", "k_new", "v_new"))
+        self._pack_inputs()
 
     def step(self):
         pkv = self.pkv
-        # slot mapping and scatter of the new tokens in one kernel (the slots
-        # are also written out), then decode attention
-        pkv.append_tokens(self.pool, self.w.layer, self.bt, self.offs, self.seq, self.pos,
-                          self.k_new, self.v_new, self.slots)
-        pkv.decode_attention(self.pool, self.w.layer, self.q, self.w.scale, self.bt, self.lens,
-                             self.offs, self.out, self.ws)
-
-    _INPUTS = ("bt", "lens", "offs", "seq", "pos", "q", "k_new", "v_new")
+        if self.quant:
+            # slot mapping and quantising scatter of the new tokens in one
+            # kernel (the slots are also written out), then decode attention
+            pkv.append_tokens(self.pool, self.w.layer, self.bt, self.offs, self.seq, self.pos,
+                              self.k_new, self.v_new, self.slots)
+            pkv.decode_attention(self.pool, self.w.layer, self.q, self.w.scale, self.bt,
+                                 self.lens, self.offs, self.out, self.ws)
+        else:
+            # the new token of sequence b (row b of k_new / v_new) is stored at
+            # its slot (position seq_len - 1) and attended to, in one pass
+            pkv.decode_step(self.pool, self.w.layer, self.q, self.w.scale, self.bt, self.lens,
+                            self.offs, self.k_new, self.v_new, self.out, self.ws)
 
     def _pack_inputs(self):
         """Lay every input of the step out in one page-locked host arena and
@@ -359,24 +369,36 @@ def timed(fn, steps: int, flush, events_hook=None):
 
 
 def step_breakdown(st: "DecodeStep", flush: torch.Tensor, steps: int) -> dict:
-    """Eager per-call device times of the step (events between the calls)."""
+    """Eager per-call device times (events between the calls): the fused
+    decode step, and for comparison the same work as two calls (append the
+    new rows, then decode attention)."""
     pkv = st.pkv
-    names = ("append_tokens", "decode_attention")
+    names = ("decode_step", "append_tokens", "decode_attention")
     acc = {n: 0.0 for n in names}
     for _ in range(steps):
         flush.zero_()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         ev[0].record()
+        pkv.decode_step(st.pool, st.w.layer, st.q, st.w.scale, st.bt, st.lens, st.offs,
+                        st.k_new, st.v_new, st.out, st.ws)
+        ev[1].record()
+        flush.zero_()
+        ev[2].record()
         pkv.append_tokens(st.pool, st.w.layer, st.bt, st.offs, st.seq, st.pos, st.k_new,
                           st.v_new, st.slots)
-        ev[1].record()
+        ev3 = torch.cuda.Event(enable_timing=True)
+        ev3.record()
         pkv.decode_attention(st.pool, st.w.layer, st.q, st.w.scale, st.bt, st.lens, st.offs,
                              st.out, st.ws)
-        ev[2].record()
+        ev[3].record()
         torch.cuda.synchronize()
-        for i, n in enumerate(names):
-            acc[n] += ev[i].elapsed_time(ev[i + 1])
-    return {n: round(v / steps, 4) for n, v in acc.items()}
+        acc["decode_step"] += ev[0].elapsed_time(ev[1])
+        acc["append_tokens"] += ev[2].elapsed_time(ev3)
+        acc["decode_attention"] += ev3.elapsed_time(ev[3])
+    out = {n: round(v / steps, 4) for n, v in acc.items()}
+    return {"decode_step": out["decode_step"],
+            "unfused": {"append_tokens": out["append_tokens"],
+                        "decode_attention": out["decode_attention"]}}
 
 
 def run_ours(args, rank, local_rank, world):
@@ -493,8 +515,8 @@ def run_ours(args, rank, local_rank, world):
         "config": {
             "workload": "decode_gqa: pool 16384x32x16x8x128 bf16 (layer 7), Hq 32 (GQA 4), "
                         "batch 64, seq_len U[1024,8192], random non-contiguous tables; step = "
-                        "slot mapping + scatter of 64 new tokens (one fused kernel) + paged "
-                        "decode attention",
+                        "the 64 new tokens' K/V stored at their slots and paged decode attention "
+                        "in one fused pass (pkv_decode_step), then the split-K combine",
             "batch": int(w.batch.batch),
             "kv_read_bytes_per_step": kv,
             "l2": "flushed between steps outside the events (512 MiB write, then a 512 MiB read "

@@ -216,6 +216,33 @@ PKV_API pkv_status pkv_decode_attention(const pkv_pool* pool, int32_t layer, con
                                 int32_t batch, void* out, void* workspace,
                                 size_t workspace_bytes, cudaStream_t stream);
 
+/* One decode step in one pass over the pool: for every sequence b with
+ * seq_lens[b] > 0, the new token at logical position p = seq_lens[b] - 1
+ * (already counted in seq_lens) has its K and V rows k_new[b], v_new[b]
+ * stored at its slot table[b][(off + p) / bs] * bs + (off + p) % bs of
+ * `layer` ([vllm-notes] §2.2 slot mapping and scatter; [step14_2] the
+ * relation between writing the new K/V and reading them back), and decode
+ * attention then runs over positions 0..p exactly as pkv_decode_attention.
+ * The result equals pkv_append_tokens with token b at position
+ * seq_lens[b] - 1, followed by pkv_decode_attention: same pool bytes, same
+ * output.  The new rows are staged straight from k_new / v_new into the
+ * attention pipeline and stored to the pool from there, so the step is one
+ * pass over K/V instead of a scatter launch followed by a read.
+ * k_new, v_new: [batch, num_kv_heads, head_dim] contiguous, pool dtype,
+ * device, 16-byte aligned (PKV_ERR_INVALID_ARG otherwise).  Sequences with
+ * seq_lens[b] == 0 store nothing.  The new token's block must not appear in
+ * another sequence's table in the same call (copy-on-write guarantees it).
+ * bf16 and fp32 pools; PKV_I8 pools return PKV_ERR_UNSUPPORTED (use
+ * pkv_append_tokens, which quantises, then pkv_decode_attention).  All other
+ * arguments, checks and errors are those of pkv_decode_attention. */
+PKV_API pkv_status pkv_decode_step(const pkv_pool* pool, int32_t layer, const void* q,
+                                   int32_t num_q_heads, float scale,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* seq_lens, const int32_t* offsets,
+                                   int32_t batch, const void* k_new, const void* v_new,
+                                   void* out, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream);
+
 /* Paged prefill attention (the prefill batch of
  * "vLLM PagedAttention source notes" §2.4: the prompt tokens' K/V are written
  * into their blocks, then attention runs over them), on tcgen05 tensor cores.

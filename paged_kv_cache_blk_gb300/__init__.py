@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     build_slot_mapping,
     copy_blocks,
     decode_attention,
+    decode_step,
     decode_attention_static,
     decode_workspace_size,
     device_error,

@@ -60,6 +60,8 @@ _SIGS = {
                                     _SZ, _P]),
     "pkv_decode_attention_static": (_I32, [_P, _I32, _P, _I32, _F32, _P, _I32, _P, _P, _I32,
                                            _P, _P]),
+    "pkv_decode_step": (_I32, [_P, _I32, _P, _I32, _F32, _P, _I32, _P, _P, _I32, _P, _P, _P, _P,
+                               _SZ, _P]),
     "pkv_copy_blocks": (_I32, [_P, _I32, _P, _P, _I32, _P]),
     "pkv_swap_out": (_I32, [_P, _I32, _P, _I32, _P, _P, _SZ, _P]),
     "pkv_swap_in": (_I32, [_P, _I32, _P, _I32, _P, _P, _SZ, _P]),
@@ -267,6 +269,24 @@ def decode_attention(pool: Pool, layer: int, q: torch.Tensor, scale: float,
                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _stream(pool.device))
     _check(st, "pkv_decode_attention")
+
+
+def decode_step(pool: Pool, layer: int, q: torch.Tensor, scale: float,
+                block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                offsets: Optional[torch.Tensor], k_new: torch.Tensor, v_new: torch.Tensor,
+                out: torch.Tensor, workspace: torch.Tensor) -> None:
+    """One decode step: store each sequence's new K/V row (``k_new``,
+    ``v_new`` [B, Hkv, D]) at its last position, then paged decode attention
+    of ``q`` [B, Hq, D] into ``out``, in one pass over the pool."""
+    lib = load()
+    with _dev(pool):
+        st = lib.pkv_decode_step(pool.ref, layer, _ptr(q), q.shape[1], float(scale),
+                                 _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+                                 _ptr(offsets), seq_lens.numel(), _ptr(k_new), _ptr(v_new),
+                                 _ptr(out), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(),
+                                 _stream(pool.device))
+    _check(st, "pkv_decode_step")
 
 
 def decode_attention_static(pool: Pool, layer: int, q: torch.Tensor, scale: float,

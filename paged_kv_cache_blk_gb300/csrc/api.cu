@@ -317,11 +317,14 @@ size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t hea
   return pkv::decode_workspace_bytes(batch, num_q_heads, head_dim, decode_grid(*d));
 }
 
-pkv_status pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void* q,
-                                int32_t num_q_heads, float scale, const int32_t* block_tables,
-                                int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                                const int32_t* offsets, int32_t batch, void* out, void* workspace,
-                                size_t workspace_bytes, cudaStream_t stream) {
+// Decode attention, and with new K/V rows (k_new != nullptr) the fused
+// decode step that first stores them at each sequence's last position.
+static pkv_status decode_call(const pkv_pool* pool, int32_t layer, const void* q,
+                              int32_t num_q_heads, float scale, const int32_t* block_tables,
+                              int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                              const int32_t* offsets, int32_t batch, const void* k_new,
+                              const void* v_new, bool step, void* out, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
   pkv::PoolView v;
   pkv_status st = check_pool(pool, true, &v);
   if (st != PKV_OK) return st;
@@ -330,10 +333,13 @@ pkv_status pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void*
   if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
   if (pkv::decode_supported(v, num_q_heads) != 0) return PKV_ERR_UNSUPPORTED;
+  if (step && v.quant) return PKV_ERR_UNSUPPORTED;  // int8 pools: append_tokens + decode
   if (batch == 0) return PKV_OK;
   if (!q || !out || !block_tables || !seq_lens || max_blocks_per_seq <= 0)
     return PKV_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+  if (step && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
+    return PKV_ERR_INVALID_ARG;
   if (!workspace || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
   DevInfo* d;
   if ((st = current_device(&d)) != PKV_OK) return st;
@@ -372,11 +378,36 @@ pkv_status pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void*
     a.smem_optin = d->smem_optin;
     a.ev_start = b0 == 0 ? ev_start : nullptr;
     a.ev_stop = b0 + nb >= batch ? ev_stop : nullptr;
+    if (step) {
+      a.k_new = static_cast<const char*>(k_new) + (size_t)b0 * v.row_bytes;
+      a.v_new = static_cast<const char*>(v_new) + (size_t)b0 * v.row_bytes;
+    }
     const cudaError_t e = pkv::launch_decode(a, stream);
     if (e == cudaErrorInvalidConfiguration) return PKV_ERR_UNSUPPORTED;
     if ((st = launched(e)) != PKV_OK) return st;
   }
   return validate ? read_and_clear(d->err, stream) : PKV_OK;
+}
+
+pkv_status pkv_decode_attention(const pkv_pool* pool, int32_t layer, const void* q,
+                                int32_t num_q_heads, float scale, const int32_t* block_tables,
+                                int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                const int32_t* offsets, int32_t batch, void* out, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+  return decode_call(pool, layer, q, num_q_heads, scale, block_tables, max_blocks_per_seq,
+                     seq_lens, offsets, batch, nullptr, nullptr, false, out, workspace,
+                     workspace_bytes, stream);
+}
+
+pkv_status pkv_decode_step(const pkv_pool* pool, int32_t layer, const void* q,
+                           int32_t num_q_heads, float scale, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                           const int32_t* offsets, int32_t batch, const void* k_new,
+                           const void* v_new, void* out, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+  return decode_call(pool, layer, q, num_q_heads, scale, block_tables, max_blocks_per_seq,
+                     seq_lens, offsets, batch, k_new, v_new, true, out, workspace,
+                     workspace_bytes, stream);
 }
 
 pkv_status pkv_prefill_attention(const pkv_pool* pool, int32_t layer, const void* q,

@@ -123,6 +123,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// Orders this thread's earlier generic-proxy global writes before later
+// async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---- programmatic dependent launch -------------------------------------------
 // Every kernel of the library starts with griddep_wait(): when it was launched
 // as a programmatic dependent, this waits until the grids before it on the
@@ -254,6 +260,10 @@ struct DecodeLaunch {
   int smem_optin;  // max dynamic shared memory per block on this device
   cudaEvent_t ev_start = nullptr;  // recorded right before the partial kernel
   cudaEvent_t ev_stop = nullptr;   // recorded right after it
+  // fused decode step: the new K / V row of each sequence ([batch] rows of
+  // row_bytes), stored at its last position before it is attended to
+  const char* k_new = nullptr;
+  const char* v_new = nullptr;
 };
 
 constexpr int kDecodeMaxBatch = 2048;

@@ -96,6 +96,13 @@ struct Params {
   float qscale;
   // shared-memory carve (bytes from the start of dynamic smem)
   int off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf, off_vbuf;
+  // fused decode step: the new row of sequence b is k_new / v_new +
+  // b * row_bytes, stored into the pool through k_out / v_out (block 0, this
+  // layer, row 0)
+  const char* k_new;
+  const char* v_new;
+  char* k_out;
+  char* v_out;
 };
 
 // Tensor maps of an int8 pool (unused for bf16 / fp32 pools): K and V codes
@@ -1139,7 +1146,7 @@ __device__ void run_consumer_fma(const Params& p, const Pipe& pp, int warp, int 
 
 // ---- the partial-pass kernel -------------------------------------------------
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool FUSED>
 __global__ void __launch_bounds__((consumer_warps<T>() + 1) * 32, 1)
     decode_partial_kernel(const Params p, const __grid_constant__ I8Maps maps) {
   constexpr int NW = consumer_warps<T>();
@@ -1201,6 +1208,37 @@ __global__ void __launch_bounds__((consumer_warps<T>() + 1) * 32, 1)
     if (tid == 0) { p.ws_meta[0] = W; p.ws_meta[1] = total; }
   }
   if (x0 >= x1) return;
+
+  if constexpr (FUSED) {
+    // The decode step: this CTA's block range holds the last block of some
+    // sequences; their new K/V rows go into the pool here, before any bulk
+    // copy of this CTA reads it.  No other CTA reads those rows: a
+    // sequence's last block lies in exactly one range, and the block of a
+    // new token belongs to its sequence alone.
+    int b = 0, hi = B;  // first sequence ending at or after block x0
+    while (b < hi) {
+      const int mid = (b + hi) >> 1;
+      if (s_cu[mid + 1] - 1 < x0) b = mid + 1; else hi = mid;
+    }
+    const int pieces = p.row_bytes / 16;
+    for (; b < B && s_cu[b + 1] - 1 < x1; ++b) {
+      if (s_cu[b + 1] == s_cu[b]) continue;  // empty (or refused) sequence
+      const long long pos = (long long)(p.offs ? p.offs[b] : 0) + p.lens[b] - 1;
+      const int blk = p.bt[(long long)b * p.mb + pos / p.bs];
+      if (blk < 0 || (long long)blk >= p.num_blocks) continue;  // the producer reports it
+      const long long dst = (long long)blk * p.block_stride + (pos % p.bs) * p.row_bytes;
+      for (int i = tid; i < 2 * pieces; i += kThreads) {
+        const bool vh = i >= pieces;
+        const long long o = 16ll * (vh ? i - pieces : i);
+        const uint4 x = *reinterpret_cast<const uint4*>((vh ? p.v_new : p.k_new) +
+                                                        (long long)b * p.row_bytes + o);
+        *reinterpret_cast<uint4*>((vh ? p.v_out : p.k_out) + dst + o) = x;
+      }
+    }
+    // the rows just stored are read next by the bulk copies (async proxy)
+    fence_proxy_async_global();
+    __syncthreads();
+  }
 
   if (warp == NW) {
     run_producer<sizeof(T) == 1>(p, pp, maps, s_cu, lane, x0, x1);
@@ -1375,7 +1413,7 @@ cudaError_t ensure_smem(K kern, int smem, int (&configured)[64]) {
   return e;
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool FUSED>
 cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   const PoolView& pv = a.pool;
   Params p{};
@@ -1426,6 +1464,10 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   p.off_pbuf = L.off_pbuf;
   p.off_mbuf = L.off_mbuf;
   p.off_vbuf = L.off_vbuf;
+  p.k_new = a.k_new;
+  p.v_new = a.v_new;
+  p.k_out = pv.k_mut ? pv.k_mut + layer_off : nullptr;
+  p.v_out = pv.v_mut ? pv.v_mut + layer_off : nullptr;
 
   I8Maps maps;
   memset(&maps, 0, sizeof(maps));
@@ -1447,7 +1489,7 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
                       sstrides, sbox, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
-  auto kern = decode_partial_kernel<T, D, G>;
+  auto kern = decode_partial_kernel<T, D, G, FUSED>;
   static int configured[64] = {0};
   cudaError_t e = ensure_smem(kern, L.smem, configured);
   if (e != cudaSuccess) return e;
@@ -1467,15 +1509,27 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
                        (const long long*)p.ws_meta, p.hq, D, static_cast<OutT*>(a.out));
 }
 
-template <typename T, int D>
-cudaError_t run_g(const DecodeLaunch& a, const Layout& L, int G, cudaStream_t s) {
+template <typename T, int D, bool FUSED>
+cudaError_t run_gf(const DecodeLaunch& a, const Layout& L, int G, cudaStream_t s) {
   switch (G) {
-    case 1: return run<T, D, 1>(a, L, s);
-    case 2: return run<T, D, 2>(a, L, s);
-    case 4: return run<T, D, 4>(a, L, s);
-    case 8: return run<T, D, 8>(a, L, s);
+    case 1: return run<T, D, 1, FUSED>(a, L, s);
+    case 2: return run<T, D, 2, FUSED>(a, L, s);
+    case 4: return run<T, D, 4, FUSED>(a, L, s);
+    case 8: return run<T, D, 8, FUSED>(a, L, s);
   }
   return cudaErrorInvalidValue;
+}
+
+// int8 pools have no fused decode step (their new rows are quantised by the
+// scatter), so only the plain instantiation exists for them
+template <typename T, int D>
+cudaError_t run_g(const DecodeLaunch& a, const Layout& L, int G, cudaStream_t s) {
+  if constexpr (sizeof(T) == 1) {
+    if (a.k_new) return cudaErrorInvalidValue;
+    return run_gf<T, D, false>(a, L, G, s);
+  } else {
+    return a.k_new ? run_gf<T, D, true>(a, L, G, s) : run_gf<T, D, false>(a, L, G, s);
+  }
 }
 
 }  // namespace

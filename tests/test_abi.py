@@ -153,6 +153,21 @@ def test_host_checks_int8_pools(lib):
     assert B.int8_row_bytes(8, 128) == 1056 and B.int8_row_bytes(3, 32) == 112
 
 
+def test_host_checks_decode_step(lib):
+    # the fused decode step: new rows required and 16-byte aligned; int8
+    # pools are refused (they take append_tokens + decode_attention)
+    p = ctypes.byref(_pool())
+    head = [0, 16, 8, 0.1, 16, 4, 16, None, 2]
+    tail = [16, 16, 1 << 20, None]
+    assert lib.pkv_decode_step(p, *head[:-1], 0, None, None, *tail) == S["PKV_OK"]
+    assert lib.pkv_decode_step(p, *head, None, 16, *tail) == S["PKV_ERR_INVALID_ARG"]
+    assert lib.pkv_decode_step(p, *head, 16, None, *tail) == S["PKV_ERR_INVALID_ARG"]
+    assert lib.pkv_decode_step(p, *head, 24, 16, *tail) == S["PKV_ERR_INVALID_ARG"]
+    p8 = ctypes.byref(_pool(dtype=2))
+    assert lib.pkv_decode_step(p8, *head, 16, 16, *tail) == S["PKV_ERR_UNSUPPORTED"]
+    assert lib.pkv_decode_step(p, 3, *head[1:], 16, 16, *tail) == S["PKV_ERR_INVALID_ARG"]
+
+
 def test_options_and_strings(lib):
     assert lib.pkv_set_decode_ctas(-1) == S["PKV_ERR_INVALID_ARG"]
     assert lib.pkv_set_decode_ctas(0) == S["PKV_OK"]
