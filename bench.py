@@ -495,7 +495,10 @@ def run_ours(args, rank, local_rank, world):
     w = make_workload(WORKLOAD)
     db = decode_bytes(w.batch, w.pool.row_bytes, w.num_q_heads, w.pool.head_dim,
                       w.pool.elem_size, w.pool.block_size)
-    achieved = db["total"] / (part_ms / 1e3) / 1e9
+    # the fused step's partial pass also reads each sequence's new K/V row
+    # (k_new, v_new) and stores it to the pool: 4 rows per sequence
+    step_bytes = db["total"] + 4 * w.batch.batch * w.pool.row_bytes
+    achieved = step_bytes / (part_ms / 1e3) / 1e9
     traffic = recorded_traffic()
     result = {
         "metric": METRIC,
@@ -528,14 +531,14 @@ def run_ours(args, rank, local_rank, world):
                             "peak_kind": peak_kind},
         "tokens_per_s": round(tokens_s, 1),
         "roofline": {
-            "kernel": "decode_partial_kernel<bf16,128,4>",
+            "kernel": "decode_partial_kernel<bf16,128,4,fused step>",
             "bound": "hbm",
             "achieved": round(achieved, 1),
             "peak": peak,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "traffic": traffic,
-            "algorithmic_bytes_per_launch": db["total"],
+            "algorithmic_bytes_per_launch": step_bytes,
             "avg_launch_ms": round(part_ms, 4),
             "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
         },
@@ -1103,6 +1106,10 @@ def ncu_case(kind: str, launches: int = 4) -> int:
         ws = torch.empty(pkv.decode_workspace_size(b.batch, w.num_q_heads, sp.head_dim, dev),
                          dtype=torch.uint8, device=dev)
         fn = lambda: pkv.decode_attention(pool, 0, q, w.scale, bt, lens, offs, out, ws)
+        if kind == "decode_step":
+            kn = rand_rows((b.batch,) + row, "bf16", 2, dev)
+            vn = rand_rows((b.batch,) + row, "bf16", 3, dev)
+            fn = lambda: pkv.decode_step(pool, 0, q, w.scale, bt, lens, offs, kn, vn, out, ws)
     else:
         T = w.tokens.num_tokens
         slots = torch.empty(T, dtype=torch.int64, device=dev)
@@ -1133,7 +1140,8 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true",
                     help="time the step from eager API calls only (no CUDA graph replay)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--ncu-case", choices=["decode", "decode_i8", "decode_long", "decode_prefix",
+    ap.add_argument("--ncu-case", choices=["decode", "decode_step", "decode_i8", "decode_long",
+                                           "decode_prefix",
                                            "gather", "scatter",
                                            "prefill"],
                     help="run a small-footprint case of one kernel (for ncu) and exit")
