@@ -269,27 +269,18 @@ class DecodeStep:
         self.host_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
         self.bytes = decode_bytes(b, spec.row_bytes, hq, D, 2, spec.block_size)
         self.quant = quant
-        # bf16: one fused decode step (new rows stored, attention) + combine;
-        # int8: slot mapping + quantising scatter, decode partial, combine
-        self.launches_per_step = 3 if quant else 2
-        self._INPUTS = (("bt", "lens", "offs", "seq", "pos", "q", "k_new", "v_new") if quant
-                        else ("bt", "lens", "offs", "q", "k_new", "v_new"))
+        # one fused decode step (new rows stored, quantised for int8, and the
+        # attention) + the split-K combine
+        self.launches_per_step = 2
+        self._INPUTS = ("bt", "lens", "offs", "q", "k_new", "v_new")
         self._pack_inputs()
 
     def step(self):
-        pkv = self.pkv
-        if self.quant:
-            # slot mapping and quantising scatter of the new tokens in one
-            # kernel (the slots are also written out), then decode attention
-            pkv.append_tokens(self.pool, self.w.layer, self.bt, self.offs, self.seq, self.pos,
-                              self.k_new, self.v_new, self.slots)
-            pkv.decode_attention(self.pool, self.w.layer, self.q, self.w.scale, self.bt,
-                                 self.lens, self.offs, self.out, self.ws)
-        else:
-            # the new token of sequence b (row b of k_new / v_new) is stored at
-            # its slot (position seq_len - 1) and attended to, in one pass
-            pkv.decode_step(self.pool, self.w.layer, self.q, self.w.scale, self.bt, self.lens,
-                            self.offs, self.k_new, self.v_new, self.out, self.ws)
+        # the new token of sequence b (row b of k_new / v_new) is stored at its
+        # slot (position seq_len - 1; quantised for an int8 pool) and attended
+        # to, in one pass
+        self.pkv.decode_step(self.pool, self.w.layer, self.q, self.w.scale, self.bt, self.lens,
+                             self.offs, self.k_new, self.v_new, self.out, self.ws)
 
     def _pack_inputs(self):
         """Lay every input of the step out in one page-locked host arena and
@@ -584,9 +575,10 @@ def graph_step_ms(step, steps: int, warmup: int, flush, dev) -> float:
 
 def int8_leg(args, dev, rank, flush, pkv) -> dict:
     """The decode step of the decode-GQA workload over an int8 pool of the
-    same geometry: slot mapping, quantising scatter of the 64 new bf16 rows,
-    decode attention.  Step time from a CUDA graph, the partial kernel alone
-    from the library's events, and its roofline over the int8 bytes."""
+    same geometry: the 64 new bf16 rows quantised into their slots and decode
+    attention, in one fused pass (pkv_decode_step), then the combine.  Step
+    time from a CUDA graph, the partial kernel alone from the library's
+    events, and its roofline over the int8 bytes."""
     st = DecodeStep(dev, seed_shift=rank, quant=True)
     for _ in range(args.warmup):
         st.step()
@@ -600,11 +592,16 @@ def int8_leg(args, dev, rank, flush, pkv) -> dict:
     ms = graph_ms if graph_ms is not None else eager_ms
     peak, kind = load_peaks()
     db = st.bytes
+    # the fused partial pass also reads each sequence's new bf16 K/V rows and
+    # stores their int8 rows
+    sp = st.spec
+    part_bytes = db["total"] + st.w.batch.batch * (2 * sp.num_kv_heads * sp.head_dim * 2
+                                                   + 2 * sp.row_bytes)
     out = {
         "what": "decode_gqa step over an int8 pool 16384x32x16x(8x128 codes + 8 fp32 scales) "
-                "(1056-byte token rows): slot mapping + quantising scatter of 64 tokens (one "
-                "fused kernel) + "
-                "paged decode attention (bf16 q / out)",
+                "(1056-byte token rows): the 64 new tokens' bf16 K/V quantised into their "
+                "slots and paged decode attention in one fused pass (pkv_decode_step), then "
+                "the combine (bf16 q / out)",
         "ms_per_step": round(ms, 4),
         "step_mode": "cuda_graph" if graph_ms is not None else "eager",
         "eager_ms_per_step": round(eager_ms, 4),
@@ -612,11 +609,11 @@ def int8_leg(args, dev, rank, flush, pkv) -> dict:
         "GB/s": round(db["kv"] / (ms / 1e3) / 1e9, 1),
         "tokens_per_s": round(st.w.batch.batch / (ms / 1e3), 1),
         "decode_partial": {
-            "kernel": "decode_partial_kernel<int8,128,4>",
+            "kernel": "decode_partial_kernel<int8,128,4,fused step>",
             "avg_launch_ms": round(part_ms, 4),
-            "algorithmic_bytes_per_launch": db["total"],
-            "achieved_GBps": round(db["total"] / (part_ms / 1e3) / 1e9, 1),
-            "frac": round(db["total"] / (part_ms / 1e3) / 1e9 / peak, 4),
+            "algorithmic_bytes_per_launch": part_bytes,
+            "achieved_GBps": round(part_bytes / (part_ms / 1e3) / 1e9, 1),
+            "frac": round(part_bytes / (part_ms / 1e3) / 1e9 / peak, 4),
             "peak": peak, "peak_kind": kind,
             "traffic": recorded_traffic("decode_partial_i8_traffic.txt"),
         },
@@ -1083,7 +1080,7 @@ def ncu_case(kind: str, launches: int = 4) -> int:
         kind, WORKLOAD if kind.startswith("decode") else LEG_WORKLOAD)
     w = make_workload(name)
     sp = w.pool
-    if kind == "decode_i8":
+    if kind in ("decode_i8", "decode_step_i8"):
         from workloads import fill_pool_i8
         one = PoolSpec(sp.num_blocks, 1, sp.block_size, sp.num_kv_heads, sp.head_dim, "i8")
         k = torch.empty(one.shape, dtype=torch.uint8, device=dev)
@@ -1106,7 +1103,7 @@ def ncu_case(kind: str, launches: int = 4) -> int:
         ws = torch.empty(pkv.decode_workspace_size(b.batch, w.num_q_heads, sp.head_dim, dev),
                          dtype=torch.uint8, device=dev)
         fn = lambda: pkv.decode_attention(pool, 0, q, w.scale, bt, lens, offs, out, ws)
-        if kind == "decode_step":
+        if kind in ("decode_step", "decode_step_i8"):
             kn = rand_rows((b.batch,) + row, "bf16", 2, dev)
             vn = rand_rows((b.batch,) + row, "bf16", 3, dev)
             fn = lambda: pkv.decode_step(pool, 0, q, w.scale, bt, lens, offs, kn, vn, out, ws)
@@ -1140,7 +1137,8 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true",
                     help="time the step from eager API calls only (no CUDA graph replay)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--ncu-case", choices=["decode", "decode_step", "decode_i8", "decode_long",
+    ap.add_argument("--ncu-case", choices=["decode", "decode_step", "decode_i8", "decode_step_i8",
+                                           "decode_long",
                                            "decode_prefix",
                                            "gather", "scatter",
                                            "prefill"],

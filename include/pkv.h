@@ -225,16 +225,17 @@ PKV_API pkv_status pkv_decode_attention(const pkv_pool* pool, int32_t layer, con
  * attention then runs over positions 0..p exactly as pkv_decode_attention.
  * The result equals pkv_append_tokens with token b at position
  * seq_lens[b] - 1, followed by pkv_decode_attention: same pool bytes, same
- * output.  The new rows are staged straight from k_new / v_new into the
- * attention pipeline and stored to the pool from there, so the step is one
- * pass over K/V instead of a scatter launch followed by a read.
- * k_new, v_new: [batch, num_kv_heads, head_dim] contiguous, pool dtype,
- * device, 16-byte aligned (PKV_ERR_INVALID_ARG otherwise).  Sequences with
- * seq_lens[b] == 0 store nothing.  The new token's block must not appear in
- * another sequence's table in the same call (copy-on-write guarantees it).
- * bf16 and fp32 pools; PKV_I8 pools return PKV_ERR_UNSUPPORTED (use
- * pkv_append_tokens, which quantises, then pkv_decode_attention).  All other
- * arguments, checks and errors are those of pkv_decode_attention. */
+ * output.  The CTA of the attention kernel whose share of the blocks holds a
+ * sequence's last block stores that sequence's new row before it starts
+ * reading, so the step is one launch (plus the combine) instead of a
+ * scatter launch followed by attention.
+ * k_new, v_new: [batch, num_kv_heads, head_dim] contiguous in q's dtype
+ * (bf16 for PKV_I8 pools, which quantise the new rows exactly as
+ * pkv_write_slots does), device, 16-byte aligned (PKV_ERR_INVALID_ARG
+ * otherwise).  Sequences with seq_lens[b] == 0 store nothing.  The new
+ * token's block must not appear in another sequence's table in the same
+ * call (copy-on-write guarantees it).  All other arguments, checks and errors
+ * are those of pkv_decode_attention. */
 PKV_API pkv_status pkv_decode_step(const pkv_pool* pool, int32_t layer, const void* q,
                                    int32_t num_q_heads, float scale,
                                    const int32_t* block_tables, int32_t max_blocks_per_seq,

@@ -333,7 +333,6 @@ static pkv_status decode_call(const pkv_pool* pool, int32_t layer, const void* q
   if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
   if (pkv::decode_supported(v, num_q_heads) != 0) return PKV_ERR_UNSUPPORTED;
-  if (step && v.quant) return PKV_ERR_UNSUPPORTED;  // int8 pools: append_tokens + decode
   if (batch == 0) return PKV_OK;
   if (!q || !out || !block_tables || !seq_lens || max_blocks_per_seq <= 0)
     return PKV_ERR_INVALID_ARG;
@@ -379,8 +378,9 @@ static pkv_status decode_call(const pkv_pool* pool, int32_t layer, const void* q
     a.ev_start = b0 == 0 ? ev_start : nullptr;
     a.ev_stop = b0 + nb >= batch ? ev_stop : nullptr;
     if (step) {
-      a.k_new = static_cast<const char*>(k_new) + (size_t)b0 * v.row_bytes;
-      a.v_new = static_cast<const char*>(v_new) + (size_t)b0 * v.row_bytes;
+      const size_t in_row = (size_t)v.num_kv_heads * v.head_dim * v.io_size;
+      a.k_new = static_cast<const char*>(k_new) + (size_t)b0 * in_row;
+      a.v_new = static_cast<const char*>(v_new) + (size_t)b0 * in_row;
     }
     const cudaError_t e = pkv::launch_decode(a, stream);
     if (e == cudaErrorInvalidConfiguration) return PKV_ERR_UNSUPPORTED;

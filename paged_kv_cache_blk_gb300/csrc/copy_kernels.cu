@@ -16,6 +16,7 @@
 // warp per row; the HBM system sees (rows x 4 x row_bytes) of traffic and no
 // re-reads.
 #include "common.cuh"
+#include "quant.cuh"
 
 namespace pkv {
 namespace {
@@ -161,59 +162,6 @@ __global__ void __launch_bounds__(kCopyThreads) write_slots_kernel(
 // fast-math flags), codes clamped to [-127, 127].  A zero absmax stores
 // scale 0 and codes 0.  The padding bytes of the row are not written.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float div_ieee(float a, float b) {
-  float r;
-  asm("div.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-  return r;
-}
-
-template <int VPL>
-__device__ __forceinline__ void load_bf16(const __nv_bfloat16* src, float (&x)[VPL]) {
-  if constexpr (VPL == 8) {
-    const uint4 r = *reinterpret_cast<const uint4*>(src);
-    x[0] = bf16_lo(r.x); x[1] = bf16_hi(r.x); x[2] = bf16_lo(r.y); x[3] = bf16_hi(r.y);
-    x[4] = bf16_lo(r.z); x[5] = bf16_hi(r.z); x[6] = bf16_lo(r.w); x[7] = bf16_hi(r.w);
-  } else if constexpr (VPL == 4) {
-    const uint2 r = *reinterpret_cast<const uint2*>(src);
-    x[0] = bf16_lo(r.x); x[1] = bf16_hi(r.x); x[2] = bf16_lo(r.y); x[3] = bf16_hi(r.y);
-  } else if constexpr (VPL == 2) {
-    const uint32_t r = *reinterpret_cast<const uint32_t*>(src);
-    x[0] = bf16_lo(r); x[1] = bf16_hi(r);
-  } else {
-    x[0] = __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(src)) << 16);
-  }
-}
-
-// Quantise one head (VPL values per lane); returns the scale, codes in c.
-template <int VPL>
-__device__ __forceinline__ float quantise_head(const float (&x)[VPL], int (&c)[VPL]) {
-  uint32_t m = 0;
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) m = max(m, __float_as_uint(x[i]) & 0x7FFFFFFFu);
-  m = __reduce_max_sync(0xffffffffu, m);
-  const float scale = div_ieee(__uint_as_float(m), 127.f);
-#pragma unroll
-  for (int i = 0; i < VPL; ++i)
-    c[i] = m == 0 ? 0 : min(127, max(-127, __float2int_rn(div_ieee(x[i], scale))));
-  return scale;
-}
-
-template <int VPL>
-__device__ __forceinline__ void store_codes(char* dst, const int (&c)[VPL]) {
-  uint32_t w[(VPL + 3) / 4] = {};
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) w[i / 4] |= (uint32_t)(c[i] & 0xFF) << (8 * (i % 4));
-  if constexpr (VPL == 8) {
-    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-  } else if constexpr (VPL == 4) {
-    *reinterpret_cast<uint32_t*>(dst) = w[0];
-  } else if constexpr (VPL == 2) {
-    *reinterpret_cast<uint16_t*>(dst) = (uint16_t)w[0];
-  } else {
-    *reinterpret_cast<uint8_t*>(dst) = (uint8_t)w[0];
-  }
-}
-
 template <int VPL, bool FUSED>
 __global__ void __launch_bounds__(kCopyThreads) quant_write_slots_kernel(
     char* __restrict__ kc, char* __restrict__ vc, const __nv_bfloat16* __restrict__ k_new,

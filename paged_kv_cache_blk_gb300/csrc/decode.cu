@@ -48,6 +48,7 @@
 #include <cuda_fp16.h>
 
 #include "common.cuh"
+#include "quant.cuh"
 #include "tma.cuh"
 
 namespace pkv {
@@ -97,12 +98,15 @@ struct Params {
   // shared-memory carve (bytes from the start of dynamic smem)
   int off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf, off_vbuf;
   // fused decode step: the new row of sequence b is k_new / v_new +
-  // b * row_bytes, stored into the pool through k_out / v_out (block 0, this
-  // layer, row 0)
+  // b * new_row_bytes (Hkv * D elements of q's dtype), stored into the pool
+  // through k_out / v_out (block 0, this layer, row 0); int8 pools quantise
+  // it (scales at byte scale_off of the row)
   const char* k_new;
   const char* v_new;
   char* k_out;
   char* v_out;
+  int new_row_bytes;
+  int scale_off;
 };
 
 // Tensor maps of an int8 pool (unused for bf16 / fp32 pools): K and V codes
@@ -1227,12 +1231,33 @@ __global__ void __launch_bounds__((consumer_warps<T>() + 1) * 32, 1)
       const int blk = p.bt[(long long)b * p.mb + pos / p.bs];
       if (blk < 0 || (long long)blk >= p.num_blocks) continue;  // the producer reports it
       const long long dst = (long long)blk * p.block_stride + (pos % p.bs) * p.row_bytes;
-      for (int i = tid; i < 2 * pieces; i += kThreads) {
-        const bool vh = i >= pieces;
-        const long long o = 16ll * (vh ? i - pieces : i);
-        const uint4 x = *reinterpret_cast<const uint4*>((vh ? p.v_new : p.k_new) +
-                                                        (long long)b * p.row_bytes + o);
-        *reinterpret_cast<uint4*>((vh ? p.v_out : p.k_out) + dst + o) = x;
+      const long long src = (long long)b * p.new_row_bytes;
+      if constexpr (sizeof(T) == 1) {
+        // int8 pool: warp g quantises kv head g of the new K and V rows,
+        // exactly as the quantising scatter does
+        constexpr int VPL = D / 32;
+        if (warp < p.hkv) {
+          const long long e = src + ((long long)warp * D + lane * VPL) * 2;
+          float xk[VPL], xv[VPL];
+          load_bf16<VPL>(reinterpret_cast<const __nv_bfloat16*>(p.k_new + e), xk);
+          load_bf16<VPL>(reinterpret_cast<const __nv_bfloat16*>(p.v_new + e), xv);
+          int ck[VPL], cv[VPL];
+          const float sk = quantise_head<VPL>(xk, ck);
+          const float sv = quantise_head<VPL>(xv, cv);
+          store_codes<VPL>(p.k_out + dst + warp * D + lane * VPL, ck);
+          store_codes<VPL>(p.v_out + dst + warp * D + lane * VPL, cv);
+          if (lane == 0) {
+            *reinterpret_cast<float*>(p.k_out + dst + p.scale_off + 4 * warp) = sk;
+            *reinterpret_cast<float*>(p.v_out + dst + p.scale_off + 4 * warp) = sv;
+          }
+        }
+      } else {
+        for (int i = tid; i < 2 * pieces; i += kThreads) {
+          const bool vh = i >= pieces;
+          const long long o = 16ll * (vh ? i - pieces : i);
+          const uint4 x = *reinterpret_cast<const uint4*>((vh ? p.v_new : p.k_new) + src + o);
+          *reinterpret_cast<uint4*>((vh ? p.v_out : p.k_out) + dst + o) = x;
+        }
       }
     }
     // the rows just stored are read next by the bulk copies (async proxy)
@@ -1468,6 +1493,8 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   p.v_new = a.v_new;
   p.k_out = pv.k_mut ? pv.k_mut + layer_off : nullptr;
   p.v_out = pv.v_mut ? pv.v_mut + layer_off : nullptr;
+  p.new_row_bytes = pv.num_kv_heads * pv.head_dim * pv.io_size;
+  p.scale_off = pv.scale_off;
 
   I8Maps maps;
   memset(&maps, 0, sizeof(maps));
@@ -1520,16 +1547,9 @@ cudaError_t run_gf(const DecodeLaunch& a, const Layout& L, int G, cudaStream_t s
   return cudaErrorInvalidValue;
 }
 
-// int8 pools have no fused decode step (their new rows are quantised by the
-// scatter), so only the plain instantiation exists for them
 template <typename T, int D>
 cudaError_t run_g(const DecodeLaunch& a, const Layout& L, int G, cudaStream_t s) {
-  if constexpr (sizeof(T) == 1) {
-    if (a.k_new) return cudaErrorInvalidValue;
-    return run_gf<T, D, false>(a, L, G, s);
-  } else {
-    return a.k_new ? run_gf<T, D, true>(a, L, G, s) : run_gf<T, D, false>(a, L, G, s);
-  }
+  return a.k_new ? run_gf<T, D, true>(a, L, G, s) : run_gf<T, D, false>(a, L, G, s);
 }
 
 }  // namespace

@@ -154,8 +154,8 @@ def test_host_checks_int8_pools(lib):
 
 
 def test_host_checks_decode_step(lib):
-    # the fused decode step: new rows required and 16-byte aligned; int8
-    # pools are refused (they take append_tokens + decode_attention)
+    # the fused decode step: new rows required and 16-byte aligned (int8
+    # pools too: they quantise the new rows)
     p = ctypes.byref(_pool())
     head = [0, 16, 8, 0.1, 16, 4, 16, None, 2]
     tail = [16, 16, 1 << 20, None]
@@ -164,7 +164,9 @@ def test_host_checks_decode_step(lib):
     assert lib.pkv_decode_step(p, *head, 16, None, *tail) == S["PKV_ERR_INVALID_ARG"]
     assert lib.pkv_decode_step(p, *head, 24, 16, *tail) == S["PKV_ERR_INVALID_ARG"]
     p8 = ctypes.byref(_pool(dtype=2))
-    assert lib.pkv_decode_step(p8, *head, 16, 16, *tail) == S["PKV_ERR_UNSUPPORTED"]
+    assert lib.pkv_decode_step(p8, *head, 24, 16, *tail) == S["PKV_ERR_INVALID_ARG"]
+    p96 = ctypes.byref(_pool(dtype=2, num_kv_heads=2, head_dim=96))
+    assert lib.pkv_decode_step(p96, *head, 16, 16, *tail) == S["PKV_ERR_UNSUPPORTED"]
     assert lib.pkv_decode_step(p, 3, *head[1:], 16, 16, *tail) == S["PKV_ERR_INVALID_ARG"]
 
 

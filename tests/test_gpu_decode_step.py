@@ -206,3 +206,78 @@ def test_decode_step_bad_block_is_skipped_and_reported(dev):
                                    np.array([lens[0] - 1], dtype=np.int32), 16)
     oracle.write_slots(kh, vh, w.layer, to_numpy_bits(kn)[seqs], to_numpy_bits(vn)[seqs], sm)
     assert np.array_equal(to_numpy_bits(k), kh) and np.array_equal(to_numpy_bits(v), vh)
+
+
+I8_CASES = [
+    # H, G, D, bs, lens, ctas
+    (8, 4, 128, 16, [300, 37, 129, 1, 16, 17], 0),
+    (2, 2, 64, 8, [90, 0, 33, 7], 0),
+    (4, 4, 128, 16, [700, 333, 64, 5], 5),
+]
+
+
+@pytest.mark.parametrize("H,G,D,bs,lens,ctas", I8_CASES,
+                         ids=[f"i8-H{c[0]}G{c[1]}D{c[2]}-bs{c[3]}-ctas{c[5]}" for c in I8_CASES])
+def test_decode_step_int8_matches_oracle(dev, H, G, D, bs, lens, ctas):
+    """int8 pools: the new rows are quantised into the pool exactly as the
+    oracle's quantising scatter does (bit-exact), and attention over the
+    dequantised pool matches within the bf16 tolerance."""
+    from oracle import quant as Q
+    from workloads import PoolSpec, fill_pool_i8
+    seed = 101 + len(lens) + ctas
+    w = _case(seed, "bf16", H, D, bs, lens)
+    spec = PoolSpec(w.pool.num_blocks, w.pool.num_layers, bs, H, D, "i8")
+    k = torch.zeros(spec.shape, dtype=torch.uint8, device=dev)
+    v = torch.zeros_like(k)
+    fill_pool_i8(k, v, spec, w.layer, seed)
+    kh, vh = to_numpy_bits(k), to_numpy_bits(v)
+    B = len(lens)
+    kn = rand_rows((B, H, D), "bf16", seed + 1, dev)
+    vn = rand_rows((B, H, D), "bf16", seed + 2, dev)
+    q = rand_rows((B, H * G, D), "bf16", seed + 3, dev)
+    pool = pkv.Pool(k, v, H, D)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device=dev)
+    pkv.set_decode_ctas(ctas)
+    try:
+        out = _step(pool, w, q, kn, vn, lens_t, dev)
+        torch.cuda.synchronize()
+    finally:
+        pkv.set_decode_ctas(0)
+    seqs = np.array([b for b in range(B) if lens[b] > 0], dtype=np.int32)
+    pos = np.array([lens[b] - 1 for b in seqs], dtype=np.int32)
+    sm = oracle.build_slot_mapping(w.batch.block_tables, w.batch.offsets, seqs, pos, bs)
+    Q.write_slots_i8(kh, vh, w.layer, to_numpy_bits(kn)[seqs], to_numpy_bits(vn)[seqs], sm, H, D)
+    assert np.array_equal(to_numpy_bits(k), kh) and np.array_equal(to_numpy_bits(v), vh)
+    ref = Q.decode_attention_i8(kh, vh, w.layer, to_numpy_bits(q), w.batch.block_tables,
+                                np.asarray(lens), w.batch.offsets, w.scale)
+    assert max_abs(widen_out(out), ref) <= 2e-2
+    assert pkv.device_error() == "PKV_OK"
+
+
+def test_decode_step_int8_equals_append_then_decode(dev):
+    from workloads import PoolSpec, fill_pool_i8
+    lens = [2048, 517, 1, 64, 1000, 33, 4095, 16]
+    H, D, bs = 8, 128, 16
+    w = _case(171, "bf16", H, D, bs, lens)
+    spec = PoolSpec(w.pool.num_blocks, w.pool.num_layers, bs, H, D, "i8")
+    k = torch.zeros(spec.shape, dtype=torch.uint8, device=dev)
+    v = torch.zeros_like(k)
+    fill_pool_i8(k, v, spec, w.layer, 171)
+    k2, v2 = k.clone(), v.clone()
+    B = len(lens)
+    kn = rand_rows((B, H, D), "bf16", 172, dev)
+    vn = rand_rows((B, H, D), "bf16", 173, dev)
+    q = rand_rows((B, 4 * H, D), "bf16", 174, dev)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device=dev)
+    out = _step(pkv.Pool(k, v, H, D), w, q, kn, vn, lens_t, dev)
+    bt, _, offs, _ = dev_batch(w.batch, dev)
+    pool2 = pkv.Pool(k2, v2, H, D)
+    seq = torch.arange(B, dtype=torch.int32, device=dev)
+    pkv.append_tokens(pool2, w.layer, bt, offs, seq, lens_t - 1, kn, vn, None)
+    out2 = torch.empty_like(q)
+    ws = torch.empty(pkv.decode_workspace_size(B, q.shape[1], D, dev), dtype=torch.uint8,
+                     device=dev)
+    pkv.decode_attention(pool2, w.layer, q, w.scale, bt, lens_t, offs, out2, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(k, k2) and torch.equal(v, v2)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
