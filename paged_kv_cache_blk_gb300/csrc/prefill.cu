@@ -219,12 +219,15 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
       x[j] = f;
     }
   };
-  // P of one chunk against the maximum mu as bf16 pairs, and their sum
+  // P of one chunk against the maximum mu as bf16 pairs, and their sum (a row
+  // with no maximum yet uses 0; a finite score then raises it and this P is
+  // recomputed)
   auto p_chunk = [&](const float (&x)[32], float mu, uint32_t (&w)[16]) {
     float psum = 0.f;
+    const float ms = mu == -INFINITY ? 0.f : mu;
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      const float y0 = fmaf(x[2 * e], qe, -mu), y1 = fmaf(x[2 * e + 1], qe, -mu);
+      const float y0 = fmaf(x[2 * e], qe, -ms), y1 = fmaf(x[2 * e + 1], qe, -ms);
       const float a0 = exp2f(y0), a1 = exp2f(y1);
       psum += a0 + a1;
       w[e] = pack_bf16x2(a0, a1);
@@ -251,14 +254,16 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
   // S(t) was issued after it and its commit (the "S ready" barrier) covers
   // every earlier product.
   float psum = 0.f, alpha = 1.f;
-  const bool first = st.m_used == -INFINITY;  // this row has no maximum yet
-  if (!__any_sync(0xffffffffu, first)) {
+  {
     // One pass against the maximum in use.  Each chunk's maximum is checked
-    // before its P is stored: a row whose chunk maximum lies more than 8
-    // above the maximum in use raises it to that chunk maximum, scales the P
-    // it stored for earlier chunks (bf16, in place) and their sum by
+    // before its P is kept: a row whose chunk maximum lies more than 8 above
+    // the maximum in use raises it to that chunk maximum, scales the P it
+    // stored for earlier chunks (bf16, in place) and their sum by
     // 2^(old - new), and recomputes the chunk's P.  So no stored P exceeds
-    // 2^8 and no exponential overflows, however far a later score jumps.
+    // 2^8 and no exponential overflows, however far a later score jumps.  A
+    // row with no maximum yet (-inf: its first tile) takes the first chunk
+    // holding one of its keys as its maximum the same way (its earlier P are
+    // zeros); a padding row, all keys masked, keeps P = 0 throughout.
     float mu = st.m_used;
 #pragma unroll 1
     for (int c0 = 0; c0 < kKeys; c0 += 32) {
@@ -281,7 +286,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
       tmem_st16(tS + lane_base + (c0 >> 1), w);
       if (__any_sync(0xffffffffu, cm > mu + 8.f)) {
         const float nm = cm > mu + 8.f ? cm : mu;
-        const float beta = exp2f(mu - nm);  // 1 for rows that keep their maximum
+        const float beta = nm == mu ? 1.f : exp2f(mu - nm);
         mu = nm;
         psum *= beta;
         alpha *= beta;
@@ -304,36 +309,6 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
       psum += ps;
     }
     st.m_used = mu;
-  } else {
-    // some row still needs its first maximum: find the maxima first, then P
-    float mt = -INFINITY;
-#pragma unroll 1
-    for (int c0 = 0; c0 < kKeys; c0 += 32) {
-      float x[32];
-      load_chunk(c0, x);
-      mt = fmaxf(mt, chunk_max(x));
-    }
-    const float mt_s = mt * qe;
-    if (first) {
-      // a real row finds its first keys in tile 0 (nothing accumulated yet); a
-      // padding row (all keys masked) keeps P = 0 and is never written out
-      if (mt_s != -INFINITY) {
-        st.m_used = mt_s;
-        alpha = 0.f;
-      }
-    } else if (mt_s > st.m_used + 8.f) {
-      alpha = exp2f(st.m_used - mt_s);
-      st.m_used = mt_s;
-    }
-    const float mu = st.m_used == -INFINITY ? 0.f : st.m_used;
-#pragma unroll 1
-    for (int c0 = 0; c0 < kKeys; c0 += 32) {
-      float x[32];
-      load_chunk(c0, x);
-      uint32_t w[16];
-      psum += p_chunk(x, mu, w);
-      tmem_st16(tS + lane_base + (c0 >> 1), w);
-    }
   }
   if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
