@@ -15,7 +15,7 @@ Restated from:
   can_allocate; decode_append adds a slot to the last block while it has
   room, else allocates a new block), §3 (fragmentation ratio).
 
-Readings where the pages are silent (also listed in the design doc):
+Readings where the pages are silent:
 * A released block goes to the right end of the free deque (deque
   semantics: popleft to allocate, append to release).
 * Appending tokens to a sequence first fills its last block, then takes

@@ -22,7 +22,7 @@ block_size, num_kv_heads, head_dim]``; bf16 pools hold the raw uint16 bit
 patterns and fp32 pools hold float32, so copies are bit copies.  Attention
 widens the stored values exactly to fp64 and works in fp64 throughout.
 
-Readings where the pages are silent (each one also listed in the design doc):
+Readings where the pages are silent:
 
 * Logical token ``i`` of a sequence with first-block offset ``off`` sits at
   table position ``p = off + i``; its block is ``table[p // bs]`` and its row

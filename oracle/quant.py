@@ -7,8 +7,7 @@ import it.  It imports nothing from the CUDA library.
 What the pages fix.  "mini-runtime ch.12 Paged KV Cache", §6 Evolution, names
 quantised KV (int8 / int4) as the step that follows paged KV: the same block
 pool holding fewer bytes per token.  The pages give no scheme.  The readings
-taken here are the plainest ones that keep every other step unchanged (each is
-also listed in the design doc):
+taken here are the plainest ones that keep every other step unchanged:
 
 * Granularity: one scale per (token, kv head), so that a token row is written
   once by the scatter and never rewritten, and a block copy or swap still
