@@ -16,7 +16,7 @@
 //    G + head).  The CTA owns two tiles, A and B, that share the K/V stream.
 //  * Keys in tiles of 128 table positions (128 / bs whole blocks).  K(t) and
 //    V(t) are loaded by TMA (one box per block and 64-column half, 128B
-//    swizzle) into a 5-slot ring in the order K0 V0 K1 V1 ...; invalid table
+//    swizzle) into a 4-slot ring in the order K0 V0 K1 V1 ...; invalid table
 //    entries load zeros.
 //  * Warp 9 issues S_x = Q_x K^T (M 128, N 128, K 128: 8 tcgen05.mma, fp32
 //    in TMEM) and O_x += P_x V (V is the MN-major operand) in the order
@@ -53,7 +53,7 @@ constexpr int kKeys = 128;   // keys per KV tile (MMA N of Q K^T, K of P V)
 constexpr int kD = 128;      // head_dim
 constexpr int kHalf = 128 * 64 * 2;  // one 128-row x 64-column bf16 half tile (16 KB)
 constexpr int kTileBytes = 2 * kHalf;  // 32 KB
-constexpr int kSlots = 5;              // K / V ring: K(t) V(t) .. two tiles ahead
+constexpr int kSlots = 4;              // K / V ring: K(t) V(t) K(t+1) V(t+1)
 constexpr uint32_t kTmemCols = 512;    // S_A, S_B, O_A, O_B
 constexpr float kLog2e = 1.4426950408889634f;
 
