@@ -627,6 +627,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tmem_ld32(tO(x) + lane_base + c0, v);
         tmem_wait_ld();
         if (row_ok) {
+          if ((reinterpret_cast<uintptr_t>(p.out) & 31) == 0) {
+            // 32-byte stores (full sectors) when the output allows them
+#pragma unroll
+            for (int j = 0; j < 32; j += 16) {
+              uint32_t o[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                o[k] = pack_bf16x2(__uint_as_float(v[j + 2 * k]) * inv,
+                                   __uint_as_float(v[j + 2 * k + 1]) * inv);
+              asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(orow + c0 + j),
+                           "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]),
+                           "r"(o[6]), "r"(o[7])
+                           : "memory");
+            }
+          } else {
 #pragma unroll
           for (int j = 0; j < 32; j += 8) {
             uint4 o;
@@ -635,6 +650,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             o.z = pack_bf16x2(__uint_as_float(v[j + 4]) * inv, __uint_as_float(v[j + 5]) * inv);
             o.w = pack_bf16x2(__uint_as_float(v[j + 6]) * inv, __uint_as_float(v[j + 7]) * inv);
             *reinterpret_cast<uint4*>(orow + c0 + j) = o;
+          }
           }
         }
       }

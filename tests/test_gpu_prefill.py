@@ -184,3 +184,21 @@ def test_prefill_bench_workloads_sampled(dev, kind):
     err = max(float(np.max(np.abs(got[t_, h] - r))) for (t_, h), r in ref.items())
     assert err <= 2e-2, err
     assert pkv.device_error() == "PKV_OK"
+
+
+def test_prefill_output_16_byte_aligned_only(dev):
+    """An output that is 16-byte but not 32-byte aligned takes the 16-byte
+    store path and gives the same result."""
+    spec, batch, cu, k, v, q, layer = _case(dev, 61, [300, 130], [300, 64], 4)
+    pool = pkv.Pool(k, v)
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+    args = (t(batch.block_tables, torch.int32), t(batch.seq_lens, torch.int32),
+            t(batch.offsets, torch.int32), t(cu, torch.int64), 300)
+    out = torch.empty_like(q)
+    pkv.prefill_attention(pool, layer, q, 128 ** -0.5, *args[:4], args[4], out)
+    buf = torch.empty(q.numel() + 8, dtype=q.dtype, device=dev)
+    out2 = buf[8:].view(q.shape)
+    assert out2.data_ptr() % 32 == 16
+    pkv.prefill_attention(pool, layer, q, 128 ** -0.5, *args[:4], args[4], out2)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
