@@ -41,6 +41,18 @@ __device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap* m, int x
       : "memory");
 }
 
+// The same 4-D copy delivered to the same shared-memory offset, with its
+// completion counted on the mbarrier at the same offset, in every CTA of the
+// cluster named in cta_mask (a load from this GPU's own memory).
+__device__ __forceinline__ void tma_4d_mc(uint32_t dst, const CUtensorMap* m, int x, int y, int z,
+                                          int w, uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"((uint64_t)m), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "h"(cta_mask)
+      : "memory");
+}
+
 // Encode a tiled tensor map (element strides 1, no interleave, 256-byte L2
 // promotion, zero fill out of range).  strides[i] is the byte stride of
 // dimension i + 1.  False when the driver entry point is missing or refuses
