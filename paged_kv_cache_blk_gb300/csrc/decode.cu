@@ -150,6 +150,25 @@ __device__ __forceinline__ void load_pv(const char* p, float (&f)[PVE]) {
   }
 }
 
+// Stores of the split-K states and the block prefix sums, which the combine
+// reads after the whole K/V stream has passed through L2: the evict_last
+// policy keeps them there instead of letting the stream push them to DRAM.
+__device__ __forceinline__ uint64_t l2_keep_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void st_keep(float* a, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(a), "f"(v), "l"(pol)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_keep(long long* a, long long v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.s64 [%0], %1, %2;" ::"l"(a), "l"(v), "l"(pol)
+               : "memory");
+}
+
 template <typename T>
 __device__ __forceinline__ void store_elem(void* base, long long idx, float x) {
   if constexpr (sizeof(T) == 2) {
@@ -466,14 +485,15 @@ __device__ __forceinline__ bool mma_segment_end(const Params& p, const Pipe& pp,
                                     o[kt][2 + hh] * inv);
         }
       } else {
+        const uint64_t pol = l2_keep_policy();
 #pragma unroll
         for (int kt = 0; kt < KS; ++kt) {
-          p.ws_acc[row_ws * D + kt * 16 + gl] = o[kt][hh];
-          p.ws_acc[row_ws * D + kt * 16 + gl + 8] = o[kt][2 + hh];
+          st_keep(p.ws_acc + row_ws * D + kt * 16 + gl, o[kt][hh], pol);
+          st_keep(p.ws_acc + row_ws * D + kt * 16 + gl + 8, o[kt][2 + hh], pol);
         }
         if (gl == 0) {
-          p.ws_ml[row_ws * 2] = Mh;
-          p.ws_ml[row_ws * 2 + 1] = Lh;
+          st_keep(p.ws_ml + row_ws * 2, Mh, pol);
+          st_keep(p.ws_ml + row_ws * 2 + 1, Lh, pol);
         }
       }
     }
@@ -1130,11 +1150,13 @@ __device__ void run_consumer_fma(const Params& p, const Pipe& pp, int warp, int 
             for (int e = 0; e < C::PVE; ++e)
               store_elem<T>(p.out, row_out * D + lane * C::PVE + e, acc[hh][e] * inv);
           } else {
+            const uint64_t pol = l2_keep_policy();
 #pragma unroll
-            for (int e = 0; e < C::PVE; ++e) p.ws_acc[row_ws * D + lane * C::PVE + e] = acc[hh][e];
+            for (int e = 0; e < C::PVE; ++e)
+              st_keep(p.ws_acc + row_ws * D + lane * C::PVE + e, acc[hh][e], pol);
             if (lane == 0) {
-              p.ws_ml[row_ws * 2] = mh[hh];
-              p.ws_ml[row_ws * 2 + 1] = lh[hh];
+              st_keep(p.ws_ml + row_ws * 2, mh[hh], pol);
+              st_keep(p.ws_ml + row_ws * 2 + 1, lh[hh], pol);
             }
           }
         }
@@ -1208,8 +1230,12 @@ __global__ void __launch_bounds__((consumer_warps<T>() + 1) * 32, 1)
   const long long x0 = min(total, (long long)blockIdx.x * W);
   const long long x1 = min(total, x0 + W);
   if (blockIdx.x == 0) {
-    for (int b = tid; b <= B; b += kThreads) p.ws_cu[b] = s_cu[b];
-    if (tid == 0) { p.ws_meta[0] = W; p.ws_meta[1] = total; }
+    const uint64_t pol = l2_keep_policy();
+    for (int b = tid; b <= B; b += kThreads) st_keep(p.ws_cu + b, s_cu[b], pol);
+    if (tid == 0) {
+      st_keep(p.ws_meta, W, pol);
+      st_keep(p.ws_meta + 1, total, pol);
+    }
   }
   if (x0 >= x1) return;
 
@@ -1278,8 +1304,10 @@ __global__ void __launch_bounds__((consumer_warps<T>() + 1) * 32, 1)
 
 // Merge the partial states of every segment of a sequence, one thread per
 // output element (sequence, q head, d); sequences handled by a single CTA were
-// written by the partial pass already.  Segments are read eight at a time so
-// the loads of a batch are in flight together.  Grid: (ceil(hq*D / 256), batch).
+// written by the partial pass already.  One pass over the segments, eight at a
+// time with all their loads in flight together, keeps a running maximum and
+// rescales the sums when it rises.  The loads are marked evict-first: the
+// states are dead once read.  Grid: (ceil(hq*D / 256), batch).
 template <typename T>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const float* __restrict__ ws_acc,
                                                              const float* __restrict__ ws_ml,
@@ -1291,13 +1319,13 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float* __rest
   const int b = blockIdx.y;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= hq * D) return;
-  const long long c0 = ws_cu[b], c1 = ws_cu[b + 1];
+  const long long c0 = __ldcs(ws_cu + b), c1 = __ldcs(ws_cu + b + 1);
+  const long long W = __ldcs(ws_meta);
   T* o = out + (long long)b * hq * D;
   if (c1 <= c0) {  // no tokens (or an invalid sequence): zeros
     o[i] = T(0.f);
     return;
   }
-  const long long W = ws_meta[0];
   const long long cf = c0 / W, cl = (c1 - 1) / W;
   if (cf == cl) return;
   const int n = (int)(cl - cf + 1);
@@ -1306,33 +1334,31 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float* __rest
   const float* mlp = ws_ml + ((cf + b) * hq + h) * 2;
   const float* accp = ws_acc + ((cf + b) * hq + h) * D + d;
   constexpr int U = 8;
-  float M = -INFINITY;
+  float M = -INFINITY, num = 0.f, den = 0.f;
   for (int k0 = 0; k0 < n; k0 += U) {
-    float mv[U];
+    float mv[U], lv[U], av[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) mv[u] = k0 + u < n ? mlp[(k0 + u) * ml_stride] : -INFINITY;
-#pragma unroll
-    for (int u = 0; u < U; ++u) M = fmaxf(M, mv[u]);
-  }
-  float num = 0.f, den = 0.f;
-  if (M != -INFINITY) {
-    for (int k0 = 0; k0 < n; k0 += U) {
-      float mv[U], lv[U], av[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const bool in = k0 + u < n;
-        mv[u] = in ? mlp[(k0 + u) * ml_stride] : -INFINITY;
-        lv[u] = in ? mlp[(k0 + u) * ml_stride + 1] : 0.f;
-        av[u] = in ? accp[(k0 + u) * acc_stride] : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (mv[u] == -INFINITY) continue;
-        const float w = exp2f(mv[u] - M);
-        num += w * av[u];
-        den += w * lv[u];
-      }
+    for (int u = 0; u < U; ++u) {
+      const bool in = k0 + u < n;
+      mv[u] = in ? __ldcs(mlp + (k0 + u) * ml_stride) : -INFINITY;
+      lv[u] = in ? __ldcs(mlp + (k0 + u) * ml_stride + 1) : 0.f;
+      av[u] = in ? __ldcs(accp + (k0 + u) * acc_stride) : 0.f;
     }
+    float bm = M;
+#pragma unroll
+    for (int u = 0; u < U; ++u) bm = fmaxf(bm, mv[u]);
+    if (bm == -INFINITY) continue;
+    const float r = exp2f(M - bm);  // 0 while M is still -inf (the sums are 0 then)
+    num *= r;
+    den *= r;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (mv[u] == -INFINITY) continue;
+      const float w = exp2f(mv[u] - bm);
+      num += w * av[u];
+      den += w * lv[u];
+    }
+    M = bm;
   }
   o[i] = T(den > 0.f ? num / den : 0.f);
 }
