@@ -71,6 +71,10 @@ CASES = [
     (4, 8, [250], [250]),
     (4, 128, [600, 1], [300, 1]),
     (4, 64, [513, 128, 129], [513, 1, 2]),
+    # CTA pairs: odd and even pair counts side by side (a pair's second CTA
+    # without an item of its own), and one box per 64-column half per tile
+    (4, 16, [1000, 520, 33, 95], [1000, 520, 33, 95]),
+    (2, 128, [1500, 700], [900, 700]),
 ]
 
 
