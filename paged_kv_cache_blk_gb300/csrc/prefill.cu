@@ -34,7 +34,9 @@
 //    pairs over the S columns in TMEM, the A operand of the second MMA.
 //  * Epilogue: O row / l -> bf16 -> global (only rows that are real queries).
 // Every wait is bounded; on a timeout the CTA records the error, drains its
-// MMAs and frees its TMEM before returning.
+// MMAs, waits (bounded) for the last use of every ring slot and frees its
+// TMEM; the two CTAs of a cluster then meet at a cluster barrier, so neither
+// leaves while the other may still address its shared memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
