@@ -329,7 +329,8 @@ def test_decode_pairs_match_full():
         np.testing.assert_allclose(x, full[b, h], atol=1e-13)
 
 
-def test_split_combine_equals_direct():
+def check_split_combine(combine):
+    """Any split of the tokens, merged, equals direct attention."""
     rng = np.random.default_rng(12)
     D = 16
     for n in (1, 2, 17, 100):
@@ -339,9 +340,13 @@ def test_split_combine_equals_direct():
         direct = O.attention_fp64(q, k, v, 0.9)
         for nsplit in (1, 2, 3, 7, n):
             cuts = sorted(set([0, n] + list(rng.integers(0, n + 1, size=nsplit - 1))))
-            got = O.combine_partials(O.split_partials(q, k, v, 0.9, cuts), D)
+            got = combine(O.split_partials(q, k, v, 0.9, cuts), D)
             np.testing.assert_allclose(got, direct, atol=1e-13)
-    assert np.array_equal(O.combine_partials([], 4), np.zeros(4))
+    assert np.array_equal(combine([], 4), np.zeros(4))
+
+
+def test_split_combine_equals_direct():
+    check_split_combine(O.combine_partials)
 
 
 def test_widen_bf16_bits():
@@ -429,6 +434,44 @@ def _decode_with(attn=None, gqa_mod=False):
     return f
 
 
+def _prefill_with(extra_keys=0, first_positions=False, gqa_mod=False):
+    """A copy of the prefill oracle with one mistake planted."""
+    def f(k_cache, v_cache, layer, q, bt, lens, offs, cu, scale):
+        T, Hq, D = q.shape
+        Hkv = k_cache.shape[3]
+        out = np.zeros((T, Hq, D))
+        for b in range(len(lens)):
+            n, L = int(cu[b + 1] - cu[b]), int(lens[b])
+            if n == 0:
+                continue
+            kb = O.widen(O.gather_loop(k_cache, layer, bt[b], L, int(offs[b])))
+            vb = O.widen(O.gather_loop(v_cache, layer, bt[b], L, int(offs[b])))
+            for i in range(n):
+                P = i if first_positions else L - n + i
+                hi = min(L, P + 1 + extra_keys)
+                for h in range(Hq):
+                    g = h % Hkv if gqa_mod else h // (Hq // Hkv)
+                    out[cu[b] + i, h] = O.attention_fp64(O.widen(q[cu[b] + i, h]), kb[:hi, g],
+                                                         vb[:hi, g], scale)
+        return out
+    return f
+
+
+def _combine_unweighted(parts, head_dim):
+    if not parts:
+        return np.zeros(head_dim)
+    return sum(acc for _, _, acc in parts) / sum(l for _, l, _ in parts)
+
+
+def _combine_weight_sign(parts, head_dim):
+    if not parts:
+        return np.zeros(head_dim)
+    M = max(m for m, _, _ in parts)
+    num = sum(math.exp(M - m) * acc for m, _, acc in parts)
+    den = sum(math.exp(M - m) * l for m, l, _ in parts)
+    return num / den
+
+
 PLANTED = [
     ("slot ignores offset", lambda: check_slot_walk(_slot_no_offset)),
     ("slot quotient/remainder swapped", lambda: check_slot_walk(_slot_swapped)),
@@ -445,6 +488,12 @@ PLANTED = [
     ("attention unnormalised", lambda: check_attention_closed_forms(_attn_unnormalised)),
     ("attention reads K for V", lambda: check_attention_closed_forms(_attn_keys_for_values)),
     ("GQA head map h % Hkv", lambda: check_attention_vs_sdpa(_decode_with(gqa_mod=True))),
+    ("prefill mask admits the next key", lambda: check_prefill_vs_sdpa(_prefill_with(extra_keys=1))),
+    ("prefill queries at the first positions",
+     lambda: check_prefill_vs_sdpa(_prefill_with(first_positions=True))),
+    ("prefill GQA head map h % Hkv", lambda: check_prefill_vs_sdpa(_prefill_with(gqa_mod=True))),
+    ("combine without the max weights", lambda: check_split_combine(_combine_unweighted)),
+    ("combine weights with the sign flipped", lambda: check_split_combine(_combine_weight_sign)),
 ]
 
 
@@ -523,11 +572,12 @@ def _prefill_case(rng, group=2, B=3, maxlen=40):
     return k, v, q, bt, lens, offs, cu
 
 
-def test_prefill_vs_sdpa_with_explicit_causal_mask():
+def check_prefill_vs_sdpa(prefill):
+    """Prefill equals SDPA with a bottom-right aligned causal mask."""
     rng = np.random.default_rng(15)
     for group in (1, 2, 4):
         k, v, q, bt, lens, offs, cu = _prefill_case(rng, group=group)
-        got = O.prefill_attention(k, v, 1, q, bt, lens, offs, cu, 0.31)
+        got = prefill(k, v, 1, q, bt, lens, offs, cu, 0.31)
         for b in range(len(lens)):
             n, L = int(cu[b + 1] - cu[b]), int(lens[b])
             if n == 0:
@@ -542,6 +592,10 @@ def test_prefill_vs_sdpa_with_explicit_causal_mask():
             ref = torch.nn.functional.scaled_dot_product_attention(
                 qt, kt, vt, attn_mask=mask, scale=0.31).permute(1, 0, 2).numpy()
             np.testing.assert_allclose(got[cu[b]:cu[b + 1]], ref, rtol=0, atol=1e-12)
+
+
+def test_prefill_vs_sdpa_with_explicit_causal_mask():
+    check_prefill_vs_sdpa(O.prefill_attention)
 
 
 def test_prefill_rows_vs_sdpa():
