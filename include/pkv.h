@@ -279,11 +279,11 @@ PKV_API pkv_status pkv_prefill_attention(const pkv_pool* pool, int32_t layer, co
  * loads the library until the process exits).
  *
  * It is meant for callers that cannot allocate device memory where they run
- * decode attention: code that runs while a stream is being captured in
- * global capture mode (cudaMalloc is refused there), serving hosts and
- * plugin runtimes that own all device memory and forbid allocation on the
- * hot path, and plain C programs that link only this library and have no
- * device allocator for scratch.  The call itself allocates nothing.
+ * decode attention: serving processes whose memory manager reserves the
+ * GPU's memory up front and hands out nothing on the hot path, plugin
+ * runtimes whose execute step must not allocate, and plain C programs that
+ * link only this library and have no device allocator for scratch.  The call
+ * itself allocates nothing.
  *
  * Limits and rules:
  *   - A shape whose scratch (pkv_decode_workspace_size for the same batch,
@@ -349,6 +349,34 @@ PKV_API pkv_status pkv_set_decode_ctas(int32_t num_ctas);
  * kernel alone with cudaEventElapsedTime.  Events are the caller's (created
  * with timing enabled); pass NULLs to stop recording.  Process-wide. */
 PKV_API pkv_status pkv_set_decode_events(cudaEvent_t start, cudaEvent_t stop);
+
+/* Bound on every device-side wait of the kernels (mbarrier waits between the
+ * copy, tensor-core and softmax warps of one CTA), in nanoseconds of the GPU's
+ * global timer; 0 restores the default (4 s).  Accepted range 1 us .. 60 s,
+ * else PKV_ERR_INVALID_ARG.  A healthy wait lasts microseconds; the bound only
+ * ends waits that can never complete.  The first wait of a launch to reach it
+ * sets the timeout bit of the device error word (PKV_ERR_TIMEOUT in validate
+ * mode or from pkv_device_error); every other pending wait of that launch
+ * then gives up within a few polls, so the whole launch ends about one bound
+ * after it stalled.  Copies a CTA has issued are always waited for (with the
+ * default bound) before it exits.  The timeout bit stays set until cleared
+ * (pkv_device_error with clear != 0, or a validate-mode call that reports
+ * it).  Each launch carries its own number, so a give-up never cuts short a
+ * later launch; the one exception is a launch replayed from a CUDA graph,
+ * which keeps the number it was captured with: after such a replay gave up,
+ * clear the error word before the next replay.  Process-wide; read at each
+ * launch. */
+PKV_API pkv_status pkv_set_wait_limit_ns(uint64_t ns);
+PKV_API uint64_t pkv_get_wait_limit_ns(void);
+
+/* Test hook for the give-up path, process-wide, default 0 (off).  With
+ * mode 1 the first CTA, with mode 2 every CTA, of each decode partial pass
+ * leaves its first pipeline stage unfilled, and of each prefill launch its
+ * first K tile unloaded: nothing is copied into them, so the waits on them
+ * can only give up at the wait bound.  Results of such launches are not
+ * valid; the call reports PKV_ERR_TIMEOUT in validate mode.  Other modes:
+ * PKV_ERR_INVALID_ARG.  Never needed outside tests. */
+PKV_API pkv_status pkv_set_debug_skip_fill(int32_t mode);
 
 /* Validate mode (process-wide, default off): see "Errors" above. */
 PKV_API pkv_status pkv_set_validate(int32_t on);

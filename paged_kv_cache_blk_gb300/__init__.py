@@ -19,13 +19,16 @@ from ._binding import (  # noqa: F401
     device_error,
     gather,
     get_validate,
+    get_wait_limit_ns,
     int8_row_bytes,
     library_path,
     load,
     prefill_attention,
     set_decode_ctas,
+    set_debug_skip_fill,
     set_decode_events,
     set_validate,
+    set_wait_limit_ns,
     status_string,
     swap_in,
     swap_out,

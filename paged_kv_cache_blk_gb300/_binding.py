@@ -70,6 +70,9 @@ _SIGS = {
     "pkv_set_decode_ctas": (_I32, [_I32]),
     "pkv_set_decode_events": (_I32, [_P, _P]),
     "pkv_set_validate": (_I32, [_I32]),
+    "pkv_set_wait_limit_ns": (_I32, [ctypes.c_uint64]),
+    "pkv_get_wait_limit_ns": (ctypes.c_uint64, []),
+    "pkv_set_debug_skip_fill": (_I32, [_I32]),
     "pkv_get_validate": (_I32, []),
     "pkv_device_error": (_I32, [ctypes.POINTER(ctypes.c_int32), _I32]),
     "pkv_alloc_create": (_I32, [_I64, _I32, _P, ctypes.POINTER(ctypes.c_void_p)]),
@@ -367,6 +370,22 @@ def set_decode_events(start: Optional[torch.cuda.Event], stop: Optional[torch.cu
 
 def set_validate(on: bool) -> None:
     _check(load().pkv_set_validate(1 if on else 0), "pkv_set_validate")
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Bound of every device-side wait in nanoseconds (0 = the default)."""
+    _check(load().pkv_set_wait_limit_ns(int(ns)), "pkv_set_wait_limit_ns")
+
+
+def get_wait_limit_ns() -> int:
+    return int(load().pkv_get_wait_limit_ns())
+
+
+def set_debug_skip_fill(mode: int) -> None:
+    """Test hook: with 1 the first CTA, with 2 every CTA, of each decode /
+    prefill launch leaves its first stage unfilled, so a wait there can only
+    give up; 0 turns it off."""
+    _check(load().pkv_set_debug_skip_fill(int(mode)), "pkv_set_debug_skip_fill")
 
 
 def get_validate() -> bool:

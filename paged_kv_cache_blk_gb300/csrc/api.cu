@@ -11,14 +11,19 @@
 
 namespace {
 
-// Sticky device error word (one per device context); kernels OR pkv::kErr*
-// bits into it through the pointer obtained for the current device.
-__device__ int g_pkv_error_word;
+// Per device context: [0] the sticky error word, into which kernels OR
+// pkv::kErr* bits through the pointer obtained for the current device;
+// [1] the abort word, holding the number of the last launch whose bounded
+// wait gave up (see pkv::WaitCtl).  Both are cleared together.
+__device__ int g_pkv_error_word[2];
 
 std::atomic<int> g_validate{0};
 std::atomic<int> g_decode_ctas{0};
 std::atomic<cudaEvent_t> g_ev_start{nullptr};
 std::atomic<cudaEvent_t> g_ev_stop{nullptr};
+std::atomic<unsigned long long> g_wait_ns{0};
+std::atomic<int> g_skip_fill{0};
+std::atomic<unsigned> g_epoch{0};
 
 constexpr int kMaxDevices = 64;
 
@@ -122,7 +127,7 @@ pkv_status read_and_clear(int* err, cudaStream_t s) {
     return PKV_ERR_CUDA;
   }
   if (h != 0) {
-    if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess ||
+    if (cudaMemsetAsync(err, 0, 2 * sizeof(int), s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {
       cudaGetLastError();
       return PKV_ERR_CUDA;
@@ -132,7 +137,7 @@ pkv_status read_and_clear(int* err, cudaStream_t s) {
 }
 
 pkv_status clear_word(int* err, cudaStream_t s) {
-  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) {
+  if (cudaMemsetAsync(err, 0, 2 * sizeof(int), s) != cudaSuccess) {
     cudaGetLastError();
     return PKV_ERR_CUDA;
   }
@@ -169,6 +174,16 @@ int device_facts(int* smem_optin, int** err_word, int* grid, int* validate) {
   *grid = decode_grid(*d);
   *validate = g_validate.load();
   return PKV_OK;
+}
+
+unsigned long long wait_limit_ns() { return g_wait_ns.load(); }
+
+int debug_skip_fill() { return g_skip_fill.load(); }
+
+int next_launch_epoch() {
+  unsigned e = g_epoch.fetch_add(1) + 1;
+  while ((e & 0x7fffffffu) == 0) e = g_epoch.fetch_add(1) + 1;
+  return (int)(e & 0x7fffffffu);
 }
 
 int clear_error_word(int* err, cudaStream_t s) { return clear_word(err, s); }
@@ -460,6 +475,23 @@ pkv_status pkv_set_decode_events(cudaEvent_t start, cudaEvent_t stop) {
   return PKV_OK;
 }
 
+pkv_status pkv_set_wait_limit_ns(uint64_t ns) {
+  if (ns != 0 && (ns < 1000ull || ns > 60000000000ull)) return PKV_ERR_INVALID_ARG;
+  g_wait_ns.store(ns);
+  return PKV_OK;
+}
+
+uint64_t pkv_get_wait_limit_ns(void) {
+  const unsigned long long ns = g_wait_ns.load();
+  return ns ? ns : 4000000000ull;
+}
+
+pkv_status pkv_set_debug_skip_fill(int32_t mode) {
+  if (mode < 0 || mode > 2) return PKV_ERR_INVALID_ARG;
+  g_skip_fill.store(mode);
+  return PKV_OK;
+}
+
 pkv_status pkv_set_validate(int32_t on) {
   g_validate.store(on ? 1 : 0);
   return PKV_OK;
@@ -478,7 +510,7 @@ pkv_status pkv_device_error(pkv_status* status, int32_t clear) {
     cudaGetLastError();
     return PKV_ERR_CUDA;
   }
-  if (clear && h != 0 && cudaMemset(d->err, 0, sizeof(int)) != cudaSuccess) {
+  if (clear && cudaMemset(d->err, 0, 2 * sizeof(int)) != cudaSuccess) {
     cudaGetLastError();
     return PKV_ERR_CUDA;
   }

@@ -16,9 +16,9 @@ enum : int {
   kErrTimeout = 4,   // a bounded mbarrier wait gave up
 };
 
-// Upper bound on a bounded wait, in nanoseconds of %globaltimer.  A healthy
-// wait in these kernels lasts microseconds; this only ends a wait that can
-// never complete.
+// Default bound on one wait, in nanoseconds of %globaltimer.  A healthy wait
+// in these kernels lasts microseconds; this only ends a wait that can never
+// complete.  The host may set a shorter bound (pkv_set_wait_limit_ns).
 constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;
 
 __device__ __forceinline__ void set_error(int* err, int bits) {
@@ -82,30 +82,91 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
-// Wait for the phase of parity `parity` to complete, giving up after
-// kWaitTimeoutNs (or 2^30 polls): on giving up, set kErrTimeout and return
-// false so the caller can leave cleanly.  Polls: for the short waits of the
-// streaming kernels.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
+// How the waits of one kernel launch give up.  Each wait is bounded by
+// limit_ns.  Besides, once any wait of the launch has given up, every other
+// pending wait of that launch leaves within a few polls, so a stuck launch
+// costs about one bound, not one per CTA and wait.  The signal is the abort
+// word that follows the sticky error word in device memory (err[1]): the wait
+// that gives up stores its launch's number there (`epoch`, distinct and
+// nonzero for every launch the host makes), and the others compare it with
+// their own.  A launch therefore never reacts to an earlier launch's give-up.
+struct WaitCtl {
+  int* err;
+  unsigned long long limit_ns;
+  int epoch;
+};
+
+__device__ __forceinline__ int ld_volatile(const int* p) {
+  int v;
+  asm volatile("ld.volatile.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ WaitCtl make_wait_ctl(int* err, unsigned long long limit_ns,
+                                                 int epoch) {
+  WaitCtl w;
+  w.err = err;
+  w.limit_ns = limit_ns ? limit_ns : kWaitTimeoutNs;
+  w.epoch = epoch;
+  return w;
+}
+
+// True once another wait of this launch has given up.
+__device__ __forceinline__ bool launch_gave_up(const WaitCtl& w) {
+  return w.err != nullptr && w.epoch != 0 && ld_volatile(w.err + 1) == w.epoch;
+}
+
+// Record a give-up: the sticky timeout bit, and this launch's number in the
+// abort word so the launch's other waits leave too.
+__device__ __forceinline__ void give_up(const WaitCtl& w) {
+  if (w.err == nullptr) return;
+  atomicOr(w.err, kErrTimeout);
+  if (w.epoch != 0) atomicExch(w.err + 1, w.epoch);
+}
+
+// Wait for the phase of parity `parity` to complete.  On giving up (bound
+// reached, or the launch gave up elsewhere) returns false, the first with
+// kErrTimeout set, so the caller can leave cleanly.  Polls: for the short
+// waits of the streaming kernels.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) break;
+    if ((it & 63u) == 0) {
+      if (global_timer_ns() - t0 > w.limit_ns) break;
+      if (launch_gave_up(w)) return false;
+    }
   }
-  set_error(err, kErrTimeout);
+  give_up(w);
   return false;
 }
 
 // The same bound, sleeping between checks (suspend-time hint): for waits that
 // last as long as a tensor-core product, where a polling warp would take issue
 // slots from the warp working beside it.
-__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, int* err) {
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
+  const uint32_t hint = w.limit_ns < 1000000ull ? 1000u : 100000u;
   for (uint32_t it = 1; it < (1u << 26); ++it) {
-    if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) break;
+    if (mbar_try_wait_sleep(bar, parity, hint)) return true;
+    if (global_timer_ns() - t0 > w.limit_ns) break;
+    if (launch_gave_up(w)) return false;
+  }
+  give_up(w);
+  return false;
+}
+
+// Wait for asynchronous copies this CTA issued to land before it leaves (or
+// re-arms their stage).  Copies complete whatever the other warps do, so this
+// wait ignores the launch's give-up and keeps the default bound.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) break;
   }
   set_error(err, kErrTimeout);
   return false;
@@ -279,6 +340,15 @@ cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num
                            float scale, const int32_t* bt, int mb, const int32_t* lens,
                            const int32_t* offs, const int64_t* cu_q, int batch, long long total_q,
                            int max_q_len, void* out, int* err, int sm_count, cudaStream_t s);
+
+// Process-wide settings of the bounded waits (pkv_set_wait_limit_ns; 0 = the
+// default bound) and the test hook that makes the first CTA of the decode
+// partial pass leave its first pipeline stage unfilled
+// (pkv_set_debug_skip_fill), read by every launch; and the number of the next
+// launch with bounded waits (distinct, nonzero; see WaitCtl).
+unsigned long long wait_limit_ns();
+int debug_skip_fill();
+int next_launch_epoch();
 
 // Current-device facts for entry points defined outside api.cu: dynamic
 // shared memory limit, the sticky error word, the decode grid size and the

@@ -38,8 +38,11 @@
 //    entirely inside this CTA) or the partial state (m, l, acc) to the
 //    workspace; the combine kernel merges partial states with the log-sum-exp
 //    rule  out = sum_c 2^(m_c-M) acc_c / sum_c 2^(m_c-M) l_c.
-//  * Every mbarrier wait is bounded (mbar_wait); a wait that gives up sets the
-//    error word and the warp leaves after the producer has drained its copies.
+//  * Every mbarrier wait is bounded (mbar_wait), and once one CTA gives up the
+//    pending waits of every other CTA leave too.  A wait that gives up sets
+//    the error word and the warp leaves; the producer always waits for every
+//    copy it issued to land before it returns, so no CTA exits with a copy
+//    into its shared memory still in flight.
 #include <cfloat>
 #include <cmath>
 #include <cstring>
@@ -107,6 +110,9 @@ struct Params {
   char* v_out;
   int new_row_bytes;
   int scale_off;
+  unsigned long long wait_ns;  // bound of one wait (0 = the default)
+  int epoch;  // this launch's number (see WaitCtl)
+  int skip_fill;  // test hook: 1 = CTA 0, 2 = every CTA leaves its first stage unfilled
 };
 
 // Tensor maps of an int8 pool (unused for bf16 / fp32 pools): K and V codes
@@ -273,10 +279,11 @@ struct Pipe {
 
 // Reusable barrier over the consumer warps (mbarrier with nw arrivals),
 // bounded like every other wait.
-__device__ __forceinline__ bool group_sync(const Pipe& pp, uint32_t& gph, int lane, int* err) {
+__device__ __forceinline__ bool group_sync(const Pipe& pp, uint32_t& gph, int lane,
+                                           const WaitCtl& w) {
   __syncwarp();
   if (lane == 0) mbar_arrive(pp.group());
-  const bool ok = mbar_wait(pp.group(), gph, err);
+  const bool ok = mbar_wait(pp.group(), gph, w);
   gph ^= 1;
   return ok;
 }
@@ -286,6 +293,7 @@ __device__ __forceinline__ bool group_sync(const Pipe& pp, uint32_t& gph, int la
 template <bool TMA>
 __device__ void run_producer(const Params& p, const Pipe& pp, const I8Maps& maps,
                              const long long* s_cu, int lane, long long x0, long long x1) {
+  const WaitCtl w = make_wait_ctl(p.err, p.wait_ns, p.epoch);
   const int B = p.batch;
   const int ST = p.st;
   int lo = 0, hi = B;  // sequence holding block x0: largest b with s_cu[b] <= x0
@@ -339,7 +347,14 @@ __device__ void run_producer(const Params& p, const Pipe& pp, const I8Maps& maps
         if (seg_end && re == kr1) flags |= kEnd;
         if (kx == x1 - 1 && re == kr1) flags |= kLast;
         if (single) flags |= kSingle;
-        if (!mbar_wait(pp.empty(s), ph, p.err)) { ok = false; break; }
+        if (!mbar_wait(pp.empty(s), ph, w)) { ok = false; break; }
+        if ((p.skip_fill == 2 || (p.skip_fill == 1 && blockIdx.x == 0)) && kx == x0 && rs0 == kr0) {
+          // test hook: this stage is never filled, so the consumers' wait on
+          // it can only give up; nothing is issued into it
+          if (++s == pp.stages) { s = 0; ph ^= 1; }
+          rs0 = re;
+          continue;
+        }
         if constexpr (TMA) {
           // int8 pools: four tensor copies per stage (K and V codes, K and V
           // scales), always whole boxes of st rows starting at row rs0; rows
@@ -383,12 +398,13 @@ __device__ void run_producer(const Params& p, const Pipe& pp, const I8Maps& maps
     }
     bseq = __shfl_sync(kFull, bl, cnt - 1);
   }
-  if (!ok) {
-    // a consumer stopped answering: let the copies already issued land before
-    // the CTA (and its shared memory) goes away
-    for (int t = 0; t < pp.stages; ++t)
-      if (filled & (1u << t)) mbar_wait(pp.full(t), (fill_par >> t) & 1u, p.err);
-  }
+  // Let every copy already issued land before the CTA (and its shared memory)
+  // may go away: the consumers normally waited for them all, but consumers
+  // that gave up did not.  Each stage holds at most one fill in flight (a
+  // stage is refilled only after its consumers released it).
+  for (int t = 0; t < pp.stages; ++t)
+    if (filled & (1u << t)) mbar_wait_drain(pp.full(t), (fill_par >> t) & 1u, p.err);
+  (void)ok;
 }
 
 // End of a segment for the tensor-core consumers: sum the row shares of l,
@@ -399,7 +415,8 @@ template <int D, int G>
 __device__ __forceinline__ bool mma_segment_end(const Params& p, const Pipe& pp, uint32_t& gph,
                                                 float (&o)[D / 16][4], float m0, float m1,
                                                 float l0, float l1, bool mv, int b, int seg,
-                                                int flags, int warp, int lane) {
+                                                int flags, int warp, int lane,
+                                                const WaitCtl& w) {
   constexpr int KS = D / 16;
   const int hkv = p.hkv;
   const int g = warp % hkv;
@@ -430,7 +447,7 @@ __device__ __forceinline__ bool mma_segment_end(const Params& p, const Pipe& pp,
       if (h0 < G) { mw[h0 * (D + 2) + D] = M0; mw[h0 * (D + 2) + D + 1] = L0; }
       if (h1 < G) { mw[h1 * (D + 2) + D] = M1; mw[h1 * (D + 2) + D + 1] = L1; }
     }
-    if (!group_sync(pp, gph, lane, p.err)) return false;
+    if (!group_sync(pp, gph, lane, w)) return false;
     if (wsub == 0) {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -464,7 +481,7 @@ __device__ __forceinline__ bool mma_segment_end(const Params& p, const Pipe& pp,
         if (hh == 0) { M0 = Mx; L0 = Ls; } else { M1 = Mx; L1 = Ls; }
       }
     }
-    if (!group_sync(pp, gph, lane, p.err)) return false;
+    if (!group_sync(pp, gph, lane, w)) return false;
   }
   if (wsub == 0) {
 #pragma unroll
@@ -505,6 +522,7 @@ __device__ __forceinline__ bool mma_segment_end(const Params& p, const Pipe& pp,
 
 template <int D, int G>
 __device__ void run_consumer_mma(const Params& p, const Pipe& pp, int warp, int lane) {
+  const WaitCtl w = make_wait_ctl(p.err, p.wait_ns, p.epoch);
   constexpr int KS = D / 16;  // k-steps of Q.K = m-tiles of P.V
   const int hkv = p.hkv;
   const int g = warp % hkv;
@@ -531,7 +549,7 @@ __device__ void run_consumer_mma(const Params& p, const Pipe& pp, int warp, int 
   int s = 0;
   uint32_t ph = 0, gph = 0;
   while (true) {
-    if (!mbar_wait(pp.full(s), ph, p.err)) return;
+    if (!mbar_wait(pp.full(s), ph, w)) return;
     const int4 dsc = pp.desc[s];
     const int b = dsc.x, n = dsc.y, flags = dsc.z, seg = dsc.w;
     const uint32_t sK = smem_addr(pp.smem + (size_t)s * pp.stage_bytes) + head_off;
@@ -608,7 +626,7 @@ __device__ void run_consumer_mma(const Params& p, const Pipe& pp, int warp, int 
 
     if (flags & kEnd) {
       if (!mma_segment_end<D, G>(p, pp, gph, o, m0, m1, l0, l1, mv, b, seg, flags, warp,
-                                        lane))
+                                        lane, w))
         return;
     }
 
@@ -701,6 +719,7 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
 
 template <int D, int G>
 __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int lane) {
+  const WaitCtl w = make_wait_ctl(p.err, p.wait_ns, p.epoch);
   constexpr int KS = D / 16;  // k-steps of Q.K = m-tiles of P.V
   constexpr int QW = D / 4;   // codes (bytes) of one K row a lane reads
   const int hkv = p.hkv;
@@ -751,7 +770,7 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
   uint32_t ph = 0, gph = 0;
   int turn = 0;  // the wph warps of a kv head take the stages in turn
   while (true) {
-    if (!mbar_wait(pp.full(s), ph, p.err)) return;
+    if (!mbar_wait(pp.full(s), ph, w)) return;
     const int4 dsc = pp.desc[s];
     const int b = dsc.x, flags = dsc.z, seg = dsc.w;
     const int n = turn == wsub ? dsc.y : 0;  // rows this warp processes
@@ -923,7 +942,7 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
         o[kt][3] = (o[kt][3] - vb1) * back;
       }
       if (!mma_segment_end<D, G>(p, pp, gph, o, m0, m1, l0, l1, mv, b, seg, flags, warp,
-                                 lane))
+                                 lane, w))
         return;
     }
 
@@ -950,6 +969,7 @@ struct FmaCfg {
 
 template <typename T, int D, int G>
 __device__ void run_consumer_fma(const Params& p, const Pipe& pp, int warp, int lane) {
+  const WaitCtl w = make_wait_ctl(p.err, p.wait_ns, p.epoch);
   using C = FmaCfg<T, D, G>;
   const int hkv = p.hkv;
   const int g = warp % hkv;
@@ -973,7 +993,7 @@ __device__ void run_consumer_fma(const Params& p, const Pipe& pp, int warp, int 
   int s = 0;
   uint32_t ph = 0, gph = 0;
   while (true) {
-    if (!mbar_wait(pp.full(s), ph, p.err)) return;
+    if (!mbar_wait(pp.full(s), ph, w)) return;
     const int4 d = pp.desc[s];
     const int b = d.x, n = d.y, flags = d.z, seg = d.w;
     const char* sK = reinterpret_cast<const char*>(pp.smem) + (size_t)s * pp.stage_bytes;
@@ -1110,7 +1130,7 @@ __device__ void run_consumer_fma(const Params& p, const Pipe& pp, int warp, int 
           for (int e = 0; e < C::PVE; ++e) mw[hh * (D + 2) + lane * C::PVE + e] = acc[hh][e];
           if (lane == 0) { mw[hh * (D + 2) + D] = mh[hh]; mw[hh * (D + 2) + D + 1] = lh[hh]; }
         }
-        if (!group_sync(pp, gph, lane, p.err)) return;
+        if (!group_sync(pp, gph, lane, w)) return;
         if (wsub == 0) {
 #pragma unroll
           for (int hh = 0; hh < G; ++hh) {
@@ -1137,7 +1157,7 @@ __device__ void run_consumer_fma(const Params& p, const Pipe& pp, int warp, int 
             for (int e = 0; e < C::PVE; ++e) acc[hh][e] = a[e];
           }
         }
-        if (!group_sync(pp, gph, lane, p.err)) return;
+        if (!group_sync(pp, gph, lane, w)) return;
       }
       if (wsub == 0) {
 #pragma unroll
@@ -1521,6 +1541,9 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   p.v_out = pv.v_mut ? pv.v_mut + layer_off : nullptr;
   p.new_row_bytes = pv.num_kv_heads * pv.head_dim * pv.io_size;
   p.scale_off = pv.scale_off;
+  p.wait_ns = wait_limit_ns();
+  p.epoch = next_launch_epoch();
+  p.skip_fill = debug_skip_fill();
 
   I8Maps maps;
   memset(&maps, 0, sizeof(maps));

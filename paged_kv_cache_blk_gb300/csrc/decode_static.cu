@@ -1,10 +1,10 @@
 // Allocation-free entry point for paged decode attention.
 //
 // Some callers cannot allocate device memory where they run decode attention:
-// code running while a stream is captured in global capture mode (cudaMalloc
-// is refused there), serving hosts and plugin runtimes that own all device
-// memory and forbid allocation on the hot path, and plain C programs that link
-// only this library and have no device allocator of their own.  For them,
+// serving processes whose memory manager reserves the GPU's memory up front
+// and hands out nothing on the hot path, plugin runtimes whose execute step
+// must not allocate, and plain C programs that link only this library and
+// have no device allocator of their own for scratch.  For them,
 // pkv_decode_attention_static keeps the split-K scratch of the decode pass in
 // a fixed array in device global memory that this file defines, so the caller
 // passes only inputs and outputs.  It runs the same kernels as

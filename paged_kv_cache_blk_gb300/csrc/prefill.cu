@@ -10,18 +10,14 @@
 // reads kv head h / (Hq / Hkv).
 //
 // Work items are (pair of query tiles, sequence, kv head), taken in turn by a
-// persistent grid of one CTA per SM, in clusters of two CTAs:
+// persistent grid of one CTA per SM:
 //  * A query tile is 128 MMA rows = (128 / G) query tokens x the G query
 //    heads of kv head g, so each K/V tile feeds all G heads (row r = token *
 //    G + head).  The CTA owns two tiles, A and B, that share the K/V stream.
-//  * The two CTAs of a cluster take neighbouring pairs of the same sequence
-//    and kv head, so four query tiles share one K/V stream: each CTA loads
-//    half of every K/V tile and multicasts it into both CTAs' rings.
 //  * Keys in tiles of 128 table positions (128 / bs whole blocks).  K(t) and
 //    V(t) are loaded by TMA (one box per block and 64-column half, 128B
 //    swizzle) into a 4-slot ring in the order K0 V0 K1 V1 ...; invalid table
-//    entries load zeros.  A slot is refilled once the products that read it
-//    have completed in both CTAs.
+//    entries load zeros.
 //  * Warp 9 issues S_x = Q_x K^T (M 128, N 128, K 128: 8 tcgen05.mma, fp32
 //    in TMEM) and O_x += P_x V (V is the MN-major operand) in the order
 //    S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ..., so the softmax
@@ -34,9 +30,7 @@
 //    pairs over the S columns in TMEM, the A operand of the second MMA.
 //  * Epilogue: O row / l -> bf16 -> global (only rows that are real queries).
 // Every wait is bounded; on a timeout the CTA records the error, drains its
-// MMAs, waits (bounded) for the last use of every ring slot and frees its
-// TMEM; the two CTAs of a cluster then meet at a cluster barrier, so neither
-// leaves while the other may still address its shared memory.
+// MMAs and frees its TMEM before returning.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -79,9 +73,12 @@ struct PfParams {
   long long total_q;
   long long blk_coord_limit;  // N * L (coordinate of the combined block/layer dimension)
   long long num_blocks;
-  long long n_items;  // cluster items: pairs of pairs x batch x kv heads
+  long long n_items;  // pairs x batch x kv heads
   int mb, batch, hq, hkv, G, TQ, bs, L, layer, max_q_len;
   float qscale;
+  unsigned long long wait_ns;  // bound of one wait (0 = the default)
+  int epoch;  // this launch's number (see WaitCtl)
+  int skip_fill;  // test hook: 1 = CTA 0, 2 = every CTA leaves its first K tile unloaded
 };
 
 // ---- tcgen05 / TMA helpers ----------------------------------------------------
@@ -125,41 +122,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
-}
-
-// The same, arriving on the mbarrier at this offset in every CTA of cta_mask.
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
-// ---- cluster helpers (pairs of CTAs that share their K/V stream) -------------
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// shared::cluster address of this CTA's shared address `a` in CTA `rank`
-__device__ __forceinline__ uint32_t peer_addr(uint32_t a, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::
-          : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_after() {
@@ -413,18 +375,8 @@ __device__ __forceinline__ Item make_item(const PfParams& p, long long i, int ti
   return it;
 }
 
-// The item of CTA `rank` in cluster item c: pairs 2 c' and 2 c' + 1 of one
-// (sequence, kv head), so the two CTAs of a cluster stream the same K/V tiles
-// (rank 0 holds the later pair, whose tiles cover the other's).
-__device__ __forceinline__ long long item_of(const PfParams& p, long long c, uint32_t rank) {
-  const long long per = (long long)p.batch * p.hkv;
-  const long long pc = c / per;
-  return (2 * pc + rank) * per + (c - pc * per);
-}
-
-// Persistent: each cluster of two CTAs walks the cluster items c, c + C,
-// c + 2 C, ... for C clusters (pairs of every sequence and head in order of
-// decreasing key count).  The
+// Persistent: one CTA per SM walks the items c, c + grid, c + 2 grid, ...
+// (pairs of every sequence and head in order of decreasing key count).  The
 // K/V ring, the barrier phases and the TMEM allocation carry over from item
 // to item, so the next item's loads and first products overlap the previous
 // item's epilogue.
@@ -465,7 +417,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     mbar_init(b_qempty, 1);
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(slot_full(i), 1);
-      mbar_init(slot_empty(i), 2);  // released by the MMA warps of both CTAs
+      mbar_init(slot_empty(i), 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(b_sfull0 + 8u * x, 1);
@@ -485,81 +437,79 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  // the peer's multicast copies and releases target these barriers
-  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tslot;
   // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512)
   auto tS = [&](int x) { return tmem + 128u * x; };
   auto tO = [&](int x) { return tmem + 256u + 128u * x; };
   const long long n_items = p.n_items;
-  const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
-  const long long c0 = blockIdx.x >> 1, cstride = gridDim.x >> 1;
+  const WaitCtl w = make_wait_ctl(p.err, p.wait_ns, p.epoch);
   bool ok = true;
 
   if (warp == kWarpTma) {
     // ================= TMA producer: per item Q, then K(0) V(0) K(1) V(1) ... =================
-    // Both CTAs of a cluster hold the same K/V ring: each issues half of the
-    // boxes of every tile, multicast to both, and counts the whole tile on its
-    // own full barrier.  A slot is refilled once both CTAs have released it.
     const int box_bytes = p.bs * 128;
-    long long ld = 0;  // K / V loads issued so far (ring position)
-    int jq = 0;        // items whose Q was loaded
-    for (long long c = c0; c < n_items && ok; c += cstride) {
-      const Item it = make_item(p, item_of(p, c, rank), tid);
-      const Item lead = rank == 0 ? it : make_item(p, item_of(p, c, 0), tid);
-      if (!lead.valid) continue;
-      if (it.valid) {
-        // Q of this item once the previous item's S products have read the old one
-        if (jq > 0 && !mbar_wait_sleep(b_qempty, (jq - 1) & 1, p.err)) { ok = false; break; }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(b_qfull, (it.nA > 0 ? 2 : 1) * kTileBytes);
-          for (int x = (it.nA > 0 ? 0 : 1); x < 2; ++x) {
-            const int z = (int)(it.q0 + (x == 0 ? it.qtA : it.qtB) * TQ);
-            for (int h = 0; h < 2; ++h)
-              tma_3d(smem_addr(sQ + x * kTileBytes + h * kHalf), &tq, h * 64, it.g * G, z,
-                     b_qfull);
-          }
+    long long ld = 0;        // K / V loads issued so far (ring position)
+    long long skipped = -1;  // the load the test hook left out
+    int jq = 0;              // items whose Q was loaded
+    for (long long i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      const Item it = make_item(p, i, tid);
+      if (!it.valid) continue;
+      // Q of this item once the previous item's S products have read the old one
+      if (jq > 0 && !mbar_wait_sleep(b_qempty, (jq - 1) & 1, w)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(b_qfull, (it.nA > 0 ? 2 : 1) * kTileBytes);
+        for (int x = (it.nA > 0 ? 0 : 1); x < 2; ++x) {
+          const int z = (int)(it.q0 + (x == 0 ? it.qtA : it.qtB) * TQ);
+          for (int h = 0; h < 2; ++h)
+            tma_3d(smem_addr(sQ + x * kTileBytes + h * kHalf), &tq, h * 64, it.g * G, z, b_qfull);
         }
-        ++jq;
       }
-      for (int li = 0; li < 2 * lead.nB && ok; ++li, ++ld) {
+      ++jq;
+      for (int li = 0; li < 2 * it.nB && ok; ++li, ++ld) {
         const int slot = (int)(ld % kSlots);
         const long long use = ld / kSlots;
-        if (use > 0 && !mbar_wait_sleep(slot_empty(slot), (uint32_t)((use - 1) & 1), p.err)) {
+        if (use > 0 && !mbar_wait_sleep(slot_empty(slot), (uint32_t)((use - 1) & 1), w)) {
           ok = false;
           break;
         }
         const int t = li >> 1, is_v = li & 1;
+        if ((p.skip_fill == 2 || (p.skip_fill == 1 && blockIdx.x == 0)) && ld == 0) {
+          // test hook: K(0) of the first item is never loaded, so the MMA
+          // warp's wait on it can only give up; nothing is issued into it
+          skipped = ld;
+          continue;
+        }
         if (lane == 0) mbar_arrive_expect_tx(slot_full(slot), kTileBytes);
         __syncwarp();
-        for (int k2 = 2 * lane + (int)rank; k2 < 2 * blocks_per_tile; k2 += 64) {
+        for (int k2 = lane; k2 < 2 * blocks_per_tile; k2 += 32) {
           const int h = k2 / blocks_per_tile;
           const int k = k2 % blocks_per_tile;
           const long long lb = (long long)t * blocks_per_tile + k;  // logical block
           long long coord = p.blk_coord_limit;                       // out of range: zeros
-          if (lb < lead.spanned) {
-            const int blk = p.bt[(long long)lead.b * p.mb + lb];
+          if (lb < it.spanned) {
+            const int blk = p.bt[(long long)it.b * p.mb + lb];
             if (blk >= 0 && blk < p.num_blocks) {
               coord = (long long)blk * p.L + p.layer;
             } else {
               set_error(p.err, kErrIndex);
             }
           }
-          tma_4d_mc(smem_addr(slot_ptr(slot) + h * kHalf + k * box_bytes), is_v ? &tv : &tk,
-                    h * 64, lead.g, 0, (int)coord, slot_full(slot), (uint16_t)0x3);
+          tma_4d(smem_addr(slot_ptr(slot) + h * kHalf + k * box_bytes), is_v ? &tv : &tk, h * 64,
+                 it.g, 0, (int)coord, slot_full(slot));
         }
         __syncwarp();
       }
     }
-    // Drain: both CTAs have released the last use of every slot, so every
-    // copy the peer issued into this CTA has landed and its releases of this
-    // CTA's barriers have arrived before the CTA may leave.
+    // Every load issued must land before the CTA may leave: when the other
+    // warps gave up, nothing else waited for the last ones.  A slot holds at
+    // most one load in flight (it is refilled only after its release), so the
+    // last load of each slot and the last Q load are the ones to wait for.
     for (long long idx = ld - kSlots; idx < ld; ++idx) {
-      if (idx < 0) continue;
-      if (!mbar_wait_sleep(slot_empty((int)(idx % kSlots)), (uint32_t)((idx / kSlots) & 1), p.err))
-        break;
+      if (idx < 0 || idx == skipped) continue;
+      mbar_wait_drain(slot_full((int)(idx % kSlots)), (uint32_t)((idx / kSlots) & 1), p.err);
     }
+    if (jq > 0) mbar_wait_drain(b_qfull, (uint32_t)((jq - 1) & 1), p.err);
   } else if (warp == kWarpMma) {
     // ================= MMA issuer =================
     // per item: S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ..., so
@@ -572,10 +522,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       int ne[2] = {0, 0};          // epilogues of A / B across items
       auto slot_of = [&](long long idx) { return (int)(idx % kSlots); };
       auto ready = [&](long long idx) {
-        return mbar_wait_sleep(slot_full(slot_of(idx)), (uint32_t)((idx / kSlots) & 1), p.err);
+        return mbar_wait_sleep(slot_full(slot_of(idx)), (uint32_t)((idx / kSlots) & 1), w);
       };
-      // a slot is free once the products reading it completed in both CTAs
-      auto release = [&](long long idx) { umma_commit_mc(slot_empty(slot_of(idx)), 0x3); };
       auto issue_s = [&](int x, long long k_idx) {
         const uint32_t k_addr = smem_addr(slot_ptr(slot_of(k_idx)));
         const uint32_t qa = q_addr + x * kTileBytes;
@@ -597,66 +545,55 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         umma_commit(b_pvdone0 + 8u * x);
       };
-      for (long long c = c0; c < n_items && ok; c += cstride) {
-        const Item it = make_item(p, item_of(p, c, rank), tid);
-        const Item lead = rank == 0 ? it : make_item(p, item_of(p, c, 0), tid);
-        if (!lead.valid) continue;
+      for (long long i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+        const Item it = make_item(p, i, tid);
+        if (!it.valid) continue;
+        const int nA = it.nA, nB = it.nB;
         const long long base = ld;  // load index of K(0) of this item
-        const int nA = it.valid ? it.nA : 0, nB = it.valid ? it.nB : 0;
-        ld = base + 2 * lead.nB;
-        if (it.valid) {
-          if (!mbar_wait_sleep(b_qfull, jq & 1, p.err) || !ready(base)) { ok = false; break; }
-          ++jq;
-          if (nA > 0) issue_s(0, base);
-          issue_s(1, base);
-          // Q may be replaced once the last S product of the item completes: the
-          // next item's loads then overlap this item's last products and epilogue
-          if (nB == 1) umma_commit(b_qempty);
-          for (int t = 0; t < nB && ok; ++t) {
-            const long long ki = base + 2 * t, vi = ki + 1;
-            // K(t) is released after the S products that read it
-            release(ki);
-            if (!ready(vi)) { ok = false; break; }
-            if (t < nA) {
-              // O_A is overwritten by the first product: the previous epilogue
-              // must have read it
-              if (t == 0 && ne[0] > 0 && !mbar_wait_sleep(b_ofree0, (ne[0] - 1) & 1, p.err)) {
-                ok = false;
-                break;
-              }
-              if (!mbar_wait_sleep(b_pfull0, (uint32_t)(nt[0] & 1), p.err)) { ok = false; break; }
-              ++nt[0];
-              issue_pv(0, vi, t == 0);
-              if (t + 1 < nA) {
-                if (!ready(ki + 2)) { ok = false; break; }
-                issue_s(0, ki + 2);
-              }
-            }
-            if (t == 0 && ne[1] > 0 && !mbar_wait_sleep(b_ofree0 + 8u, (ne[1] - 1) & 1, p.err)) {
+        if (!mbar_wait_sleep(b_qfull, jq & 1, w) || !ready(base)) { ok = false; break; }
+        ++jq;
+        if (nA > 0) issue_s(0, base);
+        issue_s(1, base);
+        // Q may be replaced once the last S product of the item completes: the
+        // next item's loads then overlap this item's last products and epilogue
+        if (nB == 1) umma_commit(b_qempty);
+        for (int t = 0; t < nB && ok; ++t) {
+          const long long ki = base + 2 * t, vi = ki + 1;
+          // K(t) is released after the S products that read it
+          umma_commit(slot_empty(slot_of(ki)));
+          if (!ready(vi)) { ok = false; break; }
+          if (t < nA) {
+            // O_A is overwritten by the first product: the previous epilogue
+            // must have read it
+            if (t == 0 && ne[0] > 0 && !mbar_wait_sleep(b_ofree0, (ne[0] - 1) & 1, w)) {
               ok = false;
               break;
             }
-            if (!mbar_wait_sleep(b_pfull0 + 8u, (uint32_t)(nt[1] & 1), p.err)) { ok = false; break; }
-            ++nt[1];
-            issue_pv(1, vi, t == 0);
-            release(vi);
-            if (t + 1 < nB) {
-              if (!(t + 1 < nA) && !ready(ki + 2)) { ok = false; break; }
-              issue_s(1, ki + 2);
-              if (t + 2 == nB) umma_commit(b_qempty);
+            if (!mbar_wait_sleep(b_pfull0, (uint32_t)(nt[0] & 1), w)) { ok = false; break; }
+            ++nt[0];
+            issue_pv(0, vi, t == 0);
+            if (t + 1 < nA) {
+              if (!ready(ki + 2)) { ok = false; break; }
+              issue_s(0, ki + 2);
             }
           }
-          if (nA > 0) ++ne[0];
-          ++ne[1];
+          if (t == 0 && ne[1] > 0 && !mbar_wait_sleep(b_ofree0 + 8u, (ne[1] - 1) & 1, w)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait_sleep(b_pfull0 + 8u, (uint32_t)(nt[1] & 1), w)) { ok = false; break; }
+          ++nt[1];
+          issue_pv(1, vi, t == 0);
+          umma_commit(slot_empty(slot_of(vi)));
+          if (t + 1 < nB) {
+            if (!(t + 1 < nA) && !ready(ki + 2)) { ok = false; break; }
+            issue_s(1, ki + 2);
+            if (t + 2 == nB) umma_commit(b_qempty);
+          }
         }
-        // tiles only the peer's item reads: wait for them, release in both CTAs
-        for (int li = 2 * nB; li < 2 * lead.nB && ok; ++li) {
-          const long long idx = base + li;
-          if (!ready(idx)) { ok = false; break; }
-          const uint32_t e = slot_empty(slot_of(idx));
-          mbar_arrive(e);
-          mbar_arrive_remote(peer_addr(e, peer));
-        }
+        ld = base + 2 * nB;
+        if (nA > 0) ++ne[0];
+        ++ne[1];
       }
       umma_commit(b_drain);  // arrives once every MMA issued above has completed
     }
@@ -669,8 +606,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t b_sfull = b_sfull0 + 8u * x, b_pfull = b_pfull0 + 8u * x;
     const uint32_t b_pvdone = b_pvdone0 + 8u * x, b_ofree = b_ofree0 + 8u * x;
     long long nt = 0;  // tiles of this warpgroup across items (barrier phases)
-    for (long long c = c0; c < n_items && ok; c += cstride) {
-      const Item it = make_item(p, item_of(p, c, rank), tid);
+    for (long long i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
+      const Item it = make_item(p, i, tid);
       if (!it.valid) continue;
       const int nX = x == 0 ? it.nA : it.nB;
       if (nX == 0) continue;
@@ -684,7 +621,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const bool rows_full = (qt + 1) * TQ <= it.nq;
       RowState st{-INFINITY, 0.f};
       for (int t = 0; t < nX && ok; ++t, ++nt) {
-        const bool waited = mbar_wait_sleep(b_sfull, (uint32_t)(nt & 1), p.err);
+        const bool waited = mbar_wait_sleep(b_sfull, (uint32_t)(nt & 1), w);
         if (!__all_sync(0xffffffffu, waited)) { ok = false; break; }
         tc_fence_after();
         const long long tp0 = (long long)t * kKeys;
@@ -698,7 +635,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       if (!ok) break;
       // epilogue: O row / l -> bf16 -> out, then hand O back to the MMA warp
-      const bool waited = mbar_wait_sleep(b_pvdone, (uint32_t)((nt - 1) & 1), p.err);
+      const bool waited = mbar_wait_sleep(b_pvdone, (uint32_t)((nt - 1) & 1), w);
       if (!__all_sync(0xffffffffu, waited)) { ok = false; break; }
       tc_fence_after();
       const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
@@ -747,15 +684,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
-    mbar_wait_sleep(b_drain, 0, p.err);
+    mbar_wait_drain(b_drain, 0, p.err);
     __syncwarp();  // the dealloc below is warp-wide
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
                  : "memory");
   }
-  // neither CTA leaves while the other may still address its shared memory
-  cluster_sync_all();
 }
 
 // ---- host side ------------------------------------------------------------------
@@ -821,46 +756,24 @@ cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num
   p.layer = layer;
   p.max_q_len = max_q_len;
   p.qscale = scale * kLog2e;
-  // clusters of two CTAs (one per SM) that share each K/V tile
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kPfThreads);
-  cfg.dynamicSmemBytes = (size_t)kSmemBytes;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  static int max_clusters[64] = {0};
+  p.wait_ns = wait_limit_ns();
+  p.epoch = next_launch_epoch();
+  p.skip_fill = debug_skip_fill();
+  static int configured[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (max_clusters[dev] == 0) {
+  if (dev >= 0 && dev < 64 && configured[dev] == 0) {
     e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes);
     if (e != cudaSuccess) return e;
-    // co-resident clusters: a persistent grid larger than this would queue
-    cfg.gridDim = dim3(2 * (unsigned)(sm_count / 2 > 0 ? sm_count / 2 : 1));
-    int n = 0;
-    cfg.numAttrs = 1;  // the cluster shape alone
-    e = cudaOccupancyMaxActiveClusters(&n, prefill_kernel, &cfg);
-    cfg.numAttrs = 2;
-    if (e != cudaSuccess) return e;
-    max_clusters[dev] = n > 0 ? n : 1;
+    configured[dev] = 1;
   }
   const long long ntq = (max_q_len + TQ - 1) / TQ;
-  const long long npairs = (ntq + 1) / 2;
-  p.n_items = (npairs + 1) / 2 * (long long)batch * pv.num_kv_heads;
-  long long nc = sm_count / 2 < max_clusters[dev] ? sm_count / 2 : max_clusters[dev];
-  if (nc < 1) nc = 1;
-  if (p.n_items < nc) nc = p.n_items;
-  cfg.gridDim = dim3((unsigned)(2 * nc));
-  return cudaLaunchKernelEx(&cfg, prefill_kernel, tq, tk, tv, p);
+  p.n_items = (ntq + 1) / 2 * (long long)batch * pv.num_kv_heads;
+  const long long grid = p.n_items < sm_count ? p.n_items : sm_count;
+  return launch_kernel(prefill_kernel, dim3((unsigned)grid), dim3(kPfThreads), (size_t)kSmemBytes,
+                       s, true, tq, tk, tv, p);
 }
 
 }  // namespace pkv

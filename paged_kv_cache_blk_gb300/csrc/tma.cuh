@@ -32,15 +32,12 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* m, int x
       : "memory");
 }
 
-// A 4-D tile copy delivered to the same shared-memory offset, with its
-// completion counted on the mbarrier at the same offset, in every CTA of the
-// cluster named in cta_mask (a load from this GPU's own memory).
-__device__ __forceinline__ void tma_4d_mc(uint32_t dst, const CUtensorMap* m, int x, int y, int z,
-                                          int w, uint32_t bar, uint16_t cta_mask) {
+__device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap* m, int x, int y, int z,
+                                       int w, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
-      "l"((uint64_t)m), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "h"(cta_mask)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+      "[%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"((uint64_t)m), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
       : "memory");
 }
 
