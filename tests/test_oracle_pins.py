@@ -472,6 +472,89 @@ def _combine_weight_sign(parts, head_dim):
     return num / den
 
 
+# ---------------------------------------------------------------------------
+# gather_batch: the batch form every GPU gather test checks against
+# ---------------------------------------------------------------------------
+
+# Hand-enumerated (block, row) pairs of three sequences at block_size 4, found
+# by walking each table in storage order from its first-block offset, the way
+# the ch.12 §2.1 figure walks the table [7, 3, 12]:
+#   seq 0: table [5, 2],    offset 1, 6 tokens -> rows 1..3 of block 5, 0..2 of block 2
+#   seq 1: table [7],       offset 3, 0 tokens -> nothing
+#   seq 2: table [0, 3, 6], offset 2, 7 tokens -> rows 2..3 of 0, 0..3 of 3, 0 of 6
+#   seq 3: table [4],       offset 0, 1 token  -> row 0 of block 4
+GATHER_BATCH_EXAMPLE = dict(
+    bs=4,
+    tables=[[5, 2, -1], [7, -1, -1], [0, 3, 6], [4, -1, -1]],
+    offsets=[1, 3, 2, 0],
+    lens=[6, 0, 7, 1],
+    rows=[(5, 1), (5, 2), (5, 3), (2, 0), (2, 1), (2, 2),
+          (0, 2), (0, 3), (3, 0), (3, 1), (3, 2), (3, 3), (6, 0),
+          (4, 0)],
+)
+
+
+def _tagged_pools(N, L, bs, H, D):
+    """K and V pools whose every element names its own coordinates (V
+    negated), so a misplaced, mixed-up or dropped row is visible."""
+    idx = np.indices((N, L, bs, H, D)).astype(np.int64)
+    tag = (((idx[0] * L + idx[1]) * bs + idx[2]) * H + idx[3]) * D + idx[4] + 1
+    return tag, -tag
+
+
+def check_gather_batch(gather_batch):
+    ex = GATHER_BATCH_EXAMPLE
+    bs, layer = ex["bs"], 1
+    k, v = _tagged_pools(8, 2, bs, 2, 3)
+    bt = np.array(ex["tables"], np.int32)
+    lens = np.array(ex["lens"], np.int32)
+    offs = np.array(ex["offsets"], np.int32)
+    ko, vo = gather_batch(k, v, layer, bt, lens, offs)
+    want_k = np.stack([k[blk, layer, row] for blk, row in ex["rows"]])
+    want_v = np.stack([v[blk, layer, row] for blk, row in ex["rows"]])
+    assert ko.shape == want_k.shape and vo.shape == want_v.shape
+    assert np.array_equal(ko, want_k) and np.array_equal(vo, want_v)
+    # per sequence it is the flat-index gather of step14_2 "Solution", in order
+    rng = np.random.default_rng(41)
+    N, bs2 = 40, 8
+    k2, v2 = _tagged_pools(N, 1, bs2, 1, 2)
+    lens2 = rng.integers(0, 30, size=6).astype(np.int32)
+    offs2 = rng.integers(0, bs2, size=6).astype(np.int32)
+    perm = rng.permutation(N)
+    tables, used = np.full((6, 6), -1, np.int32), 0
+    for b in range(6):
+        nb = O.blocks_needed(int(lens2[b]), bs2, int(offs2[b])) if lens2[b] else 0
+        tables[b, :nb] = perm[used:used + nb]
+        used += nb
+    ko2, vo2 = gather_batch(k2, v2, 0, tables, lens2, offs2)
+    parts_k = [O.gather_indexed(k2, 0, tables[b], int(lens2[b]), int(offs2[b])) for b in range(6)]
+    parts_v = [O.gather_indexed(v2, 0, tables[b], int(lens2[b]), int(offs2[b])) for b in range(6)]
+    assert np.array_equal(ko2, np.concatenate(parts_k)) and np.array_equal(vo2, np.concatenate(parts_v))
+
+
+def test_gather_batch_hand_example():
+    check_gather_batch(O.gather_batch)
+
+
+def _gather_batch_first_offset(k, v, layer, bt, lens, offs):
+    return O.gather_batch(k, v, layer, bt, lens, np.full_like(offs, offs[0]))
+
+
+def _gather_batch_reversed(k, v, layer, bt, lens, offs):
+    ko, vo = O.gather_batch(k, v, layer, bt[::-1], lens[::-1], offs[::-1])
+    return ko, vo
+
+
+def _gather_batch_kv_swapped(k, v, layer, bt, lens, offs):
+    ko, vo = O.gather_batch(k, v, layer, bt, lens, offs)
+    return vo, ko
+
+
+def _gather_batch_v_from_k(k, v, layer, bt, lens, offs):
+    ko, _ = O.gather_batch(k, v, layer, bt, lens, offs)
+    return ko, O.gather_batch(k, k, layer, bt, lens, offs)[1]
+
+
 PLANTED = [
     ("slot ignores offset", lambda: check_slot_walk(_slot_no_offset)),
     ("slot quotient/remainder swapped", lambda: check_slot_walk(_slot_swapped)),
@@ -494,6 +577,11 @@ PLANTED = [
     ("prefill GQA head map h % Hkv", lambda: check_prefill_vs_sdpa(_prefill_with(gqa_mod=True))),
     ("combine without the max weights", lambda: check_split_combine(_combine_unweighted)),
     ("combine weights with the sign flipped", lambda: check_split_combine(_combine_weight_sign)),
+    ("batch gather takes the first offset for all",
+     lambda: check_gather_batch(_gather_batch_first_offset)),
+    ("batch gather in reverse order", lambda: check_gather_batch(_gather_batch_reversed)),
+    ("batch gather with K and V swapped", lambda: check_gather_batch(_gather_batch_kv_swapped)),
+    ("batch gather reads V from K", lambda: check_gather_batch(_gather_batch_v_from_k)),
 ]
 
 
