@@ -59,6 +59,11 @@ def test_decode_gqa_last_blocks_private():
             for b in range(bt.batch)]
     assert len(set(last)) == bt.batch
     assert np.array_equal(w.tokens.token_pos, bt.seq_lens - 1)
+    # no sequence reads a block that another sequence's new token goes into
+    for b in range(bt.batch):
+        n = oracle.blocks_needed(int(bt.seq_lens[b]), 16)
+        others = set(bt.block_tables[b, :n - 1].tolist())
+        assert not (others & (set(last) - {last[b]})), b
 
 
 def test_long_splitk_fits_pool():

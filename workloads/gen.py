@@ -227,16 +227,18 @@ def _decode_gqa(seed: int) -> Workload:
     rng = np.random.default_rng(seed)
     B = 64
     lens = rng.integers(1024, 8192 + 1, size=B)
-    # The last block of every sequence is private (distinct across the
-    # batch) so that a decode-step append never hits the same row twice; the
-    # other blocks are drawn per sequence without replacement and may repeat
-    # across sequences (the batch spans more blocks than the pool holds).
+    # The last block of every sequence is private: distinct across the batch
+    # and in no other sequence's table, so a decode-step append never hits the
+    # same row twice and never writes a block another sequence reads in the
+    # same step.  The other blocks are drawn per sequence without replacement
+    # and may repeat across sequences (the batch spans more blocks than the
+    # pool holds).
     last = rng.permutation(spec.num_blocks)[:B]
     tables = []
     for b in range(B):
         nblk = _span_blocks(int(lens[b]), 0, spec.block_size)
         others = rng.permutation(spec.num_blocks)
-        others = others[others != last[b]][:nblk - 1]
+        others = others[~np.isin(others, last)][:nblk - 1]
         tables.append(list(others) + [int(last[b])])
     batch = _pack(tables, lens, np.zeros(B, np.int32))
     # one new token per sequence: its last logical position
