@@ -1,10 +1,11 @@
 """The allocation-free decode entry point (pkv_decode_attention_static).
 
 Callers that cannot allocate device memory where they run decode attention
-(stream capture in global mode, hosts that own all device memory, plain C
-programs without a device allocator) pass no workspace: the library keeps the
-scratch in its own fixed device array.  This checks, through the C ABI, that
-two calls in a row give the same results as pkv_decode_attention with a
+(serving processes whose memory manager owns all device memory, plugin
+runtimes whose execute step must not allocate, plain C programs without a
+device allocator) pass no workspace: the library keeps the scratch in its own
+fixed device array.  This checks, through the C ABI, that two calls in a row
+give the oracle's results and the same results as pkv_decode_attention with a
 caller workspace, and that a shape too large for the array is refused.
 
 The file is named to be collected last, so a run that stops at the first
@@ -17,11 +18,12 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_blk_gb300 as pkv
 from paged_kv_cache_blk_gb300 import _binding as B
-from workloads import rand_rows, small_workload
+from workloads import rand_rows, small_workload, to_numpy_bits
 
-from gpu_util import dev_batch, gpu_decode, make_pools, need_gpu
+from gpu_util import dev_batch, gpu_decode, host_layer, make_pools, max_abs, need_gpu, widen_out
 
 pytestmark = pytest.mark.gpu
 
@@ -52,6 +54,7 @@ def test_static_scratch_matches_workspace_entry(dev):
     k, v = make_pools(w, dev)
     pool = pkv.Pool(k, v)
     bt, lens, offs, _ = dev_batch(w.batch, dev)
+    kh, vh = host_layer(k, w.layer), host_layer(v, w.layer)
     for call, seed in enumerate((83, 84)):          # two calls in a row
         q = rand_rows((12, 32, 128), "bf16", seed, dev)
         ref = gpu_decode(pool, w.layer, q, w.scale, w.batch, dev)
@@ -61,6 +64,9 @@ def test_static_scratch_matches_workspace_entry(dev):
         assert torch.isfinite(out.float()).all(), call
         err = (out.double() - ref.double()).abs().max().item()
         assert err <= TOL, (call, err)
+        want = oracle.decode_attention(kh, vh, 0, to_numpy_bits(q), w.batch.block_tables,
+                                       w.batch.seq_lens, w.batch.offsets, w.scale)
+        assert max_abs(widen_out(out), want) <= TOL, call
 
 
 def test_static_scratch_binding_and_fp32(dev):
@@ -70,6 +76,7 @@ def test_static_scratch_binding_and_fp32(dev):
     k, v = make_pools(w, dev)
     pool = pkv.Pool(k, v)
     bt, lens, offs, _ = dev_batch(w.batch, dev)
+    kh, vh = host_layer(k, 0), host_layer(v, 0)
     for seed in (86, 87):
         q = rand_rows((5, 4, 64), "f32", seed, dev)
         ref = gpu_decode(pool, 0, q, w.scale, w.batch, dev)
@@ -77,6 +84,9 @@ def test_static_scratch_binding_and_fp32(dev):
         pkv.decode_attention_static(pool, 0, q, w.scale, bt, lens, offs, out)
         torch.cuda.synchronize()
         assert (out.double() - ref.double()).abs().max().item() <= 1e-5
+        want = oracle.decode_attention(kh, vh, 0, to_numpy_bits(q), w.batch.block_tables,
+                                       w.batch.seq_lens, w.batch.offsets, w.scale)
+        assert max_abs(widen_out(out), want) <= 1e-5
 
 
 def test_static_scratch_refuses_oversized_shape(dev):
