@@ -96,6 +96,20 @@ def decode_bytes(batch, row_bytes: int, hq: int, head_dim: int, elem: int, bs: i
     return {"kv": kv, "total": kv + qo + tables}
 
 
+def unique_kv_bytes(batch, row_bytes: int, bs: int, num_blocks: int) -> int:
+    """K and V bytes of the distinct pool rows a decode call reads: a row that
+    several sequences cover (a shared prefix block, or a block id that repeats
+    across tables) counts once."""
+    covered = np.zeros((num_blocks, bs), dtype=bool)
+    for b in range(batch.batch):
+        n = int(batch.seq_lens[b])
+        if n <= 0:
+            continue
+        p = int(batch.offsets[b]) + np.arange(n, dtype=np.int64)
+        covered[batch.block_tables[b, p // bs], p % bs] = True
+    return int(covered.sum()) * 2 * row_bytes
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -491,6 +505,9 @@ def run_ours(args, rank, local_rank, world):
     step_bytes = db["total"] + 4 * w.batch.batch * w.pool.row_bytes
     achieved = step_bytes / (part_ms / 1e3) / 1e9
     traffic = recorded_traffic()
+    # block ids repeat across the decode-GQA tables: the distinct rows read
+    uniq = unique_kv_bytes(w.batch, w.pool.row_bytes, w.pool.block_size, w.pool.num_blocks)
+    uniq_step = step_bytes - db["kv"] + uniq
     result = {
         "metric": METRIC,
         "value": round(value_gbs, 1),
@@ -522,6 +539,10 @@ def run_ours(args, rank, local_rank, world):
             "algorithmic_bytes_per_launch": step_bytes,
             "avg_launch_ms": round(part_ms, 4),
             "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
+            "unique_bytes_per_launch": uniq_step,
+            "frac_unique": round(uniq_step / (part_ms / 1e3) / 1e9 / peak, 4),
+            "frac_dram": (None if traffic is None
+                          else round(traffic / (part_ms / 1e3) / 1e9 / peak, 4)),
         },
         "step_timing": timing,
         "step_breakdown_ms": breakdown,
@@ -534,6 +555,8 @@ def run_ours(args, rank, local_rank, world):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds, seed_shift=0, dev=dev)
+    result["legs_detail"] = result.pop("legs")
+    result["legs"] = compact_legs(result["legs_detail"], peak)
     return result
 
 
@@ -688,7 +711,40 @@ def run_legs(args, dev, rank, flush, pkv):
     out["allocator"] = allocator_leg()
     out["prefill"] = prefill_leg(args, dev, flush, pkv)
     out["int8_decode"] = int8_leg(args, dev, rank, flush, pkv)
+    for name in ("long_splitk", "prefix_mix"):
+        out["decode_" + name] = decode_leg(name, args, dev, flush, pkv, min(args.steps, 100))
     return out
+
+
+def compact_legs(legs: dict, peak: float) -> dict:
+    """The legs' headline figures in a few short keys: printed last on the
+    JSON line so that a tail of the output keeps them."""
+    f = lambda x: None if x is None else round(x, 4)
+    c = {}
+    for name in ("scatter", "gather", "copy_blocks", "swap_out", "swap_in"):
+        if name in legs:
+            c[name + "_GBps"] = legs[name]["GB/s"]
+    for name in ("scatter", "gather", "copy_blocks"):
+        if name in legs:
+            c[name + "_frac"] = f(legs[name]["GB/s"] / peak)
+    for name in ("long_splitk", "prefix_mix"):
+        d = legs.get("decode_" + name)
+        if d:
+            c["decode_" + name] = {k: d[k] for k in ("partial_frac", "call_kv_frac",
+                                                     "call_unique_frac", "partial_dram_frac",
+                                                     "call_kv_GBps", "call_unique_GBps")}
+    i8 = legs.get("int8_decode")
+    if i8:
+        c["int8_step"] = {"ms": i8["ms_per_step"], "tokens_per_s": i8["tokens_per_s"],
+                          "partial_frac": i8["decode_partial"]["frac"]}
+    pf = legs.get("prefill")
+    if pf:
+        c["prefill"] = {k: {"TFLOPs": pf[k]["TFLOP/s"], "frac": pf[k]["frac_of_bf16_peak"]}
+                        for k in ("prompts", "chunk")}
+    al = legs.get("allocator")
+    if al:
+        c["allocator_ops_per_s"] = al["lib_ops_per_s"]
+    return c
 
 
 def prefill_case(dev, kind: str, seed: int = 0):
@@ -997,63 +1053,70 @@ def run_reference(args, rank, world):
     }
 
 
+def decode_leg(name: str, args, dev, flush, pkv, steps: int) -> dict:
+    """Paged decode attention (pkv_decode_attention) on one bf16 decode
+    workload: the partial-pass kernel alone (events the library records
+    around it) and the whole call (partial + combine), with the L2 flush
+    between calls.  Throughput on the algorithmic bytes (every sequence's
+    rows counted), on the distinct rows read, and on the DRAM bytes of the
+    committed ncu capture of the same kernel source."""
+    w = make_workload(name)
+    k, v = new_pool(w.pool, dev)
+    fill_pool(k, v, w.pool, w.layer, w.seed, w.k_boost_frac, w.k_boost)
+    pool = pkv.Pool(k, v)
+    b = w.batch
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
+    bt, lens, offs = (t(b.block_tables, torch.int32), t(b.seq_lens, torch.int32),
+                      t(b.offsets, torch.int32))
+    q = rand_rows((b.batch, w.num_q_heads, w.pool.head_dim), "bf16", 5, dev)
+    out = torch.empty_like(q)
+    ws = torch.empty(pkv.decode_workspace_size(b.batch, w.num_q_heads, w.pool.head_dim, dev),
+                     dtype=torch.uint8, device=dev)
+    call = lambda: pkv.decode_attention(pool, w.layer, q, w.scale, bt, lens, offs, out, ws)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    times, kev = timed(call, steps, flush, lambda: decode_events_hook(pkv))
+    pkv.set_decode_events(None, None)
+    call_ms = reduce_max(statistics.mean(times))
+    part_ms = statistics.mean(a.elapsed_time(e) for a, e in kev)
+    peak, kind = load_peaks()
+    db = decode_bytes(b, w.pool.row_bytes, w.num_q_heads, w.pool.head_dim, w.pool.elem_size,
+                      w.pool.block_size)
+    uniq = unique_kv_bytes(b, w.pool.row_bytes, w.pool.block_size, w.pool.num_blocks)
+    dram = recorded_traffic(f"decode_partial_{name}_traffic.txt")
+    gbs = lambda nbytes, ms: nbytes / (ms / 1e3) / 1e9
+    entry = {
+        "partial_ms": round(part_ms, 4), "call_ms": round(call_ms, 4),
+        "kv_bytes": db["kv"], "unique_kv_bytes": uniq, "algorithmic_bytes": db["total"],
+        "partial_GBps": round(gbs(db["total"], part_ms), 1),
+        "partial_frac": round(gbs(db["total"], part_ms) / peak, 4),
+        "call_kv_GBps": round(gbs(db["kv"], call_ms), 1),
+        "call_kv_frac": round(gbs(db["kv"], call_ms) / peak, 4),
+        "call_unique_GBps": round(gbs(uniq, call_ms), 1),
+        "call_unique_frac": round(gbs(uniq, call_ms) / peak, 4),
+        "dram_bytes": dram,
+        "partial_dram_frac": None if dram is None else round(gbs(dram, part_ms) / peak, 4),
+        "tokens_per_s": round(b.batch / (call_ms / 1e3), 1),
+        "peak": peak, "peak_kind": kind,
+    }
+    del pool, k, v, ws
+    torch.cuda.empty_cache()
+    return entry
+
+
 def decode_sweep(args) -> int:
     """Decode-attention throughput on every bf16 decode workload (not the
-    bench line): partial-pass kernel alone (library events) and the whole
-    decode call, each over `--steps` launches with the clean L2 flush."""
+    bench line): partial-pass kernel alone and the whole decode call."""
     import paged_kv_cache_blk_gb300 as pkv
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     pkv.build()
     pkv.load()
     flush = L2Flush(dev)
-    peak, kind = load_peaks()
-    res = {}
-    for name in ("decode_gqa", "long_splitk", "prefix_mix"):
-        w = make_workload(name)
-        k, v = new_pool(w.pool, dev)
-        fill_pool(k, v, w.pool, w.layer, w.seed, w.k_boost_frac, w.k_boost)
-        pool = pkv.Pool(k, v)
-        b = w.batch
-        t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev, dt)
-        bt, lens, offs = (t(b.block_tables, torch.int32), t(b.seq_lens, torch.int32),
-                          t(b.offsets, torch.int32))
-        q = rand_rows((b.batch, w.num_q_heads, w.pool.head_dim), "bf16", 5, dev)
-        out = torch.empty_like(q)
-        ws = torch.empty(pkv.decode_workspace_size(b.batch, w.num_q_heads, w.pool.head_dim, dev),
-                         dtype=torch.uint8, device=dev)
-        call = lambda: pkv.decode_attention(pool, w.layer, q, w.scale, bt, lens, offs, out, ws)
-        for _ in range(args.warmup):
-            call()
-        torch.cuda.synchronize()
-
-        def hook():
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(); e1.record()
-            pkv.set_decode_events(e0, e1)
-            return e0, e1
-
-        times, kev = timed(call, args.steps, flush, hook)
-        pkv.set_decode_events(None, None)
-        call_ms = statistics.mean(times)
-        part_ms = statistics.mean(a.elapsed_time(e) for a, e in kev)
-        db = decode_bytes(b, w.pool.row_bytes, w.num_q_heads, w.pool.head_dim,
-                          w.pool.elem_size, w.pool.block_size)
-        entry = {"kv_read_bytes": db["kv"], "algorithmic_bytes": db["total"],
-                 "partial_ms": round(part_ms, 4), "call_ms": round(call_ms, 4),
-                 "partial_GBps": round(db["total"] / part_ms / 1e6, 1),
-                 "call_kv_GBps": round(db["kv"] / call_ms / 1e6, 1),
-                 "partial_frac_of_" + kind: round(db["total"] / part_ms / 1e6 / peak, 4),
-                 "tokens_per_s": round(b.batch / call_ms * 1e3, 1)}
-        if name == "prefix_mix":
-            prefix = 64 * 16 * w.pool.row_bytes * 2
-            entry["unique_kv_bytes"] = db["kv"] - (b.batch - 1) * prefix + int(
-                (b.offsets.astype(np.int64) * w.pool.row_bytes * 2).sum())
-            entry["call_unique_GBps"] = round(entry["unique_kv_bytes"] / call_ms / 1e6, 1)
-        res[name] = entry
-        del pool, k, v, ws
-        torch.cuda.empty_cache()
-    print(json.dumps({"decode_sweep": res, "peak_GBps": peak, "peak_kind": kind}), flush=True)
+    res = {name: decode_leg(name, args, dev, flush, pkv, args.steps)
+           for name in ("decode_gqa", "long_splitk", "prefix_mix")}
+    print(json.dumps({"decode_sweep": res}), flush=True)
     return 0
 
 
