@@ -21,6 +21,10 @@ enum : int {
 // complete.  The host may set a shorter bound (pkv_set_wait_limit_ns).
 constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;
 
+// A wait looks at its launch's abort word only once it has lasted this long:
+// healthy waits end well before, so they never pay for that global load.
+constexpr unsigned long long kAbortCheckNs = 100000ull;
+
 __device__ __forceinline__ void set_error(int* err, int bits) {
   if (err) atomicOr(err, bits);
 }
@@ -124,16 +128,17 @@ __device__ __forceinline__ void give_up(const WaitCtl& w) {
   if (w.epoch != 0) atomicExch(w.err + 1, w.epoch);
 }
 
-// Wait for the phase of parity `parity` to complete.  On giving up (bound
-// reached, or the launch gave up elsewhere) returns false, the first with
-// kErrTimeout set, so the caller can leave cleanly.  Polls: for the short
-// waits of the streaming kernels.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_timer_ns();
+// The slow part of a wait, entered only after kAbortCheckNs: the bound, the
+// launch's abort word, and the give-up.  Kept out of line so the tight poll
+// of the healthy case stays as short as a plain one.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                                   const WaitCtl w, unsigned long long t0,
+                                                   uint32_t hint_ns) {
+#pragma unroll 1
   for (uint32_t it = 1; it < (1u << 30); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if (hint_ns ? mbar_try_wait_sleep(bar, parity, hint_ns) : mbar_try_wait(bar, parity))
+      return true;
+    if (hint_ns || (it & 63u) == 0) {
       if (global_timer_ns() - t0 > w.limit_ns) break;
       if (launch_gave_up(w)) return false;
     }
@@ -142,20 +147,33 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   return false;
 }
 
-// The same bound, sleeping between checks (suspend-time hint): for waits that
-// last as long as a tensor-core product, where a polling warp would take issue
+// Wait for the phase of parity `parity` to complete.  On giving up (bound
+// reached, or the launch gave up elsewhere) returns false, the first with
+// kErrTimeout set, so the caller can leave cleanly.  Polls: for the short
+// waits of the streaming kernels.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+#pragma unroll 1
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0 && global_timer_ns() - t0 > kAbortCheckNs) break;
+  }
+  return mbar_wait_slow(bar, parity, w, t0, 0);
+}
+
+// The same, sleeping between checks (suspend-time hint): for waits that last
+// as long as a tensor-core product, where a polling warp would take issue
 // slots from the warp working beside it.
 __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
-  const uint32_t hint = w.limit_ns < 1000000ull ? 1000u : 100000u;
-  for (uint32_t it = 1; it < (1u << 26); ++it) {
-    if (mbar_try_wait_sleep(bar, parity, hint)) return true;
-    if (global_timer_ns() - t0 > w.limit_ns) break;
-    if (launch_gave_up(w)) return false;
+#pragma unroll 1
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (global_timer_ns() - t0 > kAbortCheckNs) break;
   }
-  give_up(w);
-  return false;
+  return mbar_wait_slow(bar, parity, w, t0, w.limit_ns < 1000000ull ? 1000u : 100000u);
 }
 
 // Wait for asynchronous copies this CTA issued to land before it leaves (or
@@ -164,6 +182,7 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, c
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
+#pragma unroll 1
   for (uint32_t it = 1; it < (1u << 30); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) break;

@@ -112,7 +112,7 @@ struct Params {
   int scale_off;
   unsigned long long wait_ns;  // bound of one wait (0 = the default)
   int epoch;  // this launch's number (see WaitCtl)
-  int skip_fill;  // test hook: 1 = CTA 0, 2 = every CTA leaves its first stage unfilled
+  int skip_fill;  // test hook: 1 = CTA 0, 2 = every CTA stalls its consumers
 };
 
 // Tensor maps of an int8 pool (unused for bf16 / fp32 pools): K and V codes
@@ -275,6 +275,8 @@ struct Pipe {
   __device__ uint32_t full(int s) const { return bar0 + 8u * s; }
   __device__ uint32_t empty(int s) const { return bar0 + 8u * (stages + s); }
   __device__ uint32_t group() const { return bar0 + 8u * (2 * stages); }
+  // never arrived at: the test hook's stalled wait
+  __device__ uint32_t stall() const { return bar0 + 8u * (2 * stages + 1); }
 };
 
 // Reusable barrier over the consumer warps (mbarrier with nw arrivals),
@@ -348,13 +350,6 @@ __device__ void run_producer(const Params& p, const Pipe& pp, const I8Maps& maps
         if (kx == x1 - 1 && re == kr1) flags |= kLast;
         if (single) flags |= kSingle;
         if (!mbar_wait(pp.empty(s), ph, w)) { ok = false; break; }
-        if ((p.skip_fill == 2 || (p.skip_fill == 1 && blockIdx.x == 0)) && kx == x0 && rs0 == kr0) {
-          // test hook: this stage is never filled, so the consumers' wait on
-          // it can only give up; nothing is issued into it
-          if (++s == pp.stages) { s = 0; ph ^= 1; }
-          rs0 = re;
-          continue;
-        }
         if constexpr (TMA) {
           // int8 pools: four tensor copies per stage (K and V codes, K and V
           // scales), always whole boxes of st rows starting at row rs0; rows
@@ -1232,6 +1227,7 @@ __global__ void __launch_bounds__((consumer_warps<T>() + 1) * 32, 1)
       mbar_init(pp.empty(s), NW);
     }
     mbar_init(pp.group(), NW);
+    mbar_init(pp.stall(), 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -1313,7 +1309,16 @@ __global__ void __launch_bounds__((consumer_warps<T>() + 1) * 32, 1)
 
   if (warp == NW) {
     run_producer<sizeof(T) == 1>(p, pp, maps, s_cu, lane, x0, x1);
-  } else if constexpr (sizeof(T) == 1) {
+    return;
+  }
+  if (p.skip_fill == 2 || (p.skip_fill == 1 && blockIdx.x == 0)) {
+    // test hook: the consumers first wait on a barrier nothing arrives at,
+    // which can only give up at the bound; they then leave without
+    // releasing a stage, so the producer's wait for a free stage gives up too
+    mbar_wait(pp.stall(), 0, make_wait_ctl(p.err, p.wait_ns, p.epoch));
+    return;
+  }
+  if constexpr (sizeof(T) == 1) {
     run_consumer_i8<D, G>(p, pp, warp, lane);
   } else if constexpr (sizeof(T) == 2) {
     run_consumer_mma<D, G>(p, pp, warp, lane);
@@ -1426,7 +1431,7 @@ Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int 
   // merge buffers of warps sharing a kv head
   const int mbuf = hkv < nw ? 4 * nw * G * (D + 2) : 0;
   int fixed = 0;
-  fixed += 8 * (2 * kMaxStages + 1);              // barriers
+  fixed += 8 * (2 * kMaxStages + 2);              // barriers
   fixed = align_up(fixed, 16) + 16 * kMaxStages;  // descriptors
   fixed = align_up(fixed, 16) + 8 * (batch + 1);  // cu
   fixed = align_up(fixed, 16) + 8 * 32;           // scan scratch
@@ -1440,7 +1445,7 @@ Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int 
   if (stages > kMaxStages) stages = kMaxStages;
   L.stages = stages;
   int off = align_up(stages * stage_bytes, 128);
-  L.off_bar = off;   off += 8 * (2 * stages + 1);
+  L.off_bar = off;   off += 8 * (2 * stages + 2);
   off = align_up(off, 16); L.off_desc = off; off += 16 * stages;
   off = align_up(off, 16); L.off_cu = off;   off += 8 * (batch + 1);
   off = align_up(off, 16); L.off_scan = off; off += 8 * 32;

@@ -78,7 +78,7 @@ struct PfParams {
   float qscale;
   unsigned long long wait_ns;  // bound of one wait (0 = the default)
   int epoch;  // this launch's number (see WaitCtl)
-  int skip_fill;  // test hook: 1 = CTA 0, 2 = every CTA leaves its first K tile unloaded
+  int skip_fill;  // test hook: 1 = CTA 0, 2 = every CTA stalls its MMA warp
 };
 
 // ---- tcgen05 / TMA helpers ----------------------------------------------------
@@ -408,6 +408,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t b_ofree0 = smem_addr(&bars[7 + 2 * kSlots]);  // O of A / B read by the epilogue
   const uint32_t b_drain = smem_addr(&bars[9 + 2 * kSlots]);
   const uint32_t b_qempty = smem_addr(&bars[10 + 2 * kSlots]);  // an item's S products read Q
+  const uint32_t b_stall = smem_addr(&bars[11 + 2 * kSlots]);   // never arrived at (test hook)
   auto slot_full = [&](int i) { return b_full0 + 8u * i; };
   auto slot_empty = [&](int i) { return b_empty0 + 8u * i; };
   auto slot_ptr = [&](int i) { return smem + kOffKV + i * kTileBytes; };
@@ -426,6 +427,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(b_ofree0 + 8u * x, 4);
     }
     mbar_init(b_drain, 1);
+    mbar_init(b_stall, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -449,9 +451,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (warp == kWarpTma) {
     // ================= TMA producer: per item Q, then K(0) V(0) K(1) V(1) ... =================
     const int box_bytes = p.bs * 128;
-    long long ld = 0;        // K / V loads issued so far (ring position)
-    long long skipped = -1;  // the load the test hook left out
-    int jq = 0;              // items whose Q was loaded
+    long long ld = 0;  // K / V loads issued so far (ring position)
+    int jq = 0;        // items whose Q was loaded
     for (long long i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       const Item it = make_item(p, i, tid);
       if (!it.valid) continue;
@@ -474,12 +475,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           break;
         }
         const int t = li >> 1, is_v = li & 1;
-        if ((p.skip_fill == 2 || (p.skip_fill == 1 && blockIdx.x == 0)) && ld == 0) {
-          // test hook: K(0) of the first item is never loaded, so the MMA
-          // warp's wait on it can only give up; nothing is issued into it
-          skipped = ld;
-          continue;
-        }
         if (lane == 0) mbar_arrive_expect_tx(slot_full(slot), kTileBytes);
         __syncwarp();
         for (int k2 = lane; k2 < 2 * blocks_per_tile; k2 += 32) {
@@ -506,7 +501,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // most one load in flight (it is refilled only after its release), so the
     // last load of each slot and the last Q load are the ones to wait for.
     for (long long idx = ld - kSlots; idx < ld; ++idx) {
-      if (idx < 0 || idx == skipped) continue;
+      if (idx < 0) continue;
       mbar_wait_drain(slot_full((int)(idx % kSlots)), (uint32_t)((idx / kSlots) & 1), p.err);
     }
     if (jq > 0) mbar_wait_drain(b_qfull, (uint32_t)((jq - 1) & 1), p.err);
@@ -515,6 +510,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // per item: S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ..., so
     // each warpgroup's softmax overlaps the other tile's products
     if (lane == 0) {
+      if (p.skip_fill == 2 || (p.skip_fill == 1 && blockIdx.x == 0)) {
+        // test hook: a wait on a barrier nothing arrives at, which can only
+        // give up at the bound; no product is issued, so the other warps'
+        // waits give up in turn
+        mbar_wait_sleep(b_stall, 0, w);
+        ok = false;
+      }
       const uint32_t q_addr = smem_addr(sQ);
       long long ld = 0;            // K / V loads consumed so far
       int jq = 0;                  // items started
