@@ -292,6 +292,31 @@ __device__ __forceinline__ bool group_sync(const Pipe& pp, uint32_t& gph, int la
 
 // ---- producer warp -----------------------------------------------------------
 
+// Table entries, first-block offsets and lengths of 32 consecutive blocks of
+// the flat list, one block per lane: loaded one batch ahead of their use, so
+// their global-load latency overlaps the stages of the batch before.
+struct Lookup {
+  int bl;           // sequence of this lane's block
+  long long j, nb;  // its index in the sequence, the sequence's block count
+  int blk, off, len;
+};
+
+__device__ __forceinline__ Lookup lookup_batch(const Params& p, const long long* s_cu, int lane,
+                                               long long base, long long x1, int bseq) {
+  Lookup L;
+  const long long xl = base + lane;
+  const bool valid = xl < x1;
+  int bl = bseq;
+  if (valid) while (s_cu[bl + 1] <= xl) ++bl;
+  L.bl = bl;
+  L.j = valid ? xl - s_cu[bl] : 0;
+  L.nb = s_cu[bl + 1] - s_cu[bl];
+  L.blk = valid ? __ldg(p.bt + (long long)bl * p.mb + L.j) : 0;
+  L.off = valid && p.offs ? __ldg(p.offs + bl) : 0;
+  L.len = valid ? __ldg(p.lens + bl) : 0;
+  return L;
+}
+
 template <bool TMA>
 __device__ void run_producer(const Params& p, const Pipe& pp, const I8Maps& maps,
                              const long long* s_cu, int lane, long long x0, long long x1) {
@@ -311,36 +336,33 @@ __device__ void run_producer(const Params& p, const Pipe& pp, const I8Maps& maps
   bool ok = true;
   const int r_lane = lane & 15;
   const bool v_lane = lane >= 16;
+  const uint32_t dst_lane = smem_addr(pp.smem) + (v_lane ? ST * p.rs : 0) + r_lane * p.rs;
+  const char* src_lane = (v_lane ? p.v_base : p.k_base) + (long long)r_lane * p.row_bytes;
+  Lookup nxt = lookup_batch(p, s_cu, lane, x0, x1, bseq);
   for (long long base = x0; base < x1 && ok; base += 32) {
-    // lane-parallel lookup of 32 consecutive blocks: sequence, table entry, rows
-    const long long xl = base + lane;
-    const bool valid = xl < x1;
-    int bl = bseq;
-    if (valid) while (s_cu[bl + 1] <= xl) ++bl;
-    const long long j = valid ? xl - s_cu[bl] : 0;
-    const long long nb = s_cu[bl + 1] - s_cu[bl];
-    int blk = 0, r0 = 0, r1 = p.bs;
-    if (valid) {
-      blk = p.bt[(long long)bl * p.mb + j];
-      const int off = p.offs ? p.offs[bl] : 0;
-      if (j == 0) r0 = off;
-      if (j == nb - 1) r1 = (int)(((long long)off + p.lens[bl] - 1) % p.bs) + 1;
-    }
+    // this batch of 32 blocks (looked up one batch ago); then start the
+    // next batch's loads
+    const Lookup cur = nxt;
     const int cnt = (int)min((long long)32, x1 - base);
+    if (base + 32 < x1)
+      nxt = lookup_batch(p, s_cu, lane, base + 32, x1, __shfl_sync(kFull, cur.bl, cnt - 1));
+    int r0 = 0, r1 = p.bs;
+    if (cur.j == 0) r0 = cur.off;
+    if (cur.j == cur.nb - 1) r1 = (int)(((long long)cur.off + cur.len - 1) % p.bs) + 1;
     for (int k = 0; k < cnt && ok; ++k) {
-      const int kb = __shfl_sync(kFull, bl, k);
-      const int kblk = __shfl_sync(kFull, blk, k);
+      const int kb = __shfl_sync(kFull, cur.bl, k);
+      const int kblk = __shfl_sync(kFull, cur.blk, k);
       const int kr0 = __shfl_sync(kFull, r0, k);
       const int kr1 = __shfl_sync(kFull, r1, k);
-      const long long kj = __shfl_sync(kFull, j, k);
-      const long long knb = __shfl_sync(kFull, nb, k);
+      const long long kj = __shfl_sync(kFull, cur.j, k);
+      const long long knb = __shfl_sync(kFull, cur.nb, k);
       const long long kx = base + k;
       const bool blk_ok = kblk >= 0 && (long long)kblk < p.num_blocks;
       if (!blk_ok && lane == 0) set_error(p.err, kErrIndex);
       const bool seg_start = (kj == 0) || (kx == x0);
       const bool seg_end = (kj == knb - 1) || (kx == x1 - 1);
       const bool single = s_cu[kb] >= x0 && s_cu[kb + 1] <= x1;
-      const long long blk_src = (long long)kblk * p.block_stride;
+      const char* blk_src = src_lane + (long long)kblk * p.block_stride;
       for (int rs0 = kr0; rs0 < kr1;) {
         const int re = min(kr1, (rs0 / ST + 1) * ST);
         const int n = re - rs0;
@@ -349,49 +371,48 @@ __device__ void run_producer(const Params& p, const Pipe& pp, const I8Maps& maps
         if (seg_end && re == kr1) flags |= kEnd;
         if (kx == x1 - 1 && re == kr1) flags |= kLast;
         if (single) flags |= kSingle;
+        const int4 desc = make_int4(kb, blk_ok ? n : 0, flags, (int)blockIdx.x + kb);
+        const uint32_t full = pp.full(s);
+        const uint32_t stage = (uint32_t)s * pp.stage_bytes;
         if (!mbar_wait(pp.empty(s), ph, w)) { ok = false; break; }
         if constexpr (TMA) {
           // int8 pools: four tensor copies per stage (K and V codes, K and V
           // scales), always whole boxes of st rows starting at row rs0; rows
           // past n are never read (past the pool they arrive as zeros)
           if (lane == 0) {
-            pp.desc[s] = make_int4(kb, blk_ok ? n : 0, flags, (int)blockIdx.x + kb);
+            pp.desc[s] = desc;
             if (blk_ok) {
-              const uint32_t full = pp.full(s);
               mbar_arrive_expect_tx(full, (uint32_t)p.tx_bytes);
               const int row = (int)(kblk * p.rows_per_block + p.layer_row + rs0);
-              const uint32_t base = smem_addr(pp.smem + (size_t)s * pp.stage_bytes);
-              tma_3d(base + p.off_kc, &maps.kc, 0, row, 0, full);
-              tma_3d(base + p.off_vc, &maps.vc, 0, row, 0, full);
-              tma_2d(base + p.off_ks, &maps.ks, 0, row, full);
-              tma_2d(base + p.off_vs, &maps.vs, 0, row, full);
+              const uint32_t base_s = smem_addr(pp.smem) + stage;
+              tma_3d(base_s + p.off_kc, &maps.kc, 0, row, 0, full);
+              tma_3d(base_s + p.off_vc, &maps.vc, 0, row, 0, full);
+              tma_2d(base_s + p.off_ks, &maps.ks, 0, row, full);
+              tma_2d(base_s + p.off_vs, &maps.vs, 0, row, full);
             } else {
-              mbar_arrive(pp.full(s));
+              mbar_arrive(full);
             }
           }
-          __syncwarp();
         } else {
-        if (lane == 0) {
-          pp.desc[s] = make_int4(kb, blk_ok ? n : 0, flags, (int)blockIdx.x + kb);
-          if (blk_ok) mbar_arrive_expect_tx(pp.full(s), 2u * n * p.row_bytes);
-          else mbar_arrive(pp.full(s));
+          // lane 0 posts the stage's byte count while lanes 0-15 (K) and
+          // 16-31 (V) issue one row copy each: a copy that completes before
+          // the count is posted drives the count below zero for a moment,
+          // and the phase cannot complete before lane 0's arrival
+          if (lane == 0) {
+            pp.desc[s] = desc;
+            if (blk_ok) mbar_arrive_expect_tx(full, 2u * n * p.row_bytes);
+            else mbar_arrive(full);
+          }
+          if (blk_ok && r_lane < n)
+            bulk_g2s(dst_lane + stage, blk_src + (long long)rs0 * p.row_bytes, p.row_bytes, full);
         }
         __syncwarp();
-        if (blk_ok && r_lane < n) {
-          const long long src = blk_src + (long long)(rs0 + r_lane) * p.row_bytes;
-          const uint32_t dst = smem_addr(pp.smem + (size_t)s * pp.stage_bytes +
-                                         (v_lane ? ST * p.rs : 0) + r_lane * p.rs);
-          bulk_g2s(dst, (v_lane ? p.v_base : p.k_base) + src, p.row_bytes, pp.full(s));
-        }
-        __syncwarp();
-        }
         filled |= 1u << s;
         fill_par = (fill_par & ~(1u << s)) | (((ph ^ 1u) & 1u) << s);
         if (++s == pp.stages) { s = 0; ph ^= 1; }
         rs0 = re;
       }
     }
-    bseq = __shfl_sync(kFull, bl, cnt - 1);
   }
   // Let every copy already issued land before the CTA (and its shared memory)
   // may go away: the consumers normally waited for them all, but consumers
