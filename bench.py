@@ -713,6 +713,10 @@ def run_legs(args, dev, rank, flush, pkv):
     out["int8_decode"] = int8_leg(args, dev, rank, flush, pkv)
     for name in ("long_splitk", "prefix_mix"):
         out["decode_" + name] = decode_leg(name, args, dev, flush, pkv, min(args.steps, 100))
+    # the prefix-mix batch through shared-prefix decode: its 64 shared blocks
+    # read once (pkv_decode_attention_shared_prefix)
+    out["decode_prefix_mix_shared"] = decode_leg("prefix_mix", args, dev, flush, pkv,
+                                                 min(args.steps, 100), prefix_blocks=64)
     return out
 
 
@@ -727,7 +731,7 @@ def compact_legs(legs: dict, peak: float) -> dict:
     for name in ("scatter", "gather", "copy_blocks"):
         if name in legs:
             c[name + "_frac"] = f(legs[name]["GB/s"] / peak)
-    for name in ("long_splitk", "prefix_mix"):
+    for name in ("long_splitk", "prefix_mix", "prefix_mix_shared"):
         d = legs.get("decode_" + name)
         if d:
             c["decode_" + name] = {k: d[k] for k in ("partial_frac", "call_kv_frac",
@@ -1053,7 +1057,7 @@ def run_reference(args, rank, world):
     }
 
 
-def decode_leg(name: str, args, dev, flush, pkv, steps: int) -> dict:
+def decode_leg(name: str, args, dev, flush, pkv, steps: int, prefix_blocks: int = 0) -> dict:
     """Paged decode attention (pkv_decode_attention) on one bf16 decode
     workload: the partial-pass kernel alone (events the library records
     around it) and the whole call (partial + combine), with the L2 flush
@@ -1073,6 +1077,14 @@ def decode_leg(name: str, args, dev, flush, pkv, steps: int) -> dict:
     ws = torch.empty(pkv.decode_workspace_size(b.batch, w.num_q_heads, w.pool.head_dim, dev),
                      dtype=torch.uint8, device=dev)
     call = lambda: pkv.decode_attention(pool, w.layer, q, w.scale, bt, lens, offs, out, ws)
+    if prefix_blocks:
+        # shared-prefix decode: the library records the events around its
+        # suffix pass, which then stands for the "partial" figures
+        ws = torch.empty(pkv.decode_shared_prefix_workspace_size(pool, b.batch, w.num_q_heads,
+                                                                 prefix_blocks),
+                         dtype=torch.uint8, device=dev)
+        call = lambda: pkv.decode_attention_shared_prefix(pool, w.layer, q, w.scale, bt, lens,
+                                                          offs, prefix_blocks, out, ws)
     for _ in range(args.warmup):
         call()
     torch.cuda.synchronize()

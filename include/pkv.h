@@ -244,6 +244,49 @@ PKV_API pkv_status pkv_decode_step(const pkv_pool* pool, int32_t layer, const vo
                                    void* out, void* workspace, size_t workspace_bytes,
                                    cudaStream_t stream);
 
+/* Paged decode attention over a batch whose sequences share a prefix of
+ * whole blocks (mini-runtime "ch.12 Paged KV Cache" §2.2: a sequence that
+ * hits a cached prefix starts at an offset inside its first block; §2.4:
+ * the prefix blocks are shared through their ref_count, not copied;
+ * "vLLM PagedAttention source notes" §3: shared prefixes are why paging
+ * wastes so little).  The result is that of pkv_decode_attention with the
+ * same arguments; only the way the pool is read differs: the shared prefix is
+ * read once for the whole batch instead of once per sequence.
+ *
+ * Contract: the first num_prefix_blocks entries of row 0 of block_tables
+ * name the shared prefix blocks (all of them, even where sequence 0 ends
+ * earlier), and every sequence's table agrees with row 0 on each of those
+ * entries it spans (a sequence may end inside the prefix; its offset is its
+ * first-block offset as usual).  Validate mode checks both (PKV_ERR_INDEX);
+ * without it, a disagreeing table gives wrong results for that sequence and
+ * an invalid id in row 0 reads zeros and sets the device error word (never
+ * an out-of-range access).  0 <= num_prefix_blocks <=
+ * max_blocks_per_seq, else PKV_ERR_INVALID_ARG.
+ *
+ * How it runs: a suffix pass (the decode partial kernel over the table
+ * entries after the prefix), a prefix pass on the tcgen05 tensor cores (the
+ * queries of all sequences, 128 / G sequences x G heads per MMA tile,
+ * against the prefix's key tiles, split over the GPU; per-row masks from each
+ * sequence's offset and length), and a combine of both by the log-sum-exp
+ * rule.  That path needs bf16 pools with head_dim 128 and block_size 8..128
+ * dividing 128, and batch <= 2048; for other shapes, or num_prefix_blocks ==
+ * 0, the call runs pkv_decode_attention's path instead (same result).
+ * workspace: >= pkv_decode_shared_prefix_workspace_size bytes (contents need
+ * no initialisation).  All other arguments, checks and errors are those of
+ * pkv_decode_attention. */
+PKV_API size_t pkv_decode_shared_prefix_workspace_size(const pkv_pool* pool, int32_t batch,
+                                                       int32_t num_q_heads,
+                                                       int32_t num_prefix_blocks);
+PKV_API pkv_status pkv_decode_attention_shared_prefix(const pkv_pool* pool, int32_t layer,
+                                                      const void* q, int32_t num_q_heads,
+                                                      float scale, const int32_t* block_tables,
+                                                      int32_t max_blocks_per_seq,
+                                                      const int32_t* seq_lens,
+                                                      const int32_t* offsets, int32_t batch,
+                                                      int32_t num_prefix_blocks, void* out,
+                                                      void* workspace, size_t workspace_bytes,
+                                                      cudaStream_t stream);
+
 /* Paged prefill attention (the prefill batch of
  * "vLLM PagedAttention source notes" §2.4: the prompt tokens' K/V are written
  * into their blocks, then attention runs over them), on tcgen05 tensor cores.

@@ -13,6 +13,8 @@ from ._binding import (  # noqa: F401
     build_slot_mapping,
     copy_blocks,
     decode_attention,
+    decode_attention_shared_prefix,
+    decode_shared_prefix_workspace_size,
     decode_step,
     decode_attention_static,
     decode_workspace_size,

@@ -60,6 +60,9 @@ _SIGS = {
                                     _SZ, _P]),
     "pkv_decode_attention_static": (_I32, [_P, _I32, _P, _I32, _F32, _P, _I32, _P, _P, _I32,
                                            _P, _P]),
+    "pkv_decode_shared_prefix_workspace_size": (_SZ, [_P, _I32, _I32, _I32]),
+    "pkv_decode_attention_shared_prefix": (_I32, [_P, _I32, _P, _I32, _F32, _P, _I32, _P, _P,
+                                                  _I32, _I32, _P, _P, _SZ, _P]),
     "pkv_decode_step": (_I32, [_P, _I32, _P, _I32, _F32, _P, _I32, _P, _P, _I32, _P, _P, _P, _P,
                                _SZ, _P]),
     "pkv_copy_blocks": (_I32, [_P, _I32, _P, _P, _I32, _P]),
@@ -272,6 +275,29 @@ def decode_attention(pool: Pool, layer: int, q: torch.Tensor, scale: float,
                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _stream(pool.device))
     _check(st, "pkv_decode_attention")
+
+
+def decode_shared_prefix_workspace_size(pool: Pool, batch: int, num_q_heads: int,
+                                        num_prefix_blocks: int) -> int:
+    with _dev(pool):
+        return int(load().pkv_decode_shared_prefix_workspace_size(pool.ref, batch, num_q_heads,
+                                                                  num_prefix_blocks))
+
+
+def decode_attention_shared_prefix(pool: Pool, layer: int, q: torch.Tensor, scale: float,
+                                   block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                                   offsets: Optional[torch.Tensor], num_prefix_blocks: int,
+                                   out: torch.Tensor, workspace: torch.Tensor) -> None:
+    """Paged decode attention of ``q`` [B, Hq, D] whose sequences share their
+    first ``num_prefix_blocks`` table entries: the prefix is read once."""
+    lib = load()
+    with _dev(pool):
+        st = lib.pkv_decode_attention_shared_prefix(
+            pool.ref, layer, _ptr(q), q.shape[1], float(scale), _ptr(block_tables),
+            block_tables.shape[1], _ptr(seq_lens), _ptr(offsets), seq_lens.numel(),
+            int(num_prefix_blocks), _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _stream(pool.device))
+    _check(st, "pkv_decode_attention_shared_prefix")
 
 
 def decode_step(pool: Pool, layer: int, q: torch.Tensor, scale: float,

@@ -425,6 +425,128 @@ pkv_status pkv_decode_step(const pkv_pool* pool, int32_t layer, const void* q,
                      workspace_bytes, stream);
 }
 
+// Shared-prefix decode: which path a call takes, and the workspace carve of
+// the two-pass path ([decode workspace][prefix m, l][prefix acc]).
+struct PrefixPlan {
+  bool two_pass;  // false: the plain decode path computes the same result
+  int nsplit, per_split;
+  size_t decode_ws, ml_off, acc_off, total;
+};
+
+static PrefixPlan plan_prefix(const pkv::PoolView& v, int32_t batch, int32_t num_q_heads,
+                              int32_t prefix_blocks, const DevInfo& d) {
+  PrefixPlan pl{};
+  const int grid = decode_grid(d);
+  pl.decode_ws = pkv::decode_workspace_bytes(batch, num_q_heads, v.head_dim, grid);
+  pl.total = pl.decode_ws;
+  pl.two_pass = prefix_blocks > 0 && batch > 0 && batch <= pkv::kDecodeMaxBatch &&
+                pkv::prefill_supported(v, num_q_heads) == 0 &&
+                pkv::decode_supported(v, num_q_heads) == 0;
+  if (!pl.two_pass) return pl;
+  pkv::prefix_plan(v, num_q_heads, batch, prefix_blocks, d.sm_count, &pl.nsplit, &pl.per_split);
+  const size_t rows = (size_t)pl.nsplit * batch * num_q_heads;
+  pl.ml_off = (pl.decode_ws + 255) / 256 * 256;
+  pl.acc_off = pl.ml_off + (rows * 2 * 4 + 255) / 256 * 256;
+  pl.total = pl.acc_off + rows * v.head_dim * 4;
+  return pl;
+}
+
+size_t pkv_decode_shared_prefix_workspace_size(const pkv_pool* pool, int32_t batch,
+                                               int32_t num_q_heads, int32_t num_prefix_blocks) {
+  pkv::PoolView v;
+  if (check_pool(pool, false, &v) != PKV_OK) return 0;
+  if (batch < 0 || num_q_heads <= 0 || num_prefix_blocks < 0) return 0;
+  if (num_q_heads % pool->num_kv_heads != 0) return 0;
+  DevInfo* d;
+  if (current_device(&d) != PKV_OK) return 0;
+  return plan_prefix(v, batch, num_q_heads, num_prefix_blocks, *d).total;
+}
+
+pkv_status pkv_decode_attention_shared_prefix(const pkv_pool* pool, int32_t layer, const void* q,
+                                              int32_t num_q_heads, float scale,
+                                              const int32_t* block_tables,
+                                              int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                              const int32_t* offsets, int32_t batch,
+                                              int32_t num_prefix_blocks, void* out,
+                                              void* workspace, size_t workspace_bytes,
+                                              cudaStream_t stream) {
+  pkv::PoolView v;
+  pkv_status st = check_pool(pool, true, &v);
+  if (st != PKV_OK) return st;
+  if (num_prefix_blocks < 0 || (batch > 0 && num_prefix_blocks > max_blocks_per_seq))
+    return PKV_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= pool->num_layers || batch < 0 || num_q_heads <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % pool->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+  if (pkv::decode_supported(v, num_q_heads) != 0) return PKV_ERR_UNSUPPORTED;
+  if (batch == 0) return PKV_OK;
+  DevInfo* d;
+  if ((st = current_device(&d)) != PKV_OK) return st;
+  const PrefixPlan pl = plan_prefix(v, batch, num_q_heads, num_prefix_blocks, *d);
+  if (!pl.two_pass)
+    return decode_call(pool, layer, q, num_q_heads, scale, block_tables, max_blocks_per_seq,
+                       seq_lens, offsets, batch, nullptr, nullptr, false, out, workspace,
+                       workspace_bytes, stream);
+  if (!q || !out || !block_tables || !seq_lens || max_blocks_per_seq <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return PKV_ERR_WORKSPACE;
+  if (workspace_bytes < pl.total) return PKV_ERR_WORKSPACE;
+  const bool validate = g_validate.load() != 0;
+  if (validate) {
+    if ((st = clear_word(d->err, stream)) != PKV_OK) return st;
+    if ((st = launched(pkv::launch_validate_tables(v, block_tables, max_blocks_per_seq, seq_lens,
+                                                   offsets, batch, nullptr, 0, d->err,
+                                                   stream))) != PKV_OK)
+      return st;
+    if ((st = launched(pkv::launch_validate_prefix(v, block_tables, max_blocks_per_seq, seq_lens,
+                                                   offsets, batch, num_prefix_blocks, d->err,
+                                                   stream))) != PKV_OK)
+      return st;
+    if ((st = read_and_clear(d->err, stream)) != PKV_OK) return st;
+  }
+  char* ws = static_cast<char*>(workspace);
+  float* pre_ml = reinterpret_cast<float*>(ws + pl.ml_off);
+  float* pre_acc = reinterpret_cast<float*>(ws + pl.acc_off);
+  pkv::DecodeLaunch a;
+  a.pool = v;
+  a.layer = layer;
+  a.q = q;
+  a.out = out;
+  a.num_q_heads = num_q_heads;
+  a.scale = scale;
+  a.bt = block_tables;
+  a.mb = max_blocks_per_seq;
+  a.lens = seq_lens;
+  a.offs = offsets;
+  a.batch = batch;
+  a.workspace = workspace;
+  a.grid = decode_grid(*d);
+  a.err = d->err;
+  a.smem_optin = d->smem_optin;
+  a.prefix_blocks = num_prefix_blocks;
+  cudaEvent_t ev_start = g_ev_start.load(), ev_stop = g_ev_stop.load();
+  if (ev_start && ev_stop) {
+    a.ev_start = ev_start;
+    a.ev_stop = ev_stop;
+  }
+  // the suffix pass first: the prefix states written after it stay in L2
+  // for the combine
+  cudaError_t e = pkv::launch_decode(a, stream);
+  if (e == cudaErrorInvalidConfiguration) return PKV_ERR_UNSUPPORTED;
+  if ((st = launched(e)) != PKV_OK) return st;
+  if ((st = launched(pkv::launch_prefix_pass(v, layer, q, num_q_heads, scale, block_tables,
+                                             max_blocks_per_seq, seq_lens, offsets, batch,
+                                             num_prefix_blocks, pre_ml, pre_acc, d->err,
+                                             d->sm_count, stream))) != PKV_OK)
+    return st;
+  if ((st = launched(pkv::launch_decode_combine_prefix(a, pre_ml, pre_acc, pl.nsplit, stream))) !=
+      PKV_OK)
+    return st;
+  return validate ? read_and_clear(d->err, stream) : PKV_OK;
+}
+
 pkv_status pkv_prefill_attention(const pkv_pool* pool, int32_t layer, const void* q,
                                  int32_t num_q_heads, float scale, const int32_t* block_tables,
                                  int32_t max_blocks_per_seq, const int32_t* seq_lens,

@@ -318,6 +318,12 @@ cudaError_t launch_validate_tables(const PoolView& p, const int32_t* bt, int mb,
 cudaError_t launch_validate_slots(const PoolView& p, const int64_t* slots, long long n, int* err,
                                   cudaStream_t s);
 
+// Shared-prefix decode: row 0 holds prefix_blocks valid block ids, and every
+// table agrees with row 0 on those of them it spans (kErrIndex otherwise).
+cudaError_t launch_validate_prefix(const PoolView& p, const int32_t* bt, int mb,
+                                   const int32_t* lens, const int32_t* offs, int batch,
+                                   int prefix_blocks, int* err, cudaStream_t s);
+
 cudaError_t launch_validate_tokens(const PoolView& p, const int32_t* bt, int mb,
                                    const int32_t* offs, int batch, const int32_t* tok_seq,
                                    const int32_t* tok_pos, long long n, int* err, cudaStream_t s);
@@ -344,6 +350,10 @@ struct DecodeLaunch {
   // row_bytes), stored at its last position before it is attended to
   const char* k_new = nullptr;
   const char* v_new = nullptr;
+  // shared-prefix decode: > 0 runs the suffix pass over the table entries
+  // after the first prefix_blocks ones, and leaves the combine to
+  // launch_decode_combine_prefix
+  int prefix_blocks = 0;
 };
 
 constexpr int kDecodeMaxBatch = 2048;
@@ -352,6 +362,12 @@ size_t decode_workspace_bytes(int batch, int num_q_heads, int head_dim, int grid
 // 0 = ok; 1 = unsupported shape
 int decode_supported(const PoolView& p, int num_q_heads);
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s);
+// Shared-prefix decode, after the suffix pass (launch_decode with
+// prefix_blocks > 0) and the prefix pass: merge the prefix states
+// (pre_ml [nsplit, batch, hq, 2], pre_acc [nsplit, batch, hq, D], fp32) with
+// the suffix segments in a.workspace and write a.out (bf16).
+cudaError_t launch_decode_combine_prefix(const DecodeLaunch& a, const float* pre_ml,
+                                         const float* pre_acc, int nsplit, cudaStream_t s);
 
 // 0 = the prefill kernel handles this pool and head count; 1 = unsupported
 int prefill_supported(const PoolView& pv, int num_q_heads);
@@ -368,6 +384,18 @@ cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num
 unsigned long long wait_limit_ns();
 int debug_skip_fill();
 int next_launch_epoch();
+
+// Shared-prefix decode, prefix pass (on the prefill kernel): the key tiles of
+// the shared prefix are split in *nsplit ranges of *per_split tiles so that
+// the pass fills the GPU; launch_prefix_pass writes the prefix states of
+// every (split, sequence, q head) to pre_ml [nsplit, batch, hq, 2] and
+// pre_acc [nsplit, batch, hq, D] (fp32).  Supported where prefill_supported.
+void prefix_plan(const PoolView& pv, int num_q_heads, int batch, int prefix_blocks, int sm_count,
+                 int* nsplit, int* per_split);
+cudaError_t launch_prefix_pass(const PoolView& pv, int layer, const void* q, int num_q_heads,
+                               float scale, const int32_t* bt, int mb, const int32_t* lens,
+                               const int32_t* offs, int batch, int prefix_blocks, float* pre_ml,
+                               float* pre_acc, int* err, int sm_count, cudaStream_t s);
 
 // Current-device facts for entry points defined outside api.cu: dynamic
 // shared memory limit, the sticky error word, the decode grid size and the

@@ -295,6 +295,37 @@ __global__ void validate_tables_kernel(const int32_t* __restrict__ bt, int mb,
   }
 }
 
+// Shared-prefix decode: every sequence's table agrees with row 0 on each of
+// the first prefix_blocks entries it spans.
+__global__ void validate_prefix_kernel(const int32_t* __restrict__ bt, int mb,
+                                       const int32_t* __restrict__ lens,
+                                       const int32_t* __restrict__ offs, int batch,
+                                       int prefix_blocks, long long num_blocks, int bs,
+                                       int* err) {
+  griddep_wait();
+  griddep_launch_dependents();
+  // row 0 names every prefix block
+  if (blockIdx.x == 0 && threadIdx.x == 0)
+    for (int k = 0; k < prefix_blocks; ++k)
+      if (bt[k] < 0 || bt[k] >= num_blocks) {
+        set_error(err, kErrIndex);
+        break;
+      }
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < batch; b += gridDim.x * blockDim.x) {
+    const int off = offs ? offs[b] : 0;
+    const int len = lens[b];
+    if (off < 0 || off >= bs || len < 0 || (long long)off + len > (long long)mb * bs) continue;
+    const long long nblk = len > 0 ? ((long long)off + len + bs - 1) / bs : 0;
+    const long long n = nblk < prefix_blocks ? nblk : prefix_blocks;
+    for (long long k = 0; k < n; ++k) {
+      if (bt[(long long)b * mb + k] != bt[k]) {
+        set_error(err, kErrIndex);
+        break;
+      }
+    }
+  }
+}
+
 __global__ void validate_slots_kernel(const int64_t* __restrict__ slots, long long n,
                                       long long limit, int* err) {
   griddep_wait();
@@ -410,6 +441,15 @@ cudaError_t launch_validate_tables(const PoolView& p, const int32_t* bt, int mb,
   if (batch == 0) return cudaSuccess;
   validate_tables_kernel<<<grid_for(batch, 128, 4096), 128, 0, s>>>(
       bt, mb, lens, offs, batch, cu, total, p.num_blocks, p.block_size, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_validate_prefix(const PoolView& p, const int32_t* bt, int mb,
+                                   const int32_t* lens, const int32_t* offs, int batch,
+                                   int prefix_blocks, int* err, cudaStream_t s) {
+  if (batch == 0 || prefix_blocks == 0) return cudaSuccess;
+  validate_prefix_kernel<<<grid_for(batch, 128, 4096), 128, 0, s>>>(
+      bt, mb, lens, offs, batch, prefix_blocks, p.num_blocks, p.block_size, err);
   return cudaGetLastError();
 }
 

@@ -72,6 +72,11 @@ constexpr unsigned kFull = 0xffffffffu;
 
 enum : int { kStart = 1, kEnd = 2, kLast = 4, kSingle = 8 };
 
+// Kernel modes: plain decode attention, the fused decode step (new rows
+// stored first), and the suffix pass of shared-prefix decode (the table
+// entries after the shared prefix; every state goes to the workspace).
+enum : int { kModePlain = 0, kModeStep = 1, kModeSuffix = 2 };
+
 struct Params {
   const char* k_base;  // block 0, this layer, row 0
   const char* v_base;
@@ -110,6 +115,7 @@ struct Params {
   char* v_out;
   int new_row_bytes;
   int scale_off;
+  int prefix_blocks;  // shared-prefix suffix pass: table entries of the shared prefix
   unsigned long long wait_ns;  // bound of one wait (0 = the default)
   int epoch;  // this launch's number (see WaitCtl)
   int skip_fill;  // test hook: 1 = CTA 0, 2 = every CTA stalls its consumers
@@ -254,6 +260,7 @@ __device__ __forceinline__ float butterfly(float (&v)[G], int lane) {
 
 // Blocks spanned by sequence b; 0 for an empty or invalid sequence (reported
 // by CTA 0 only, so the error word is touched once per launch).
+template <int MODE>
 __device__ __forceinline__ long long seq_blocks(const Params& p, int b, bool report) {
   const int len = p.lens[b];
   const int off = p.offs ? p.offs[b] : 0;
@@ -262,7 +269,9 @@ __device__ __forceinline__ long long seq_blocks(const Params& p, int b, bool rep
     return 0;
   }
   if (len == 0) return 0;
-  return ((long long)off + len + p.bs - 1) / p.bs;
+  const long long nb = ((long long)off + len + p.bs - 1) / p.bs;
+  if constexpr (MODE == kModeSuffix) return nb > p.prefix_blocks ? nb - p.prefix_blocks : 0;
+  return nb;
 }
 
 // Shared-memory pipeline handles.
@@ -301,6 +310,7 @@ struct Lookup {
   int blk, off, len;
 };
 
+template <int MODE>
 __device__ __forceinline__ Lookup lookup_batch(const Params& p, const long long* s_cu, int lane,
                                                long long base, long long x1, int bseq) {
   Lookup L;
@@ -314,10 +324,17 @@ __device__ __forceinline__ Lookup lookup_batch(const Params& p, const long long*
   L.blk = valid ? __ldg(p.bt + (long long)bl * p.mb + L.j) : 0;
   L.off = valid && p.offs ? __ldg(p.offs + bl) : 0;
   L.len = valid ? __ldg(p.lens + bl) : 0;
+  if constexpr (MODE == kModeSuffix) {
+    // the blocks after the shared prefix, read from row 0 of the block: the
+    // suffix starts on a fresh block
+    L.blk = valid ? __ldg(p.bt + (long long)bl * p.mb + p.prefix_blocks + L.j) : 0;
+    L.len = L.off + L.len - p.prefix_blocks * p.bs;
+    L.off = 0;
+  }
   return L;
 }
 
-template <bool TMA>
+template <bool TMA, int MODE>
 __device__ void run_producer(const Params& p, const Pipe& pp, const I8Maps& maps,
                              const long long* s_cu, int lane, long long x0, long long x1) {
   const WaitCtl w = make_wait_ctl(p.err, p.wait_ns, p.epoch);
@@ -338,14 +355,15 @@ __device__ void run_producer(const Params& p, const Pipe& pp, const I8Maps& maps
   const bool v_lane = lane >= 16;
   const uint32_t dst_lane = smem_addr(pp.smem) + (v_lane ? ST * p.rs : 0) + r_lane * p.rs;
   const char* src_lane = (v_lane ? p.v_base : p.k_base) + (long long)r_lane * p.row_bytes;
-  Lookup nxt = lookup_batch(p, s_cu, lane, x0, x1, bseq);
+  Lookup nxt = lookup_batch<MODE>(p, s_cu, lane, x0, x1, bseq);
   for (long long base = x0; base < x1 && ok; base += 32) {
     // this batch of 32 blocks (looked up one batch ago); then start the
     // next batch's loads
     const Lookup cur = nxt;
     const int cnt = (int)min((long long)32, x1 - base);
     if (base + 32 < x1)
-      nxt = lookup_batch(p, s_cu, lane, base + 32, x1, __shfl_sync(kFull, cur.bl, cnt - 1));
+      nxt = lookup_batch<MODE>(p, s_cu, lane, base + 32, x1,
+                               __shfl_sync(kFull, cur.bl, cnt - 1));
     int r0 = 0, r1 = p.bs;
     if (cur.j == 0) r0 = cur.off;
     if (cur.j == cur.nb - 1) r1 = (int)(((long long)cur.off + cur.len - 1) % p.bs) + 1;
@@ -361,7 +379,9 @@ __device__ void run_producer(const Params& p, const Pipe& pp, const I8Maps& maps
       if (!blk_ok && lane == 0) set_error(p.err, kErrIndex);
       const bool seg_start = (kj == 0) || (kx == x0);
       const bool seg_end = (kj == knb - 1) || (kx == x1 - 1);
-      const bool single = s_cu[kb] >= x0 && s_cu[kb + 1] <= x1;
+      // a sequence wholly inside this CTA is finished here, unless its
+      // shared-prefix state still has to be merged in
+      const bool single = MODE != kModeSuffix && s_cu[kb] >= x0 && s_cu[kb + 1] <= x1;
       const char* blk_src = src_lane + (long long)kblk * p.block_stride;
       for (int rs0 = kr0; rs0 < kr1;) {
         const int re = min(kr1, (rs0 / ST + 1) * ST);
@@ -1208,7 +1228,7 @@ __device__ void run_consumer_fma(const Params& p, const Pipe& pp, int warp, int 
 
 // ---- the partial-pass kernel -------------------------------------------------
 
-template <typename T, int D, int G, bool FUSED>
+template <typename T, int D, int G, int MODE>
 __global__ void __launch_bounds__((consumer_warps<T>() + 1) * 32, 1)
     decode_partial_kernel(const Params p, const __grid_constant__ I8Maps maps) {
   constexpr int NW = consumer_warps<T>();
@@ -1234,7 +1254,7 @@ __global__ void __launch_bounds__((consumer_warps<T>() + 1) * 32, 1)
   const int beg = min(B, tid * per), end = min(B, beg + per);
   const bool report = blockIdx.x == 0;
   long long local = 0;
-  for (int b = beg; b < end; ++b) local += seq_blocks(p, b, report);
+  for (int b = beg; b < end; ++b) local += seq_blocks<MODE>(p, b, report);
   long long x = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -1256,7 +1276,7 @@ __global__ void __launch_bounds__((consumer_warps<T>() + 1) * 32, 1)
   for (int w = 0; w < warp; ++w) run += s_scan[w];
   for (int b = beg; b < end; ++b) {
     s_cu[b] = run;
-    run += seq_blocks(p, b, false);
+    run += seq_blocks<MODE>(p, b, false);
   }
   long long total = 0;
   for (int w = 0; w < kThreads / 32; ++w) total += s_scan[w];
@@ -1276,7 +1296,7 @@ __global__ void __launch_bounds__((consumer_warps<T>() + 1) * 32, 1)
   }
   if (x0 >= x1) return;
 
-  if constexpr (FUSED) {
+  if constexpr (MODE == kModeStep) {
     // The decode step: this CTA's block range holds the last block of some
     // sequences; their new K/V rows go into the pool here, before any bulk
     // copy of this CTA reads it.  No other CTA reads those rows: a
@@ -1329,7 +1349,7 @@ __global__ void __launch_bounds__((consumer_warps<T>() + 1) * 32, 1)
   }
 
   if (warp == NW) {
-    run_producer<sizeof(T) == 1>(p, pp, maps, s_cu, lane, x0, x1);
+    run_producer<sizeof(T) == 1, MODE>(p, pp, maps, s_cu, lane, x0, x1);
     return;
   }
   if (p.skip_fill == 2 || (p.skip_fill == 1 && blockIdx.x == 0)) {
@@ -1407,6 +1427,54 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const float* __rest
     M = bm;
   }
   o[i] = T(den > 0.f ? num / den : 0.f);
+}
+
+// Shared-prefix decode: per output element (sequence, q head, d), merge the
+// prefix pass's states of the sequence (one per split of the prefix keys)
+// with the suffix pass's segments of it (none when the sequence ends inside
+// the prefix), by the same log-sum-exp rule.  Grid: (ceil(hq*D / 256), batch).
+template <typename T>
+__global__ void __launch_bounds__(256)
+    decode_combine_prefix_kernel(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml,
+                                 const long long* __restrict__ ws_cu,
+                                 const long long* __restrict__ ws_meta,
+                                 const float* __restrict__ pre_acc,
+                                 const float* __restrict__ pre_ml, int nsplit, int batch, int hq,
+                                 int D, T* __restrict__ out) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int b = blockIdx.y;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= hq * D) return;
+  const int h = i / D, d = i - h * D;
+  float M = -INFINITY, num = 0.f, den = 0.f;
+  auto merge = [&](float m, float l, float a) {
+    if (m == -INFINITY) return;
+    if (m > M) {
+      const float r = exp2f(M - m);  // 0 while M is still -inf (the sums are 0 then)
+      num *= r;
+      den *= r;
+      M = m;
+    }
+    const float w = exp2f(m - M);
+    num += w * a;
+    den += w * l;
+  };
+#pragma unroll 4
+  for (int c = 0; c < nsplit; ++c) {
+    const long long row = ((long long)c * batch + b) * hq + h;
+    merge(__ldcs(pre_ml + 2 * row), __ldcs(pre_ml + 2 * row + 1), __ldcs(pre_acc + row * D + d));
+  }
+  const long long c0 = __ldcs(ws_cu + b), c1 = __ldcs(ws_cu + b + 1);
+  if (c1 > c0) {
+    const long long W = __ldcs(ws_meta);
+    const long long cf = c0 / W, cl = (c1 - 1) / W;
+    for (long long seg = cf; seg <= cl; ++seg) {
+      const long long row = (seg + b) * hq + h;
+      merge(__ldcs(ws_ml + 2 * row), __ldcs(ws_ml + 2 * row + 1), __ldcs(ws_acc + row * D + d));
+    }
+  }
+  out[(long long)b * hq * D + i] = T(den > 0.f ? num / den : 0.f);
 }
 
 // ---- host side -----------------------------------------------------------------
@@ -1510,7 +1578,7 @@ cudaError_t ensure_smem(K kern, int smem, int (&configured)[64]) {
   return e;
 }
 
-template <typename T, int D, int G, bool FUSED>
+template <typename T, int D, int G, int MODE>
 cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   const PoolView& pv = a.pool;
   Params p{};
@@ -1567,6 +1635,7 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   p.v_out = pv.v_mut ? pv.v_mut + layer_off : nullptr;
   p.new_row_bytes = pv.num_kv_heads * pv.head_dim * pv.io_size;
   p.scale_off = pv.scale_off;
+  p.prefix_blocks = a.prefix_blocks;
   p.wait_ns = wait_limit_ns();
   p.epoch = next_launch_epoch();
   p.skip_fill = debug_skip_fill();
@@ -1591,7 +1660,7 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
                       sstrides, sbox, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
-  auto kern = decode_partial_kernel<T, D, G, FUSED>;
+  auto kern = decode_partial_kernel<T, D, G, MODE>;
   static int configured[64] = {0};
   cudaError_t e = ensure_smem(kern, L.smem, configured);
   if (e != cudaSuccess) return e;
@@ -1603,6 +1672,9 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
                     maps);
   if (e != cudaSuccess) return e;
   if (a.ev_stop && (e = cudaEventRecord(a.ev_stop, s)) != cudaSuccess) return e;
+  // the suffix pass of shared-prefix decode: its combine runs after the
+  // prefix pass (launch_decode_combine_prefix)
+  if constexpr (MODE == kModeSuffix) return cudaSuccess;
   // int8 pools take and return bf16
   using OutT = std::conditional_t<sizeof(T) == 1, __nv_bfloat16, T>;
   const dim3 cgrid((p.hq * D + 255) / 256, a.batch);
@@ -1611,20 +1683,26 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
                        (const long long*)p.ws_meta, p.hq, D, static_cast<OutT*>(a.out));
 }
 
-template <typename T, int D, bool FUSED>
+template <typename T, int D, int MODE>
 cudaError_t run_gf(const DecodeLaunch& a, const Layout& L, int G, cudaStream_t s) {
   switch (G) {
-    case 1: return run<T, D, 1, FUSED>(a, L, s);
-    case 2: return run<T, D, 2, FUSED>(a, L, s);
-    case 4: return run<T, D, 4, FUSED>(a, L, s);
-    case 8: return run<T, D, 8, FUSED>(a, L, s);
+    case 1: return run<T, D, 1, MODE>(a, L, s);
+    case 2: return run<T, D, 2, MODE>(a, L, s);
+    case 4: return run<T, D, 4, MODE>(a, L, s);
+    case 8: return run<T, D, 8, MODE>(a, L, s);
   }
   return cudaErrorInvalidValue;
 }
 
 template <typename T, int D>
 cudaError_t run_g(const DecodeLaunch& a, const Layout& L, int G, cudaStream_t s) {
-  return a.k_new ? run_gf<T, D, true>(a, L, G, s) : run_gf<T, D, false>(a, L, G, s);
+  if (a.prefix_blocks > 0) {
+    // the suffix pass exists for the shapes the prefix pass supports
+    if constexpr (std::is_same_v<T, __nv_bfloat16> && D == 128)
+      return run_gf<T, D, kModeSuffix>(a, L, G, s);
+    return cudaErrorInvalidConfiguration;
+  }
+  return a.k_new ? run_gf<T, D, kModeStep>(a, L, G, s) : run_gf<T, D, kModePlain>(a, L, G, s);
 }
 
 }  // namespace
@@ -1661,6 +1739,20 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s) {
                               : run_g<__nv_bfloat16, 64>(a, L, G, s);
   }
   return pv.head_dim == 128 ? run_g<float, 128>(a, L, G, s) : run_g<float, 64>(a, L, G, s);
+}
+
+cudaError_t launch_decode_combine_prefix(const DecodeLaunch& a, const float* pre_ml,
+                                         const float* pre_acc, int nsplit, cudaStream_t s) {
+  const int D = a.pool.head_dim;
+  const WsLayout W = ws_layout(a.batch, a.num_q_heads, D, a.grid);
+  const char* ws = static_cast<const char*>(a.workspace);
+  const dim3 cgrid((a.num_q_heads * D + 255) / 256, a.batch);
+  return launch_kernel(decode_combine_prefix_kernel<__nv_bfloat16>, cgrid, dim3(256), 0, s, true,
+                       reinterpret_cast<const float*>(ws + W.acc),
+                       reinterpret_cast<const float*>(ws + W.ml),
+                       reinterpret_cast<const long long*>(ws + W.cu),
+                       reinterpret_cast<const long long*>(ws + W.meta), pre_acc, pre_ml, nsplit,
+                       a.batch, a.num_q_heads, D, static_cast<__nv_bfloat16*>(a.out));
 }
 
 }  // namespace pkv

@@ -76,6 +76,13 @@ struct PfParams {
   long long n_items;  // pairs x batch x kv heads
   int mb, batch, hq, hkv, G, TQ, bs, L, layer, max_q_len;
   float qscale;
+  // shared-prefix decode (prefix pass): the queries are the decode queries of
+  // the batch's sequences (q [batch, hq, D]); the keys are the first
+  // prefix_blocks entries of table row 0, in key_tiles tiles split into
+  // nsplit ranges of per_split tiles; the states go to pre_ml / pre_acc
+  int prefix_blocks, key_tiles, nsplit, per_split;
+  float* pre_ml;
+  float* pre_acc;
   unsigned long long wait_ns;  // bound of one wait (0 = the default)
   int epoch;  // this launch's number (see WaitCtl)
   int skip_fill;  // test hook: 1 = CTA 0, 2 = every CTA stalls its MMA warp
@@ -336,6 +343,7 @@ struct Item {
   int b, g, nA, nB;
   long long q0, nq, qtA, qtB, first_pos, spanned;
   int off;
+  int t0, c;  // shared-prefix prefix pass: first key tile and split index
 };
 
 __device__ __forceinline__ Item make_item(const PfParams& p, long long i, int tid) {
@@ -375,11 +383,42 @@ __device__ __forceinline__ Item make_item(const PfParams& p, long long i, int ti
   return it;
 }
 
+// Prefix pass of shared-prefix decode: item i is (query-tile pair px, key
+// split c, kv head g).  Tile B = 2 px always exists, tile A = 2 px + 1 when
+// the batch has it; both attend to the key tiles [t0, t0 + nB) of the
+// prefix, read through table row 0 (every sequence's table starts with the
+// same prefix blocks).  Per-row key masks come from each sequence's offset
+// and length (softmax).
+__device__ __forceinline__ Item make_item_prefix(const PfParams& p, long long i) {
+  Item it{};
+  const long long per = (long long)p.nsplit * p.hkv;
+  const long long px = i / per;
+  const long long rem = i - px * per;
+  it.c = (int)(rem / p.hkv);
+  it.g = (int)(rem - (long long)it.c * p.hkv);
+  it.b = 0;
+  it.q0 = 0;
+  it.nq = p.batch;
+  const long long ntq = (it.nq + p.TQ - 1) / p.TQ;
+  if (px >= (ntq + 1) / 2) return it;
+  it.t0 = it.c * p.per_split;
+  const int nkt = min(p.key_tiles, it.t0 + p.per_split) - it.t0;
+  if (nkt <= 0) return it;
+  it.qtB = 2 * px;
+  it.qtA = 2 * px + 1;
+  it.nB = nkt;
+  it.nA = it.qtA < ntq ? nkt : 0;
+  it.spanned = p.prefix_blocks;
+  it.valid = true;
+  return it;
+}
+
 // Persistent: one CTA per SM walks the items c, c + grid, c + 2 grid, ...
 // (pairs of every sequence and head in order of decreasing key count).  The
 // K/V ring, the barrier phases and the TMEM allocation carry over from item
 // to item, so the next item's loads and first products overlap the previous
 // item's epilogue.
+template <bool PREFIX>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const PfParams p) {
@@ -454,7 +493,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     long long ld = 0;  // K / V loads issued so far (ring position)
     int jq = 0;        // items whose Q was loaded
     for (long long i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-      const Item it = make_item(p, i, tid);
+      const Item it = PREFIX ? make_item_prefix(p, i) : make_item(p, i, tid);
       if (!it.valid) continue;
       // Q of this item once the previous item's S products have read the old one
       if (jq > 0 && !mbar_wait_sleep(b_qempty, (jq - 1) & 1, w)) { ok = false; break; }
@@ -480,7 +519,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int k2 = lane; k2 < 2 * blocks_per_tile; k2 += 32) {
           const int h = k2 / blocks_per_tile;
           const int k = k2 % blocks_per_tile;
-          const long long lb = (long long)t * blocks_per_tile + k;  // logical block
+          const long long lb = (long long)(PREFIX ? it.t0 + t : t) * blocks_per_tile + k;
           long long coord = p.blk_coord_limit;                       // out of range: zeros
           if (lb < it.spanned) {
             const int blk = p.bt[(long long)it.b * p.mb + lb];
@@ -548,7 +587,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         umma_commit(b_pvdone0 + 8u * x);
       };
       for (long long i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-        const Item it = make_item(p, i, tid);
+        const Item it = PREFIX ? make_item_prefix(p, i) : make_item(p, i, tid);
         if (!it.valid) continue;
         const int nA = it.nA, nB = it.nB;
         const long long base = ld;  // load index of K(0) of this item
@@ -609,7 +648,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t b_pvdone = b_pvdone0 + 8u * x, b_ofree = b_ofree0 + 8u * x;
     long long nt = 0;  // tiles of this warpgroup across items (barrier phases)
     for (long long i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-      const Item it = make_item(p, i, tid);
+      const Item it = PREFIX ? make_item_prefix(p, i) : make_item(p, i, tid);
       if (!it.valid) continue;
       const int nX = x == 0 ? it.nA : it.nB;
       if (nX == 0) continue;
@@ -621,15 +660,38 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       // tile has no padding rows (and t = 0 only without a first-block offset)
       const int t_mask_lo = (int)((it.off + it.first_pos + qt * TQ) / kKeys);
       const bool rows_full = (qt + 1) * TQ <= it.nq;
+      // prefix pass: the row is the decode query of sequence qi, whose keys
+      // in the prefix are the table positions [key_lo, key_hi) (its offset
+      // up to the end of its tokens or of the prefix); a sequence whose
+      // offset or length is out of range has none
+      long long key_lo = 0, key_hi = 0;
+      if (PREFIX && row_ok) {
+        const long long ob = p.offs ? p.offs[qi] : 0;
+        const long long lb = p.lens[qi];
+        if (ob >= 0 && ob < p.bs && lb >= 0 && ob + lb <= (long long)p.mb * p.bs) {
+          key_lo = ob;
+          key_hi = min((long long)p.prefix_blocks * p.bs, ob + lb);
+        }
+      }
       RowState st{-INFINITY, 0.f};
       for (int t = 0; t < nX && ok; ++t, ++nt) {
         const bool waited = mbar_wait_sleep(b_sfull, (uint32_t)(nt & 1), w);
         if (!__all_sync(0xffffffffu, waited)) { ok = false; break; }
         tc_fence_after();
-        const long long tp0 = (long long)t * kKeys;
-        const int c_lo = (int)max(0ll, (long long)it.off - tp0);
-        const int c_hi = row_ok ? (int)min((long long)kKeys - 1, pos + it.off - tp0) : -1;
-        const bool full_tile = (t > 0 || it.off == 0) && t < t_mask_lo && rows_full;
+        int c_lo, c_hi;
+        bool full_tile;
+        if constexpr (PREFIX) {
+          const long long tp0 = (long long)(it.t0 + t) * kKeys;
+          c_lo = (int)max(0ll, key_lo - tp0);
+          c_hi = (int)max(-1ll, min((long long)kKeys - 1, key_hi - 1 - tp0));
+          // warp-uniform: the tile is full only if it is for every row of the warp
+          full_tile = __all_sync(0xffffffffu, c_lo == 0 && c_hi == kKeys - 1);
+        } else {
+          const long long tp0 = (long long)t * kKeys;
+          c_lo = (int)max(0ll, (long long)it.off - tp0);
+          c_hi = row_ok ? (int)min((long long)kKeys - 1, pos + it.off - tp0) : -1;
+          full_tile = (t > 0 || it.off == 0) && t < t_mask_lo && rows_full;
+        }
         softmax_tile(tS(x), tO(x), lane_base, t, c_lo, c_hi, full_tile, p.qscale, st);
         tc_fence_before();
         __syncwarp();
@@ -640,6 +702,31 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const bool waited = mbar_wait_sleep(b_pvdone, (uint32_t)((nt - 1) & 1), w);
       if (!__all_sync(0xffffffffu, waited)) { ok = false; break; }
       tc_fence_after();
+      if constexpr (PREFIX) {
+        // the row's state (m, l, unnormalised O) for the decode combine
+        const long long row = ((long long)it.c * p.batch + qi) * p.hq + (long long)it.g * G + hh;
+        if (row_ok) {
+          p.pre_ml[2 * row] = st.m_used;
+          p.pre_ml[2 * row + 1] = st.l;
+        }
+        float* arow = p.pre_acc + row * kD;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kD; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tO(x) + lane_base + c0, v);
+          tmem_wait_ld();
+          if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<uint4*>(arow + c0 + j) = make_uint4(v[j], v[j + 1], v[j + 2],
+                                                                    v[j + 3]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_ofree);
+        continue;
+      }
       const float inv = st.l > 0.f ? 1.f / st.l : 0.f;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
                             ((it.q0 + qi) * p.hq + (long long)it.g * G + hh) * kD;
@@ -708,19 +795,22 @@ int prefill_supported(const PoolView& pv, int num_q_heads) {
   return 0;
 }
 
-cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num_q_heads,
-                           float scale, const int32_t* bt, int mb, const int32_t* lens,
-                           const int32_t* offs, const int64_t* cu_q, int batch, long long total_q,
-                           int max_q_len, void* out, int* err, int sm_count, cudaStream_t s) {
-  if (batch == 0 || total_q == 0 || max_q_len == 0) return cudaSuccess;
+namespace {
+
+// Tensor maps and the common parameters of a prefill-kernel launch: q as
+// (d, q head, token) boxes of (64, G, TQ), the pool as (d, kv head, row,
+// block*L + layer) boxes of one block per 64-column half.
+cudaError_t prefill_setup(const PoolView& pv, int layer, const void* q, int num_q_heads,
+                          float scale, const int32_t* bt, int mb, const int32_t* lens,
+                          const int32_t* offs, int batch, long long total_q, int* err,
+                          CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv, PfParams* pp) {
   const int G = num_q_heads / pv.num_kv_heads;
   const int TQ = kRows / G;
-  CUtensorMap tq, tk, tv;
   {
     cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
     cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)num_q_heads * kD * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)TQ};
-    if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box,
+    if (!encode_tiled(tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
@@ -731,9 +821,9 @@ cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num
     cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)pv.row_bytes,
                              (cuuint64_t)pv.row_bytes * pv.block_size};
     cuuint32_t box[4] = {64, 1, (cuuint32_t)pv.block_size, 1};
-    if (!encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pv.k, dims, strides, box,
+    if (!encode_tiled(tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pv.k, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pv.v, dims, strides, box,
+        !encode_tiled(tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, pv.v, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
@@ -741,8 +831,6 @@ cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num
   p.bt = bt;
   p.lens = lens;
   p.offs = offs;
-  p.cu_q = reinterpret_cast<const long long*>(cu_q);
-  p.out = out;
   p.err = err;
   p.total_q = total_q;
   p.blk_coord_limit = nl;
@@ -756,26 +844,88 @@ cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num
   p.bs = pv.block_size;
   p.L = pv.num_layers;
   p.layer = layer;
-  p.max_q_len = max_q_len;
   p.qscale = scale * kLog2e;
   p.wait_ns = wait_limit_ns();
   p.epoch = next_launch_epoch();
   p.skip_fill = debug_skip_fill();
+  *pp = p;
+  return cudaSuccess;
+}
+
+template <bool PREFIX>
+cudaError_t prefill_launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const PfParams& p, int sm_count, cudaStream_t s) {
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && configured[dev] == 0) {
-    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(prefill_kernel<PREFIX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  const long long ntq = (max_q_len + TQ - 1) / TQ;
-  p.n_items = (ntq + 1) / 2 * (long long)batch * pv.num_kv_heads;
   const long long grid = p.n_items < sm_count ? p.n_items : sm_count;
-  return launch_kernel(prefill_kernel, dim3((unsigned)grid), dim3(kPfThreads), (size_t)kSmemBytes,
-                       s, true, tq, tk, tv, p);
+  return launch_kernel(prefill_kernel<PREFIX>, dim3((unsigned)grid), dim3(kPfThreads),
+                       (size_t)kSmemBytes, s, true, tq, tk, tv, p);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num_q_heads,
+                           float scale, const int32_t* bt, int mb, const int32_t* lens,
+                           const int32_t* offs, const int64_t* cu_q, int batch, long long total_q,
+                           int max_q_len, void* out, int* err, int sm_count, cudaStream_t s) {
+  if (batch == 0 || total_q == 0 || max_q_len == 0) return cudaSuccess;
+  CUtensorMap tq, tk, tv;
+  PfParams p;
+  cudaError_t e = prefill_setup(pv, layer, q, num_q_heads, scale, bt, mb, lens, offs, batch,
+                                total_q, err, &tq, &tk, &tv, &p);
+  if (e != cudaSuccess) return e;
+  p.cu_q = reinterpret_cast<const long long*>(cu_q);
+  p.out = out;
+  p.max_q_len = max_q_len;
+  const long long ntq = (max_q_len + p.TQ - 1) / p.TQ;
+  p.n_items = (ntq + 1) / 2 * (long long)batch * pv.num_kv_heads;
+  return prefill_launch<false>(tq, tk, tv, p, sm_count, s);
+}
+
+void prefix_plan(const PoolView& pv, int num_q_heads, int batch, int prefix_blocks, int sm_count,
+                 int* nsplit, int* per_split) {
+  const int G = num_q_heads / pv.num_kv_heads;
+  const long long TQ = kRows / G;
+  const long long ntq = (batch + TQ - 1) / TQ;
+  const long long base = (ntq + 1) / 2 * pv.num_kv_heads;  // items of one key split
+  const long long kt = ((long long)prefix_blocks * pv.block_size + kKeys - 1) / kKeys;
+  long long want = base > 0 ? (sm_count + base - 1) / base : 1;  // splits that fill the GPU
+  if (want < 1) want = 1;
+  if (want > kt) want = kt;
+  const long long ps = (kt + want - 1) / want;
+  *per_split = (int)ps;
+  *nsplit = (int)((kt + ps - 1) / ps);
+}
+
+cudaError_t launch_prefix_pass(const PoolView& pv, int layer, const void* q, int num_q_heads,
+                               float scale, const int32_t* bt, int mb, const int32_t* lens,
+                               const int32_t* offs, int batch, int prefix_blocks, float* pre_ml,
+                               float* pre_acc, int* err, int sm_count, cudaStream_t s) {
+  if (batch == 0 || prefix_blocks == 0) return cudaSuccess;
+  CUtensorMap tq, tk, tv;
+  PfParams p;
+  cudaError_t e = prefill_setup(pv, layer, q, num_q_heads, scale, bt, mb, lens, offs, batch,
+                                batch, err, &tq, &tk, &tv, &p);
+  if (e != cudaSuccess) return e;
+  int nsplit = 1, per_split = 1;
+  prefix_plan(pv, num_q_heads, batch, prefix_blocks, sm_count, &nsplit, &per_split);
+  p.prefix_blocks = prefix_blocks;
+  p.key_tiles = (int)(((long long)prefix_blocks * pv.block_size + kKeys - 1) / kKeys);
+  p.nsplit = nsplit;
+  p.per_split = per_split;
+  p.pre_ml = pre_ml;
+  p.pre_acc = pre_acc;
+  const long long ntq = (batch + p.TQ - 1) / p.TQ;
+  p.n_items = (ntq + 1) / 2 * (long long)nsplit * pv.num_kv_heads;
+  return prefill_launch<true>(tq, tk, tv, p, sm_count, s);
 }
 
 }  // namespace pkv
