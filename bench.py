@@ -1156,7 +1156,8 @@ def ncu_case(kind: str, launches: int = 4) -> int:
         torch.cuda.synchronize()
         print(f"ncu case prefill: {launches} launches done")
         return 0
-    name = {"decode_long": "long_splitk", "decode_prefix": "prefix_mix"}.get(
+    name = {"decode_long": "long_splitk", "decode_prefix": "prefix_mix",
+            "decode_prefix_shared": "prefix_mix"}.get(
         kind, WORKLOAD if kind.startswith("decode") else LEG_WORKLOAD)
     w = make_workload(name)
     sp = w.pool
@@ -1183,6 +1184,12 @@ def ncu_case(kind: str, launches: int = 4) -> int:
         ws = torch.empty(pkv.decode_workspace_size(b.batch, w.num_q_heads, sp.head_dim, dev),
                          dtype=torch.uint8, device=dev)
         fn = lambda: pkv.decode_attention(pool, 0, q, w.scale, bt, lens, offs, out, ws)
+        if kind == "decode_prefix_shared":
+            ws = torch.empty(pkv.decode_shared_prefix_workspace_size(pool, b.batch, w.num_q_heads,
+                                                                     64),
+                             dtype=torch.uint8, device=dev)
+            fn = lambda: pkv.decode_attention_shared_prefix(pool, 0, q, w.scale, bt, lens, offs,
+                                                            64, out, ws)
         if kind in ("decode_step", "decode_step_i8"):
             kn = rand_rows((b.batch,) + row, "bf16", 2, dev)
             vn = rand_rows((b.batch,) + row, "bf16", 3, dev)
@@ -1219,7 +1226,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ncu-case", choices=["decode", "decode_step", "decode_i8", "decode_step_i8",
                                            "decode_long",
-                                           "decode_prefix",
+                                           "decode_prefix", "decode_prefix_shared",
                                            "gather", "scatter",
                                            "prefill"],
                     help="run a small-footprint case of one kernel (for ncu) and exit")

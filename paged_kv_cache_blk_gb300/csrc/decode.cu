@@ -1368,113 +1368,96 @@ __global__ void __launch_bounds__((consumer_warps<T>() + 1) * 32, 1)
   }
 }
 
-// Merge the partial states of every segment of a sequence, one thread per
-// output element (sequence, q head, d); sequences handled by a single CTA were
-// written by the partial pass already.  One pass over the segments, eight at a
-// time with all their loads in flight together, keeps a running maximum and
-// rescales the sums when it rises.  The loads are marked evict-first: the
-// states are dead once read.  Grid: (ceil(hq*D / 256), batch).
-template <typename T>
-__global__ void __launch_bounds__(256) decode_combine_kernel(const float* __restrict__ ws_acc,
-                                                             const float* __restrict__ ws_ml,
-                                                             const long long* __restrict__ ws_cu,
-                                                             const long long* __restrict__ ws_meta,
-                                                             int hq, int D, T* __restrict__ out) {
-  griddep_wait();
-  griddep_launch_dependents();
-  const int b = blockIdx.y;
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= hq * D) return;
-  const long long c0 = __ldcs(ws_cu + b), c1 = __ldcs(ws_cu + b + 1);
-  const long long W = __ldcs(ws_meta);
-  T* o = out + (long long)b * hq * D;
-  if (c1 <= c0) {  // no tokens (or an invalid sequence): zeros
-    o[i] = T(0.f);
-    return;
-  }
-  const long long cf = c0 / W, cl = (c1 - 1) / W;
-  if (cf == cl) return;
-  const int n = (int)(cl - cf + 1);
-  const int h = i / D, d = i - h * D;
-  const long long ml_stride = (long long)hq * 2, acc_stride = (long long)hq * D;
-  const float* mlp = ws_ml + ((cf + b) * hq + h) * 2;
-  const float* accp = ws_acc + ((cf + b) * hq + h) * D + d;
-  constexpr int U = 8;
-  float M = -INFINITY, num = 0.f, den = 0.f;
-  for (int k0 = 0; k0 < n; k0 += U) {
-    float mv[U], lv[U], av[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const bool in = k0 + u < n;
-      mv[u] = in ? __ldcs(mlp + (k0 + u) * ml_stride) : -INFINITY;
-      lv[u] = in ? __ldcs(mlp + (k0 + u) * ml_stride + 1) : 0.f;
-      av[u] = in ? __ldcs(accp + (k0 + u) * acc_stride) : 0.f;
-    }
-    float bm = M;
-#pragma unroll
-    for (int u = 0; u < U; ++u) bm = fmaxf(bm, mv[u]);
-    if (bm == -INFINITY) continue;
-    const float r = exp2f(M - bm);  // 0 while M is still -inf (the sums are 0 then)
-    num *= r;
-    den *= r;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (mv[u] == -INFINITY) continue;
-      const float w = exp2f(mv[u] - bm);
-      num += w * av[u];
-      den += w * lv[u];
-    }
-    M = bm;
-  }
-  o[i] = T(den > 0.f ? num / den : 0.f);
-}
-
-// Shared-prefix decode: per output element (sequence, q head, d), merge the
-// prefix pass's states of the sequence (one per split of the prefix keys)
-// with the suffix pass's segments of it (none when the sequence ends inside
-// the prefix), by the same log-sum-exp rule.  Grid: (ceil(hq*D / 256), batch).
-template <typename T>
+// Merge the partial states of every segment of a sequence.  One warp per
+// (sequence, q head); lane i holds the D/32 consecutive outputs d = i D/32 ..
+// The segments are the shared-prefix states (nsplit of them, prefix pass of
+// shared-prefix decode; none otherwise) followed by the sequence's segments
+// of the partial pass.  The lanes load 32 segments' (m, l) at once, take
+// their maximum and weights by warp reductions, then every lane adds the
+// weighted accumulators of those segments with independent vector loads:
+// two dependent memory round trips per 32 segments, and one wave of warps
+// for the batch.  Sequences the partial pass finished itself (wholly inside
+// one CTA, no prefix states) are skipped; a sequence with no tokens gets
+// zeros.  The loads are evict-first: the states are dead once read.
+template <typename T, int D>
 __global__ void __launch_bounds__(256)
-    decode_combine_prefix_kernel(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml,
-                                 const long long* __restrict__ ws_cu,
-                                 const long long* __restrict__ ws_meta,
-                                 const float* __restrict__ pre_acc,
-                                 const float* __restrict__ pre_ml, int nsplit, int batch, int hq,
-                                 int D, T* __restrict__ out) {
+    decode_combine_kernel(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml,
+                          const long long* __restrict__ ws_cu,
+                          const long long* __restrict__ ws_meta,
+                          const float* __restrict__ pre_acc, const float* __restrict__ pre_ml,
+                          int nsplit, int batch, int hq, T* __restrict__ out) {
+  constexpr int VPL = D / 32;
   griddep_wait();
   griddep_launch_dependents();
-  const int b = blockIdx.y;
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= hq * D) return;
-  const int h = i / D, d = i - h * D;
-  float M = -INFINITY, num = 0.f, den = 0.f;
-  auto merge = [&](float m, float l, float a) {
-    if (m == -INFINITY) return;
-    if (m > M) {
-      const float r = exp2f(M - m);  // 0 while M is still -inf (the sums are 0 then)
-      num *= r;
-      den *= r;
-      M = m;
-    }
-    const float w = exp2f(m - M);
-    num += w * a;
-    den += w * l;
-  };
-#pragma unroll 4
-  for (int c = 0; c < nsplit; ++c) {
-    const long long row = ((long long)c * batch + b) * hq + h;
-    merge(__ldcs(pre_ml + 2 * row), __ldcs(pre_ml + 2 * row + 1), __ldcs(pre_acc + row * D + d));
-  }
+  const int lane = threadIdx.x & 31;
+  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (wid >= (long long)batch * hq) return;
+  const int b = (int)(wid / hq), h = (int)(wid - (long long)b * hq);
+  T* o = out + wid * D + lane * VPL;
   const long long c0 = __ldcs(ws_cu + b), c1 = __ldcs(ws_cu + b + 1);
+  long long cf = 0, nsuf = 0;
   if (c1 > c0) {
     const long long W = __ldcs(ws_meta);
-    const long long cf = c0 / W, cl = (c1 - 1) / W;
-    for (long long seg = cf; seg <= cl; ++seg) {
-      const long long row = (seg + b) * hq + h;
-      merge(__ldcs(ws_ml + 2 * row), __ldcs(ws_ml + 2 * row + 1), __ldcs(ws_acc + row * D + d));
+    cf = c0 / W;
+    nsuf = (c1 - 1) / W - cf + 1;
+  }
+  if (nsplit == 0 && nsuf <= 1) {
+    if (nsuf == 0) {  // no tokens (or an invalid sequence): zeros
+#pragma unroll
+      for (int e = 0; e < VPL; ++e) o[e] = T(0.f);
+    }
+    return;
+  }
+  const long long nseg = nsplit + nsuf;
+  // state row of segment sg: a prefix state, or a partial-pass segment
+  auto row_of = [&](long long sg) -> long long {
+    return sg < nsplit ? ((long long)sg * batch + b) * hq + h : (cf + (sg - nsplit) + b) * hq + h;
+  };
+  float M = -INFINITY, den = 0.f, acc[VPL];
+#pragma unroll
+  for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
+  for (long long base = 0; base < nseg; base += 32) {
+    const long long sl = base + lane;
+    float m = -INFINITY, l = 0.f;
+    if (sl < nseg) {
+      const float2 v =
+          __ldcs(reinterpret_cast<const float2*>((sl < nsplit ? pre_ml : ws_ml) + 2 * row_of(sl)));
+      m = v.x;
+      l = v.y;
+    }
+    float cm = m;
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) cm = fmaxf(cm, __shfl_xor_sync(kFull, cm, x));
+    if (cm == -INFINITY) continue;  // no keys in these segments
+    const float nM = fmaxf(M, cm);
+    const float r = exp2f(M - nM);  // 0 while M is still -inf (the sums are 0 then)
+    den *= r;
+#pragma unroll
+    for (int e = 0; e < VPL; ++e) acc[e] *= r;
+    M = nM;
+    const float wgt = m == -INFINITY ? 0.f : exp2f(m - nM);
+    float wl = wgt * l;
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) wl += __shfl_xor_sync(kFull, wl, x);
+    den += wl;
+    const int n = (int)min(32ll, nseg - base);
+#pragma unroll 4
+    for (int j = 0; j < n; ++j) {
+      const float wj = __shfl_sync(kFull, wgt, j);
+      const long long sg = base + j;
+      const float* a = (sg < nsplit ? pre_acc : ws_acc) + row_of(sg) * D + lane * VPL;
+      if constexpr (VPL == 4) {
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(a));
+        acc[0] += wj * v.x; acc[1] += wj * v.y; acc[2] += wj * v.z; acc[3] += wj * v.w;
+      } else {
+        const float2 v = __ldcs(reinterpret_cast<const float2*>(a));
+        acc[0] += wj * v.x; acc[1] += wj * v.y;
+      }
     }
   }
-  out[(long long)b * hq * D + i] = T(den > 0.f ? num / den : 0.f);
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+  for (int e = 0; e < VPL; ++e) o[e] = T(acc[e] * inv);
 }
 
 // ---- host side -----------------------------------------------------------------
@@ -1677,10 +1660,11 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   if constexpr (MODE == kModeSuffix) return cudaSuccess;
   // int8 pools take and return bf16
   using OutT = std::conditional_t<sizeof(T) == 1, __nv_bfloat16, T>;
-  const dim3 cgrid((p.hq * D + 255) / 256, a.batch);
-  return launch_kernel(decode_combine_kernel<OutT>, cgrid, dim3(256), 0, s, pdl,
+  const unsigned cgrid = (unsigned)(((long long)a.batch * p.hq + 7) / 8);
+  return launch_kernel(decode_combine_kernel<OutT, D>, dim3(cgrid), dim3(256), 0, s, pdl,
                        (const float*)p.ws_acc, (const float*)p.ws_ml, (const long long*)p.ws_cu,
-                       (const long long*)p.ws_meta, p.hq, D, static_cast<OutT*>(a.out));
+                       (const long long*)p.ws_meta, (const float*)nullptr, (const float*)nullptr,
+                       0, a.batch, p.hq, static_cast<OutT*>(a.out));
 }
 
 template <typename T, int D, int MODE>
@@ -1746,13 +1730,14 @@ cudaError_t launch_decode_combine_prefix(const DecodeLaunch& a, const float* pre
   const int D = a.pool.head_dim;
   const WsLayout W = ws_layout(a.batch, a.num_q_heads, D, a.grid);
   const char* ws = static_cast<const char*>(a.workspace);
-  const dim3 cgrid((a.num_q_heads * D + 255) / 256, a.batch);
-  return launch_kernel(decode_combine_prefix_kernel<__nv_bfloat16>, cgrid, dim3(256), 0, s, true,
-                       reinterpret_cast<const float*>(ws + W.acc),
+  if (D != 128) return cudaErrorInvalidValue;
+  const unsigned cgrid = (unsigned)(((long long)a.batch * a.num_q_heads + 7) / 8);
+  return launch_kernel(decode_combine_kernel<__nv_bfloat16, 128>, dim3(cgrid), dim3(256), 0, s,
+                       true, reinterpret_cast<const float*>(ws + W.acc),
                        reinterpret_cast<const float*>(ws + W.ml),
                        reinterpret_cast<const long long*>(ws + W.cu),
                        reinterpret_cast<const long long*>(ws + W.meta), pre_acc, pre_ml, nsplit,
-                       a.batch, a.num_q_heads, D, static_cast<__nv_bfloat16*>(a.out));
+                       a.batch, a.num_q_heads, static_cast<__nv_bfloat16*>(a.out));
 }
 
 }  // namespace pkv
