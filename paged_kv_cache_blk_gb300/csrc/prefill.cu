@@ -423,7 +423,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const PfParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  griddep_wait();
+  // Prefix pass of shared-prefix decode: it reads nothing the grid before it
+  // (the suffix pass) writes, and that grid's own inputs were complete when
+  // it let this one launch, so its CTAs start as soon as the suffix pass
+  // frees their SMs; each waits for the suffix pass only before it exits, so
+  // the combine after this grid still sees both.
+  if constexpr (!PREFIX) griddep_wait();
   griddep_launch_dependents();
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -780,6 +785,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                  "r"(kTmemCols)
                  : "memory");
   }
+  if constexpr (PREFIX) griddep_wait();
 }
 
 // ---- host side ------------------------------------------------------------------
