@@ -1099,13 +1099,22 @@ def decode_leg(name: str, args, dev, flush, pkv, steps: int, prefix_blocks: int 
     db = decode_bytes(b, w.pool.row_bytes, w.num_q_heads, w.pool.head_dim, w.pool.elem_size,
                       w.pool.block_size)
     uniq = unique_kv_bytes(b, w.pool.row_bytes, w.pool.block_size, w.pool.num_blocks)
-    dram = recorded_traffic(f"decode_partial_{name}_traffic.txt")
+    part_bytes = db["total"]
+    if prefix_blocks:
+        # the partial pass is the suffix pass: the rows after the shared
+        # prefix, the queries, the states and table entries it reads
+        tot = b.offsets.astype(np.int64) + b.seq_lens.astype(np.int64)
+        suffix_rows = np.maximum(0, tot - prefix_blocks * w.pool.block_size)
+        part_bytes = db["total"] - db["kv"] + int(suffix_rows.sum()) * 2 * w.pool.row_bytes
+    dram = recorded_traffic(f"decode_partial_{name}{'_shared' if prefix_blocks else ''}"
+                            "_traffic.txt")
     gbs = lambda nbytes, ms: nbytes / (ms / 1e3) / 1e9
     entry = {
         "partial_ms": round(part_ms, 4), "call_ms": round(call_ms, 4),
         "kv_bytes": db["kv"], "unique_kv_bytes": uniq, "algorithmic_bytes": db["total"],
-        "partial_GBps": round(gbs(db["total"], part_ms), 1),
-        "partial_frac": round(gbs(db["total"], part_ms) / peak, 4),
+        "partial_bytes": part_bytes,
+        "partial_GBps": round(gbs(part_bytes, part_ms), 1),
+        "partial_frac": round(gbs(part_bytes, part_ms) / peak, 4),
         "call_kv_GBps": round(gbs(db["kv"], call_ms), 1),
         "call_kv_frac": round(gbs(db["kv"], call_ms) / peak, 4),
         "call_unique_GBps": round(gbs(uniq, call_ms), 1),
