@@ -84,9 +84,10 @@ typedef enum {
  * next step of paged caches; the scheme below is this library's reading).
  * Its token row (all kv heads of one token) is a byte row of
  *     R = num_kv_heads * head_dim + pad16(4 * num_kv_heads)
- * bytes: the num_kv_heads * head_dim int8 codes (head-major), then one fp32
- * scale per kv head (little-endian), then padding to a multiple of 16 bytes.
- * The stored value of element d of head g is code[g][d] * scale[g]. */
+ * bytes: the num_kv_heads * head_dim codes (head-major, each stored offset
+ * binary as the byte code + 128, codes in [-127, 127]), then one fp32 scale
+ * per kv head (little-endian), then padding to a multiple of 16 bytes.  The
+ * stored value of element d of head g is code[g][d] * scale[g]. */
 typedef enum { PKV_F32 = 0, PKV_BF16 = 1, PKV_I8 = 2 } pkv_dtype;
 
 /* Pool descriptor: two device tensors [num_blocks, num_layers, block_size,

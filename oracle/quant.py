@@ -19,8 +19,9 @@ taken here are the plainest ones that keep every other step unchanged:
   of zeros has scale 0 and codes 0.  Dequantised value: ``code * scale``.
 * Row format: a pool is bytes ``[num_blocks, num_layers, block_size, R]``
   with ``R = Hkv * D + pad16(4 * Hkv)``; a token row holds the Hkv * D codes
-  (int8, head-major) followed by the Hkv scales (fp32, little-endian) and
-  padding up to a multiple of 16 bytes.  The scatter leaves the padding
+  (head-major, each stored offset binary as the byte ``code + 128``, so the
+  kernels turn a byte into a number without a sign fix-up) followed by the
+  Hkv scales (fp32, little-endian) and padding up to a multiple of 16 bytes.  The scatter leaves the padding
   bytes untouched; nothing reads them.
 * Attention over an int8 pool is attention over the dequantised K and V, in
   fp64, with the bf16 query (the decode definition of ``oracle.oracle``).
@@ -39,7 +40,7 @@ import numpy as np
 from .oracle import attention_fp64, gather_loop, widen
 
 __all__ = [
-    "QMAX", "row_bytes", "quantize_head", "quantize_rows", "write_slots_i8",
+    "QMAX", "row_bytes", "code_bytes", "quantize_head", "quantize_rows", "write_slots_i8",
     "unpack_rows", "dequantize_rows", "decode_attention_i8", "decode_attention_i8_pairs",
 ]
 
@@ -85,11 +86,17 @@ def quantize_rows(x_bits: np.ndarray):
     return codes, scales
 
 
+def code_bytes(codes: np.ndarray) -> np.ndarray:
+    """The stored byte of each code: offset binary, ``code + 128`` (codes in
+    [-127, 127] become bytes 1..255)."""
+    return (np.asarray(codes).astype(np.int16) + 128).astype(np.uint8)
+
+
 def _store_row(row: np.ndarray, codes: np.ndarray, scales: np.ndarray) -> None:
     """Write one token's codes ``[Hkv, D]`` and scales ``[Hkv]`` into its byte
     row, leaving the padding bytes as they were."""
     H, D = codes.shape
-    row[:H * D] = codes.reshape(-1).view(np.uint8)
+    row[:H * D] = code_bytes(codes).reshape(-1)
     row[H * D:H * D + 4 * H] = np.asarray(scales, dtype="<f4").view(np.uint8)
 
 
@@ -123,7 +130,7 @@ def unpack_rows(rows: np.ndarray, num_kv_heads: int, head_dim: int):
     rows = np.ascontiguousarray(rows, dtype=np.uint8)
     n = rows.shape[0]
     H, D = num_kv_heads, head_dim
-    codes = rows[:, :H * D].copy().view(np.int8).reshape(n, H, D)
+    codes = (rows[:, :H * D].astype(np.int16) - 128).astype(np.int8).reshape(n, H, D)
     scales = rows[:, H * D:H * D + 4 * H].copy().view("<f4").reshape(n, H).astype(np.float32)
     return codes, scales
 

@@ -694,16 +694,15 @@ __device__ void run_consumer_mma(const Params& p, const Pipe& pp, int warp, int 
 // an fp16 tile in the warp's shared memory so the ldmatrix.trans path of the
 // bf16 consumer serves unchanged.
 
-// Four int8 codes -> two fp16x2 holding code + 1152 (codes 0,1 and 2,3):
-// each code, offset by 128, becomes the low mantissa byte of 1024 + u.  The
-// bias is removed after the products (kBias times the sum of the other
-// operand), so the conversion is one XOR and two byte permutes.
+// Four stored code bytes (offset binary: u = code + 128) -> two fp16x2
+// holding code + 1152 (codes 0,1 and 2,3): each byte becomes the low mantissa
+// byte of 1024 + u.  The bias is removed after the products (kBias times the
+// sum of the other operand), so the conversion is two byte permutes.
 constexpr float kBias = 1152.f;
 constexpr uint32_t kBiasF16x2 = 0x64806480u;  // (1152, 1152) in fp16
 __device__ __forceinline__ void i8x4_to_f16b(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t x = w ^ 0x80808080u;
-  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(x), "r"(0x64646464u));
-  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(x), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(w), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(w), "r"(0x64646464u));
 }
 
 // Address of 16-byte unit u of line `line` of a code tile written by a tensor

@@ -53,11 +53,12 @@ __device__ __forceinline__ float quantise_head(const float (&x)[VPL], int (&c)[V
   return scale;
 }
 
+// Codes are stored offset binary: the byte of code c is c + 128.
 template <int VPL>
 __device__ __forceinline__ void store_codes(char* dst, const int (&c)[VPL]) {
   uint32_t w[(VPL + 3) / 4] = {};
 #pragma unroll
-  for (int i = 0; i < VPL; ++i) w[i / 4] |= (uint32_t)(c[i] & 0xFF) << (8 * (i % 4));
+  for (int i = 0; i < VPL; ++i) w[i / 4] |= (uint32_t)((c[i] + 128) & 0xFF) << (8 * (i % 4));
   if constexpr (VPL == 8) {
     *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
   } else if constexpr (VPL == 4) {

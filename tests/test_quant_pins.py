@@ -158,14 +158,14 @@ def check_row_format(write_slots_i8, unpack_rows):
         for g in range(H):
             sk = struct.unpack("<f", rk[H * D + 4 * g:H * D + 4 * g + 4].tobytes())[0]
             assert sk == float(np.float32(2.0 ** (g - t)) / np.float32(127))
-            ck = rk[g * D:(g + 1) * D].view(np.int8)
+            ck = rk[g * D:(g + 1) * D].astype(np.int16) - 128       # offset-binary bytes
             assert ck[(t + g) % D] == 127
             # -absmax/2: the fp32 quotient is exactly -63.5, which ties to -64
             assert ck[(t + g + 1) % D] == -64
             assert np.count_nonzero(ck) == 2
             sv = struct.unpack("<f", rv[H * D + 4 * g:H * D + 4 * g + 4].tobytes())[0]
             assert sv == float(np.float32(g + 1.0) / np.float32(127))
-            cv = rv[g * D:(g + 1) * D].view(np.int8)
+            cv = rv[g * D:(g + 1) * D].astype(np.int16) - 128
             assert cv[g] == -127 and np.count_nonzero(cv) == 1
         # padding untouched
         assert np.array_equal(rk[H * D + 4 * H:], k0[blk, layer, row, H * D + 4 * H:])
@@ -177,6 +177,10 @@ def check_row_format(write_slots_i8, unpack_rows):
     codes, scales = unpack_rows(k[1, 1, 1:2], H, D)
     assert codes.shape == (1, H, D) and scales.shape == (1, H)
     assert scales[0, 2] == np.float32(4.0) / np.float32(127)
+    # the byte of code c is c + 128: 0 -> 128, 127 -> 255, -64 -> 64, -127 -> 1
+    rk = k[1, 1, 1]
+    assert rk[(0 + 0) % D] == 255 and rk[(0 + 1) % D] == 64 and rk[5] == 128
+    assert v[1, 1, 1, 0] == 1
 
 
 def check_dequant_formula(dequantize_rows):
@@ -184,7 +188,7 @@ def check_dequant_formula(dequantize_rows):
     R = Q.row_bytes(H, D)
     row = np.zeros((1, R), np.uint8)
     codes = np.arange(-16, 16, dtype=np.int8).reshape(H, D)
-    row[0, :H * D] = codes.reshape(-1).view(np.uint8)
+    row[0, :H * D] = (codes.reshape(-1).astype(np.int16) + 128).astype(np.uint8)
     row[0, H * D:H * D + 8] = np.frombuffer(struct.pack("<ff", 0.5, -3.0), np.uint8)
     got = dequantize_rows(row, H, D)
     want = np.stack([codes[0] * 0.5, codes[1] * -3.0])[None].astype(np.float64)
@@ -359,7 +363,19 @@ def _write_scales_first(k, v, layer, kn, vn, sm, H, D):
             codes, scales = Q.quantize_rows(np.asarray(new[t:t + 1]))
             r = pool[s // bs, layer, s % bs]
             r[:4 * H] = scales[0].astype("<f4").view(np.uint8)
-            r[4 * H:4 * H + H * D] = codes[0].reshape(-1).view(np.uint8)
+            r[4 * H:4 * H + H * D] = Q.code_bytes(codes[0]).reshape(-1)
+
+
+def _write_twos_complement(k, v, layer, kn, vn, sm, H, D):
+    """Codes stored as two's-complement bytes instead of offset binary."""
+    Q.write_slots_i8(k, v, layer, kn, vn, sm, H, D)
+    bs = k.shape[2]
+    for s in sm:
+        if s < 0:
+            continue
+        for pool in (k, v):
+            r = pool[s // bs, layer, s % bs]
+            r[:H * D] = (r[:H * D].astype(np.int16) - 128).astype(np.int8).view(np.uint8)
 
 
 def _deq_divides(rows, H, D):
@@ -395,6 +411,7 @@ PLANTED = [
     ("one scale per token", lambda: check_per_head_scale(_qr_per_token)),
     ("scales big-endian", lambda: check_row_format(_write_big_endian, Q.unpack_rows)),
     ("scales before codes", lambda: check_row_format(_write_scales_first, Q.unpack_rows)),
+    ("codes two's complement", lambda: check_row_format(_write_twos_complement, Q.unpack_rows)),
     ("dequant divides", lambda: check_dequant_formula(_deq_divides)),
     ("decode reads V for K", lambda: check_representable_exact(Q.write_slots_i8,
                                                                _decode_i8_kv_swapped)),

@@ -408,8 +408,8 @@ def fill_pool_i8(k_cache: torch.Tensor, v_cache: torch.Tensor, spec: PoolSpec,
                  k_boost: float = 3.0) -> None:
     """Fill one layer of two int8 pools with seeded random rows: codes are
     N(0,1) * 42 rounded and clipped to [-127, 127] (the spread of absmax-coded
-    Gaussian rows), scales are uniform in [0.01, 0.04] (a Gaussian head's
-    absmax / 127), padding bytes are random.  With ``k_boost_frac`` > 0 the
+    Gaussian rows), stored as the bytes code + 128, scales are uniform in
+    [0.01, 0.04] (a Gaussian head's absmax / 127), padding bytes are random.  With ``k_boost_frac`` > 0 the
     K scales of that fraction of token rows are multiplied by ``k_boost``.
     Drawn on the pool's device in fixed chunks of blocks."""
     dev = k_cache.device
@@ -435,7 +435,7 @@ def fill_pool_i8(k_cache: torch.Tensor, v_cache: torch.Tensor, spec: PoolSpec,
             sc = torch.rand((hi - lo, bs, H), generator=g, device=dev) * 0.03 + 0.01
             if which == 0 and boost is not None:
                 sc = torch.where(boost[lo:hi, :, None], sc * k_boost, sc)
-            rows[:, :, :H * D] = codes.view(torch.uint8)
+            rows[:, :, :H * D] = (codes.to(torch.int16) + 128).to(torch.uint8)  # offset binary
             rows[:, :, H * D:H * D + 4 * H] = sc.contiguous().view(torch.uint8).view(
                 hi - lo, bs, 4 * H)
             pool[lo:hi, layer].copy_(rows)
