@@ -1393,10 +1393,11 @@ __global__ void __launch_bounds__(256)
   if (wid >= (long long)batch * hq) return;
   const int b = (int)(wid / hq), h = (int)(wid - (long long)b * hq);
   T* o = out + wid * D + lane * VPL;
+  // the three index words in one round trip
   const long long c0 = __ldcs(ws_cu + b), c1 = __ldcs(ws_cu + b + 1);
+  const long long W = __ldcs(ws_meta);
   long long cf = 0, nsuf = 0;
   if (c1 > c0) {
-    const long long W = __ldcs(ws_meta);
     cf = c0 / W;
     nsuf = (c1 - 1) / W - cf + 1;
   }
@@ -1412,10 +1413,22 @@ __global__ void __launch_bounds__(256)
   auto row_of = [&](long long sg) -> long long {
     return sg < nsplit ? ((long long)sg * batch + b) * hq + h : (cf + (sg - nsplit) + b) * hq + h;
   };
+  auto load_acc = [&](long long sg, float (&v)[VPL]) {
+    const float* a = (sg < nsplit ? pre_acc : ws_acc) + row_of(sg) * D + lane * VPL;
+    if constexpr (VPL == 4) {
+      const float4 x = __ldcs(reinterpret_cast<const float4*>(a));
+      v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    } else {
+      const float2 x = __ldcs(reinterpret_cast<const float2*>(a));
+      v[0] = x.x; v[1] = x.y;
+    }
+  };
+  constexpr int kAhead = 4;  // accumulators loaded together with the chunk's (m, l)
   float M = -INFINITY, den = 0.f, acc[VPL];
 #pragma unroll
   for (int e = 0; e < VPL; ++e) acc[e] = 0.f;
   for (long long base = 0; base < nseg; base += 32) {
+    const int n = (int)min(32ll, nseg - base);
     const long long sl = base + lane;
     float m = -INFINITY, l = 0.f;
     if (sl < nseg) {
@@ -1423,6 +1436,15 @@ __global__ void __launch_bounds__(256)
           __ldcs(reinterpret_cast<const float2*>((sl < nsplit ? pre_ml : ws_ml) + 2 * row_of(sl)));
       m = v.x;
       l = v.y;
+    }
+    // the first accumulators of the chunk, in flight with the (m, l) loads
+    float av[kAhead][VPL];
+#pragma unroll
+    for (int j = 0; j < kAhead; ++j) {
+      if (j < n) load_acc(base + j, av[j]);
+      else
+#pragma unroll
+        for (int e = 0; e < VPL; ++e) av[j][e] = 0.f;
     }
     float cm = m;
 #pragma unroll
@@ -1439,19 +1461,19 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int x = 16; x > 0; x >>= 1) wl += __shfl_xor_sync(kFull, wl, x);
     den += wl;
-    const int n = (int)min(32ll, nseg - base);
+#pragma unroll
+    for (int j = 0; j < kAhead; ++j) {
+      const float wj = __shfl_sync(kFull, wgt, j);  // 0 past n: no segment
+#pragma unroll
+      for (int e = 0; e < VPL; ++e) acc[e] += wj * av[j][e];
+    }
 #pragma unroll 4
-    for (int j = 0; j < n; ++j) {
+    for (int j = kAhead; j < n; ++j) {
       const float wj = __shfl_sync(kFull, wgt, j);
-      const long long sg = base + j;
-      const float* a = (sg < nsplit ? pre_acc : ws_acc) + row_of(sg) * D + lane * VPL;
-      if constexpr (VPL == 4) {
-        const float4 v = __ldcs(reinterpret_cast<const float4*>(a));
-        acc[0] += wj * v.x; acc[1] += wj * v.y; acc[2] += wj * v.z; acc[3] += wj * v.w;
-      } else {
-        const float2 v = __ldcs(reinterpret_cast<const float2*>(a));
-        acc[0] += wj * v.x; acc[1] += wj * v.y;
-      }
+      float v[VPL];
+      load_acc(base + j, v);
+#pragma unroll
+      for (int e = 0; e < VPL; ++e) acc[e] += wj * v[e];
     }
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
