@@ -777,6 +777,7 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
   float m0 = 0.f, m1 = 0.f, l0 = 0.f, l1 = 0.f;
   bool mv = false;
   int ev = 0;  // biased exponent E of the V-weight normaliser 2^(E-127)
+  float f = __uint_as_float(254u << 23);  // 2^(127-E): the weight factor
   // Offsets of this lane's code units within a stage's code tile.  Every row
   // of a tile holds real data (a tensor copy always fills all ST rows, past
   // the pool with zeros), so rows past n are read as they are: their scores
@@ -821,6 +822,7 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
       m0 = m1 = l0 = l1 = 0.f;
       vb0 = vb1 = 0.f;
       ev = 0;
+      f = __uint_as_float(254u << 23);
 #pragma unroll
       for (int kt = 0; kt < KS; ++kt)
 #pragma unroll
@@ -900,15 +902,21 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
       sc[2] = t1 < n ? ((sa[2] + sq[2]) - kb0) * qs0 * sk1 : -INFINITY;
       sc[3] = t1 < n ? ((sa[3] + sq[3]) - kb1) * qs1 * sk1 : -INFINITY;
       float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+      // The running maxima move only when some lane's stage maximum passes
+      // them (rare after the first tiles); otherwise the reduction would
+      // return them unchanged and the correction factors would be exactly 1.
+      float n0 = m0, n1 = m1, a0 = 1.f, a1 = 1.f;
+      if (!mv || __any_sync(kFull, mx0 > m0 || mx1 > m1)) {
 #pragma unroll
-      for (int o2 = 4; o2 < 32; o2 <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o2));
+        for (int o2 = 4; o2 < 32; o2 <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, o2));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, o2));
+        }
+        n0 = mv ? fmaxf(m0, mx0) : mx0;
+        n1 = mv ? fmaxf(m1, mx1) : mx1;
+        a0 = mv ? exp2f(m0 - n0) : 0.f;
+        a1 = mv ? exp2f(m1 - n1) : 0.f;
       }
-      const float n0 = mv ? fmaxf(m0, mx0) : mx0;
-      const float n1 = mv ? fmaxf(m1, mx1) : mx1;
-      const float a0 = mv ? exp2f(m0 - n0) : 0.f;
-      const float a1 = mv ? exp2f(m1 - n1) : 0.f;
       const float p0 = exp2f(sc[0] - n0), p1 = exp2f(sc[1] - n1);
       const float p2 = exp2f(sc[2] - n0), p3 = exp2f(sc[3] - n1);
       l0 = l0 * a0 + p0 + p2;  // this thread's share; summed over rows at the end
@@ -916,19 +924,23 @@ __device__ void run_consumer_i8(const Params& p, const Pipe& pp, int warp, int l
       m0 = n0;
       m1 = n1;
       mv = true;
-      // running power-of-two normaliser of the V-scaled weights
+      // running power-of-two normaliser of the V-scaled weights, raised only
+      // when some lane's scale exponent passes it (else it stays, and the
+      // rescale is exactly 1)
       int et = max((int)((__float_as_uint(sv0) >> 23) & 0xFF),
                    (int)((__float_as_uint(sv1) >> 23) & 0xFF));
-      et = max(et, __shfl_xor_sync(kFull, et, 4));
-      et = max(et, __shfl_xor_sync(kFull, et, 8));
-      et = max(et, __shfl_xor_sync(kFull, et, 16));
-      const int en = min(253, max(ev, et));
-      // O in units of 2^(ev-127) -> 2^(en-127): an exact power of two (or 0
-      // when the old terms are below 2^-126 of the new scale)
-      const float rescale = ev - en >= -126 ? __uint_as_float((uint32_t)(127 + ev - en) << 23)
-                                            : 0.f;
-      const float f = __uint_as_float((uint32_t)(254 - en) << 23);  // 2^(127-en)
-      ev = en;
+      float rescale = 1.f;
+      if (__any_sync(kFull, et > ev)) {
+        et = max(et, __shfl_xor_sync(kFull, et, 4));
+        et = max(et, __shfl_xor_sync(kFull, et, 8));
+        et = max(et, __shfl_xor_sync(kFull, et, 16));
+        const int en = min(253, max(ev, et));
+        // O in units of 2^(ev-127) -> 2^(en-127): an exact power of two (or 0
+        // when the old terms are below 2^-126 of the new scale)
+        rescale = ev - en >= -126 ? __uint_as_float((uint32_t)(127 + ev - en) << 23) : 0.f;
+        f = __uint_as_float((uint32_t)(254 - en) << 23);  // 2^(127-en)
+        ev = en;
+      }
       const float ra0 = a0 * rescale, ra1 = a1 * rescale;
       // O only changes scale when a running maximum moved (rare after the
       // first tiles): skip the multiplies when no column of the warp moved
