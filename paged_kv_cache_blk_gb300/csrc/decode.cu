@@ -394,7 +394,14 @@ __device__ void run_producer(const Params& p, const Pipe& pp, const I8Maps& maps
         const int4 desc = make_int4(kb, blk_ok ? n : 0, flags, (int)blockIdx.x + kb);
         const uint32_t full = pp.full(s);
         const uint32_t stage = (uint32_t)s * pp.stage_bytes;
-        if (!mbar_wait(pp.empty(s), ph, w)) { ok = false; break; }
+        if constexpr (TMA) {
+          // int8 pools: the consumers are the slower side, so the producer
+          // mostly waits here; it sleeps rather than polls, leaving the issue
+          // slots of its SMSP to the two consumer warps beside it
+          if (!mbar_wait_sleep(pp.empty(s), ph, w)) { ok = false; break; }
+        } else {
+          if (!mbar_wait(pp.empty(s), ph, w)) { ok = false; break; }
+        }
         if constexpr (TMA) {
           // int8 pools: four tensor copies per stage (K and V codes, K and V
           // scales), always whole boxes of st rows starting at row rs0; rows
