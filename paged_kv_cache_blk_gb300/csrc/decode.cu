@@ -14,13 +14,18 @@
 //    into segments; the segment of sequence b inside CTA c has index c + b
 //    (unique because both the ranges and the sequences are in order).
 //  * Inside a CTA one producer warp streams the K and V rows of each block
-//    into a ring of shared-memory stages with bulk copies (cp.async.bulk,
-//    completion counted on an mbarrier).  The 32 lanes issue the 2 x 16 row
-//    copies of a block at once; each token row (all kv heads, 2 KB for Hkv 8,
-//    D 128, bf16) lands in a shared-memory row padded by 16 bytes, so the 8
-//    rows an ldmatrix reads fall in 8 different bank groups.  Only the rows a
-//    sequence covers are fetched (first-block offset and partly filled last
-//    block are trimmed): every byte read from HBM is used once.
+//    into a ring of shared-memory stages, completion counted on an mbarrier.
+//    bf16 pools: per stage, tensor copies (cp.async.bulk.tensor) of boxes of
+//    64 elements x the stage's token rows x all kv heads, K then V, with the
+//    128-byte swizzle, so the 8 rows an ldmatrix reads fall in 8 different
+//    bank groups.  Four copies move a 16-row stage (64 KB for Hkv 8, D 128):
+//    far fewer requests than one copy per row, which is what bounded the
+//    per-SM rate of row copies.  int8 pools: the same with code and scale
+//    boxes.  fp32 pools: the 32 lanes issue one bulk copy (cp.async.bulk) per
+//    token row, each landing in a row padded by 16 bytes.  A stage starts at
+//    the sequence's first row in the block (the first-block offset) and the
+//    consumers use only the rows the sequence covers; a box may carry rows
+//    past them, which are never used (past the pool they arrive as zeros).
 //  * Eight consumer warps compute; warp w serves kv head w % Hkv for all
 //    G = Hq/Hkv query heads of that group, so each K/V byte is read from HBM
 //    once and used by all G heads (GQA grouping).
@@ -30,7 +35,7 @@
 //        pre-scaled scores); P^T goes to shared memory as bf16 and
 //        O^T[d][h] += V^T[d][t] P^T[t][h] with d as M.  About 110
 //        instructions per (stage, head) keep the SM far below its issue rate,
-//        so the bulk-copy pipeline alone sets the speed.
+//        so the copy pipeline alone sets the speed.
 //      fp32 pools: CUDA-core FMAs in fp32 (8 lanes per token for Q.K with a
 //        butterfly that sums and spreads the G scores; each lane owns D/32
 //        output elements for PV).
@@ -100,6 +105,9 @@ struct Params {
   // the four tensor copies of a stage deliver, the scale bytes of a row, the
   // pitch of a warp's fp16 V tile, and the token-row coordinate of a block
   int off_kc, off_vc, off_ks, off_vs, tx_bytes, sbytes, vrs;
+  // bf16 pools: rows per tensor-copy box, bytes of one box, 64-element halves
+  // of a head row (the K boxes of a stage, then the V boxes)
+  int box_rows, box_bytes, halves;
   long long rows_per_block;  // num_layers * block_size
   int layer_row;             // layer * block_size
   float qscale;
@@ -334,7 +342,12 @@ __device__ __forceinline__ Lookup lookup_batch(const Params& p, const long long*
   return L;
 }
 
-template <bool TMA, int MODE>
+// Staging of a stage: one bulk copy per token row (fp32 pools), or tensor
+// copies of whole boxes (int8 pools: codes and scales; bf16 pools: swizzled
+// halves of the head rows).
+enum : int { kStageRows = 0, kStageI8 = 1, kStageBf16 = 2 };
+
+template <int STG, int MODE>
 __device__ void run_producer(const Params& p, const Pipe& pp, const I8Maps& maps,
                              const long long* s_cu, int lane, long long x0, long long x1) {
   const WaitCtl w = make_wait_ctl(p.err, p.wait_ns, p.epoch);
@@ -394,7 +407,7 @@ __device__ void run_producer(const Params& p, const Pipe& pp, const I8Maps& maps
         const int4 desc = make_int4(kb, blk_ok ? n : 0, flags, (int)blockIdx.x + kb);
         const uint32_t full = pp.full(s);
         const uint32_t stage = (uint32_t)s * pp.stage_bytes;
-        if constexpr (TMA) {
+        if constexpr (STG == kStageI8) {
           // int8 pools: the consumers are the slower side, so the producer
           // mostly waits here; it sleeps rather than polls, leaving the issue
           // slots of its SMSP to the two consumer warps beside it
@@ -402,7 +415,25 @@ __device__ void run_producer(const Params& p, const Pipe& pp, const I8Maps& maps
         } else {
           if (!mbar_wait(pp.empty(s), ph, w)) { ok = false; break; }
         }
-        if constexpr (TMA) {
+        if constexpr (STG == kStageBf16) {
+          // bf16 pools: for each 64-element half of the head rows, one box of
+          // (64, box_rows, Hkv) from K and one from V, starting at row rs0;
+          // rows past n are masked (past the pool they arrive as zeros)
+          if (lane == 0) {
+            pp.desc[s] = desc;
+            if (blk_ok) {
+              mbar_arrive_expect_tx(full, (uint32_t)p.tx_bytes);
+              const int row = (int)(kblk * p.rows_per_block + p.layer_row + rs0);
+              const uint32_t base_s = smem_addr(pp.smem) + stage;
+              for (int h = 0; h < p.halves; ++h) {
+                tma_3d(base_s + h * p.box_bytes, &maps.kc, 64 * h, row, 0, full);
+                tma_3d(base_s + (p.halves + h) * p.box_bytes, &maps.vc, 64 * h, row, 0, full);
+              }
+            } else {
+              mbar_arrive(full);
+            }
+          }
+        } else if constexpr (STG == kStageI8) {
           // int8 pools: four tensor copies per stage (K and V codes, K and V
           // scales), always whole boxes of st rows starting at row rs0; rows
           // past n are never read (past the pool they arrive as zeros)
@@ -573,9 +604,14 @@ __device__ void run_consumer_mma(const Params& p, const Pipe& pp, int warp, int 
   const int wph = p.nw / hkv;
   const int gl = lane >> 2;  // mma group row
   const int qi = lane & 3;   // mma thread in group
-  const int rs = p.rs;
-  const int ST = p.st;
-  const uint32_t head_off = g * D * 2;
+  // The stage holds, per 64-element half of the head rows, a K box and then
+  // a V box of Hkv x box_rows lines of 128 bytes (line g * box_rows + row),
+  // written with the 128-byte swizzle: 16-byte chunk c of line L sits at
+  // chunk c ^ (L & 7).  The 8 rows one ldmatrix reads are 8 consecutive
+  // lines, so they fall in 8 different chunk positions: no bank conflicts.
+  const int R = p.box_rows;
+  const uint32_t box = p.box_bytes;
+  const uint32_t v_boxes = p.halves * box;
   const int ld_t = (lane & 7) + ((lane >> 3) & 1) * 8;  // K rows (A of Q.K, non-trans)
   const int ld_c = lane >> 4;
   const int pv_t = (lane & 7) + (lane >> 4) * 8;        // V rows (A of P.V, trans)
@@ -595,8 +631,7 @@ __device__ void run_consumer_mma(const Params& p, const Pipe& pp, int warp, int 
     if (!mbar_wait(pp.full(s), ph, w)) return;
     const int4 dsc = pp.desc[s];
     const int b = dsc.x, n = dsc.y, flags = dsc.z, seg = dsc.w;
-    const uint32_t sK = smem_addr(pp.smem + (size_t)s * pp.stage_bytes) + head_off;
-    const uint32_t sV = sK + ST * rs;
+    const uint32_t sbase = smem_addr(pp.smem) + (uint32_t)s * pp.stage_bytes;
 
     if (flags & kStart) {
       mv = false;
@@ -620,11 +655,15 @@ __device__ void run_consumer_mma(const Params& p, const Pipe& pp, int warp, int 
       // rows past n hold stale data: read a valid row instead (it is masked)
       const int rk = min(t_lo + ld_t, n - 1);
       const int rv = min(t_lo + pv_t, n - 1);
+      const int lk = g * R + rk, lv = g * R + rv;  // their lines in the boxes
+      const uint32_t k_line = sbase + lk * 128, v_line = sbase + v_boxes + lv * 128;
+      const int kx = lk & 7, vx = lv & 7;
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < KS; ++j) {
+        // chunk 2j + ld_c of the head row: box j / 4, chunk (2j % 8) + ld_c
         uint32_t a[4];
-        ldsm_x4(a, sK + rk * rs + (2 * j + ld_c) * 16);
+        ldsm_x4(a, k_line + (j >> 2) * box + ((((2 * j) & 7) + ld_c) ^ kx) * 16);
         mma_bf16(sc, a, qb[j][0], qb[j][1]);
       }
       const int t0 = t_lo + gl, t1 = t0 + 8;
@@ -661,7 +700,7 @@ __device__ void run_consumer_mma(const Params& p, const Pipe& pp, int warp, int 
 #pragma unroll
       for (int kt = 0; kt < KS; ++kt) {
         uint32_t a[4];
-        ldsm_x4_t(a, sV + rv * rs + (2 * kt + pv_c) * 16);
+        ldsm_x4_t(a, v_line + (kt >> 2) * box + ((((2 * kt) & 7) + pv_c) ^ vx) * 16);
         mma_bf16(o[kt], a, pb[0], pb[1]);
       }
       __syncwarp();
@@ -1316,10 +1355,11 @@ __global__ void __launch_bounds__((consumer_warps<T>() + 1) * 32, 1)
 
   if constexpr (MODE == kModeStep) {
     // The decode step: this CTA's block range holds the last block of some
-    // sequences; their new K/V rows go into the pool here, before any bulk
-    // copy of this CTA reads it.  No other CTA reads those rows: a
+    // sequences; their new K/V rows go into the pool here, before any
+    // copy of this CTA reads it.  No other CTA uses those rows: a
     // sequence's last block lies in exactly one range, and the block of a
-    // new token belongs to its sequence alone.
+    // new token belongs to its sequence alone (a tensor-copy box of another
+    // CTA may carry them past its own rows, but those are never read).
     int b = 0, hi = B;  // first sequence ending at or after block x0
     while (b < hi) {
       const int mid = (b + hi) >> 1;
@@ -1361,13 +1401,14 @@ __global__ void __launch_bounds__((consumer_warps<T>() + 1) * 32, 1)
         }
       }
     }
-    // the rows just stored are read next by the bulk copies (async proxy)
+    // the rows just stored are read next by the copies (async proxy)
     fence_proxy_async_global();
     __syncthreads();
   }
 
   if (warp == NW) {
-    run_producer<sizeof(T) == 1, MODE>(p, pp, maps, s_cu, lane, x0, x1);
+    run_producer<sizeof(T) == 1 ? kStageI8 : sizeof(T) == 2 ? kStageBf16 : kStageRows, MODE>(
+        p, pp, maps, s_cu, lane, x0, x1);
     return;
   }
   if (p.skip_fill == 2 || (p.skip_fill == 1 && blockIdx.x == 0)) {
@@ -1512,12 +1553,13 @@ struct Layout {
   int st, rs, vrs, stages, smem, off_bar, off_desc, off_cu, off_scan, off_pbuf, off_mbuf,
       off_vbuf;
   int stage_bytes, off_kc, off_vc, off_ks, off_vs, tx_bytes, sbytes;  // see Params
+  int box_rows, box_bytes, halves;                                    // see Params
 };
 
 int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
 Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int smem_optin,
-                   bool quant, int nw) {
+                   bool quant, bool elem2, int nw) {
   Layout L{};
   L.st = stage_tokens(bs, row_bytes);
   L.rs = row_bytes + kRowPad;
@@ -1535,6 +1577,17 @@ Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int 
     L.off_vs = align_up(L.off_ks + L.st * L.sbytes, 128);
     L.stage_bytes = align_up(L.off_vs + L.st * L.sbytes, 1024);
     L.tx_bytes = 2 * codes + 2 * L.st * L.sbytes;
+  } else if (elem2) {
+    // bf16: per stage, tensor-copy boxes of (64 elements, box_rows rows,
+    // Hkv heads) with the 128-byte swizzle, K halves then V halves; a box
+    // holds Hkv * box_rows lines of 128 bytes, at least 8 so that every box
+    // is a whole number of 1024-byte swizzle blocks
+    L.halves = D / 64;
+    L.box_rows = L.st;
+    while (hkv * L.box_rows < 8) L.box_rows *= 2;
+    L.box_bytes = hkv * L.box_rows * 128;
+    L.stage_bytes = 2 * L.halves * L.box_bytes;
+    L.tx_bytes = L.stage_bytes;
   } else {
     L.stage_bytes = 2 * L.st * L.rs;
   }
@@ -1553,6 +1606,7 @@ Layout make_layout(int bs, int row_bytes, int hkv, int G, int D, int batch, int 
   fixed = align_up(fixed, 128);
   if (quant && (L.off_vc % 1024 || L.off_ks % 128 || L.off_vs % 128 || stage_bytes % 1024))
     return L;  // stages 0: refused (every tensor copy needs an aligned destination)
+  if (elem2 && (L.box_bytes % 1024 || (D != 64 && D != 128))) return L;  // the same
   int stages = (smem_optin - fixed) / stage_bytes;
   if (stages > kMaxStages) stages = kMaxStages;
   L.stages = stages;
@@ -1642,6 +1696,9 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
   p.off_vs = L.off_vs;
   p.tx_bytes = L.tx_bytes;
   p.sbytes = L.sbytes;
+  p.box_rows = L.box_rows;
+  p.box_bytes = L.box_bytes;
+  p.halves = L.halves;
   p.rows_per_block = (long long)pv.num_layers * pv.block_size;
   p.layer_row = a.layer * pv.block_size;
   p.qscale = a.scale * kLog2e;
@@ -1681,6 +1738,19 @@ cudaError_t run(const DecodeLaunch& a, const Layout& L, cudaStream_t s) {
                       sstrides, sbox, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_tiled(&maps.vs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, pv.v + pv.scale_off, sdims,
                       sstrides, sbox, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  }
+  if constexpr (sizeof(T) == 2) {
+    // bf16: K and V as (d, token row, kv head) boxes of (64, box_rows, Hkv)
+    // elements with the 128-byte swizzle
+    const cuuint64_t rows = (cuuint64_t)pv.num_blocks * pv.num_layers * pv.block_size;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, rows, (cuuint64_t)pv.num_kv_heads};
+    const cuuint64_t strides[2] = {(cuuint64_t)pv.row_bytes, (cuuint64_t)D * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)L.box_rows, (cuuint32_t)pv.num_kv_heads};
+    if (!encode_tiled(&maps.kc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pv.k, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tiled(&maps.vc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pv.v, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
   auto kern = decode_partial_kernel<T, D, G, MODE>;
@@ -1750,7 +1820,8 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s) {
   const PoolView& pv = a.pool;
   const int G = a.num_q_heads / pv.num_kv_heads;
   const Layout L = make_layout(pv.block_size, pv.row_bytes, pv.num_kv_heads, G, pv.head_dim,
-                               a.batch, a.smem_optin, pv.quant != 0, pv.quant ? kNWI8 : kNW);
+                               a.batch, a.smem_optin, pv.quant != 0,
+                               pv.quant == 0 && pv.elem_size == 2, pv.quant ? kNWI8 : kNW);
   if (L.stages < 2) return cudaErrorInvalidConfiguration;
   if (pv.quant) {
     // tensor-copy row coordinates are 32-bit
@@ -1759,6 +1830,9 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t s) {
     return pv.head_dim == 128 ? run_g<int8_t, 128>(a, L, G, s) : run_g<int8_t, 64>(a, L, G, s);
   }
   if (pv.elem_size == 2) {
+    // tensor-copy row coordinates are 32-bit
+    if ((long long)pv.num_blocks * pv.num_layers * pv.block_size >= (1ll << 31))
+      return cudaErrorInvalidConfiguration;
     return pv.head_dim == 128 ? run_g<__nv_bfloat16, 128>(a, L, G, s)
                               : run_g<__nv_bfloat16, 64>(a, L, G, s);
   }

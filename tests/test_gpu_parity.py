@@ -180,6 +180,12 @@ SWEEP = [
     ("bf16", 128, 8, 4, 4, 1, 60),
     ("bf16", 64, 4, 2, 64, 0, 200),
     ("bf16", 128, 8, 4, 1, 1, 20),
+    # boxes taller than a stage (kv heads x stage rows < 8): the extra rows
+    # come from the next layer, or from past the pool on the last layer
+    ("bf16", 64, 1, 4, 2, 2, 30),
+    ("bf16", 128, 2, 4, 1, 2, 20),
+    ("bf16", 64, 1, 8, 4, 0, 40),
+    ("bf16", 128, 1, 2, 1, 2, 12),
     ("f32", 64, 4, 1, 16, 0, 100),
     ("f32", 128, 8, 4, 16, 1, 100),
     ("f32", 128, 2, 2, 8, 1, 80),
