@@ -58,8 +58,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// CL: acquire at cluster scope, for a barrier that CTAs of the cluster other
+// than this one arrive at (their writes before the arrive become visible).
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
+  if constexpr (CL) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+  }
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -73,9 +86,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // The same with an explicit suspend-time hint: the waiting thread sleeps until
 // the phase completes or about `hint_ns` pass, instead of polling, so a waiting
 // warp takes no issue slots from the warps that work beside it.
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
                                                     uint32_t hint_ns) {
   uint32_t ok;
+  if constexpr (CL) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+  }
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
@@ -131,12 +155,13 @@ __device__ __forceinline__ void give_up(const WaitCtl& w) {
 // The slow part of a wait, entered only after kAbortCheckNs: the bound, the
 // launch's abort word, and the give-up.  Kept out of line so the tight poll
 // of the healthy case stays as short as a plain one.
+template <bool CL = false>
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
                                                    const WaitCtl w, unsigned long long t0,
                                                    uint32_t hint_ns) {
 #pragma unroll 1
   for (uint32_t it = 1; it < (1u << 30); ++it) {
-    if (hint_ns ? mbar_try_wait_sleep(bar, parity, hint_ns) : mbar_try_wait(bar, parity))
+    if (hint_ns ? mbar_try_wait_sleep<CL>(bar, parity, hint_ns) : mbar_try_wait<CL>(bar, parity))
       return true;
     if (hint_ns || (it & 63u) == 0) {
       if (global_timer_ns() - t0 > w.limit_ns) break;
@@ -151,29 +176,31 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
 // reached, or the launch gave up elsewhere) returns false, the first with
 // kErrTimeout set, so the caller can leave cleanly.  Polls: for the short
 // waits of the streaming kernels.
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<CL>(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
 #pragma unroll 1
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<CL>(bar, parity)) return true;
     if ((it & 63u) == 0 && global_timer_ns() - t0 > kAbortCheckNs) break;
   }
-  return mbar_wait_slow(bar, parity, w, t0, 0);
+  return mbar_wait_slow<CL>(bar, parity, w, t0, 0);
 }
 
 // The same, sleeping between checks (suspend-time hint): for waits that last
 // as long as a tensor-core product, where a polling warp would take issue
 // slots from the warp working beside it.
+template <bool CL = false>
 __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const WaitCtl& w) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<CL>(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
 #pragma unroll 1
   for (;;) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (mbar_try_wait_sleep<CL>(bar, parity, 20000u)) return true;
     if (global_timer_ns() - t0 > kAbortCheckNs) break;
   }
-  return mbar_wait_slow(bar, parity, w, t0, w.limit_ns < 1000000ull ? 1000u : 100000u);
+  return mbar_wait_slow<CL>(bar, parity, w, t0, w.limit_ns < 1000000ull ? 1000u : 100000u);
 }
 
 // Wait for asynchronous copies this CTA issued to land before it leaves (or

@@ -10,7 +10,8 @@
 // reads kv head h / (Hq / Hkv).
 //
 // Work items are (pair of query tiles, sequence, kv head), taken in turn by a
-// persistent grid of one CTA per SM:
+// persistent grid of one CTA per SM; for prefill the CTAs run in pairs (two-
+// CTA clusters) that share every K/V tile (below):
 //  * A query tile is 128 MMA rows = (128 / G) query tokens x the G query
 //    heads of kv head g, so each K/V tile feeds all G heads (row r = token *
 //    G + head).  The CTA owns two tiles, A and B, that share the K/V stream.
@@ -29,6 +30,11 @@
 //    P is stored; the O row is then rescaled in TMEM), and write P as bf16
 //    pairs over the S columns in TMEM, the A operand of the second MMA.
 //  * Epilogue: O row / l -> bf16 -> global (only rows that are real queries).
+//  * CTA pairs: the two CTAs of a cluster take neighbouring tile pairs of one
+//    (sequence, kv head), so they stream the same K/V tiles.  Each loads one
+//    64-column half of every tile by TMA and copies it into the other CTA's
+//    ring (a shared-memory bulk copy within the cluster), so each tile is
+//    read from L2 once for both SMs.  No tensor copy is multicast.
 // Every wait is bounded; on a timeout the CTA records the error, drains its
 // MMAs and frees its TMEM before returning.
 #include <cuda.h>
@@ -47,7 +53,12 @@ namespace {
 constexpr int kPfWarps = 10;  // 0-3 softmax A, 4-7 softmax B, 8 TMA, 9 MMA
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
-constexpr int kPfThreads = kPfWarps * 32;
+constexpr int kWarpFwd = 10;  // CTA pairs: forwards this CTA's halves to the other CTA
+// threads of a CTA: one more warp in a CTA pair
+template <bool SHARE>
+constexpr int pf_threads() {
+  return (kPfWarps + (SHARE ? 1 : 0)) * 32;
+}
 constexpr int kRows = 128;   // MMA M: query rows per tile
 constexpr int kKeys = 128;   // keys per KV tile (MMA N of Q K^T, K of P V)
 constexpr int kD = 128;      // head_dim
@@ -61,7 +72,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kOffQ = 0;                              // Q_A, Q_B
 constexpr int kOffKV = 2 * kTileBytes;                // ring of kSlots tiles
 constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;      // barriers + TMEM slot + alignment slack
+constexpr int kOffTslot = kOffBar + 320;              // TMEM address, after the barriers
+constexpr int kSmemBytes = kOffBar + 512 + 1024;      // barriers + TMEM slot + alignment slack
 
 struct PfParams {
   const int32_t* bt;
@@ -129,6 +141,57 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
+}
+
+// The same arrive on the barrier at address `bar` in both CTAs of a pair (an
+// arrive signal only: no data moves between the CTAs).
+__device__ __forceinline__ void umma_commit_both(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
+// ---- CTA pairs (clusters of two that share their K/V tiles) -------------------------
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// shared::cluster address of this CTA's shared address `a` in CTA `rank`
+__device__ __forceinline__ uint32_t peer_addr(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+
+// arrive on a barrier of the other CTA of the pair (cluster address)
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// bytes of this CTA's shared memory at `src` to `dst` in the other CTA's
+// (cluster address), completion counted as transaction bytes on that CTA's
+// barrier `bar` (cluster address); 16-byte aligned, a multiple of 16 bytes
+__device__ __forceinline__ void bulk_s2s(uint32_t dst, uint32_t src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst),
+      "r"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// every thread of both CTAs
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_after() {
@@ -413,15 +476,41 @@ __device__ __forceinline__ Item make_item_prefix(const PfParams& p, long long i)
   return it;
 }
 
+// CTA pairs: cluster item c gives the pair the query-tile pairs 2 c' and
+// 2 c' + 1 of one (sequence, kv head) (c' = c / (batch x Hkv)); the even CTA
+// holds the later pair, whose key tiles cover the other's.
+__device__ __forceinline__ long long item_of(const PfParams& p, long long c, uint32_t rank) {
+  const long long per = (long long)p.batch * p.hkv;
+  const long long pc = c / per;
+  return (2 * pc + rank) * per + (c - pc * per);
+}
+
 // Persistent: one CTA per SM walks the items c, c + grid, c + 2 grid, ...
 // (pairs of every sequence and head in order of decreasing key count).  The
 // K/V ring, the barrier phases and the TMEM allocation carry over from item
 // to item, so the next item's loads and first products overlap the previous
 // item's epilogue.
-template <bool PREFIX>
-__global__ void __launch_bounds__(kPfThreads, 1)
+//
+// CTA pairs (SHARE: clusters of two CTAs, one per SM, each computing its own
+// items as above) read every K/V tile from L2 once for both CTAs:
+//  * the two CTAs take neighbouring query-tile pairs of the same (sequence,
+//    kv head) and stream the same key tiles (those of the even CTA's item;
+//    the odd CTA's products skip the ones its item does not reach);
+//  * each CTA loads by TMA one 64-column half of every tile (the even CTA
+//    half 0, the odd one half 1) into its own ring, and its warp 10 then
+//    copies that half into the same slot of the other CTA (a shared-memory
+//    bulk copy between the CTAs), so each slot fills from both sides;
+//  * a slot is refilled once the products of both CTAs have read it: every
+//    release (a product commit, or an arrive for a tile not multiplied)
+//    arrives on the "slot free" barriers of both CTAs.
+// Each CTA waits for every release of its slots before it leaves (so no
+// copy or arrive of the other CTA still targets it), and the two leave
+// together (a cluster barrier).
+template <bool PREFIX, bool SHARE>
+__global__ void __launch_bounds__(pf_threads<SHARE>(), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const PfParams p) {
+  static_assert(!(PREFIX && SHARE), "the prefix pass runs on single CTAs");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // Prefix pass of shared-prefix decode: it reads nothing the grid before it
   // (the suffix pass) writes, and that grid's own inputs were complete when
@@ -439,10 +528,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   // ---- shared memory, barriers, TMEM --------------------------------------------------
   unsigned char* sQ = smem + kOffQ;  // [A | B]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffBar + 192);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffTslot);
   // barriers: Q full, ring full[kSlots], ring empty[kSlots], then per tile
-  // A / B: S ready, P written, O += P V done, O read by the epilogue
-  static_assert((2 * kSlots + 12) * 8 <= 192, "barriers overlap the TMEM address slot");
+  // A / B: S ready, P written, O += P V done, O read by the epilogue, then
+  // (CTA pairs) this CTA's own half of a slot loaded[kSlots]
+  static_assert((3 * kSlots + 12) * 8 <= kOffTslot - kOffBar,
+                "barriers overlap the TMEM address slot");
   const uint32_t b_qfull = smem_addr(&bars[0]);
   const uint32_t b_full0 = smem_addr(&bars[1]);                // ring slot filled
   const uint32_t b_empty0 = smem_addr(&bars[1 + kSlots]);      // ring slot consumed
@@ -453,8 +544,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t b_drain = smem_addr(&bars[9 + 2 * kSlots]);
   const uint32_t b_qempty = smem_addr(&bars[10 + 2 * kSlots]);  // an item's S products read Q
   const uint32_t b_stall = smem_addr(&bars[11 + 2 * kSlots]);   // never arrived at (test hook)
+  const uint32_t b_half0 = smem_addr(&bars[12 + 2 * kSlots]);   // own half of a slot loaded
   auto slot_full = [&](int i) { return b_full0 + 8u * i; };
   auto slot_empty = [&](int i) { return b_empty0 + 8u * i; };
+  auto slot_half = [&](int i) { return b_half0 + 8u * i; };
+  const uint32_t rank = SHARE ? cluster_rank() : 0u, peer = rank ^ 1u;
   auto slot_ptr = [&](int i) { return smem + kOffKV + i * kTileBytes; };
 
   if (tid == 0) {
@@ -462,7 +556,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     mbar_init(b_qempty, 1);
     for (int i = 0; i < kSlots; ++i) {
       mbar_init(slot_full(i), 1);
-      mbar_init(slot_empty(i), 1);
+      mbar_init(slot_empty(i), SHARE ? 2 : 1);  // a pair: released by both CTAs
+      mbar_init(slot_half(i), 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(b_sfull0 + 8u * x, 1);
@@ -483,12 +578,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // CTA pair: the other CTA's copies and arrivals target these barriers
+  if constexpr (SHARE) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem = *tslot;
   // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512)
   auto tS = [&](int x) { return tmem + 128u * x; };
   auto tO = [&](int x) { return tmem + 256u + 128u * x; };
   const long long n_items = p.n_items;
+  const long long i_first = SHARE ? blockIdx.x >> 1 : blockIdx.x;
+  const long long i_step = SHARE ? gridDim.x >> 1 : gridDim.x;
+  // this CTA's item of (cluster) item c, and the item whose key tiles the
+  // pair streams (the even CTA's)
+  auto own_item = [&](long long c) {
+    return PREFIX ? make_item_prefix(p, c) : make_item(p, SHARE ? item_of(p, c, rank) : c, tid);
+  };
+  auto lead_item = [&](long long c, const Item& own) {
+    return !SHARE || rank == 0 ? own : make_item(p, item_of(p, c, 0), tid);
+  };
   const WaitCtl w = make_wait_ctl(p.err, p.wait_ns, p.epoch);
   bool ok = true;
 
@@ -497,21 +604,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int box_bytes = p.bs * 128;
     long long ld = 0;  // K / V loads issued so far (ring position)
     int jq = 0;        // items whose Q was loaded
-    for (long long i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-      const Item it = PREFIX ? make_item_prefix(p, i) : make_item(p, i, tid);
-      if (!it.valid) continue;
-      // Q of this item once the previous item's S products have read the old one
-      if (jq > 0 && !mbar_wait_sleep(b_qempty, (jq - 1) & 1, w)) { ok = false; break; }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(b_qfull, (it.nA > 0 ? 2 : 1) * kTileBytes);
-        for (int x = (it.nA > 0 ? 0 : 1); x < 2; ++x) {
-          const int z = (int)(it.q0 + (x == 0 ? it.qtA : it.qtB) * TQ);
-          for (int h = 0; h < 2; ++h)
-            tma_3d(smem_addr(sQ + x * kTileBytes + h * kHalf), &tq, h * 64, it.g * G, z, b_qfull);
+    for (long long i = i_first; i < n_items && ok; i += i_step) {
+      const Item it = own_item(i);
+      const Item lead = lead_item(i, it);
+      if (!lead.valid) continue;
+      if (it.valid) {
+        // Q of this item once the previous item's S products have read the old one
+        if (jq > 0 && !mbar_wait_sleep(b_qempty, (jq - 1) & 1, w)) { ok = false; break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(b_qfull, (it.nA > 0 ? 2 : 1) * kTileBytes);
+          for (int x = (it.nA > 0 ? 0 : 1); x < 2; ++x) {
+            const int z = (int)(it.q0 + (x == 0 ? it.qtA : it.qtB) * TQ);
+            for (int h = 0; h < 2; ++h)
+              tma_3d(smem_addr(sQ + x * kTileBytes + h * kHalf), &tq, h * 64, it.g * G, z,
+                     b_qfull);
+          }
         }
+        ++jq;
       }
-      ++jq;
-      for (int li = 0; li < 2 * it.nB && ok; ++li, ++ld) {
+      for (int li = 0; li < 2 * lead.nB && ok; ++li, ++ld) {
         const int slot = (int)(ld % kSlots);
         const long long use = ld / kSlots;
         if (use > 0 && !mbar_wait_sleep(slot_empty(slot), (uint32_t)((use - 1) & 1), w)) {
@@ -519,15 +630,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           break;
         }
         const int t = li >> 1, is_v = li & 1;
-        if (lane == 0) mbar_arrive_expect_tx(slot_full(slot), kTileBytes);
+        // one CTA: both 64-column halves; a pair: this CTA's half, counted on
+        // its own "half loaded" barrier (the other half comes from the peer)
+        const uint32_t bar = SHARE ? slot_half(slot) : slot_full(slot);
+        if (lane == 0) mbar_arrive_expect_tx(bar, SHARE ? kHalf : kTileBytes);
         __syncwarp();
-        for (int k2 = lane; k2 < 2 * blocks_per_tile; k2 += 32) {
-          const int h = k2 / blocks_per_tile;
-          const int k = k2 % blocks_per_tile;
-          const long long lb = (long long)(PREFIX ? it.t0 + t : t) * blocks_per_tile + k;
+        for (int k2 = lane; k2 < (SHARE ? 1 : 2) * blocks_per_tile; k2 += 32) {
+          const int h = SHARE ? (int)rank : k2 / blocks_per_tile;
+          const int k = SHARE ? k2 : k2 % blocks_per_tile;
+          const long long lb = (long long)(PREFIX ? lead.t0 + t : t) * blocks_per_tile + k;
           long long coord = p.blk_coord_limit;                       // out of range: zeros
-          if (lb < it.spanned) {
-            const int blk = p.bt[(long long)it.b * p.mb + lb];
+          if (lb < lead.spanned) {
+            const int blk = p.bt[(long long)lead.b * p.mb + lb];
             if (blk >= 0 && blk < p.num_blocks) {
               coord = (long long)blk * p.L + p.layer;
             } else {
@@ -535,7 +649,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             }
           }
           tma_4d(smem_addr(slot_ptr(slot) + h * kHalf + k * box_bytes), is_v ? &tv : &tk, h * 64,
-                 it.g, 0, (int)coord, slot_full(slot));
+                 lead.g, 0, (int)coord, bar);
         }
         __syncwarp();
       }
@@ -546,9 +660,40 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // last load of each slot and the last Q load are the ones to wait for.
     for (long long idx = ld - kSlots; idx < ld; ++idx) {
       if (idx < 0) continue;
-      mbar_wait_drain(slot_full((int)(idx % kSlots)), (uint32_t)((idx / kSlots) & 1), p.err);
+      const int slot = (int)(idx % kSlots);
+      const uint32_t ph = (uint32_t)((idx / kSlots) & 1);
+      if constexpr (SHARE) {
+        // this CTA's own copies, then every release of the slot by both CTAs
+        // (after which the other CTA sends nothing more into it)
+        mbar_wait_drain(slot_half(slot), ph, p.err);
+        mbar_wait_sleep(slot_empty(slot), ph, w);
+      } else {
+        mbar_wait_drain(slot_full(slot), ph, p.err);
+      }
     }
     if (jq > 0) mbar_wait_drain(b_qfull, (uint32_t)((jq - 1) & 1), p.err);
+  } else if (SHARE && warp == kWarpFwd) {
+    // ================= CTA pair: this CTA's half of each slot to the other CTA =================
+    // once its copy landed; this CTA's "slot full" then waits only for the
+    // other CTA's half
+    if (lane == 0) {
+      const uint32_t half_off = rank * kHalf;
+      long long ld = 0;
+      for (long long i = i_first; i < n_items && ok; i += i_step) {
+        const Item lead = lead_item(i, own_item(i));
+        if (!lead.valid) continue;
+        for (int li = 0; li < 2 * lead.nB; ++li, ++ld) {
+          const int slot = (int)(ld % kSlots);
+          if (!mbar_wait_sleep(slot_half(slot), (uint32_t)((ld / kSlots) & 1), w)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(slot_full(slot), kHalf);
+          const uint32_t src = smem_addr(slot_ptr(slot)) + half_off;
+          bulk_s2s(peer_addr(src, peer), src, kHalf, peer_addr(slot_full(slot), peer));
+        }
+      }
+    }
   } else if (warp == kWarpMma) {
     // ================= MMA issuer =================
     // per item: S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ..., so
@@ -568,7 +713,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       int ne[2] = {0, 0};          // epilogues of A / B across items
       auto slot_of = [&](long long idx) { return (int)(idx % kSlots); };
       auto ready = [&](long long idx) {
-        return mbar_wait_sleep(slot_full(slot_of(idx)), (uint32_t)((idx / kSlots) & 1), w);
+        return mbar_wait_sleep<SHARE>(slot_full(slot_of(idx)), (uint32_t)((idx / kSlots) & 1), w);
+      };
+      // a slot is free once the products reading it completed (in both CTAs
+      // of a pair)
+      auto release = [&](long long idx) {
+        if constexpr (SHARE) {
+          umma_commit_both(slot_empty(slot_of(idx)));
+        } else {
+          umma_commit(slot_empty(slot_of(idx)));
+        }
       };
       auto issue_s = [&](int x, long long k_idx) {
         const uint32_t k_addr = smem_addr(slot_ptr(slot_of(k_idx)));
@@ -591,55 +745,66 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         umma_commit(b_pvdone0 + 8u * x);
       };
-      for (long long i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-        const Item it = PREFIX ? make_item_prefix(p, i) : make_item(p, i, tid);
-        if (!it.valid) continue;
-        const int nA = it.nA, nB = it.nB;
+      for (long long i = i_first; i < n_items && ok; i += i_step) {
+        const Item it = own_item(i);
+        const Item lead = lead_item(i, it);
+        if (!lead.valid) continue;
+        const int nA = it.valid ? it.nA : 0, nB = it.valid ? it.nB : 0;
         const long long base = ld;  // load index of K(0) of this item
-        if (!mbar_wait_sleep(b_qfull, jq & 1, w) || !ready(base)) { ok = false; break; }
-        ++jq;
-        if (nA > 0) issue_s(0, base);
-        issue_s(1, base);
-        // Q may be replaced once the last S product of the item completes: the
-        // next item's loads then overlap this item's last products and epilogue
-        if (nB == 1) umma_commit(b_qempty);
-        for (int t = 0; t < nB && ok; ++t) {
-          const long long ki = base + 2 * t, vi = ki + 1;
-          // K(t) is released after the S products that read it
-          umma_commit(slot_empty(slot_of(ki)));
-          if (!ready(vi)) { ok = false; break; }
-          if (t < nA) {
-            // O_A is overwritten by the first product: the previous epilogue
-            // must have read it
-            if (t == 0 && ne[0] > 0 && !mbar_wait_sleep(b_ofree0, (ne[0] - 1) & 1, w)) {
+        ld = base + 2 * lead.nB;
+        if (it.valid) {
+          if (!mbar_wait_sleep(b_qfull, jq & 1, w) || !ready(base)) { ok = false; break; }
+          ++jq;
+          if (nA > 0) issue_s(0, base);
+          issue_s(1, base);
+          // Q may be replaced once the last S product of the item completes: the
+          // next item's loads then overlap this item's last products and epilogue
+          if (nB == 1) umma_commit(b_qempty);
+          for (int t = 0; t < nB && ok; ++t) {
+            const long long ki = base + 2 * t, vi = ki + 1;
+            // K(t) is released after the S products that read it
+            release(ki);
+            if (!ready(vi)) { ok = false; break; }
+            if (t < nA) {
+              // O_A is overwritten by the first product: the previous epilogue
+              // must have read it
+              if (t == 0 && ne[0] > 0 && !mbar_wait_sleep(b_ofree0, (ne[0] - 1) & 1, w)) {
+                ok = false;
+                break;
+              }
+              if (!mbar_wait_sleep(b_pfull0, (uint32_t)(nt[0] & 1), w)) { ok = false; break; }
+              ++nt[0];
+              issue_pv(0, vi, t == 0);
+              if (t + 1 < nA) {
+                if (!ready(ki + 2)) { ok = false; break; }
+                issue_s(0, ki + 2);
+              }
+            }
+            if (t == 0 && ne[1] > 0 && !mbar_wait_sleep(b_ofree0 + 8u, (ne[1] - 1) & 1, w)) {
               ok = false;
               break;
             }
-            if (!mbar_wait_sleep(b_pfull0, (uint32_t)(nt[0] & 1), w)) { ok = false; break; }
-            ++nt[0];
-            issue_pv(0, vi, t == 0);
-            if (t + 1 < nA) {
-              if (!ready(ki + 2)) { ok = false; break; }
-              issue_s(0, ki + 2);
+            if (!mbar_wait_sleep(b_pfull0 + 8u, (uint32_t)(nt[1] & 1), w)) { ok = false; break; }
+            ++nt[1];
+            issue_pv(1, vi, t == 0);
+            release(vi);
+            if (t + 1 < nB) {
+              if (!(t + 1 < nA) && !ready(ki + 2)) { ok = false; break; }
+              issue_s(1, ki + 2);
+              if (t + 2 == nB) umma_commit(b_qempty);
             }
           }
-          if (t == 0 && ne[1] > 0 && !mbar_wait_sleep(b_ofree0 + 8u, (ne[1] - 1) & 1, w)) {
-            ok = false;
-            break;
-          }
-          if (!mbar_wait_sleep(b_pfull0 + 8u, (uint32_t)(nt[1] & 1), w)) { ok = false; break; }
-          ++nt[1];
-          issue_pv(1, vi, t == 0);
-          umma_commit(slot_empty(slot_of(vi)));
-          if (t + 1 < nB) {
-            if (!(t + 1 < nA) && !ready(ki + 2)) { ok = false; break; }
-            issue_s(1, ki + 2);
-            if (t + 2 == nB) umma_commit(b_qempty);
-          }
+          if (nA > 0) ++ne[0];
+          ++ne[1];
         }
-        ld = base + 2 * nB;
-        if (nA > 0) ++ne[0];
-        ++ne[1];
+        // tiles only the other CTA's item reads: wait for them and release
+        // them in both CTAs
+        for (int li = 2 * nB; li < 2 * lead.nB && ok; ++li) {
+          const long long idx = base + li;
+          if (!ready(idx)) { ok = false; break; }
+          mbar_arrive(slot_empty(slot_of(idx)));
+          mbar_arrive_remote(peer_addr(slot_empty(slot_of(idx)), peer));
+        }
       }
       umma_commit(b_drain);  // arrives once every MMA issued above has completed
     }
@@ -652,8 +817,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t b_sfull = b_sfull0 + 8u * x, b_pfull = b_pfull0 + 8u * x;
     const uint32_t b_pvdone = b_pvdone0 + 8u * x, b_ofree = b_ofree0 + 8u * x;
     long long nt = 0;  // tiles of this warpgroup across items (barrier phases)
-    for (long long i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
-      const Item it = PREFIX ? make_item_prefix(p, i) : make_item(p, i, tid);
+    for (long long i = i_first; i < n_items && ok; i += i_step) {
+      const Item it = own_item(i);
       if (!it.valid) continue;
       const int nX = x == 0 ? it.nA : it.nB;
       if (nX == 0) continue;
@@ -777,8 +942,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   // ---- teardown: every MMA this CTA issued has completed before TMEM is freed ----
   tc_fence_before();
   __syncthreads();
+  if (warp == 0) mbar_wait_drain(b_drain, 0, p.err);
+  // CTA pair: neither CTA leaves while the other may still address it
+  if constexpr (SHARE) cluster_sync_all();
   if (warp == 0) {
-    mbar_wait_drain(b_drain, 0, p.err);
     __syncwarp();  // the dealloc below is warp-wide
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -866,14 +1033,56 @@ cudaError_t prefill_launch(const CUtensorMap& tq, const CUtensorMap& tk, const C
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && configured[dev] == 0) {
-    e = cudaFuncSetAttribute(prefill_kernel<PREFIX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
+    e = cudaFuncSetAttribute(prefill_kernel<PREFIX, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   const long long grid = p.n_items < sm_count ? p.n_items : sm_count;
-  return launch_kernel(prefill_kernel<PREFIX>, dim3((unsigned)grid), dim3(kPfThreads),
-                       (size_t)kSmemBytes, s, true, tq, tk, tv, p);
+  return launch_kernel(prefill_kernel<PREFIX, false>, dim3((unsigned)grid),
+                       dim3(pf_threads<false>()), (size_t)kSmemBytes, s, true, tq, tk, tv, p);
+}
+
+// CTA pairs: clusters of two CTAs, as many as can be resident at once (at
+// most one per two SMs), as a programmatic dependent of the work before.
+cudaError_t prefill_launch_pairs(const CUtensorMap& tq, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, const PfParams& p, int sm_count,
+                                 cudaStream_t s) {
+  auto kern = prefill_kernel<false, true>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(pf_threads<true>());
+  cfg.dynamicSmemBytes = (size_t)kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  static int max_pairs[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (max_pairs[dev] == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    // resident clusters: a persistent grid larger than this would queue
+    cfg.gridDim = dim3(2 * (unsigned)(sm_count / 2 > 0 ? sm_count / 2 : 1));
+    cfg.numAttrs = 1;  // the cluster shape alone
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    max_pairs[dev] = n > 0 ? n : 1;
+  }
+  long long np = sm_count / 2 < max_pairs[dev] ? sm_count / 2 : max_pairs[dev];
+  if (np < 1) np = 1;
+  if (p.n_items < np) np = p.n_items;
+  cfg.gridDim = dim3((unsigned)(2 * np));
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p);
 }
 
 }  // namespace
@@ -892,8 +1101,9 @@ cudaError_t launch_prefill(const PoolView& pv, int layer, const void* q, int num
   p.out = out;
   p.max_q_len = max_q_len;
   const long long ntq = (max_q_len + p.TQ - 1) / p.TQ;
-  p.n_items = (ntq + 1) / 2 * (long long)batch * pv.num_kv_heads;
-  return prefill_launch<false>(tq, tk, tv, p, sm_count, s);
+  // CTA pairs: pairs of query-tile pairs per (sequence, kv head)
+  p.n_items = ((ntq + 1) / 2 + 1) / 2 * (long long)batch * pv.num_kv_heads;
+  return prefill_launch_pairs(tq, tk, tv, p, sm_count, s);
 }
 
 void prefix_plan(const PoolView& pv, int num_q_heads, int batch, int prefix_blocks, int sm_count,
