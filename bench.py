@@ -331,6 +331,68 @@ class DecodeStep:
         return (self.host_arena.numel(),
                 self.host_out.numel() * self.host_out.element_size())
 
+    def e2e_pipelined(self, steps: int) -> float:
+        """Mean ms per step of `steps` end-to-end steps run as a serving loop
+        runs them: step k+1's inputs are copied host->device (into the second
+        of two device input arenas) on a copy stream while step k computes,
+        and step k's output is read back device->host on a third stream while
+        step k+1 computes.  Every step still moves its own inputs and output;
+        one pair of events spans the first copy to the last read-back.  The
+        K/V a step reads (1.27 GB) is ten times L2, so no flush runs between
+        the steps.  Checks that the last output read back equals the device
+        result bit for bit."""
+        pkv = self.pkv
+        comp = torch.cuda.current_stream(self.dev)
+        cp, rb = torch.cuda.Stream(self.dev), torch.cuda.Stream(self.dev)
+        if not hasattr(self, "_pipe"):
+            arena2 = torch.empty_like(self.dev_arena)
+            views = []
+            for arena in (self.dev_arena, arena2):
+                v = {}
+                for name in self._INPUTS:
+                    d = getattr(self, name)
+                    o = d.data_ptr() - self.dev_arena.data_ptr()
+                    nb = d.numel() * d.element_size()
+                    v[name] = arena[o:o + nb].view(d.dtype).view(d.shape)
+                views.append(v)
+            outs = [self.out, torch.empty_like(self.out)]
+            host_outs = [self.host_out, torch.empty_like(self.host_out).pin_memory()]
+            self._pipe = ((self.dev_arena, arena2), views, outs, host_outs)
+        arenas, views, outs, host_outs = self._pipe
+        ev = lambda: torch.cuda.Event(enable_timing=False)
+        h2d = [ev() for _ in range(steps)]
+        done = [ev() for _ in range(steps)]
+        d2h = [ev() for _ in range(steps)]
+        t0, t1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+        torch.cuda.synchronize(self.dev)
+        t0.record(comp)
+        cp.wait_event(t0)
+        for k in range(steps):
+            a = k & 1
+            with torch.cuda.stream(cp):
+                if k >= 2:
+                    cp.wait_event(done[k - 2])  # step k-2 has read arena a
+                arenas[a].copy_(self.host_arena, non_blocking=True)
+                h2d[k].record(cp)
+            comp.wait_event(h2d[k])
+            if k >= 2:
+                comp.wait_event(d2h[k - 2])  # output a has been read back
+            v = views[a]
+            pkv.decode_step(self.pool, self.w.layer, v["q"], self.w.scale, v["bt"], v["lens"],
+                            v["offs"], v["k_new"], v["v_new"], outs[a], self.ws)
+            done[k].record(comp)
+            with torch.cuda.stream(rb):
+                rb.wait_event(done[k])
+                host_outs[a].copy_(outs[a], non_blocking=True)
+                d2h[k].record(rb)
+        comp.wait_event(d2h[steps - 1])
+        t1.record(comp)
+        torch.cuda.synchronize(self.dev)
+        last = (steps - 1) & 1
+        if not torch.equal(host_outs[last], outs[last].cpu()):
+            raise RuntimeError("pipelined end-to-end step: read-back output differs")
+        return t0.elapsed_time(t1) / steps
+
 
 class L2Flush:
     """Between timed steps: write a buffer larger than L2 (evicting whatever
@@ -485,7 +547,12 @@ def run_ours(args, rank, local_rank, world):
     barrier()
     e2e_times, _ = timed(st.step_e2e, args.steps, flush)
     barrier()
-    e2e_ms = reduce_max(statistics.mean(e2e_times))
+    e2e_serial_ms = reduce_max(statistics.mean(e2e_times))
+    # the same steps pipelined as a serving loop runs them (copies overlap compute)
+    st.e2e_pipelined(max(3, args.warmup))
+    barrier()
+    e2e_ms = reduce_max(st.e2e_pipelined(args.steps))
+    barrier()
     h2d, d2h = st.e2e_bytes()
 
     launches = st.launches_per_step * args.steps
@@ -549,7 +616,15 @@ def run_ours(args, rank, local_rank, world):
         "legs": legs,
         "e2e": {"value": round(aggregate(kv, world, e2e_ms) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "mode": "pipelined: step k+1's inputs copied host->device (second device "
+                        "arena) and step k's output read back on two copy streams while step "
+                        "k computes; one event span over all steps; no L2 flush inside it "
+                        "(each step reads 1.27 GB of K/V)",
+                "serial": {"value": round(aggregate(kv, world, e2e_serial_ms) / 1e9, 1),
+                           "ms_per_step": round(e2e_serial_ms, 4),
+                           "mode": "copy in, step, copy out in order on one stream, per-step "
+                                   "events, L2 flushed between steps"}},
         "gpu_launches": launches,
         "clocks": clocks.summary(),
     }
