@@ -207,10 +207,11 @@ __global__ void __launch_bounds__(kCopyThreads) quant_write_slots_kernel(
 // gather: one warp per kGatherRows consecutive output rows.  The sequence of
 // the first row is found by binary search in the packed layout cu_seqlens
 // (small and cache-resident), and the warp walks forward from it, so the
-// search is paid once per group (4 rows: 2.5 % faster than one row per warp
-// on the gather_scatter workload; 16 rows leave too few warps in flight)
+// search is paid once per group.  On the gather_scatter workload 2 rows per
+// warp measured best: 3 % faster than 1 and 4 rows, 6 % faster than 8 (with
+// more rows per warp, fewer warps share the copy and the last wave is short)
 // ---------------------------------------------------------------------------
-constexpr int kGatherRows = 4;
+constexpr int kGatherRows = 2;
 
 __global__ void __launch_bounds__(kCopyThreads) gather_kernel(
     const char* __restrict__ kc, const char* __restrict__ vc, const int32_t* __restrict__ bt,

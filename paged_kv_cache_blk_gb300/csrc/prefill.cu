@@ -724,24 +724,31 @@ __global__ void __launch_bounds__(pf_threads<SHARE>(), 1)
           umma_commit(slot_empty(slot_of(idx)));
         }
       };
+      // One thread issues every product, and a K = 16 step takes the tensor
+      // cores only about 100 cycles, so the issue loop is kept short: each
+      // product builds its two descriptors once and steps them by constants
+      // (the start address is the descriptor's low field, in 16-byte units;
+      // shared addresses stay below 256 KB, so the addition never carries).
       auto issue_s = [&](int x, long long k_idx) {
-        const uint32_t k_addr = smem_addr(slot_ptr(slot_of(k_idx)));
-        const uint32_t qa = q_addr + x * kTileBytes;
+        const uint64_t a0 = desc_sw128(q_addr + x * kTileBytes, 16, 1024);
+        const uint64_t b0 = desc_sw128(smem_addr(slot_ptr(slot_of(k_idx))), 16, 1024);
         tc_fence_after();
+#pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint64_t a = desc_sw128(qa + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = desc_sw128(k_addr + (k >> 2) * kHalf + (k & 3) * 32, 16, 1024);
-          umma(tS(x), a, bd, kIdescKK, k > 0);
+          const uint64_t step = (uint64_t)(((k >> 2) * kHalf + (k & 3) * 32) >> 4);
+          umma(tS(x), a0 + step, b0 + step, kIdescKK, k > 0);
         }
         umma_commit(b_sfull0 + 8u * x);
       };
       auto issue_pv = [&](int x, long long v_idx, bool first) {
-        const uint32_t v_addr = smem_addr(slot_ptr(slot_of(v_idx)));
+        const uint64_t b0 = desc_sw128(smem_addr(slot_ptr(slot_of(v_idx))), kHalf, 1024);
+        const uint32_t p0 = tS(x), o0 = tO(x);
         tc_fence_after();
+#pragma unroll
         for (int k = 0; k < 8; ++k) {
           // A = P from TMEM (S columns of tile x), B = V MN-major
-          const uint64_t bd = desc_sw128(v_addr + k * 2048, kHalf, 1024);
-          umma_ts(tO(x), tS(x) + 8u * k, bd, kIdescKMN, (!first || k > 0) ? 1u : 0u);
+          umma_ts(o0, p0 + 8u * k, b0 + (uint64_t)((k * 2048) >> 4), kIdescKMN,
+                  (!first || k > 0) ? 1u : 0u);
         }
         umma_commit(b_pvdone0 + 8u * x);
       };
