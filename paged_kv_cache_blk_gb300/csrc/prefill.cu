@@ -341,7 +341,20 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, uint32_t 
 #pragma unroll 1
     for (int c0 = 0; c0 < kKeys; c0 += 32) {
       float x[32];
-      if (full_tile && !pre) {
+      // in a masked tile (the causal diagonal) a chunk is often outside every
+      // row's keys of the warp (its P is zero: no exponentials) or inside all
+      // of them (no mask code); the votes keep the TMEM accesses warp-uniform
+      bool plain = full_tile;
+      if (!full_tile) {
+        if (__all_sync(0xffffffffu, c0 > c_hi || c0 + 31 < c_lo)) {
+          const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u,
+                                  0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+          tmem_st16(tS + lane_base + (c0 >> 1), z);
+          continue;
+        }
+        plain = __all_sync(0xffffffffu, c0 >= c_lo && c0 + 31 <= c_hi);
+      }
+      if (plain && !pre) {
         // the common case, kept free of masking and scaling code
         uint32_t v[32];
         tmem_ld32(tS + lane_base + c0, v);
