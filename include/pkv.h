@@ -307,7 +307,9 @@ PKV_API pkv_status pkv_decode_attention_shared_prefix(const pkv_pool* pool, int3
  * sets the error word (PKV_ERR_CAPACITY in validate mode).  Supported: bf16
  * pools with head_dim 128, block_size 8..128 dividing 128, num_q_heads /
  * num_kv_heads in {1, 2, 4, 8, 16}; others PKV_ERR_UNSUPPORTED.  No
- * workspace.  fp32 accumulation; P is rounded to bf16 for the P.V product. */
+ * workspace.  fp32 accumulation; P is rounded to bf16 for the P.V product.
+ * The kernel runs as clusters of two CTAs (one per SM) whose CTAs share each
+ * K/V tile; the grid holds as many clusters as can be resident at once. */
 PKV_API pkv_status pkv_prefill_attention(const pkv_pool* pool, int32_t layer, const void* q,
                                          int32_t num_q_heads, float scale,
                                          const int32_t* block_tables, int32_t max_blocks_per_seq,
