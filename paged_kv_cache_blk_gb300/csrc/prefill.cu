@@ -73,7 +73,9 @@ constexpr int kOffQ = 0;                              // Q_A, Q_B
 constexpr int kOffKV = 2 * kTileBytes;                // ring of kSlots tiles
 constexpr int kOffBar = kOffKV + kSlots * kTileBytes;
 constexpr int kOffTslot = kOffBar + 320;              // TMEM address, after the barriers
-constexpr int kSmemBytes = kOffBar + 512 + 1024;      // barriers + TMEM slot + alignment slack
+constexpr int kItemRing = 4;                          // items the loads warp publishes ahead
+constexpr int kOffItems = kOffBar + 512;              // [kItemRing][own item, lead item]
+constexpr int kSmemBytes = kOffItems + 1024 + 1024;   // + alignment slack
 
 struct PfParams {
   const int32_t* bt;
@@ -545,8 +547,9 @@ __global__ void __launch_bounds__(pf_threads<SHARE>(), 1)
   // barriers: Q full, ring full[kSlots], ring empty[kSlots], then per tile
   // A / B: S ready, P written, O += P V done, O read by the epilogue, then
   // (CTA pairs) this CTA's own half of a slot loaded[kSlots]
-  static_assert((3 * kSlots + 12) * 8 <= kOffTslot - kOffBar,
+  static_assert((3 * kSlots + 12 + 2 * kItemRing) * 8 <= kOffTslot - kOffBar,
                 "barriers overlap the TMEM address slot");
+  static_assert(kItemRing * 2 * sizeof(Item) <= 1024, "item ring overflows its carve");
   const uint32_t b_qfull = smem_addr(&bars[0]);
   const uint32_t b_full0 = smem_addr(&bars[1]);                // ring slot filled
   const uint32_t b_empty0 = smem_addr(&bars[1 + kSlots]);      // ring slot consumed
@@ -558,6 +561,11 @@ __global__ void __launch_bounds__(pf_threads<SHARE>(), 1)
   const uint32_t b_qempty = smem_addr(&bars[10 + 2 * kSlots]);  // an item's S products read Q
   const uint32_t b_stall = smem_addr(&bars[11 + 2 * kSlots]);   // never arrived at (test hook)
   const uint32_t b_half0 = smem_addr(&bars[12 + 2 * kSlots]);   // own half of a slot loaded
+  // the items' values, computed by the loads warp (which runs ahead) and read
+  // by the MMA warp, whose thread must keep issuing products
+  const uint32_t b_ifull0 = smem_addr(&bars[12 + 3 * kSlots]);
+  const uint32_t b_iempty0 = smem_addr(&bars[12 + 3 * kSlots + kItemRing]);
+  Item* s_items = reinterpret_cast<Item*>(smem + kOffItems);
   auto slot_full = [&](int i) { return b_full0 + 8u * i; };
   auto slot_empty = [&](int i) { return b_empty0 + 8u * i; };
   auto slot_half = [&](int i) { return b_half0 + 8u * i; };
@@ -580,6 +588,10 @@ __global__ void __launch_bounds__(pf_threads<SHARE>(), 1)
     }
     mbar_init(b_drain, 1);
     mbar_init(b_stall, 1);
+    for (int r = 0; r < kItemRing; ++r) {
+      mbar_init(b_ifull0 + 8u * r, 1);
+      mbar_init(b_iempty0 + 8u * r, 1);
+    }
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -617,9 +629,23 @@ __global__ void __launch_bounds__(pf_threads<SHARE>(), 1)
     const int box_bytes = p.bs * 128;
     long long ld = 0;  // K / V loads issued so far (ring position)
     int jq = 0;        // items whose Q was loaded
-    for (long long i = i_first; i < n_items && ok; i += i_step) {
+    long long ni = 0;  // items published
+    for (long long i = i_first; i < n_items && ok; i += i_step, ++ni) {
       const Item it = own_item(i);
       const Item lead = lead_item(i, it);
+      {
+        const int r = (int)(ni % kItemRing);
+        const long long use = ni / kItemRing;
+        if (use > 0 && !mbar_wait_sleep(b_iempty0 + 8u * r, (uint32_t)((use - 1) & 1), w)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          s_items[2 * r] = it;
+          s_items[2 * r + 1] = lead;
+          mbar_arrive(b_ifull0 + 8u * r);
+        }
+      }
       if (!lead.valid) continue;
       if (it.valid) {
         // Q of this item once the previous item's S products have read the old one
@@ -765,9 +791,16 @@ __global__ void __launch_bounds__(pf_threads<SHARE>(), 1)
         }
         umma_commit(b_pvdone0 + 8u * x);
       };
-      for (long long i = i_first; i < n_items && ok; i += i_step) {
-        const Item it = own_item(i);
-        const Item lead = lead_item(i, it);
+      long long ni = 0;  // items read from the loads warp
+      for (long long i = i_first; i < n_items && ok; i += i_step, ++ni) {
+        const int r = (int)(ni % kItemRing);
+        if (!mbar_wait_sleep(b_ifull0 + 8u * r, (uint32_t)((ni / kItemRing) & 1), w)) {
+          ok = false;
+          break;
+        }
+        const Item it = s_items[2 * r];
+        const Item lead = s_items[2 * r + 1];
+        mbar_arrive(b_iempty0 + 8u * r);
         if (!lead.valid) continue;
         const int nA = it.valid ? it.nA : 0, nB = it.valid ? it.nB : 0;
         const long long base = ld;  // load index of K(0) of this item
