@@ -751,8 +751,13 @@ __global__ void __launch_bounds__(pf_threads<SHARE>(), 1)
       long long nt[2] = {0, 0};    // tiles of A / B across items (barrier phases)
       int ne[2] = {0, 0};          // epilogues of A / B across items
       auto slot_of = [&](long long idx) { return (int)(idx % kSlots); };
+      // A slot's "full" barrier completes on this CTA's own arrival and on the
+      // transaction bytes of copies (this CTA's TMA loads; in a pair, the
+      // other CTA's bulk copy into this CTA): completions of asynchronous
+      // copies, which a CTA-scope wait orders before the products that read
+      // the slot, as for any TMA load.
       auto ready = [&](long long idx) {
-        return mbar_wait_sleep<SHARE>(slot_full(slot_of(idx)), (uint32_t)((idx / kSlots) & 1), w);
+        return mbar_wait_sleep(slot_full(slot_of(idx)), (uint32_t)((idx / kSlots) & 1), w);
       };
       // a slot is free once the products reading it completed (in both CTAs
       // of a pair)
