@@ -22,9 +22,14 @@
 //  * Warp 9 issues S_x = Q_x K^T (M 128, N 128, K 128: 8 tcgen05.mma, fp32
 //    in TMEM) and O_x += P_x V (V is the MN-major operand) in the order
 //    S_A(0) S_B(0) | PV_A(t) S_A(t+1) PV_B(t) S_B(t+1) | ..., so the softmax
-//    of one tile runs while the tensor cores work on the other.
+//    of one tile runs while the tensor cores work on the other.  Its thread
+//    advances in step with the tensor cores (their queue holds about one
+//    instruction), so it does little else: the item values come from the
+//    loads warp (warp 8) through a small shared-memory ring.
 //  * Warps 0-3 (tile A) and 4-7 (tile B) own one row each: they read the S
-//    row from TMEM (tcgen05.ld 32x32b), mask only the tiles that need it, keep
+//    row from TMEM (tcgen05.ld 32x32b), mask only the tiles and 32-key
+//    chunks that need it (a chunk masked for every row of the warp gets P = 0
+//    without exponentials), keep
 //    the running sum and a maximum that moves only when a score exceeds it by
 //    more than 8 in log2 units (checked per 32-key chunk before that chunk's
 //    P is stored; the O row is then rescaled in TMEM), and write P as bf16
